@@ -1,0 +1,409 @@
+"""Benchmark of the W8A8 INT8 fused-MoE layer (DeepSeek-V3 shape) on GB300.
+
+One step = the whole hot path on one batch: route -> quantize -> align ->
+permute -> GEMM1 (gate_up) -> SiLU-mul + re-quantize -> GEMM2 (down) ->
+combine, each a call into libwq.so's C ABI on one stream.  Weights (11.3 GB
+of int8) and the step's activations are resident in HBM before the timed
+region; CUDA events between the stages give per-kernel times inside the
+timed region.  The e2e figure runs the same layer through
+wq_moe_forward_host with pinned host activations, copies included.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config prefill]
+  python bench.py --impl reference   # the CPU oracle on a bounded sample
+
+Under torchrun each rank runs an independent replica on its own GPU (the
+layer's experts are not sharded here; value = all ranks' work / max time).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from w8a8_int8_quantized_token_gb300 import synth  # noqa: E402
+
+METRIC = "INT8 MoE layer TOPS and tokens/s at DeepSeek-V3 shape; % INT8 tensor peak"
+SCHEME = {"channel": 0, "block": 1}
+ACC = {"i32": 0, "f32": 1}
+
+
+def layer_ops(T, H, I, k):
+    """Algorithmic integer ops of one layer step: 2 per multiply-add of the
+    two GEMMs over the T*k routed (token, expert) pairs."""
+    return 2.0 * T * k * (2 * I * H + H * I)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+class Layer:
+    """Preallocated buffers and the staged C-ABI calls of one layer step."""
+
+    STAGES = ["route", "quant", "align", "permute", "gemm1", "silu_mul_quant", "gemm2", "combine"]
+    # kernels per stage (align: histogram, scan, scatter; GEMMs: tile list + GEMM)
+    KERNELS = {"route": 1, "quant": 1, "align": 3, "permute": 1, "gemm1": 2, "silu_mul_quant": 1,
+               "gemm2": 2, "combine": 1}
+
+    def __init__(self, wq, cfg, dev, weights):
+        self.wq, self.lib, self.cfg, self.dev = wq, wq.lib(), cfg, dev
+        T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+        R = T * k
+        blk = cfg.scheme == "block"
+        self.g1 = H // 128 if blk else 1
+        self.g2 = I // 128 if blk else 1
+        e = lambda *s, dt: torch.empty(*s, dtype=dt, device=dev)
+        self.ids, self.w = e(R, dt=torch.int32), e(R, dt=torch.float32)
+        self.q, self.s = e(T, H, dt=torch.int8), e(T * self.g1, dt=torch.float32)
+        self.counts, self.offsets = e(E, dt=torch.int32), e(E + 1, dt=torch.int32)
+        self.sp, self.p2r = e(R, dt=torch.int32), e(R, dt=torch.int32)
+        self.aws_n = self.lib.wq_moe_align_workspace_size(T, k, E)
+        self.aws = e(max(self.aws_n, 1), dt=torch.uint8)
+        self.A, self.sa = e(R, H, dt=torch.int8), e(R * self.g1, dt=torch.float32)
+        self.gu = e(R, 2 * I, dt=torch.bfloat16)
+        self.hq, self.sh = e(R, I, dt=torch.int8), e(R * self.g2, dt=torch.float32)
+        self.y = e(R, H, dt=torch.bfloat16)
+        self.out = e(T, H, dt=torch.bfloat16)
+        self.gws_n = self.lib.wq_grouped_gemm_workspace_size(R, E)
+        self.gws = e(self.gws_n, dt=torch.uint8)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.W13, self.S13, self.W2, self.S2 = weights
+
+    def step(self, x, logits, ev=None):
+        c, L, P = self.cfg, self.lib, lambda t: ctypes.c_void_p(t.data_ptr())
+        T, H, I, E, k = c.T, c.H, c.I, c.E, c.k
+        R = T * k
+        st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        sc, ac = SCHEME[c.scheme], ACC[c.acc]
+        rec = (lambda i: ev[i].record()) if ev is not None else (lambda i: None)
+
+        def ok(rc, what):
+            if rc != 0:
+                raise RuntimeError(f"{what} failed: {rc}")
+        rec(0)
+        ok(L.wq_route_topk(P(logits), T, E, k, P(self.ids), P(self.w), st), "route")
+        rec(1)
+        if c.scheme == "channel":
+            ok(L.wq_quantize_per_token(P(x), T, H, H, P(self.q), P(self.s), st), "quant")
+        else:
+            ok(L.wq_quantize_per_token_group(P(x), T, H, H, 128, P(self.q), P(self.s), st), "quant")
+        rec(2)
+        ok(L.wq_moe_align(P(self.ids), T, k, E, 1, P(self.counts), P(self.offsets), P(self.sp),
+                          P(self.p2r), P(self.aws), self.aws_n, P(self.status), st), "align")
+        rec(3)
+        ok(L.wq_moe_permute(P(self.q), P(self.s), self.g1, T, k, H, P(self.sp), R, P(self.A),
+                            P(self.sa), st), "permute")
+        rec(4)
+        ok(L.wq_grouped_gemm_w8a8(P(self.A), P(self.sa), P(self.W13), P(self.S13), P(self.offsets),
+                                  E, R, 2 * I, H, sc, ac, 0, P(self.gu), P(self.gws), self.gws_n,
+                                  P(self.status), st), "gemm1")
+        rec(5)
+        ok(L.wq_silu_mul_quant(P(self.gu), R, I, 128 if c.scheme == "block" else 0, P(self.hq),
+                               P(self.sh), st), "silu_mul_quant")
+        rec(6)
+        ok(L.wq_grouped_gemm_w8a8(P(self.hq), P(self.sh), P(self.W2), P(self.S2), P(self.offsets),
+                                  E, R, H, I, sc, ac, 0, P(self.y), P(self.gws), self.gws_n,
+                                  P(self.status), st), "gemm2")
+        rec(7)
+        ok(L.wq_moe_combine(P(self.y), P(self.p2r), P(self.w), T, k, H, P(self.out), st), "combine")
+        rec(8)
+        return self.out
+
+
+def make_weights(wq, cfg, dev):
+    """Draw each expert's bf16 weights on the device and quantize them with
+    the library (offline step, untimed)."""
+    E, I, H = cfg.E, cfg.I, cfg.H
+    W13 = torch.empty(E, 2 * I, H, dtype=torch.int8, device=dev)
+    W2 = torch.empty(E, H, I, dtype=torch.int8, device=dev)
+    if cfg.scheme == "block":
+        S13 = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32, device=dev)
+        S2 = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=dev)
+    else:
+        S13 = torch.empty(E, 2 * I, dtype=torch.float32, device=dev)
+        S2 = torch.empty(E, H, dtype=torch.float32, device=dev)
+    for e in range(E):
+        w13, w2 = synth.expert_weights(cfg, e, device=dev)
+        wq.quantize_weight(w13, cfg.scheme, W13[e], S13[e])
+        wq.quantize_weight(w2, cfg.scheme, W2[e], S2[e])
+    torch.cuda.synchronize(dev)
+    return W13, S13, W2, S2
+
+
+class ExpertStack:
+    """Lazy [E, ...] stack for the oracle: only the experts a sample touches
+    are materialised."""
+
+    def __init__(self, arrays: dict, shape):
+        self.arrays, self.shape = arrays, shape
+
+    def __getitem__(self, e):
+        return self.arrays[e]
+
+
+def oracle_sample(cfg, n_tokens, dev):
+    """Prepare the CPU oracle's layer on the first n_tokens tokens of the
+    workload and return a function that runs it once and returns seconds.
+    Weights of the touched experts are drawn (on the device, same generator
+    as the GPU run) and quantized by the oracle itself, outside the clock."""
+    from oracle import wq_oracle as O
+    x, lg = synth.layer_inputs(cfg, device=dev)
+    x, lg = x[:n_tokens].cpu(), lg[:n_tokens].cpu()
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    ids, _ = O.route_topk(lg.numpy(), cfg.k)
+    touched = sorted(set(ids.reshape(-1).tolist()))
+    W13, S13, W2, S2 = {}, {}, {}, {}
+    bitsof = lambda t: t.cpu().view(torch.int16).numpy().view(np.uint16)
+    for e in touched:
+        w13, w2 = synth.expert_weights(cfg, e, device=dev)
+        W13[e], S13[e], W2[e], S2[e] = O.quantize_weights(bitsof(w13), bitsof(w2), cfg.scheme)
+    E, I, H = cfg.E, cfg.I, cfg.H
+    args = (ExpertStack(W13, (E, 2 * I, H)), ExpertStack(S13, None),
+            ExpertStack(W2, (E, H, I)), ExpertStack(S2, None))
+    lgn = lg.numpy()
+
+    def run():
+        t0 = time.perf_counter()
+        O.moe_forward(xb, lgn, *args, cfg.k, cfg.scheme, cfg.acc)
+        return time.perf_counter() - t0
+    return run, layer_ops(n_tokens, H, I, cfg.k), len(os.sched_getaffinity(0))
+
+
+def workload_name(cfg):
+    acc = {"i32": "int32 accumulator", "f32": "fp32 accumulator"}[cfg.acc]
+    return (f"DeepSeek-V3-shape {cfg.name} MoE layer, {cfg.scheme}-wise W8A8 INT8, {acc}: "
+            f"{cfg.T} tokens, hidden {cfg.H}, intermediate {cfg.I}, {cfg.E} experts top-{cfg.k}")
+
+
+def run_reference(args, cfg):
+    """The reference arm: the CPU oracle as it stands, on the host cores,
+    each step a bounded sample (the first --cpu-tokens tokens) of the same
+    workload; rank 0 only."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    n = args.cpu_tokens
+    run, ops, cores = oracle_sample(cfg, n, dev)
+    for _ in range(args.warmup):
+        run()
+    per = [run() for _ in range(args.steps)]
+    dt = float(np.mean(per))
+    val = ops / dt / 1e12
+    sample = f"first {n} of {cfg.T} tokens of the same workload (all top-{cfg.k} experts), full layer"
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TOPS",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {"workload": workload_name(cfg), "parallelism": "replicas"},
+            "tokens_per_s": n / dt,
+            "cpu_baseline": {"value": val, "unit": "TOPS", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="prefill", choices=[k for k in synth.CONFIGS if k != "masked"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    cfg = synth.CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from w8a8_int8_quantized_token_gb300 import binding as wq
+    from w8a8_int8_quantized_token_gb300 import build_lib
+    build_lib.build()
+    wq.init(local)
+
+    weights = make_weights(wq, cfg, dev)
+    x, logits = synth.layer_inputs(cfg, device=dev)
+    layer = Layer(wq, cfg, dev, weights)
+
+    # the staged calls reproduce the one-call layer exactly
+    ref = wq.moe_forward(x, logits, *weights, cfg.k, cfg.scheme, cfg.acc)
+    got = layer.step(x, logits)
+    torch.cuda.synchronize()
+    if not torch.equal(ref.view(torch.int16), got.view(torch.int16)):
+        raise RuntimeError("staged step differs from wq_moe_forward")
+
+    for _ in range(args.warmup):
+        layer.step(x, logits)
+    nst = len(Layer.STAGES)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    with ClockSampler(local) as clk:
+        barrier()
+        start.record()
+        for i in range(args.steps):
+            layer.step(x, logits, evs[i])
+        end.record()
+        barrier()
+    total_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]))
+                for j, s in enumerate(Layer.STAGES)}
+    if int(layer.status.item()) != 0:
+        raise RuntimeError(f"device status {int(layer.status.item())}")
+
+    ms = total_ms / args.steps
+    ops = layer_ops(cfg.T, cfg.H, cfg.I, cfg.k)
+    tops = world * ops / (ms / 1e3) / 1e12
+    tok_s = world * cfg.T / (ms / 1e3)
+
+    # end to end: host activations in, host output back, through the one-call API
+    xh, lh = x.cpu().pin_memory(), logits.cpu().pin_memory()
+    outh = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, pin_memory=True)
+    hws = wq.forward_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.scheme, dev, host=True)
+    for _ in range(args.warmup):
+        wq.moe_forward_host(xh, lh, *weights, cfg.k, cfg.scheme, cfg.acc, out_host=outh, ws=hws)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        wq.moe_forward_host(xh, lh, *weights, cfg.k, cfg.scheme, cfg.acc, out_host=outh, ws=hws)
+    e1.record()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if not torch.equal(outh.view(torch.int16), ref.cpu().view(torch.int16)):
+        raise RuntimeError("host-buffer layer differs from the device one")
+
+    peaks, src = load_peaks()
+    g1_ms = stage_ms["gemm1"]
+    g1_flops = 2.0 * cfg.T * cfg.k * (2 * cfg.I) * cfg.H
+    achieved = g1_flops / (g1_ms / 1e3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    roofline = {"bound": "tensor", "kernel": "grouped_gemm_w8a8 gate_up (GEMM1)",
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None,
+                "peak_source": f"{src} bf16 sustained (fp16 tcgen05 kind::f16 runs at the bf16 rate; "
+                               f"sm_103a has no kind::i8)"}
+    line = {"metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {"workload": workload_name(cfg), "tokens": cfg.T, "hidden": cfg.H,
+                       "intermediate": cfg.I, "experts": cfg.E, "top_k": cfg.k,
+                       "scheme": cfg.scheme, "accumulator": cfg.acc,
+                       "l2": "inputs larger than L2: 11.3 GB of int8 weights and ~2 GB of "
+                             "activations are streamed every step",
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "tokens_per_s": tok_s, "stages_ms": stage_ms,
+            "gpu_launches": args.steps * sum(Layer.KERNELS.values()),
+            "roofline": roofline,
+            "e2e": {"value": world * ops / (e2e_ms / 1e3) / 1e12, "unit": "TOPS",
+                    "h2d_bytes_per_step": cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4,
+                    "d2h_bytes_per_step": cfg.T * cfg.H * 2, "ms_per_step": e2e_ms},
+            "clocks": clk.summary()}
+    if rank == 0 and not args.no_cpu_baseline:
+        run, sops, cores = oracle_sample(cfg, args.cpu_tokens, dev)
+        dt = run()
+        line["cpu_baseline"] = {"value": sops / dt / 1e12, "unit": "TOPS", "cores": cores,
+                                "kind": "oracle", "tokens_per_s": args.cpu_tokens / dt,
+                                "sample": f"first {args.cpu_tokens} of {cfg.T} tokens of the same "
+                                          f"workload, full layer, one run ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,274 @@
+"""Parity of every step of the CUDA path with the CPU oracle, through the C
+ABI.  Integer results (codes, ids, offsets, permutations, int32
+accumulators) are compared bit-exactly; bf16 and float results are compared
+exactly too (the kernels follow the oracle's float32 operation order), and
+the layer outputs also report the stated tolerance (max abs 2e-2, relative
+Frobenius 1e-2)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import wq_oracle as O
+from w8a8_int8_quantized_token_gb300 import binding as wq
+from w8a8_int8_quantized_token_gb300 import synth
+from wq_testutil import assert_bf16_equal, bits, np_, quantized_weights, stack_oracle, tolerance_report
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _init():
+    from w8a8_int8_quantized_token_gb300 import build_lib
+    build_lib.build()
+    wq.init(0)
+
+
+# ---------------------------------------------------------------- quantization
+@pytest.mark.parametrize("T,K,outl", [(1, 8, False), (37, 384, True), (130, 7168, True),
+                                      (5, 2048, False), (3, 65536, True)])
+def test_quantize_per_token(T, K, outl):
+    x = synth.activations(T, K, outl, seed=T + K)
+    q, s = wq.quantize_per_token(x.to(DEV))
+    qo, so = O.quantize_per_token(bits(x))
+    assert np.array_equal(np_(q), qo)
+    assert np.array_equal(np_(s), so)
+
+
+def test_quantize_zero_and_constant_rows():
+    x = torch.zeros(3, 256, dtype=torch.bfloat16)
+    x[1] = -0.375
+    x[2, 7] = 3.0
+    q, s = wq.quantize_per_token(x.to(DEV))
+    qo, so = O.quantize_per_token(bits(x))
+    assert np.array_equal(np_(q), qo) and np.array_equal(np_(s), so)
+    assert np.all(np_(q)[1] == -127) and np.all(np_(q)[0] == 0)
+
+
+@pytest.mark.parametrize("group", [32, 64, 128, 256])
+def test_quantize_per_token_group(group):
+    x = synth.activations(19, 1024, True, seed=group)
+    q, s = wq.quantize_per_token_group(x.to(DEV), group)
+    qo, so = O.quantize_per_token_group(bits(x), group)
+    assert np.array_equal(np_(q), qo) and np.array_equal(np_(s), so)
+
+
+def test_quantize_weight_block():
+    g = torch.Generator().manual_seed(4)
+    w = (torch.randn(384, 640, generator=g) * 0.02).to(torch.bfloat16)
+    q, s = wq.quantize_weight_block(w.to(DEV))
+    qo, so = O.quantize_weight_block(bits(w))
+    assert np.array_equal(np_(q), qo) and np.array_equal(np_(s), so)
+
+
+# ---------------------------------------------------------------- routing / align / permute
+@pytest.mark.parametrize("T,E,k", [(16, 8, 2), (200, 256, 8), (33, 1024, 32), (9, 5, 5), (7, 300, 1)])
+def test_route_topk(T, E, k):
+    lg = synth.router_logits(T, E, seed=E + k)
+    lg[:, 3] = lg[:, 1]  # exact ties
+    ids, w = wq.route_topk(lg.to(DEV), k)
+    io, wo = O.route_topk(lg.numpy(), k)
+    assert np.array_equal(np_(ids), io)
+    assert np.array_equal(np_(w), wo)
+
+
+@pytest.mark.parametrize("T,k,E,pad", [(3, 2, 4, 1), (3, 2, 4, 4), (1000, 8, 256, 1),
+                                       (8192, 8, 256, 1), (77, 3, 4096, 1), (500, 6, 33, 128), (0, 2, 8, 1)])
+def test_moe_align(T, k, E, pad):
+    rng = np.random.default_rng(T + E)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32).reshape(T, k)
+    if T:
+        ids[: T // 2, 0] = 1  # a hot expert
+    c, o, sp, p2r = wq.moe_align(torch.from_numpy(ids).to(DEV), E, pad)
+    co, oo, spo, p2ro = O.moe_align(ids, E, pad)
+    assert np.array_equal(np_(c), co) and np.array_equal(np_(o), oo)
+    n = int(oo[-1])
+    assert np.array_equal(np_(sp)[:n], spo) and np.all(np_(sp)[n:] == -1)
+    assert np.array_equal(np_(p2r), p2ro)
+
+
+def test_moe_align_reports_bad_ids():
+    ids = torch.tensor([[0, 1], [2, 9]], dtype=torch.int32, device=DEV)
+    st = wq.new_status()
+    c, o, sp, p2r = wq.moe_align(ids, 4, 1, status=st)
+    assert int(st.item()) == -6
+    assert np_(p2r).tolist()[3] == -1 and np_(c).tolist() == [1, 1, 1, 0]
+
+
+@pytest.mark.parametrize("groups", [1, 56])
+def test_moe_permute(groups):
+    T, k, E, K = 300, 8, 64, 7168
+    rng = np.random.default_rng(groups)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    q = rng.integers(-127, 128, (T, K), dtype=np.int8)
+    s = rng.random((T, groups) if groups > 1 else T).astype(np.float32)
+    _, _, spo, _ = O.moe_align(ids, E, 4)
+    A, sa = wq.moe_permute(torch.from_numpy(q).to(DEV), torch.from_numpy(s).to(DEV),
+                           torch.from_numpy(spo).to(DEV), k)
+    Ao, sao = O.moe_permute(q, s, spo, k)
+    assert np.array_equal(np_(A), Ao) and np.array_equal(np_(sa), sao)
+
+
+# ---------------------------------------------------------------- activation / combine
+@pytest.mark.parametrize("R,I,group", [(70, 2048, 0), (5, 128, 0), (33, 2048, 128), (9, 256, 32),
+                                       (3, 16384, 0)])
+def test_silu_mul_quant(R, I, group):
+    g = torch.Generator().manual_seed(R + I)
+    gu = (torch.randn(R, 2 * I, generator=g) * 4).to(torch.bfloat16)
+    gu[0, :4] = torch.tensor([0.0, -120.0, 95.0, -0.0])  # saturated exp paths
+    hq, sh = wq.silu_mul_quant(gu.to(DEV), group)
+    hqo, sho = O.silu_mul_quant(bits(gu), I, group)
+    assert np.array_equal(np_(hq), hqo) and np.array_equal(np_(sh), sho)
+
+
+def test_moe_combine():
+    T, k, H = 129, 8, 7168
+    rng = np.random.default_rng(3)
+    y = (torch.randn(T * k + 5, H, generator=torch.Generator().manual_seed(1)) * 3).to(torch.bfloat16)
+    p2r = rng.permutation(T * k).astype(np.int32)
+    p2r[5] = -1
+    w = rng.random((T, k)).astype(np.float32)
+    out = wq.moe_combine(y.to(DEV), torch.from_numpy(p2r).to(DEV), torch.from_numpy(w).to(DEV), k)
+    yb = bits(y)
+    # the oracle's combine takes the rows by index; a -1 row contributes nothing
+    yz = np.concatenate([yb, np.zeros((1, H), np.uint16)])
+    p2r_o = np.where(p2r < 0, yb.shape[0], p2r)
+    assert_bf16_equal(bits(out), O.moe_combine(yz, p2r_o, w, k), "combine")
+
+
+# ---------------------------------------------------------------- grouped GEMM
+def _gemm_case(seed, E, counts, N, K, scheme):
+    rng = np.random.default_rng(seed)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    R = int(offsets[-1])
+    A = rng.integers(-127, 128, (R, K), dtype=np.int8)
+    W = rng.integers(-127, 128, (E, N, K), dtype=np.int8)
+    if scheme == "channel":
+        sa = (rng.random(R) * 0.05).astype(np.float32)
+        sw = (rng.random((E, N)) * 1e-3).astype(np.float32)
+    else:
+        sa = (rng.random((R, K // 128)) * 0.05).astype(np.float32)
+        sw = (rng.random((E, N // 128, K // 128)) * 1e-3).astype(np.float32)
+    return A, sa, W, sw, offsets
+
+
+@pytest.mark.parametrize("scheme,acc", [("channel", "i32"), ("channel", "f32"), ("block", "f32")])
+@pytest.mark.parametrize("counts,N,K", [([3, 0, 130, 1, 257], 256, 384),
+                                         ([0, 0, 5], 128, 128),
+                                         ([700, 64, 129], 512, 1024)])
+def test_grouped_gemm(scheme, acc, counts, N, K):
+    E = len(counts)
+    A, sa, W, sw, offs = _gemm_case(len(counts) + N + K, E, counts, N, K, scheme)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    out = wq.grouped_gemm_w8a8(t(A), t(sa), t(W), t(sw), t(offs), scheme, acc)
+    ref = O.grouped_gemm_w8a8(A, sa, W, sw, offs, scheme, acc)
+    assert_bf16_equal(bits(out), ref, f"gemm {scheme}/{acc}")
+
+
+def test_grouped_gemm_int32_accumulators_and_extremes():
+    E, counts, N, K = 3, [200, 1, 77], 256, 7168
+    A, sa, W, sw, offs = _gemm_case(9, E, counts, N, K, "channel")
+    A[0, :] = 127
+    W[0, 0, :] = 127
+    W[0, 1, :] = -127
+    A[1, :] = -127
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    C = wq.grouped_gemm_w8a8(t(A), t(sa), t(W), t(sw), t(offs), "channel", "i32", out_type="i32")
+    Co = O.grouped_gemm_i32(A, W, offs)
+    assert np.array_equal(np_(C), Co)
+    assert Co[0, 0] == 127 * 127 * 7168 and Co[0, 1] == -127 * 127 * 7168
+
+
+def test_grouped_gemm_leaves_rows_outside_segments():
+    E, N, K = 2, 128, 256
+    rng = np.random.default_rng(5)
+    offs = np.array([0, 10, 20], np.int32)
+    R = 32  # rows 20..31 belong to no expert
+    A = rng.integers(-127, 128, (R, K), dtype=np.int8)
+    W = rng.integers(-127, 128, (E, N, K), dtype=np.int8)
+    sa = np.ones(R, np.float32)
+    sw = np.full((E, N), 1e-3, np.float32)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    out = torch.full((R, N), 7.0, dtype=torch.bfloat16, device=DEV)
+    wq.grouped_gemm_w8a8(t(A), t(sa), t(W), t(sw), t(offs), out=out)
+    assert torch.all(out[20:] == 7.0)
+    assert_bf16_equal(bits(out[:20]), O.grouped_gemm_w8a8(A[:20], sa[:20], W, sw, offs))
+
+
+@pytest.mark.parametrize("scheme,acc", [("channel", "i32"), ("block", "f32")])
+def test_grouped_gemm_masked(scheme, acc):
+    E, Mmax, N, K = 5, 200, 256, 512
+    mm = np.array([0, 1, 200, 129, 64], np.int32)
+    rng = np.random.default_rng(6)
+    A = rng.integers(-127, 128, (E, Mmax, K), dtype=np.int8)
+    W = rng.integers(-127, 128, (E, N, K), dtype=np.int8)
+    if scheme == "channel":
+        sa = (rng.random((E, Mmax)) * 0.05).astype(np.float32)
+        sw = (rng.random((E, N)) * 1e-3).astype(np.float32)
+    else:
+        sa = (rng.random((E, Mmax, K // 128)) * 0.05).astype(np.float32)
+        sw = (rng.random((E, N // 128, K // 128)) * 1e-3).astype(np.float32)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    out = torch.full((E, Mmax, N), -3.0, dtype=torch.bfloat16, device=DEV)
+    wq.grouped_gemm_w8a8_masked(t(A), t(sa), t(mm), t(W), t(sw), scheme, acc, out=out)
+    ob = bits(out)
+    for e in range(E):
+        m = mm[e]
+        ref = O.grouped_gemm_w8a8(A[e, :m], sa[e, :m], W[e:e + 1], sw[e:e + 1], np.array([0, m]),
+                                  scheme, acc)
+        assert_bf16_equal(ob[e, :m], ref, f"masked expert {e}")
+        assert np.all(O.bf16_to_f32(ob[e, m:]) == -3.0)
+
+
+# ---------------------------------------------------------------- the layer
+def _layer_case(cfg):
+    x, lg = synth.layer_inputs(cfg)
+    (W13, S13, W2, S2), orc = quantized_weights(cfg, DEV)
+    ow = stack_oracle(orc, cfg.E)
+    for gpu, ref in zip((W13, S13, W2, S2), ow):
+        assert np.array_equal(np_(gpu), ref), "weight quantization differs"
+    return x, lg, (W13, S13, W2, S2), ow
+
+
+@pytest.mark.parametrize("cfg", [
+    synth.CONFIGS["tiny"],
+    synth.small_config("small_i32", T=150, H=384, I=256, E=6, k=3),
+    synth.small_config("small_f32", T=97, H=512, I=256, E=7, k=2, acc="f32"),
+    synth.small_config("small_block", T=130, H=384, I=256, E=5, k=3, scheme="block", acc="f32"),
+    synth.small_config("hot", T=300, H=256, I=128, E=4, k=1),
+], ids=lambda c: c.name)
+def test_layer_forward(cfg):
+    x, lg, w, ow = _layer_case(cfg)
+    out = wq.moe_forward(x.to(DEV), lg.to(DEV), *w, cfg.k, cfg.scheme, cfg.acc)
+    ref = O.moe_forward(bits(x), lg.numpy(), *ow, cfg.k, cfg.scheme, cfg.acc)
+    max_abs, rel = tolerance_report(bits(out), ref)
+    assert max_abs <= 2e-2 and rel <= 1e-2
+    assert_bf16_equal(bits(out), ref, f"layer {cfg.name}")
+
+
+def test_layer_forward_host_equals_device():
+    cfg = synth.small_config("host", T=64, H=256, I=128, E=8, k=2)
+    x, lg, w, _ = _layer_case(cfg)
+    dev_out = wq.moe_forward(x.to(DEV), lg.to(DEV), *w, cfg.k)
+    xh, lh = x.pin_memory(), lg.pin_memory()
+    host_out = wq.moe_forward_host(xh, lh, *w, cfg.k)
+    torch.cuda.synchronize()
+    assert torch.equal(host_out.view(torch.int16), dev_out.cpu().view(torch.int16))
+
+
+def test_layer_forward_masked():
+    cfg = synth.small_config("masked_small", T=0, H=256, I=128, E=4, k=1)
+    Mmax = 150
+    x = synth.activations(cfg.E * Mmax, cfg.H, True, 3)
+    a, sa = wq.quantize_per_token(x.to(DEV))
+    qo, so = O.quantize_per_token(bits(x))
+    mm = np.array([150, 0, 1, 77], np.int32)
+    (W13, S13, W2, S2), orc = quantized_weights(cfg, DEV)
+    y = torch.full((cfg.E, Mmax, cfg.H), 5.0, dtype=torch.bfloat16, device=DEV)
+    wq.moe_forward_masked(a.view(cfg.E, Mmax, cfg.H), sa.view(cfg.E, Mmax),
+                          torch.from_numpy(mm).to(DEV), W13, S13, W2, S2, y=y)
+    ref, valid = O.moe_forward_masked(qo.reshape(cfg.E, Mmax, cfg.H), so.reshape(cfg.E, Mmax), mm,
+                                      *stack_oracle(orc, cfg.E))
+    yb = bits(y)
+    assert_bf16_equal(yb[valid], ref[valid], "masked layer")
+    assert np.all(O.bf16_to_f32(yb[~valid]) == 5.0)

@@ -1,0 +1,93 @@
+"""Host-side checks of libwq.so that need no GPU: it loads, exports every
+entry point include/wq.h declares, sizes workspaces, and rejects bad
+arguments on the host before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from w8a8_int8_quantized_token_gb300 import binding, build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return binding.lib()
+
+
+def header_names():
+    txt = open(os.path.join(ROOT, "include", "wq.h")).read()
+    return sorted(set(re.findall(r"WQ_API\s+[\w\s\*]*?\b(wq_\w+)\s*\(", txt)))
+
+
+def test_header_declares_entry_points():
+    names = header_names()
+    assert len(names) >= 21
+    assert set(names) == set(binding.exported_names())
+
+
+def test_library_exports_every_declared_symbol(lib):
+    h = ctypes.CDLL(binding.LIB_PATH)
+    for n in header_names():
+        assert hasattr(h, n), n
+
+
+def test_status_strings(lib):
+    for code in range(0, -8, -1):
+        assert lib.wq_status_string(code) and lib.wq_status_string(code) != b"unknown status"
+    assert lib.wq_status_string(99) == b"unknown status"
+
+
+def test_workspace_sizes(lib):
+    # forward workspace holds at least A, GU, y of the prefill shape
+    T, H, I, E, k = 8192, 7168, 2048, 256, 8
+    n = lib.wq_moe_forward_workspace_size(T, H, I, E, k, 0)
+    R = T * k
+    assert n >= R * H + R * 2 * I * 2 + R * I + R * H * 2
+    assert lib.wq_moe_forward_host_workspace_size(T, H, I, E, k, 0) >= n + T * H * 4
+    assert lib.wq_moe_forward_workspace_size(T, 100, I, E, k, 0) == 0  # H % 128
+    assert lib.wq_moe_align_workspace_size(T, k, E) >= (R // 256) * E * 4
+    assert lib.wq_grouped_gemm_workspace_size(R, E) > 0
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)  # never dereferenced: argument checks fail first
+    # k > E
+    assert lib.wq_route_topk(fake, 4, 8, 9, fake, fake, None) == -1
+    # E > 1024
+    assert lib.wq_route_topk(fake, 4, 2000, 8, fake, fake, None) == -1
+    # negative sizes
+    assert lib.wq_quantize_per_token(fake, -1, 16, 16, fake, fake, None) == -1
+    # ldx < K
+    assert lib.wq_quantize_per_token(fake, 4, 16, 8, fake, fake, None) == -1
+    # K not a multiple of 8
+    assert lib.wq_quantize_per_token(fake, 4, 12, 12, fake, fake, None) == -2
+    # unsupported group
+    assert lib.wq_quantize_per_token_group(fake, 4, 256, 256, 100, fake, fake, None) == -2
+    # bad scheme / acc / raw int32 with the block scheme
+    assert lib.wq_grouped_gemm_w8a8(fake, fake, fake, fake, fake, 4, 16, 128, 128, 7, 0, 0, fake,
+                                    fake, 1 << 20, None, None) == -1
+    assert lib.wq_grouped_gemm_w8a8(fake, fake, fake, fake, fake, 4, 16, 128, 128, 1, 0, 1, fake,
+                                    fake, 1 << 20, None, None) == -1
+    # N not a multiple of 128
+    assert lib.wq_grouped_gemm_w8a8(fake, fake, fake, fake, fake, 4, 16, 96, 128, 0, 0, 0, fake,
+                                    fake, 1 << 20, None, None) == -2
+    # workspace too small
+    assert lib.wq_grouped_gemm_w8a8(fake, fake, fake, fake, fake, 4, 16, 128, 128, 0, 0, 0, fake,
+                                    fake, 1, None, None) == -5
+    assert lib.wq_moe_align(fake, 4, 2, 8, 1, fake, fake, fake, fake, fake, 0, None, None) == -5
+    # null pointers
+    assert lib.wq_moe_combine(None, fake, fake, 4, 2, 64, fake, None) == -1
+    # empty problems enqueue nothing and succeed without a device
+    assert lib.wq_quantize_per_token(None, 0, 16, 16, None, None, None) == 0
+    assert lib.wq_grouped_gemm_w8a8(None, None, None, None, None, 4, 0, 128, 128, 0, 0, 0, None,
+                                    None, 0, None, None) == 0
+
+
+def test_no_device_is_reported(lib):
+    # this check runs where no GPU is visible; on a GPU machine device 10**6 does not exist
+    assert lib.wq_init(10 ** 6) == -3

@@ -1,0 +1,193 @@
+// Expert alignment: counts, offsets (cumulative with a leading zero, as the
+// cutlass_moe_fp8 review for DeepEP asks), and the stable permutation of the
+// (token, slot) pairs by expert.  Deterministic: a counting sort whose ranks
+// come from ordered scans and warp match masks, never from atomic order.
+//
+// Also the grouped GEMM's tile list: per expert segment, ceil(rows/BM) tiles.
+#include "wq_common.cuh"
+
+namespace wq {
+
+constexpr int kAlignChunk = 256;  // pairs per chunk
+
+static inline int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+size_t align_ws_bytes(int T, int k, int E) {
+  const int64_t P = int64_t(T) * k;
+  const int64_t chunks = (P + kAlignChunk - 1) / kAlignChunk;
+  return size_t(align_up(chunks * E * 4, 256));
+}
+
+// 1) per-chunk expert histogram (shared-memory counts; order-free)
+__global__ void __launch_bounds__(kAlignChunk) align_hist_kernel(const int32_t *__restrict__ ids,
+                                                                 int64_t P, int E,
+                                                                 int32_t *__restrict__ hist,
+                                                                 int32_t *status) {
+  extern __shared__ int32_t cnt[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int64_t p = int64_t(blockIdx.x) * kAlignChunk + threadIdx.x;
+  if (p < P) {
+    const int e = ids[p];
+    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    else set_status(status, WQ_ERR_INDEX);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[int64_t(blockIdx.x) * E + e] = cnt[e];
+}
+
+// 2) one CTA: column prefix over chunks, padded counts, exclusive scan over
+//    experts -> offsets; hist[c][e] becomes the first row of chunk c's pairs
+//    of expert e.
+__global__ void __launch_bounds__(1024) align_scan_kernel(int32_t *__restrict__ hist, int chunks,
+                                                          int E, int pad_m,
+                                                          int32_t *__restrict__ counts,
+                                                          int32_t *__restrict__ offsets) {
+  __shared__ int32_t part[1024];
+  const int per = (E + blockDim.x - 1) / blockDim.x;
+  const int e0 = threadIdx.x * per;
+  int local = 0;
+  for (int e = e0; e < e0 + per && e < E; ++e) {
+    int run = 0;
+    for (int c = 0; c < chunks; ++c) {
+      const int v = hist[int64_t(c) * E + e];
+      hist[int64_t(c) * E + e] = run;
+      run += v;
+    }
+    counts[e] = run;
+    local += (run + pad_m - 1) / pad_m * pad_m;
+  }
+  part[threadIdx.x] = local;
+  __syncthreads();
+  // inclusive Hillis-Steele scan over the block
+  for (int o = 1; o < int(blockDim.x); o <<= 1) {
+    const int v = threadIdx.x >= unsigned(o) ? part[threadIdx.x - o] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int base = part[threadIdx.x] - local;
+  for (int e = e0; e < e0 + per && e < E; ++e) {
+    offsets[e] = base;
+    for (int c = 0; c < chunks; ++c) hist[int64_t(c) * E + e] += base;
+    const int cnt = counts[e];
+    base += (cnt + pad_m - 1) / pad_m * pad_m;
+  }
+  if (threadIdx.x == blockDim.x - 1) offsets[E] = part[threadIdx.x];
+}
+
+// 3) one warp per chunk walks its pairs in order, 32 at a time; a pair's row
+//    is its chunk base + the pairs of the same expert already placed + its
+//    rank among equal lanes below it (match mask).
+__global__ void __launch_bounds__(32) align_scatter_kernel(const int32_t *__restrict__ ids,
+                                                           int64_t P, int E,
+                                                           const int32_t *__restrict__ hist,
+                                                           int32_t *__restrict__ sorted_pair,
+                                                           int32_t *__restrict__ pair_to_row) {
+  extern __shared__ int32_t cur[];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) cur[e] = hist[int64_t(blockIdx.x) * E + e];
+  __syncwarp();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int step = 0; step < kAlignChunk / 32; ++step) {
+    const int64_t p = int64_t(blockIdx.x) * kAlignChunk + step * 32 + lane;
+    int e = -1;
+    if (p < P) {
+      e = ids[p];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    if (e >= 0) {
+      const int row = cur[e] + __popc(same & lt);
+      sorted_pair[row] = int32_t(p);
+      pair_to_row[p] = row;
+    } else if (p < P) {
+      pair_to_row[p] = -1;
+    }
+    __syncwarp();
+    if (e >= 0 && (same & lt) == 0) cur[e] += __popc(same);  // group leader advances
+    __syncwarp();
+  }
+}
+
+int launch_align(const int32_t *ids, int T, int k, int E, int pad_m, int32_t *counts,
+                 int32_t *offsets, int32_t *sorted_pair, int32_t *pair_to_row, void *ws,
+                 int32_t *status, cudaStream_t st) {
+  const int64_t P = int64_t(T) * k;
+  const int64_t cap = P + int64_t(E) * (pad_m - 1);
+  const int chunks = int((P + kAlignChunk - 1) / kAlignChunk);
+  int32_t *hist = static_cast<int32_t *>(ws);
+  if (cap > 0 && cudaMemsetAsync(sorted_pair, 0xff, size_t(cap) * 4, st) != cudaSuccess)
+    return WQ_ERR_LAUNCH;
+  const size_t smem = size_t(E) * 4;
+  if (chunks > 0) {
+    align_hist_kernel<<<chunks, kAlignChunk, smem, st>>>(ids, P, E, hist, status);
+  }
+  align_scan_kernel<<<1, 1024, 0, st>>>(hist, chunks, E, pad_m, counts, offsets);
+  if (chunks > 0) {
+    align_scatter_kernel<<<chunks, 32, smem, st>>>(ids, P, E, hist, sorted_pair, pair_to_row);
+  }
+  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// Tile list of the grouped GEMM.  Segment e: rows [offsets[e], offsets[e+1])
+// (contiguous layout) or [e*Mmax, e*Mmax + clamp(masked_m[e], 0, Mmax))
+// (masked layout).  Tiles are expert-major.  ntiles[0] = number written.
+__global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__restrict__ offsets,
+                                                           const int32_t *__restrict__ masked_m,
+                                                           int Mmax, int E, int BM,
+                                                           Tile *__restrict__ tiles,
+                                                           int32_t *__restrict__ ntiles) {
+  __shared__ int32_t part[1024];
+  const int per = (E + blockDim.x - 1) / blockDim.x;
+  const int e0 = threadIdx.x * per;
+  auto seg = [&](int e, int &r0, int &len) {
+    if (masked_m) {
+      int m = masked_m[e];
+      m = m < 0 ? 0 : (m > Mmax ? Mmax : m);
+      r0 = e * Mmax;
+      len = m;
+    } else {
+      r0 = offsets[e];
+      len = offsets[e + 1] - r0;
+      if (len < 0) len = 0;
+    }
+  };
+  int local = 0;
+  for (int e = e0; e < e0 + per && e < E; ++e) {
+    int r0, len;
+    seg(e, r0, len);
+    local += (len + BM - 1) / BM;
+  }
+  part[threadIdx.x] = local;
+  __syncthreads();
+  for (int o = 1; o < int(blockDim.x); o <<= 1) {
+    const int v = threadIdx.x >= unsigned(o) ? part[threadIdx.x - o] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int t = part[threadIdx.x] - local;
+  for (int e = e0; e < e0 + per && e < E; ++e) {
+    int r0, len;
+    seg(e, r0, len);
+    for (int m = 0; m < len; m += BM) {
+      Tile tl;
+      tl.expert = e;
+      tl.row0 = r0 + m;
+      tl.rows = len - m < BM ? len - m : BM;
+      tl.pad = 0;
+      tiles[t++] = tl;
+    }
+  }
+  if (threadIdx.x == blockDim.x - 1) ntiles[0] = part[threadIdx.x];
+}
+
+int launch_build_tiles(const int32_t *offsets, const int32_t *masked_m, int Mmax, int E, int BM,
+                       Tile *tiles, int32_t *ntiles, cudaStream_t st) {
+  build_tiles_kernel<<<1, 1024, 0, st>>>(offsets, masked_m, Mmax, E, BM, tiles, ntiles);
+  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+}
+
+}  // namespace wq

@@ -1,0 +1,467 @@
+// C ABI of libwq.so: host-side argument checks, workspace carving and the
+// composition of the layer's steps on one stream.  Declarations and the
+// contract of every entry point are in include/wq.h.
+#include <cstdio>
+#include <cstring>
+
+#include "wq_common.cuh"
+
+namespace wq {
+int launch_gemm_simt(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
+                     cudaStream_t st);
+int launch_gemm_tc(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
+                   cudaStream_t st);
+bool gemm_tc_supported(const GemmArgs &a);
+}  // namespace wq
+
+using namespace wq;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_dev_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return WQ_ERR_DEVICE;
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return WQ_ERR_DEVICE;
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return g_dev_ok[dev] == 1 ? WQ_OK : WQ_ERR_DEVICE;
+}
+
+inline bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool al8(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+inline size_t rup(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Sequential carving of a caller workspace into 256-byte aligned pieces.
+struct Carver {
+  char *base;
+  size_t used = 0;
+  explicit Carver(void *p) : base(static_cast<char *>(p)) {}
+  template <class T>
+  T *take(size_t count) {
+    T *p = reinterpret_cast<T *>(base ? base + used : nullptr);
+    used += rup(count * sizeof(T));
+    return p;
+  }
+};
+
+#define WQ_TRY(expr)              \
+  do {                            \
+    int _rc = (expr);             \
+    if (_rc != WQ_OK) return _rc; \
+  } while (0)
+
+int group_ok(int g) { return g == 32 || g == 64 || g == 128 || g == 256; }
+
+int64_t gemm_max_tiles(int64_t R, int E, int Mmax, bool masked, int BM) {
+  if (masked) return int64_t(E) * ((Mmax + BM - 1) / BM);
+  return (R + BM - 1) / BM + E;
+}
+
+}  // namespace
+
+namespace wq {
+
+size_t gemm_ws_bytes(int64_t R, int E, int Mmax, bool masked) {
+  // two tile lists (64-row tiles for the CUDA-core engine, 128-row tiles for
+  // the tensor-core engine), each followed by its count
+  const int64_t t64 = gemm_max_tiles(R, E, Mmax, masked, 64);
+  const int64_t t128 = gemm_max_tiles(R, E, Mmax, masked, 128);
+  return rup(size_t(t64) * sizeof(Tile)) + rup(4) + rup(size_t(t128) * sizeof(Tile)) + rup(4);
+}
+
+int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
+  const bool masked = a.masked_m != nullptr;
+  Carver c(a.ws);
+  const int64_t t64 = gemm_max_tiles(a.R, a.E, a.Mmax, masked, 64);
+  const int64_t t128 = gemm_max_tiles(a.R, a.E, a.Mmax, masked, 128);
+  Tile *tiles64 = c.take<Tile>(size_t(t64));
+  int32_t *n64 = c.take<int32_t>(1);
+  Tile *tiles128 = c.take<Tile>(size_t(t128));
+  int32_t *n128 = c.take<int32_t>(1);
+  if (gemm_tc_supported(a)) {
+    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 128, tiles128, n128, st));
+    return launch_gemm_tc(a, tiles128, n128, int(t128), st);
+  }
+  (void)tiles128;
+  (void)n128;
+  WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 64, tiles64, n64, st));
+  return launch_gemm_simt(a, tiles64, n64, int(t64), st);
+}
+
+}  // namespace wq
+
+extern "C" {
+
+int wq_init(int device) {
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || device < 0 || device >= n) return WQ_ERR_DEVICE;
+  if (cudaSetDevice(device) != cudaSuccess) return WQ_ERR_DEVICE;
+  return check_device();
+}
+
+const char *wq_status_string(int code) {
+  switch (code) {
+    case WQ_OK: return "ok";
+    case WQ_ERR_INVALID_ARG: return "invalid argument";
+    case WQ_ERR_UNSUPPORTED: return "unsupported shape or alignment";
+    case WQ_ERR_DEVICE: return "no compute capability 10.3 device";
+    case WQ_ERR_LAUNCH: return "CUDA launch or copy failed";
+    case WQ_ERR_WORKSPACE: return "workspace too small";
+    case WQ_ERR_INDEX: return "index out of range (device)";
+    case WQ_ERR_TIMEOUT: return "pipeline wait timed out (device)";
+    default: return "unknown status";
+  }
+}
+
+int wq_quantize_per_token(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int8_t *q,
+                          float *s, wq_stream_t stream) {
+  if (T < 0 || K < 0 || ldx < K) return WQ_ERR_INVALID_ARG;
+  if (T == 0 || K == 0) return WQ_OK;
+  if (!x || !q || !s) return WQ_ERR_INVALID_ARG;
+  if (K % 8 || ldx % 8 || !al16(x) || !al8(q)) return WQ_ERR_UNSUPPORTED;
+  WQ_TRY(check_device());
+  return launch_quant_rows(x, T, K, ldx, 0, q, s, stream);
+}
+
+int wq_quantize_per_token_group(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group,
+                                int8_t *q, float *s, wq_stream_t stream) {
+  if (T < 0 || K < 0 || ldx < K) return WQ_ERR_INVALID_ARG;
+  if (!group_ok(group)) return WQ_ERR_UNSUPPORTED;
+  if (T == 0 || K == 0) return WQ_OK;
+  if (!x || !q || !s) return WQ_ERR_INVALID_ARG;
+  if (K % group || ldx % 8 || !al16(x) || !al8(q)) return WQ_ERR_UNSUPPORTED;
+  WQ_TRY(check_device());
+  return launch_quant_rows(x, T, K, ldx, group, q, s, stream);
+}
+
+int wq_quantize_weight_block(const uint16_t *w, int64_t N, int64_t K, int8_t *q, float *s,
+                             wq_stream_t stream) {
+  if (N < 0 || K < 0) return WQ_ERR_INVALID_ARG;
+  if (N == 0 || K == 0) return WQ_OK;
+  if (!w || !q || !s) return WQ_ERR_INVALID_ARG;
+  if (N % 128 || K % 128 || !al16(w) || !al8(q)) return WQ_ERR_UNSUPPORTED;
+  WQ_TRY(check_device());
+  return launch_quant_weight_block(w, N, K, q, s, stream);
+}
+
+int wq_route_topk(const float *logits, int T, int E, int k, int32_t *ids, float *w,
+                  wq_stream_t stream) {
+  if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return WQ_ERR_INVALID_ARG;
+  if (T == 0) return WQ_OK;
+  if (!logits || !ids || !w) return WQ_ERR_INVALID_ARG;
+  WQ_TRY(check_device());
+  return launch_route(logits, T, E, k, ids, w, stream);
+}
+
+size_t wq_moe_align_workspace_size(int T, int k, int E) {
+  if (T < 0 || k < 1 || E < 1) return 0;
+  return align_ws_bytes(T, k, E);
+}
+
+int wq_moe_align(const int32_t *ids, int T, int k, int E, int pad_m, int32_t *counts,
+                 int32_t *offsets, int32_t *sorted_pair, int32_t *pair_to_row, void *ws,
+                 size_t ws_bytes, int32_t *status, wq_stream_t stream) {
+  if (T < 0 || k < 1 || E < 1 || E > 4096 || pad_m < 1 || pad_m > 1024) return WQ_ERR_INVALID_ARG;
+  if (int64_t(T) * k + int64_t(E) * (pad_m - 1) >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;
+  if (!counts || !offsets || (T > 0 && (!ids || !sorted_pair || !pair_to_row)))
+    return WQ_ERR_INVALID_ARG;
+  if (ws_bytes < align_ws_bytes(T, k, E) || (T > 0 && !ws)) return WQ_ERR_WORKSPACE;
+  WQ_TRY(check_device());
+  return launch_align(ids, T, k, E, pad_m, counts, offsets, sorted_pair, pair_to_row, ws, status,
+                      stream);
+}
+
+int wq_moe_permute(const int8_t *q, const float *s, int groups, int T, int k, int64_t K,
+                   const int32_t *sorted_pair, int64_t R, int8_t *A, float *sa,
+                   wq_stream_t stream) {
+  if (groups < 1 || T < 0 || k < 1 || K < 0 || R < 0) return WQ_ERR_INVALID_ARG;
+  if (R == 0) return WQ_OK;
+  if (!sorted_pair || !A || !sa || (T > 0 && (!q || !s))) return WQ_ERR_INVALID_ARG;
+  if (K % 16 || !al16(q) || !al16(A)) return WQ_ERR_UNSUPPORTED;
+  WQ_TRY(check_device());
+  return launch_permute(q, s, groups, k, K, sorted_pair, R, A, sa, stream);
+}
+
+static int check_gemm_common(const int8_t *W, const float *sw, int E, int64_t N, int64_t K,
+                             int scheme, int acc, int out_type, const void *out) {
+  if (E < 1 || N < 0 || K < 0) return WQ_ERR_INVALID_ARG;
+  if (scheme != WQ_SCHEME_CHANNEL && scheme != WQ_SCHEME_BLOCK) return WQ_ERR_INVALID_ARG;
+  if (acc != WQ_ACC_I32 && acc != WQ_ACC_F32) return WQ_ERR_INVALID_ARG;
+  if (out_type != WQ_OUT_BF16 && out_type != WQ_OUT_I32) return WQ_ERR_INVALID_ARG;
+  if (out_type == WQ_OUT_I32 && (scheme != WQ_SCHEME_CHANNEL || acc != WQ_ACC_I32))
+    return WQ_ERR_INVALID_ARG;
+  if (!W || !sw || !out) return WQ_ERR_INVALID_ARG;
+  if (N % 128 || K % 128 || N == 0 || K == 0) return WQ_ERR_UNSUPPORTED;
+  if (!al16(W) || !al16(out)) return WQ_ERR_UNSUPPORTED;
+  return WQ_OK;
+}
+
+size_t wq_grouped_gemm_workspace_size(int64_t R, int E) {
+  if (R < 0 || E < 1) return 0;
+  return gemm_ws_bytes(R, E, 0, false);
+}
+
+int wq_grouped_gemm_w8a8(const int8_t *A, const float *sa, const int8_t *W, const float *sw,
+                         const int32_t *offsets, int E, int64_t R, int64_t N, int64_t K,
+                         int scheme, int acc, int out_type, void *out, void *ws, size_t ws_bytes,
+                         int32_t *status, wq_stream_t stream) {
+  if (R < 0 || E > 4096) return WQ_ERR_INVALID_ARG;
+  if (R == 0) return WQ_OK;
+  WQ_TRY(check_gemm_common(W, sw, E, N, K, scheme, acc, out_type, out));
+  if (!A || !sa || !offsets) return WQ_ERR_INVALID_ARG;
+  if (!al16(A)) return WQ_ERR_UNSUPPORTED;
+  if (R >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;
+  if (ws_bytes < gemm_ws_bytes(R, E, 0, false) || !ws) return WQ_ERR_WORKSPACE;
+  WQ_TRY(check_device());
+  GemmArgs a{A, sa, W, sw, offsets, nullptr, 0, E, R, N, K, scheme, acc, out_type, out, ws, status};
+  return launch_grouped_gemm(a, stream);
+}
+
+size_t wq_grouped_gemm_masked_workspace_size(int E, int Mmax) {
+  if (E < 1 || Mmax < 0) return 0;
+  return gemm_ws_bytes(int64_t(E) * Mmax, E, Mmax, true);
+}
+
+int wq_grouped_gemm_w8a8_masked(const int8_t *A, const float *sa, const int32_t *masked_m, int E,
+                                int Mmax, const int8_t *W, const float *sw, int64_t N, int64_t K,
+                                int scheme, int acc, int out_type, void *out, void *ws,
+                                size_t ws_bytes, int32_t *status, wq_stream_t stream) {
+  if (Mmax < 0 || E > 4096) return WQ_ERR_INVALID_ARG;
+  if (Mmax == 0) return WQ_OK;
+  WQ_TRY(check_gemm_common(W, sw, E, N, K, scheme, acc, out_type, out));
+  if (!A || !sa || !masked_m) return WQ_ERR_INVALID_ARG;
+  if (!al16(A)) return WQ_ERR_UNSUPPORTED;
+  const int64_t R = int64_t(E) * Mmax;
+  if (R >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;
+  if (ws_bytes < gemm_ws_bytes(R, E, Mmax, true) || !ws) return WQ_ERR_WORKSPACE;
+  WQ_TRY(check_device());
+  GemmArgs a{A, sa, W, sw, nullptr, masked_m, Mmax, E, R, N, K, scheme, acc, out_type, out, ws,
+             status};
+  return launch_grouped_gemm(a, stream);
+}
+
+int wq_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group, int8_t *hq, float *sh,
+                      wq_stream_t stream) {
+  if (R < 0 || I < 0) return WQ_ERR_INVALID_ARG;
+  if (group != 0 && !group_ok(group)) return WQ_ERR_UNSUPPORTED;
+  if (R == 0 || I == 0) return WQ_OK;
+  if (!gu || !hq || !sh) return WQ_ERR_INVALID_ARG;
+  if (I % 8 || (group && I % group) || !al16(gu) || !al8(hq)) return WQ_ERR_UNSUPPORTED;
+  WQ_TRY(check_device());
+  return launch_silu_mul_quant(gu, R, I, group, nullptr, 0, hq, sh, stream);
+}
+
+int wq_moe_combine(const uint16_t *y, const int32_t *pair_to_row, const float *w, int T, int k,
+                   int64_t H, uint16_t *out, wq_stream_t stream) {
+  if (T < 0 || k < 1 || H < 0) return WQ_ERR_INVALID_ARG;
+  if (T == 0 || H == 0) return WQ_OK;
+  if (!y || !pair_to_row || !w || !out) return WQ_ERR_INVALID_ARG;
+  if (H % 8 || !al16(y) || !al16(out)) return WQ_ERR_UNSUPPORTED;
+  WQ_TRY(check_device());
+  return launch_combine(y, pair_to_row, w, T, k, H, out, stream);
+}
+
+// ---------------------------------------------------------------------------
+// The layer
+
+namespace {
+
+struct FwdBufs {
+  int32_t *ids;
+  float *w;
+  int8_t *q;
+  float *s;
+  int32_t *counts, *offsets, *sorted_pair, *pair_to_row;
+  void *align_ws;
+  int8_t *A;
+  float *sa;
+  uint16_t *gu;
+  int8_t *hq;
+  float *sh;
+  uint16_t *y;
+  void *gemm_ws;
+  size_t gemm_ws_bytes;
+};
+
+size_t carve_forward(void *ws, int T, int H, int I, int E, int k, int scheme, FwdBufs *b) {
+  Carver c(ws);
+  const int64_t R = int64_t(T) * k;
+  const int64_t g1 = scheme == WQ_SCHEME_BLOCK ? H / 128 : 1;
+  const int64_t g2 = scheme == WQ_SCHEME_BLOCK ? I / 128 : 1;
+  FwdBufs t;
+  t.ids = c.take<int32_t>(R);
+  t.w = c.take<float>(R);
+  t.q = c.take<int8_t>(size_t(T) * H);
+  t.s = c.take<float>(size_t(T) * g1);
+  t.counts = c.take<int32_t>(E);
+  t.offsets = c.take<int32_t>(E + 1);
+  t.sorted_pair = c.take<int32_t>(R);
+  t.pair_to_row = c.take<int32_t>(R);
+  t.align_ws = c.take<char>(align_ws_bytes(T, k, E));
+  t.A = c.take<int8_t>(size_t(R) * H);
+  t.sa = c.take<float>(size_t(R) * g1);
+  t.gu = c.take<uint16_t>(size_t(R) * 2 * I);
+  t.hq = c.take<int8_t>(size_t(R) * I);
+  t.sh = c.take<float>(size_t(R) * g2);
+  t.y = c.take<uint16_t>(size_t(R) * H);
+  t.gemm_ws_bytes = gemm_ws_bytes(R, E, 0, false);
+  t.gemm_ws = c.take<char>(t.gemm_ws_bytes);
+  if (b) *b = t;
+  return c.used;
+}
+
+int check_forward_shape(int T, int H, int I, int E, int k, int scheme, int acc) {
+  if (T < 0 || H <= 0 || I <= 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E)
+    return WQ_ERR_INVALID_ARG;
+  if (scheme != WQ_SCHEME_CHANNEL && scheme != WQ_SCHEME_BLOCK) return WQ_ERR_INVALID_ARG;
+  if (acc != WQ_ACC_I32 && acc != WQ_ACC_F32) return WQ_ERR_INVALID_ARG;
+  if (H % 128 || I % 128) return WQ_ERR_UNSUPPORTED;
+  if (int64_t(T) * k >= (int64_t(1) << 31) / 2) return WQ_ERR_UNSUPPORTED;
+  return WQ_OK;
+}
+
+int run_forward(const uint16_t *x, const float *logits, const int8_t *W13, const float *sw13,
+                const int8_t *W2, const float *sw2, int T, int H, int I, int E, int k, int scheme,
+                int acc, uint16_t *out, const FwdBufs &b, int32_t *status, cudaStream_t st) {
+  const int64_t R = int64_t(T) * k;
+  const bool blk = scheme == WQ_SCHEME_BLOCK;
+  WQ_TRY(launch_route(logits, T, E, k, b.ids, b.w, st));
+  WQ_TRY(launch_quant_rows(x, T, H, H, blk ? 128 : 0, b.q, b.s, st));
+  WQ_TRY(launch_align(b.ids, T, k, E, 1, b.counts, b.offsets, b.sorted_pair, b.pair_to_row,
+                      b.align_ws, status, st));
+  WQ_TRY(launch_permute(b.q, b.s, blk ? H / 128 : 1, k, H, b.sorted_pair, R, b.A, b.sa, st));
+  GemmArgs g1{b.A, b.sa, W13, sw13, b.offsets, nullptr, 0, E, R, int64_t(2) * I, H, scheme, acc,
+              WQ_OUT_BF16, b.gu, b.gemm_ws, status};
+  WQ_TRY(launch_grouped_gemm(g1, st));
+  WQ_TRY(launch_silu_mul_quant(b.gu, R, I, blk ? 128 : 0, nullptr, 0, b.hq, b.sh, st));
+  GemmArgs g2{b.hq, b.sh, W2, sw2, b.offsets, nullptr, 0, E, R, H, I, scheme, acc,
+              WQ_OUT_BF16, b.y, b.gemm_ws, status};
+  WQ_TRY(launch_grouped_gemm(g2, st));
+  return launch_combine(b.y, b.pair_to_row, b.w, T, k, H, out, st);
+}
+
+}  // namespace
+
+size_t wq_moe_forward_workspace_size(int T, int H, int I, int E, int k, int scheme) {
+  if (check_forward_shape(T, H, I, E, k, scheme, WQ_ACC_I32) != WQ_OK) return 0;
+  return carve_forward(nullptr, T, H, I, E, k, scheme, nullptr);
+}
+
+int wq_moe_forward(const uint16_t *x, const float *logits, const int8_t *W13, const float *sw13,
+                   const int8_t *W2, const float *sw2, int T, int H, int I, int E, int k,
+                   int scheme, int acc, uint16_t *out, void *ws, size_t ws_bytes,
+                   int32_t *status, wq_stream_t stream) {
+  WQ_TRY(check_forward_shape(T, H, I, E, k, scheme, acc));
+  if (T == 0) return WQ_OK;
+  if (!x || !logits || !W13 || !sw13 || !W2 || !sw2 || !out) return WQ_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(out) || !al16(W13) || !al16(W2)) return WQ_ERR_UNSUPPORTED;
+  FwdBufs b;
+  const size_t need = carve_forward(ws, T, H, I, E, k, scheme, &b);
+  if (!ws || ws_bytes < need || !al16(ws)) return WQ_ERR_WORKSPACE;
+  WQ_TRY(check_device());
+  return run_forward(x, logits, W13, sw13, W2, sw2, T, H, I, E, k, scheme, acc, out, b, status,
+                     stream);
+}
+
+size_t wq_moe_forward_host_workspace_size(int T, int H, int I, int E, int k, int scheme) {
+  const size_t inner = wq_moe_forward_workspace_size(T, H, I, E, k, scheme);
+  if (inner == 0) return 0;
+  return inner + rup(size_t(T) * H * 2) + rup(size_t(T) * E * 4) + rup(size_t(T) * H * 2);
+}
+
+int wq_moe_forward_host(const uint16_t *x_host, const float *logits_host, const int8_t *W13,
+                        const float *sw13, const int8_t *W2, const float *sw2, int T, int H, int I,
+                        int E, int k, int scheme, int acc, uint16_t *out_host, void *ws,
+                        size_t ws_bytes, int32_t *status, wq_stream_t stream) {
+  WQ_TRY(check_forward_shape(T, H, I, E, k, scheme, acc));
+  if (T == 0) return WQ_OK;
+  if (!x_host || !logits_host || !W13 || !sw13 || !W2 || !sw2 || !out_host)
+    return WQ_ERR_INVALID_ARG;
+  if (!al16(W13) || !al16(W2)) return WQ_ERR_UNSUPPORTED;
+  if (!ws || !al16(ws) || ws_bytes < wq_moe_forward_host_workspace_size(T, H, I, E, k, scheme))
+    return WQ_ERR_WORKSPACE;
+  WQ_TRY(check_device());
+  Carver c(ws);
+  uint16_t *x = c.take<uint16_t>(size_t(T) * H);
+  float *logits = c.take<float>(size_t(T) * E);
+  uint16_t *out = c.take<uint16_t>(size_t(T) * H);
+  FwdBufs b;
+  carve_forward(c.base + c.used, T, H, I, E, k, scheme, &b);
+  if (cudaMemcpyAsync(x, x_host, size_t(T) * H * 2, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return WQ_ERR_LAUNCH;
+  if (cudaMemcpyAsync(logits, logits_host, size_t(T) * E * 4, cudaMemcpyHostToDevice, stream) !=
+      cudaSuccess)
+    return WQ_ERR_LAUNCH;
+  WQ_TRY(run_forward(x, logits, W13, sw13, W2, sw2, T, H, I, E, k, scheme, acc, out, b, status,
+                     stream));
+  if (cudaMemcpyAsync(out_host, out, size_t(T) * H * 2, cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    return WQ_ERR_LAUNCH;
+  return WQ_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Masked layout
+
+namespace {
+
+size_t carve_masked(void *ws, int E, int Mmax, int H, int I, int scheme, uint16_t **gu,
+                    int8_t **hq, float **sh, void **gws, size_t *gws_bytes) {
+  Carver c(ws);
+  const int64_t R = int64_t(E) * Mmax;
+  const int64_t g2 = scheme == WQ_SCHEME_BLOCK ? I / 128 : 1;
+  uint16_t *a = c.take<uint16_t>(size_t(R) * 2 * I);
+  int8_t *b = c.take<int8_t>(size_t(R) * I);
+  float *d = c.take<float>(size_t(R) * g2);
+  const size_t gb = gemm_ws_bytes(R, E, Mmax, true);
+  void *g = c.take<char>(gb);
+  if (gu) { *gu = a; *hq = b; *sh = d; *gws = g; *gws_bytes = gb; }
+  return c.used;
+}
+
+}  // namespace
+
+size_t wq_moe_forward_masked_workspace_size(int E, int Mmax, int H, int I, int scheme) {
+  if (E < 1 || Mmax < 0 || H <= 0 || I <= 0) return 0;
+  return carve_masked(nullptr, E, Mmax, H, I, scheme, nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+int wq_moe_forward_masked(const int8_t *a, const float *sa, const int32_t *masked_m, int E,
+                          int Mmax, const int8_t *W13, const float *sw13, const int8_t *W2,
+                          const float *sw2, int H, int I, int scheme, int acc, uint16_t *y,
+                          void *ws, size_t ws_bytes, int32_t *status, wq_stream_t stream) {
+  if (E < 1 || E > 4096 || Mmax < 0 || H <= 0 || I <= 0) return WQ_ERR_INVALID_ARG;
+  if (scheme != WQ_SCHEME_CHANNEL && scheme != WQ_SCHEME_BLOCK) return WQ_ERR_INVALID_ARG;
+  if (acc != WQ_ACC_I32 && acc != WQ_ACC_F32) return WQ_ERR_INVALID_ARG;
+  if (H % 128 || I % 128) return WQ_ERR_UNSUPPORTED;
+  if (Mmax == 0) return WQ_OK;
+  if (!a || !sa || !masked_m || !W13 || !sw13 || !W2 || !sw2 || !y) return WQ_ERR_INVALID_ARG;
+  if (!al16(a) || !al16(y) || !al16(W13) || !al16(W2)) return WQ_ERR_UNSUPPORTED;
+  if (int64_t(E) * Mmax >= (int64_t(1) << 31) / 2) return WQ_ERR_UNSUPPORTED;
+  uint16_t *gu;
+  int8_t *hq;
+  float *sh;
+  void *gws;
+  size_t gwsb;
+  const size_t need = carve_masked(ws, E, Mmax, H, I, scheme, &gu, &hq, &sh, &gws, &gwsb);
+  if (!ws || !al16(ws) || ws_bytes < need) return WQ_ERR_WORKSPACE;
+  WQ_TRY(check_device());
+  const int64_t R = int64_t(E) * Mmax;
+  GemmArgs g1{a, sa, W13, sw13, nullptr, masked_m, Mmax, E, R, int64_t(2) * I, H, scheme, acc,
+              WQ_OUT_BF16, gu, gws, status};
+  WQ_TRY(launch_grouped_gemm(g1, stream));
+  WQ_TRY(launch_silu_mul_quant(gu, R, I, scheme == WQ_SCHEME_BLOCK ? 128 : 0, masked_m, Mmax, hq,
+                               sh, stream));
+  GemmArgs g2{hq, sh, W2, sw2, nullptr, masked_m, Mmax, E, R, H, I, scheme, acc, WQ_OUT_BF16, y,
+              gws, status};
+  return launch_grouped_gemm(g2, stream);
+}
+
+}  // extern "C"

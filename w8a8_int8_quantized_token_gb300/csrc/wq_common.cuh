@@ -1,0 +1,169 @@
+// Internal helpers shared by the kernels of libwq.so (sm_103a).
+//
+// Floating point here is IEEE float32 with explicit round-to-nearest
+// intrinsics (__fmul_rn, __fadd_rn, __fdiv_rn): nothing is fused or
+// approximated, so every result is reproducible and matches the plain
+// definitions stated in include/wq.h.  The library is also compiled with
+// -fmad=false as a second guard against contraction.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/wq.h"
+
+namespace wq {
+
+constexpr int kQMax = 127;
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+__device__ __forceinline__ float bf16_to_f(uint16_t v) { return __uint_as_float(uint32_t(v) << 16); }
+
+__device__ __forceinline__ uint16_t f_to_bf16(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return uint32_t(f_to_bf16(lo)) | (uint32_t(f_to_bf16(hi)) << 16);
+}
+
+// 8 bf16 in a uint4 -> 8 floats
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
+  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+  f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// exp by Cody and Waite's reduction x = n ln2 + r (ln2 split into a
+// 16-significant-bit high part and the remainder), the degree-7 Taylor
+// polynomial of exp(r) in Horner form, and an exact scaling by
+// 2^floor(n/2) * 2^(n - floor(n/2)).  Every step is one float32 operation
+// rounded to nearest even.  x >= 89 -> +inf, x <= -104 -> 0, NaN -> NaN.
+__device__ __forceinline__ float exp_cw(float x) {
+  if (x != x) return x;
+  if (x >= 89.0f) return __uint_as_float(0x7f800000u);
+  if (x <= -104.0f) return 0.0f;
+  const float kLog2e = __uint_as_float(0x3fb8aa3bu);   // nearest float to 1/ln 2
+  const float kLn2Hi = __uint_as_float(0x3f317200u);   // floor(ln2 * 2^16) / 2^16
+  const float kLn2Lo = __uint_as_float(0x35bfbe8eu);   // nearest float to ln2 - kLn2Hi
+  const float c7 = __uint_as_float(0x39500d01u);       // 1/7!
+  const float c6 = __uint_as_float(0x3ab60b61u);       // 1/6!
+  const float c5 = __uint_as_float(0x3c088889u);       // 1/5!
+  const float c4 = __uint_as_float(0x3d2aaaabu);       // 1/4!
+  const float c3 = __uint_as_float(0x3e2aaaabu);       // 1/3!
+  const float c2 = 0.5f, c1 = 1.0f, c0 = 1.0f;
+  float n = rintf(__fmul_rn(x, kLog2e));
+  float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, kLn2Hi)), __fmul_rn(n, kLn2Lo));
+  float p = c7;
+  p = __fadd_rn(__fmul_rn(p, r), c6);
+  p = __fadd_rn(__fmul_rn(p, r), c5);
+  p = __fadd_rn(__fmul_rn(p, r), c4);
+  p = __fadd_rn(__fmul_rn(p, r), c3);
+  p = __fadd_rn(__fmul_rn(p, r), c2);
+  p = __fadd_rn(__fmul_rn(p, r), c1);
+  p = __fadd_rn(__fmul_rn(p, r), c0);
+  int ni = __float2int_rn(n);
+  int n1 = ni >> 1;  // floor(n / 2)
+  int n2 = ni - n1;
+  float s1 = __uint_as_float(uint32_t(n1 + 127) << 23);
+  float s2 = __uint_as_float(uint32_t(n2 + 127) << 23);
+  return __fmul_rn(__fmul_rn(p, s1), s2);
+}
+
+// silu(g) = g / (1 + exp(-g))
+__device__ __forceinline__ float silu(float g) {
+  return __fdiv_rn(g, __fadd_rn(1.0f, exp_cw(-g)));
+}
+
+// Quantization scale from an absolute maximum: max(a, 1e-10) / 127.
+__device__ __forceinline__ float quant_scale(float amax) {
+  return __fdiv_rn(fmaxf(amax, 1e-10f), 127.0f);
+}
+
+// One code: clamp(rint(x / s), -127, 127).
+__device__ __forceinline__ int quant_code(float x, float s) {
+  float q = rintf(__fdiv_rn(x, s));
+  q = fminf(fmaxf(q, -127.0f), 127.0f);
+  return __float2int_rn(q);
+}
+
+__device__ __forceinline__ uint32_t pack_s8x4(int a, int b, int c, int d) {
+  return (uint32_t(a) & 0xffu) | ((uint32_t(b) & 0xffu) << 8) | ((uint32_t(c) & 0xffu) << 16) |
+         ((uint32_t(d) & 0xffu) << 24);
+}
+
+__device__ __forceinline__ void set_status(int32_t *status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide maximum (blockDim.x a multiple of 32, at most 1024).
+__device__ __forceinline__ float block_max(float v, float *red) {
+  v = warp_max(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float r = (l < nw) ? red[l] : 0.0f;
+  return warp_max(r);
+}
+
+// A tile of rows that one grouped-GEMM CTA computes.
+struct Tile {
+  int expert;  // expert index
+  int row0;    // first row in A / out
+  int rows;    // valid rows (<= the kernel's tile height)
+  int pad;
+};
+
+}  // namespace wq
+
+// Launchers implemented in the kernel translation units (host side).
+namespace wq {
+int launch_quant_rows(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group, int8_t *q,
+                      float *s, cudaStream_t st);
+int launch_quant_weight_block(const uint16_t *w, int64_t N, int64_t K, int8_t *q, float *s,
+                              cudaStream_t st);
+int launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w, cudaStream_t st);
+size_t align_ws_bytes(int T, int k, int E);
+int launch_align(const int32_t *ids, int T, int k, int E, int pad_m, int32_t *counts,
+                 int32_t *offsets, int32_t *sorted_pair, int32_t *pair_to_row, void *ws,
+                 int32_t *status, cudaStream_t st);
+int launch_permute(const int8_t *q, const float *s, int groups, int k, int64_t K,
+                   const int32_t *sorted_pair, int64_t R, int8_t *A, float *sa, cudaStream_t st);
+int launch_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group,
+                          const int32_t *masked_m, int Mmax, int8_t *hq, float *sh,
+                          cudaStream_t st);
+int launch_combine(const uint16_t *y, const int32_t *pair_to_row, const float *w, int T, int k,
+                   int64_t H, uint16_t *out, cudaStream_t st);
+
+// Grouped GEMM: segments come from offsets (contiguous) or masked_m (strided).
+struct GemmArgs {
+  const int8_t *A;
+  const float *sa;
+  const int8_t *W;
+  const float *sw;
+  const int32_t *offsets;   // contiguous layout, or nullptr
+  const int32_t *masked_m;  // masked layout, or nullptr
+  int Mmax;
+  int E;
+  int64_t R;  // rows of A / out
+  int64_t N;
+  int64_t K;
+  int scheme, acc, out_type;
+  void *out;
+  void *ws;
+  int32_t *status;
+};
+int launch_build_tiles(const int32_t *offsets, const int32_t *masked_m, int Mmax, int E, int BM,
+                       Tile *tiles, int32_t *ntiles, cudaStream_t st);
+size_t gemm_ws_bytes(int64_t R, int E, int Mmax, bool masked);
+int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st);
+}  // namespace wq

@@ -1,0 +1,398 @@
+// Memory-bound steps of the W8A8 fused-MoE layer: activation and weight
+// quantization, top-k routing, permute (scatter by expert), SiLU-and-mul with
+// re-quantization, and the weighted combine.  All are coalesced 16-byte
+// vector accesses with warp-shuffle reductions for the absolute maxima.
+#include "wq_common.cuh"
+
+namespace wq {
+
+// ---------------------------------------------------------------------------
+// Per-token quantization: one CTA per row, the row held in registers.
+// (Meituan INT8 DeepSeek R1 article, 量化技术的探索: online per-token
+// activation quantization of the channel-wise scheme.)
+template <int V>
+__global__ void __launch_bounds__(1024) quant_row_kernel(const uint16_t *__restrict__ x, int64_t K,
+                                                         int64_t ldx, int8_t *__restrict__ q,
+                                                         float *__restrict__ s) {
+  __shared__ float red[32];
+  const int64_t row = blockIdx.x;
+  const uint4 *xr = reinterpret_cast<const uint4 *>(x + row * ldx);
+  const int nvec = int(K >> 3);
+  uint4 v[V];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int idx = threadIdx.x + i * blockDim.x;
+    if (idx < nvec) {
+      v[i] = __ldcs(xr + idx);
+      float f[8];
+      unpack8(v[i], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    }
+  }
+  amax = block_max(amax, red);
+  const float sc = quant_scale(amax);
+  uint2 *qr = reinterpret_cast<uint2 *>(q + row * K);
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int idx = threadIdx.x + i * blockDim.x;
+    if (idx < nvec) {
+      float f[8];
+      unpack8(v[i], f);
+      uint2 o;
+      o.x = pack_s8x4(quant_code(f[0], sc), quant_code(f[1], sc), quant_code(f[2], sc),
+                      quant_code(f[3], sc));
+      o.y = pack_s8x4(quant_code(f[4], sc), quant_code(f[5], sc), quant_code(f[6], sc),
+                      quant_code(f[7], sc));
+      qr[idx] = o;
+    }
+  }
+  if (threadIdx.x == 0) s[row] = sc;
+}
+
+// Per-token-group quantization: each thread owns 8 consecutive elements; the
+// GV = group/8 lanes of one group reduce with xor shuffles (the block-wise
+// scheme's per-token-group activation quantization).
+template <int GV>
+__global__ void __launch_bounds__(256) quant_group_kernel(const uint16_t *__restrict__ x, int64_t T,
+                                                          int64_t K, int64_t ldx,
+                                                          int8_t *__restrict__ q,
+                                                          float *__restrict__ s) {
+  const int64_t vpr = K >> 3;  // vectors per row
+  const int64_t total = T * vpr;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx - threadIdx.x % 32 < total;
+       idx += stride) {
+    const bool live = idx < total;
+    const int64_t row = live ? idx / vpr : 0;
+    const int64_t vec = live ? idx - row * vpr : 0;
+    float f[8];
+    float amax = 0.0f;
+    if (live) {
+      const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(x + row * ldx) + vec);
+      unpack8(v, f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    }
+#pragma unroll
+    for (int o = GV / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (live) {
+      const float sc = quant_scale(amax);
+      uint2 o;
+      o.x = pack_s8x4(quant_code(f[0], sc), quant_code(f[1], sc), quant_code(f[2], sc),
+                      quant_code(f[3], sc));
+      o.y = pack_s8x4(quant_code(f[4], sc), quant_code(f[5], sc), quant_code(f[6], sc),
+                      quant_code(f[7], sc));
+      reinterpret_cast<uint2 *>(q + row * K)[vec] = o;
+      if (vec % GV == 0) s[row * (vpr / GV) + vec / GV] = sc;
+    }
+  }
+}
+
+int launch_quant_rows(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group, int8_t *q,
+                      float *s, cudaStream_t st) {
+  if (T == 0 || K == 0) return WQ_OK;
+  if (group == 0) {
+    const int64_t nvec = K / 8;
+    constexpr int V = 8;
+    if (nvec > int64_t(V) * 1024 || T > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
+    int threads = int((nvec + V - 1) / V);
+    threads = ((threads + 31) / 32) * 32;
+    if (threads < 128) threads = nvec >= 128 ? 128 : 32;
+    if (threads > 1024) threads = 1024;
+    quant_row_kernel<V><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s);
+  } else {
+    const int64_t total = T * (K / 8);
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 64) blocks = 152 * 64;
+    switch (group) {
+      case 32: quant_group_kernel<4><<<unsigned(blocks), 256, 0, st>>>(x, T, K, ldx, q, s); break;
+      case 64: quant_group_kernel<8><<<unsigned(blocks), 256, 0, st>>>(x, T, K, ldx, q, s); break;
+      case 128: quant_group_kernel<16><<<unsigned(blocks), 256, 0, st>>>(x, T, K, ldx, q, s); break;
+      case 256: quant_group_kernel<32><<<unsigned(blocks), 256, 0, st>>>(x, T, K, ldx, q, s); break;
+      default: return WQ_ERR_UNSUPPORTED;
+    }
+  }
+  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// [128,128] block weight quantization: one CTA of 256 threads per block,
+// 8 vectors (64 elements) per thread held in registers.
+__global__ void __launch_bounds__(256) quant_wblock_kernel(const uint16_t *__restrict__ w, int64_t K,
+                                                           int8_t *__restrict__ q,
+                                                           float *__restrict__ s) {
+  __shared__ float red[32];
+  const int64_t kb_n = K / 128;
+  const int64_t nb = blockIdx.x / kb_n, kb = blockIdx.x % kb_n;
+  uint4 v[8];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = threadIdx.x + i * 256;  // vector 0..2047 of the block
+    const int r = e >> 4, c = e & 15;     // 16 vectors per 128-wide row
+    v[i] = __ldcs(reinterpret_cast<const uint4 *>(w + (nb * 128 + r) * K + kb * 128) + c);
+    float f[8];
+    unpack8(v[i], f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+  }
+  amax = block_max(amax, red);
+  const float sc = quant_scale(amax);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = threadIdx.x + i * 256;
+    const int r = e >> 4, c = e & 15;
+    float f[8];
+    unpack8(v[i], f);
+    uint2 o;
+    o.x = pack_s8x4(quant_code(f[0], sc), quant_code(f[1], sc), quant_code(f[2], sc),
+                    quant_code(f[3], sc));
+    o.y = pack_s8x4(quant_code(f[4], sc), quant_code(f[5], sc), quant_code(f[6], sc),
+                    quant_code(f[7], sc));
+    reinterpret_cast<uint2 *>(q + (nb * 128 + r) * K + kb * 128)[c] = o;
+  }
+  if (threadIdx.x == 0) s[nb * kb_n + kb] = sc;
+}
+
+int launch_quant_weight_block(const uint16_t *w, int64_t N, int64_t K, int8_t *q, float *s,
+                              cudaStream_t st) {
+  const int64_t blocks = (N / 128) * (K / 128);
+  if (blocks == 0) return WQ_OK;
+  if (blocks > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
+  quant_wblock_kernel<<<unsigned(blocks), 256, 0, st>>>(w, K, q, s);
+  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// Top-k routing: one warp per token; lane l holds logits l, l+32, ...
+template <int NPER>
+__global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ logits, int T, int E,
+                                                    int k, int32_t *__restrict__ ids,
+                                                    float *__restrict__ wout) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float v[NPER];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < NPER; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? logits[int64_t(t) * E + e] : 0.0f;
+    if (e >= E) taken |= 1u << i;
+  }
+  float my_l = 0.0f;
+  int my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    // lane-local best: larger value, then lower expert id
+    float bv = 0.0f;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) {
+      if (!(taken >> i & 1u)) {
+        const int e = lane + 32 * i;
+        if (bi == 0x7fffffff || v[i] > bv || (v[i] == bv && e < bi)) { bv = v[i]; bi = e; }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const bool better = (bi == 0x7fffffff) ||
+                          (oi != 0x7fffffff && (ov > bv || (ov == bv && oi < bi)));
+      if (better) { bv = ov; bi = oi; }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) { my_l = bv; my_id = bi; }
+  }
+  const float m = __shfl_sync(0xffffffffu, my_l, 0);
+  const float e = lane < k ? exp_cw(__fsub_rn(my_l, m)) : 0.0f;
+  float S = 0.0f;
+  for (int j = 0; j < k; ++j) S = __fadd_rn(S, __shfl_sync(0xffffffffu, e, j));
+  if (lane < k) {
+    ids[int64_t(t) * k + lane] = my_id;
+    wout[int64_t(t) * k + lane] = __fdiv_rn(e, S);
+  }
+}
+
+int launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w, cudaStream_t st) {
+  if (T == 0) return WQ_OK;
+  const int blocks = (T + 7) / 8;
+  const int nper = (E + 31) / 32;
+  if (nper <= 1) route_kernel<1><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
+  else if (nper <= 2) route_kernel<2><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
+  else if (nper <= 4) route_kernel<4><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
+  else if (nper <= 8) route_kernel<8><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
+  else if (nper <= 16) route_kernel<16><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
+  else route_kernel<32><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
+  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// Permute (ep_scatter): one CTA per destination row, 16-byte copies.
+__global__ void __launch_bounds__(128) permute_kernel(const int8_t *__restrict__ q,
+                                                      const float *__restrict__ s, int groups,
+                                                      int k, int64_t K,
+                                                      const int32_t *__restrict__ sorted_pair,
+                                                      int8_t *__restrict__ A,
+                                                      float *__restrict__ sa) {
+  const int64_t r = blockIdx.x;
+  const int p = sorted_pair[r];
+  const int64_t nvec = K >> 4;
+  uint4 *dst = reinterpret_cast<uint4 *>(A + r * K);
+  if (p < 0) {
+    for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+    for (int g = threadIdx.x; g < groups; g += blockDim.x) sa[r * groups + g] = 0.0f;
+    return;
+  }
+  const int64_t tok = p / k;
+  const uint4 *src = reinterpret_cast<const uint4 *>(q + tok * K);
+  for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) __stcs(dst + i, __ldg(src + i));
+  for (int g = threadIdx.x; g < groups; g += blockDim.x) sa[r * groups + g] = s[tok * groups + g];
+}
+
+int launch_permute(const int8_t *q, const float *s, int groups, int k, int64_t K,
+                   const int32_t *sorted_pair, int64_t R, int8_t *A, float *sa, cudaStream_t st) {
+  if (R == 0) return WQ_OK;
+  if (R > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
+  permute_kernel<<<unsigned(R), 128, 0, st>>>(q, s, groups, k, K, sorted_pair, A, sa);
+  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// SiLU-and-mul + re-quantization: one CTA per row, V vector pairs per thread.
+template <int V, int GV>  // GV = 0: one scale per row; else lanes per group
+__global__ void __launch_bounds__(1024) silu_mul_quant_kernel(
+    const uint16_t *__restrict__ gu, int64_t I, const int32_t *__restrict__ masked_m, int Mmax,
+    int8_t *__restrict__ hq, float *__restrict__ sh) {
+  __shared__ float red[32];
+  const int64_t row = blockIdx.x;
+  if (masked_m != nullptr) {
+    const int e = int(row / Mmax), m = int(row % Mmax);
+    if (m >= masked_m[e]) return;  // whole CTA leaves together
+  }
+  const uint4 *g4 = reinterpret_cast<const uint4 *>(gu + row * 2 * I);
+  const uint4 *u4 = reinterpret_cast<const uint4 *>(gu + row * 2 * I + I);
+  const int nvec = int(I >> 3);
+  float h[V][8];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int idx = threadIdx.x + i * blockDim.x;
+    float ga[8], ua[8];
+    if (idx < nvec) {
+      unpack8(__ldcs(g4 + idx), ga);
+      unpack8(__ldcs(u4 + idx), ua);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        h[i][j] = __fmul_rn(silu(ga[j]), ua[j]);
+        amax = fmaxf(amax, fabsf(h[i][j]));
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) h[i][j] = 0.0f;
+    }
+  }
+  if constexpr (GV == 0) {
+    amax = block_max(amax, red);
+    const float sc = quant_scale(amax);
+    uint2 *dst = reinterpret_cast<uint2 *>(hq + row * I);
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int idx = threadIdx.x + i * blockDim.x;
+      if (idx < nvec) {
+        uint2 o;
+        o.x = pack_s8x4(quant_code(h[i][0], sc), quant_code(h[i][1], sc), quant_code(h[i][2], sc),
+                        quant_code(h[i][3], sc));
+        o.y = pack_s8x4(quant_code(h[i][4], sc), quant_code(h[i][5], sc), quant_code(h[i][6], sc),
+                        quant_code(h[i][7], sc));
+        dst[idx] = o;
+      }
+    }
+    if (threadIdx.x == 0) sh[row] = sc;
+  } else {
+    static_assert(V == 1, "group mode keeps one vector per thread");
+    const int idx = threadIdx.x;
+#pragma unroll
+    for (int o = GV / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (idx < nvec) {
+      const float sc = quant_scale(amax);
+      uint2 o;
+      o.x = pack_s8x4(quant_code(h[0][0], sc), quant_code(h[0][1], sc), quant_code(h[0][2], sc),
+                      quant_code(h[0][3], sc));
+      o.y = pack_s8x4(quant_code(h[0][4], sc), quant_code(h[0][5], sc), quant_code(h[0][6], sc),
+                      quant_code(h[0][7], sc));
+      reinterpret_cast<uint2 *>(hq + row * I)[idx] = o;
+      if (idx % GV == 0) sh[row * (nvec / GV) + idx / GV] = sc;
+    }
+  }
+}
+
+int launch_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group,
+                          const int32_t *masked_m, int Mmax, int8_t *hq, float *sh,
+                          cudaStream_t st) {
+  if (R == 0 || I == 0) return WQ_OK;
+  if (R > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
+  const int64_t nvec = I / 8;
+  auto rnd = [](int64_t t) { int v = int(((t + 31) / 32) * 32); return v < 32 ? 32 : v; };
+  if (group == 0) {
+    if (nvec <= 1024) {
+      silu_mul_quant_kernel<1, 0><<<unsigned(R), rnd(nvec), 0, st>>>(gu, I, masked_m, Mmax, hq, sh);
+    } else if (nvec <= 4096) {
+      silu_mul_quant_kernel<4, 0><<<unsigned(R), rnd((nvec + 3) / 4), 0, st>>>(gu, I, masked_m, Mmax, hq, sh);
+    } else {
+      return WQ_ERR_UNSUPPORTED;
+    }
+  } else {
+    if (nvec > 1024) return WQ_ERR_UNSUPPORTED;
+    const int th = rnd(nvec);
+    switch (group) {
+      case 32: silu_mul_quant_kernel<1, 4><<<unsigned(R), th, 0, st>>>(gu, I, masked_m, Mmax, hq, sh); break;
+      case 64: silu_mul_quant_kernel<1, 8><<<unsigned(R), th, 0, st>>>(gu, I, masked_m, Mmax, hq, sh); break;
+      case 128: silu_mul_quant_kernel<1, 16><<<unsigned(R), th, 0, st>>>(gu, I, masked_m, Mmax, hq, sh); break;
+      case 256: silu_mul_quant_kernel<1, 32><<<unsigned(R), th, 0, st>>>(gu, I, masked_m, Mmax, hq, sh); break;
+      default: return WQ_ERR_UNSUPPORTED;
+    }
+  }
+  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// Weighted combine (the gather after the down GEMM): one CTA per token.
+__global__ void __launch_bounds__(128) combine_kernel(const uint16_t *__restrict__ y,
+                                                      const int32_t *__restrict__ p2r,
+                                                      const float *__restrict__ w, int k,
+                                                      int64_t H, uint16_t *__restrict__ out) {
+  const int64_t t = blockIdx.x;
+  const int64_t nvec = H >> 3;
+  for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const int row = p2r[t * k + j];
+      if (row < 0) continue;
+      const float wj = w[t * k + j];
+      float f[8];
+      unpack8(__ldcs(reinterpret_cast<const uint4 *>(y + int64_t(row) * H) + i), f);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[c] = __fadd_rn(acc[c], __fmul_rn(wj, f[c]));
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    reinterpret_cast<uint4 *>(out + t * H)[i] = o;
+  }
+}
+
+int launch_combine(const uint16_t *y, const int32_t *pair_to_row, const float *w, int T, int k,
+                   int64_t H, uint16_t *out, cudaStream_t st) {
+  if (T == 0 || H == 0) return WQ_OK;
+  combine_kernel<<<unsigned(T), 128, 0, st>>>(y, pair_to_row, w, k, H, out);
+  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+}
+
+}  // namespace wq
