@@ -76,7 +76,7 @@ def test_route_topk(T, E, k):
                                        (8192, 8, 256, 1), (77, 3, 4096, 1), (500, 6, 33, 128), (0, 2, 8, 1)])
 def test_moe_align(T, k, E, pad):
     rng = np.random.default_rng(T + E)
-    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32).reshape(T, k)
+    ids = np.array([rng.choice(E, k, replace=False) for _ in range(T)], np.int32).reshape(T, k)
     if T:
         ids[: T // 2, 0] = 1  # a hot expert
     c, o, sp, p2r = wq.moe_align(torch.from_numpy(ids).to(DEV), E, pad)

@@ -136,7 +136,7 @@ int launch_align(const int32_t *ids, int T, int k, int E, int pad_m, int32_t *co
 // (masked layout).  Tiles are expert-major.  ntiles[0] = number written.
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__restrict__ offsets,
                                                            const int32_t *__restrict__ masked_m,
-                                                           int Mmax, int E, int BM,
+                                                           int Mmax, int E, int BM, int64_t R,
                                                            Tile *__restrict__ tiles,
                                                            int32_t *__restrict__ ntiles) {
   __shared__ int32_t part[1024];
@@ -149,9 +149,12 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
       r0 = e * Mmax;
       len = m;
     } else {
-      r0 = offsets[e];
-      len = offsets[e + 1] - r0;
-      if (len < 0) len = 0;
+      // clamp to [0, R): the tile list can never outgrow ceil(R/BM) + E
+      int64_t a = offsets[e], b = offsets[e + 1];
+      a = a < 0 ? 0 : (a > R ? R : a);
+      b = b < a ? a : (b > R ? R : b);
+      r0 = int(a);
+      len = int(b - a);
     }
   };
   int local = 0;
@@ -185,8 +188,8 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
 }
 
 int launch_build_tiles(const int32_t *offsets, const int32_t *masked_m, int Mmax, int E, int BM,
-                       Tile *tiles, int32_t *ntiles, cudaStream_t st) {
-  build_tiles_kernel<<<1, 1024, 0, st>>>(offsets, masked_m, Mmax, E, BM, tiles, ntiles);
+                       int64_t R, Tile *tiles, int32_t *ntiles, cudaStream_t st) {
+  build_tiles_kernel<<<1, 1024, 0, st>>>(offsets, masked_m, Mmax, E, BM, R, tiles, ntiles);
   return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
 }
 

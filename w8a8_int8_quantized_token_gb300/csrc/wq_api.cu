@@ -86,12 +86,12 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
   Tile *tiles128 = c.take<Tile>(size_t(t128));
   int32_t *n128 = c.take<int32_t>(1);
   if (gemm_tc_supported(a)) {
-    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 128, tiles128, n128, st));
+    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 128, a.R, tiles128, n128, st));
     return launch_gemm_tc(a, tiles128, n128, int(t128), st);
   }
   (void)tiles128;
   (void)n128;
-  WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 64, tiles64, n64, st));
+  WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 64, a.R, tiles64, n64, st));
   return launch_gemm_simt(a, tiles64, n64, int(t64), st);
 }
 
