@@ -155,13 +155,16 @@ def _gemm_case(seed, E, counts, N, K, scheme):
 @pytest.mark.parametrize("scheme,acc", [("channel", "i32"), ("channel", "f32"), ("block", "f32")])
 @pytest.mark.parametrize("counts,N,K", [([3, 0, 130, 1, 257], 256, 384),
                                          ([0, 0, 5], 128, 128),
-                                         ([700, 64, 129], 512, 1024)])
+                                         ([700, 64, 129], 512, 1024),
+                                         ([300, 0, 1, 555], 768, 2304)])
 def test_grouped_gemm(scheme, acc, counts, N, K):
     E = len(counts)
     A, sa, W, sw, offs = _gemm_case(len(counts) + N + K, E, counts, N, K, scheme)
     t = lambda a: torch.from_numpy(a).to(DEV)
-    out = wq.grouped_gemm_w8a8(t(A), t(sa), t(W), t(sw), t(offs), scheme, acc)
+    st = wq.new_status()
+    out = wq.grouped_gemm_w8a8(t(A), t(sa), t(W), t(sw), t(offs), scheme, acc, status=st)
     ref = O.grouped_gemm_w8a8(A, sa, W, sw, offs, scheme, acc)
+    assert int(st.item()) == 0
     assert_bf16_equal(bits(out), ref, f"gemm {scheme}/{acc}")
 
 
@@ -173,8 +176,11 @@ def test_grouped_gemm_int32_accumulators_and_extremes():
     W[0, 1, :] = -127
     A[1, :] = -127
     t = lambda a: torch.from_numpy(a).to(DEV)
-    C = wq.grouped_gemm_w8a8(t(A), t(sa), t(W), t(sw), t(offs), "channel", "i32", out_type="i32")
+    st = wq.new_status()
+    C = wq.grouped_gemm_w8a8(t(A), t(sa), t(W), t(sw), t(offs), "channel", "i32", out_type="i32",
+                             status=st)
     Co = O.grouped_gemm_i32(A, W, offs)
+    assert int(st.item()) == 0
     assert np.array_equal(np_(C), Co)
     assert Co[0, 0] == 127 * 127 * 7168 and Co[0, 1] == -127 * 127 * 7168
 
@@ -239,8 +245,10 @@ def _layer_case(cfg):
 ], ids=lambda c: c.name)
 def test_layer_forward(cfg):
     x, lg, w, ow = _layer_case(cfg)
-    out = wq.moe_forward(x.to(DEV), lg.to(DEV), *w, cfg.k, cfg.scheme, cfg.acc)
+    st = wq.new_status()
+    out = wq.moe_forward(x.to(DEV), lg.to(DEV), *w, cfg.k, cfg.scheme, cfg.acc, status=st)
     ref = O.moe_forward(bits(x), lg.numpy(), *ow, cfg.k, cfg.scheme, cfg.acc)
+    assert int(st.item()) == 0
     max_abs, rel = tolerance_report(bits(out), ref)
     assert max_abs <= 2e-2 and rel <= 1e-2
     assert_bf16_equal(bits(out), ref, f"layer {cfg.name}")
