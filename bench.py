@@ -282,8 +282,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling)")
+    ap.add_argument("--experts", type=int, default=0, help="override the expert count (profiling)")
     args = ap.parse_args()
     cfg = synth.CONFIGS[args.config]
+    if args.tokens or args.experts:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, name=cfg.name + "-reduced", T=args.tokens or cfg.T,
+                                  E=args.experts or cfg.E)
     if args.impl == "reference":
         run_reference(args, cfg)
         return
@@ -325,10 +331,12 @@ def main():
 
     with ClockSampler(local) as clk:
         barrier()
+        torch.cuda.nvtx.range_push("timed")
         start.record()
         for i in range(args.steps):
             layer.step(x, logits, evs[i])
         end.record()
+        torch.cuda.nvtx.range_pop()
         barrier()
     total_ms = start.elapsed_time(end)
     if world > 1:

@@ -138,8 +138,10 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
                                                            const int32_t *__restrict__ masked_m,
                                                            int Mmax, int E, int BM, int64_t R,
                                                            Tile *__restrict__ tiles,
-                                                           int32_t *__restrict__ ntiles) {
+                                                           int32_t *__restrict__ ntiles,
+                                                           int32_t *__restrict__ zero_word) {
   __shared__ int32_t part[1024];
+  if (zero_word != nullptr && threadIdx.x == 0) *zero_word = 0;
   const int per = (E + blockDim.x - 1) / blockDim.x;
   const int e0 = threadIdx.x * per;
   auto seg = [&](int e, int &r0, int &len) {
@@ -188,8 +190,10 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
 }
 
 int launch_build_tiles(const int32_t *offsets, const int32_t *masked_m, int Mmax, int E, int BM,
-                       int64_t R, Tile *tiles, int32_t *ntiles, cudaStream_t st) {
-  build_tiles_kernel<<<1, 1024, 0, st>>>(offsets, masked_m, Mmax, E, BM, R, tiles, ntiles);
+                       int64_t R, Tile *tiles, int32_t *ntiles, int32_t *zero_word,
+                       cudaStream_t st) {
+  build_tiles_kernel<<<1, 1024, 0, st>>>(offsets, masked_m, Mmax, E, BM, R, tiles, ntiles,
+                                         zero_word);
   return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
 }
 

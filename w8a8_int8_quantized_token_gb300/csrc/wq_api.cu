@@ -8,10 +8,13 @@
 
 namespace wq {
 int launch_gemm_simt(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
-                     cudaStream_t st);
+                     const int32_t *gate, cudaStream_t st);
 int launch_gemm_tc(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
-                   cudaStream_t st);
+                   const int32_t *gate, cudaStream_t st);
 bool gemm_tc_supported(const GemmArgs &a);
+int launch_gemm_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
+                    int32_t *redo, cudaStream_t st);
+bool gemm_tc2_supported(const GemmArgs &a);
 }  // namespace wq
 
 using namespace wq;
@@ -68,31 +71,59 @@ int64_t gemm_max_tiles(int64_t R, int E, int Mmax, bool masked, int BM) {
 
 namespace wq {
 
+// Workspace of one grouped GEMM: three tile lists (64-row tiles for the
+// CUDA-core engine, 128-row tiles for the chunked tensor-core engine, 256-row
+// token tiles for the fast int32 engine), each with its count, and the flag
+// the fast engine raises when a tile needs the exact chunked recompute.
+struct GemmWs {
+  Tile *t64, *t128, *t256;
+  int32_t *n64, *n128, *n256, *redo;
+  int64_t m64, m128, m256;
+  size_t bytes;
+};
+
+GemmWs carve_gemm_ws(void *ws, int64_t R, int E, int Mmax, bool masked) {
+  GemmWs w;
+  Carver c(ws);
+  w.m64 = gemm_max_tiles(R, E, Mmax, masked, 64);
+  w.m128 = gemm_max_tiles(R, E, Mmax, masked, 128);
+  w.m256 = gemm_max_tiles(R, E, Mmax, masked, 256);
+  w.t64 = c.take<Tile>(size_t(w.m64));
+  w.n64 = c.take<int32_t>(1);
+  w.t128 = c.take<Tile>(size_t(w.m128));
+  w.n128 = c.take<int32_t>(1);
+  w.t256 = c.take<Tile>(size_t(w.m256));
+  w.n256 = c.take<int32_t>(1);
+  w.redo = c.take<int32_t>(1);
+  w.bytes = c.used;
+  return w;
+}
+
 size_t gemm_ws_bytes(int64_t R, int E, int Mmax, bool masked) {
-  // two tile lists (64-row tiles for the CUDA-core engine, 128-row tiles for
-  // the tensor-core engine), each followed by its count
-  const int64_t t64 = gemm_max_tiles(R, E, Mmax, masked, 64);
-  const int64_t t128 = gemm_max_tiles(R, E, Mmax, masked, 128);
-  return rup(size_t(t64) * sizeof(Tile)) + rup(4) + rup(size_t(t128) * sizeof(Tile)) + rup(4);
+  return carve_gemm_ws(nullptr, R, E, Mmax, masked).bytes;
 }
 
 int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
   const bool masked = a.masked_m != nullptr;
-  Carver c(a.ws);
-  const int64_t t64 = gemm_max_tiles(a.R, a.E, a.Mmax, masked, 64);
-  const int64_t t128 = gemm_max_tiles(a.R, a.E, a.Mmax, masked, 128);
-  Tile *tiles64 = c.take<Tile>(size_t(t64));
-  int32_t *n64 = c.take<int32_t>(1);
-  Tile *tiles128 = c.take<Tile>(size_t(t128));
-  int32_t *n128 = c.take<int32_t>(1);
-  if (gemm_tc_supported(a)) {
-    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 128, a.R, tiles128, n128, st));
-    return launch_gemm_tc(a, tiles128, n128, int(t128), st);
+  GemmWs w = carve_gemm_ws(a.ws, a.R, a.E, a.Mmax, masked);
+  const int32_t *gate = nullptr;
+  if (gemm_tc2_supported(a)) {
+    // fast int32 engine; it raises *redo for any tile whose single-pass
+    // float32 sums it cannot prove exact, and the chunked engine below then
+    // recomputes the launch (it exits at once when *redo == 0)
+    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 256, a.R, w.t256, w.n256,
+                              w.redo, st));
+    WQ_TRY(launch_gemm_tc2(a, w.t256, w.n256, int(w.m256), w.redo, st));
+    gate = w.redo;
   }
-  (void)tiles128;
-  (void)n128;
-  WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 64, a.R, tiles64, n64, st));
-  return launch_gemm_simt(a, tiles64, n64, int(t64), st);
+  if (gemm_tc_supported(a)) {
+    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 128, a.R, w.t128, w.n128,
+                              nullptr, st));
+    return launch_gemm_tc(a, w.t128, w.n128, int(w.m128), gate, st);
+  }
+  WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 64, a.R, w.t64, w.n64, nullptr,
+                            st));
+  return launch_gemm_simt(a, w.t64, w.n64, int(w.m64), gate, st);
 }
 
 }  // namespace wq

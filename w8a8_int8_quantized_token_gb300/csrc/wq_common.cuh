@@ -163,7 +163,8 @@ struct GemmArgs {
   int32_t *status;
 };
 int launch_build_tiles(const int32_t *offsets, const int32_t *masked_m, int Mmax, int E, int BM,
-                       int64_t R, Tile *tiles, int32_t *ntiles, cudaStream_t st);
+                       int64_t R, Tile *tiles, int32_t *ntiles, int32_t *zero_word,
+                       cudaStream_t st);
 size_t gemm_ws_bytes(int64_t R, int E, int Mmax, bool masked);
 int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st);
 }  // namespace wq

@@ -4,9 +4,9 @@
 // accumulator) and of the Meituan article's block-wise scheme.
 //
 // Tile: 64 rows x 64 output channels x 128 K, 256 threads, 4x4 outputs per
-// thread.  Used for small row counts per expert (decode), where the tensor
-// core engine's 128-row tiles would be mostly padding, and as a second,
-// independent engine for the int32 accumulators.
+// thread.  Serves the shapes the tensor-core engines do not take (output
+// width not a multiple of 256 in the chunked modes) and is their exact
+// fallback there.
 #include "wq_common.cuh"
 
 namespace wq {
@@ -14,9 +14,11 @@ namespace wq {
 constexpr int kSBM = 64, kSBN = 64, kSBK = 128;
 
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a, const Tile *__restrict__ tiles,
-                                                        const int32_t *__restrict__ ntiles) {
+                                                        const int32_t *__restrict__ ntiles,
+                                                        const int32_t *__restrict__ gate) {
   __shared__ int32_t As[kSBM][kSBK / 4 + 1];
   __shared__ int32_t Ws[kSBN][kSBK / 4 + 1];
+  if (gate != nullptr && *gate == 0) return;
   if (int(blockIdx.y) >= ntiles[0]) return;
   const Tile tl = tiles[blockIdx.y];
   const int e = tl.expert;
@@ -120,12 +122,13 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a, const Tile *
   }
 }
 
+// `gate`: nullptr to always run; otherwise the kernel runs only if *gate != 0.
 int launch_gemm_simt(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
-                     cudaStream_t st) {
+                     const int32_t *gate, cudaStream_t st) {
   if (max_tiles <= 0) return WQ_OK;
   if (max_tiles > 65535) return WQ_ERR_UNSUPPORTED;
   dim3 grid(unsigned(a.N / kSBN), unsigned(max_tiles));
-  gemm_simt_kernel<<<grid, 256, 0, st>>>(a, tiles, ntiles);
+  gemm_simt_kernel<<<grid, 256, 0, st>>>(a, tiles, ntiles, gate);
   return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
 }
 

@@ -1,0 +1,360 @@
+// Grouped W8A8 GEMM, int32-accumulator fast engine (tcgen05, sm_103a).
+//
+// The channel-wise INT8 GEMM of "[Feature] DeepSeek V3/R1 INT8 Quantization
+// (channel-wise)" with the int32 accumulator: C = A_e W_e^T exactly, then
+// v = (float(C) * sa[r]) * sw[e][n].  Codes are widened to fp16 (exact) and
+// multiplied by tcgen05.mma kind::f16 with float32 accumulation in tensor
+// memory over the whole K range in one pass.  That single pass is exact when
+// every partial sum stays an integer of magnitude below 2^24; by the
+// Cauchy-Schwarz inequality every partial sum of a row a and a channel w is
+// at most ||a||_2 ||w||_2 in magnitude, so the converter warps accumulate the
+// squared norms of all rows and channels of a tile (dp4a) while they widen
+// the codes, and the epilogue checks  max||a||^2 * max||w||^2 < 2^48.
+// A tile that fails the check raises a device flag; the chunked exact engine
+// (wq_gemm_tc.cu) then recomputes the whole launch.  Realistic activations
+// and weights pass with a wide margin (||a|| ||w|| ~ 1e6).
+//
+// Operand roles are swapped relative to the row-major problem: the MMA's
+// M = 128 rows are output channels (weights, A operand) and its N = 16..256
+// columns are tokens (B operand), so a ragged expert wastes at most 15 token
+// columns.  Persistent CTAs; work item = (token tile <= 256 rows of one expert)
+// x (128 output channels).  Two tensor-memory accumulators (columns [0,256)
+// and [256,512)) let the epilogue of one item overlap the MMAs of the next.
+//   warp 0      TMA producer (weights 128 x 64, tokens box x 64 int8)
+//   warp 1      TMEM allocator and MMA issuer (one thread)
+//   warps 2-9   converters: int8 -> fp16 (128-byte swizzled K-major) + norms
+//   warps 10-13 epilogue: dequant, bf16, coalesced stores (32 channels/warp)
+// Every wait is bounded (1 s); on expiry the kernel records WQ_ERR_TIMEOUT,
+// waits (bounded) for its own copies and MMAs, frees tensor memory and exits.
+#include "wq_tc.cuh"
+
+namespace wq {
+namespace {
+
+using namespace tc;
+
+constexpr int WM = 128, TN = 256, BK = 64;
+constexpr int S8 = 3, S16 = 3;
+constexpr int W8 = WM * BK, T8 = TN * BK;  // int8 bytes per stage
+constexpr int W16 = 2 * W8, T16 = 2 * T8;  // fp16 bytes per stage
+constexpr int ST8 = W8 + T8, ST16 = W16 + T16;
+constexpr int OFF_F16 = 0;
+constexpr int OFF_I8 = OFF_F16 + S16 * ST16;
+constexpr int OFF_BAR = OFF_I8 + S8 * ST8;
+constexpr int B_S8_FULL = 0, B_S8_EMPTY = S8, B_F16_FULL = 2 * S8, B_F16_EMPTY = 2 * S8 + S16,
+              B_ACC_FULL = 2 * S8 + 2 * S16,  // [2]
+    B_ACC_EMPTY = B_ACC_FULL + 2,             // [2]
+    B_NORM_READY = B_ACC_FULL + 4,            // [2]
+    B_NORM_FREE = B_ACC_FULL + 6,             // [2]
+    B_NORM_READ = B_ACC_FULL + 8,             // [2]
+    B_MMA_DONE = B_ACC_FULL + 10, NBAR = B_ACC_FULL + 11;
+constexpr int OFF_NORM = OFF_BAR + NBAR * 8;  // int32 [2 buffers][weights, tokens]
+constexpr int OFF_TMEM = OFF_NORM + 16;
+constexpr int OFF_ABORT = OFF_TMEM + 4;
+constexpr int SMEM_USED = OFF_ABORT + 4;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;
+constexpr int NTHREADS = 448;
+constexpr int NCONV = 256;  // converter threads
+
+__device__ __forceinline__ int sq4(uint32_t w, int acc) { return __dp4a(int(w), int(w), acc); }
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT16,
+                    const __grid_constant__ CUtensorMap tmT64,
+                    const __grid_constant__ CUtensorMap tmT256, const GemmArgs a,
+                    const Tile *__restrict__ tiles, const int32_t *__restrict__ ntiles,
+                    int32_t *__restrict__ redo) {
+  extern __shared__ uint8_t smem_raw[];
+  const int NB = int(a.N / WM);
+  const int items = ntiles[0] * NB;
+  if (int(blockIdx.x) >= items) return;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *sm = smem_raw + (base - raw);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_ABORT);
+  volatile int *norm = reinterpret_cast<volatile int *>(sm + OFF_NORM);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_TMEM);
+  auto bar = [&](int i) { return base + OFF_BAR + 8u * uint32_t(i); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KT = int(a.K / BK);
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < 4; ++i) norm[i] = 0;
+    for (int s = 0; s < S8; ++s) {
+      mbar_init(bar(B_S8_FULL + s), 1);
+      mbar_init(bar(B_S8_EMPTY + s), NCONV / 32);
+    }
+    for (int s = 0; s < S16; ++s) {
+      mbar_init(bar(B_F16_FULL + s), NCONV / 32);
+      mbar_init(bar(B_F16_EMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(B_ACC_FULL + b), 1);
+      mbar_init(bar(B_ACC_EMPTY + b), 4);
+      mbar_init(bar(B_NORM_READY + b), NCONV / 32);
+      mbar_init(bar(B_NORM_FREE + b), 1);
+      mbar_init(bar(B_NORM_READ + b), 4);
+    }
+    mbar_init(bar(B_MMA_DONE), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    set_status(a.status, WQ_ERR_TIMEOUT);
+  };
+  // token box height for a tile of `rows` tokens, and the MMA's N
+  auto nmma_of = [](int rows) { return (rows + 15) & ~15; };
+  auto box_of = [](int nmma) { return nmma <= 16 ? 16 : (nmma <= 64 ? 64 : 256); };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int g = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+        const Tile tl = tiles[it / NB];
+        const int wb = it % NB;
+        const int box = box_of(nmma_of(tl.rows));
+        const CUtensorMap *tmT = box == 16 ? &tmT16 : (box == 64 ? &tmT64 : &tmT256);
+        const uint32_t tx = W8 + box * BK;
+        const int wrow = int(int64_t(tl.expert) * a.N + int64_t(wb) * WM);
+        for (int i = 0; i < KT; ++i, ++g) {
+          const int s = g % S8;
+          if (!mbar_wait<200>(bar(B_S8_EMPTY + s), ((g / S8) & 1) ^ 1, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          const uint32_t dst = base + OFF_I8 + uint32_t(s) * ST8;
+          mbar_expect_tx(bar(B_S8_FULL + s), tx);
+          tma_load_2d(dst, &tmW, i * BK, wrow, bar(B_S8_FULL + s));
+          tma_load_2d(dst + W8, tmT, i * BK, tl.row0, bar(B_S8_FULL + s));
+        }
+      }
+      if (!ok) {
+        for (int j = g > S8 ? g - S8 : 0; j < g; ++j)
+          mbar_wait_bounded(bar(B_S8_FULL + j % S8), (j / S8) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int g = 0, ii = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++ii) {
+        const Tile tl = tiles[it / NB];
+        const uint32_t idesc = idesc_f16(WM, nmma_of(tl.rows));
+        const int b = ii & 1;
+        if (!mbar_wait(bar(B_ACC_EMPTY + b), ((ii >> 1) & 1) ^ 1, abort_flag)) {
+          fail();
+          break;
+        }
+        const uint32_t d = tmem + uint32_t(b) * 256u;
+        for (int i = 0; i < KT; ++i, ++g) {
+          const int s = g % S16;
+          if (!mbar_wait(bar(B_F16_FULL + s), (g / S16) & 1, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t w0 = base + OFF_F16 + uint32_t(s) * ST16;
+          const uint32_t t0 = w0 + W16;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_f16(d, sdesc(w0 + 32u * kk), sdesc(t0 + 32u * kk), idesc, (i | kk) ? 1u : 0u);
+          mma_commit(bar(B_F16_EMPTY + s));
+        }
+        if (ok) mma_commit(bar(B_ACC_FULL + b));
+      }
+      mma_commit(bar(B_MMA_DONE));
+      mbar_wait_bounded(bar(B_MMA_DONE), 0);
+    }
+  } else if (warp < 2 + NCONV / 32) {
+    // ------------------------------------------------------------ converters
+    const int t = threadIdx.x - 64;  // 0..255
+    int g = 0, ii = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++ii) {
+      const Tile tl = tiles[it / NB];
+      const int box = box_of(nmma_of(tl.rows));
+      const int tchunks = box * 4;  // 16-byte pieces of the token tile
+      int nrm[6] = {0, 0, 0, 0, 0, 0};
+      for (int i = 0; i < KT; ++i, ++g) {
+        const int s8 = g % S8, s16 = g % S16;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S8_FULL + s8), (g / S8) & 1, abort_flag))) {
+          fail();
+          ok = false;
+          break;
+        }
+        const uint8_t *src = sm + OFF_I8 + s8 * ST8;
+        uint4 v[6];
+#pragma unroll
+        for (int j = 0; j < 6; ++j) {
+          const int c = (j < 2 ? j : j - 2) * NCONV + t;
+          v[j] = (j < 2 || c < tchunks)
+                     ? *reinterpret_cast<const uint4 *>(src + (j < 2 ? 0 : W8) + c * 16)
+                     : make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_S8_EMPTY + s8));
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(bar(B_F16_EMPTY + s16), ((g / S16) & 1) ^ 1, abort_flag))) {
+          fail();
+          ok = false;
+          break;
+        }
+        uint8_t *dst = sm + OFF_F16 + s16 * ST16;
+#pragma unroll
+        for (int j = 0; j < 6; ++j) {
+          const int c = (j < 2 ? j : j - 2) * NCONV + t;
+          if (j < 2 || c < tchunks) {
+            const int row = c >> 2;
+            store_f16_row_piece(dst + (j < 2 ? 0 : W16) + row * 128, row, c & 3, v[j]);
+            nrm[j] = sq4(v[j].w, sq4(v[j].z, sq4(v[j].y, sq4(v[j].x, nrm[j]))));
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_F16_FULL + s16));
+      }
+      if (!ok) break;
+      // squared norms: the 4 lanes 4m..4m+3 hold the 4 pieces of one row
+      int wmax = 0, tmax = 0;
+#pragma unroll
+      for (int j = 0; j < 6; ++j) {
+        int n2 = nrm[j];
+        n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
+        n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
+        if (j < 2) {
+          wmax = max(wmax, n2);
+        } else {
+          const int row = ((j - 2) * NCONV + t) >> 2;
+          if (row < tl.rows) tmax = max(tmax, n2);
+        }
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        wmax = max(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+        tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+      }
+      const int b = ii & 1;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(bar(B_NORM_FREE + b), ((ii >> 1) & 1) ^ 1, abort_flag))) {
+        fail();
+        break;
+      }
+      if (lane == 0) {
+        atomicMax(const_cast<int *>(norm + 2 * b), wmax);
+        atomicMax(const_cast<int *>(norm + 2 * b + 1), tmax);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_NORM_READY + b));
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // tensor-memory lane quarter of this warp
+    int ii = 0;
+    for (int it = blockIdx.x; it < items; it += gridDim.x, ++ii) {
+      const Tile tl = tiles[it / NB];
+      const int wb = it % NB;
+      const int b = ii & 1, par = (ii >> 1) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait<500>(bar(B_ACC_FULL + b), par, abort_flag)) ||
+          !__all_sync(0xffffffffu, mbar_wait(bar(B_NORM_READY + b), par, abort_flag))) {
+        fail();
+        break;
+      }
+      tc_fence_after();
+      const long long nw = norm[2 * b], nt = norm[2 * b + 1];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_NORM_READ + b));
+      if (warp == 10 && lane == 0) {
+        // once all four epilogue warps have read the norms, clear them for the
+        // item after next and hand the slots back to the converters
+        if (mbar_wait(bar(B_NORM_READ + b), par, abort_flag)) {
+          norm[2 * b] = 0;
+          norm[2 * b + 1] = 0;
+          mbar_arrive(bar(B_NORM_FREE + b));
+        } else {
+          fail();
+        }
+      }
+      if (nw * nt >= (1ll << 48) && q == 0 && lane == 0) atomicExch(redo, 1);
+      const int64_t n = int64_t(wb) * WM + q * 32 + lane;  // this thread's output channel
+      const float swn = a.sw[int64_t(tl.expert) * a.N + n];
+      const int nmma = nmma_of(tl.rows);
+      const uint32_t taddr = tmem + (uint32_t(q * 32) << 16) + uint32_t(b) * 256u;
+      for (int p = 0; p * 32 < nmma; ++p) {
+        uint32_t v[32];
+        tmem_ld32(taddr + 32u * p, v);
+        const int tok0 = p * 32;
+        const float sal = (tok0 + lane < tl.rows) ? a.sa[int64_t(tl.row0) + tok0 + lane] : 0.0f;
+        tmem_wait_ld();
+        const int lim = min(32, tl.rows - tok0);
+        if (a.out_type == WQ_OUT_I32) {
+          int32_t *o = static_cast<int32_t *>(a.out) + (int64_t(tl.row0) + tok0) * a.N + n;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < lim) o[int64_t(j) * a.N] = __float2int_rn(__uint_as_float(v[j]));
+        } else {
+          uint16_t *o = static_cast<uint16_t *>(a.out) + (int64_t(tl.row0) + tok0) * a.N + n;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float s = __shfl_sync(0xffffffffu, sal, j);
+            if (j < lim)
+              o[int64_t(j) * a.N] = f_to_bf16(__fmul_rn(__fmul_rn(__uint_as_float(v[j]), s), swn));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_ACC_EMPTY + b));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+bool gemm_tc2_supported(const GemmArgs &a) {
+  return a.scheme == WQ_SCHEME_CHANNEL && a.acc == WQ_ACC_I32 && a.N % WM == 0 &&
+         a.K % BK == 0 && a.K <= 65536 && a.E * a.N < (int64_t(1) << 31) &&
+         a.R < (int64_t(1) << 31) && tma_available();
+}
+
+int launch_gemm_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
+                    int32_t *redo, cudaStream_t st) {
+  if (max_tiles <= 0) return WQ_OK;
+  CUtensorMap mW, m16, m64, m256;
+  if (!make_tma_2d_u8(&mW, a.W, int64_t(a.E) * a.N, a.K, BK, WM) ||
+      !make_tma_2d_u8(&m16, a.A, a.R, a.K, BK, 16) || !make_tma_2d_u8(&m64, a.A, a.R, a.K, BK, 64) ||
+      !make_tma_2d_u8(&m256, a.A, a.R, a.K, BK, 256))
+    return WQ_ERR_LAUNCH;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess)
+      return WQ_ERR_LAUNCH;
+    attr = true;
+  }
+  const int64_t max_items = int64_t(max_tiles) * (a.N / WM);
+  const int grid = int(max_items < num_sms() ? max_items : num_sms());
+  gemm_tc2_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(mW, m16, m64, m256, a, tiles, ntiles, redo);
+  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+}
+
+}  // namespace wq
