@@ -173,6 +173,26 @@ WQ_API int wq_grouped_gemm_w8a8(const int8_t *A, const float *sa, const int8_t *
                          int scheme, int acc, int out_type, void *out, void *ws,
                          size_t ws_bytes, int32_t *status, wq_stream_t stream);
 
+/* Grouped W8A8 GEMM without a workspace argument.  The pages have no
+ * counterpart: this entry point exists for callers that may not allocate
+ * device memory at run time (a plug-in inside a host framework that owns
+ * the device memory pool and gives plug-ins no allocator; a serving loop that
+ * cannot accept cudaMalloc's implicit device synchronisation once started).
+ * Arguments, results and requirements are those of wq_grouped_gemm_w8a8
+ * minus ws/ws_bytes.  The scratch lives in a static device array of
+ * WQ_NOALLOC_SCRATCH_BYTES that every GPU loading libwq.so holds until the
+ * process exits; the first call on a device looks up that array's address
+ * (cudaGetSymbolAddress) with the device current.  All calls on a device
+ * share the array; calls that overlap on the GPU race on it.  A problem whose
+ * scratch need (wq_grouped_gemm_workspace_size(R, E)) exceeds the array
+ * returns WQ_ERR_UNSUPPORTED before any work is enqueued.  Nothing is
+ * allocated. */
+#define WQ_NOALLOC_SCRATCH_BYTES (256 * 1024)
+WQ_API int wq_grouped_gemm_w8a8_noalloc(const int8_t *A, const float *sa, const int8_t *W,
+                                        const float *sw, const int32_t *offsets, int E, int64_t R,
+                                        int64_t N, int64_t K, int scheme, int acc, int out_type,
+                                        void *out, int32_t *status, wq_stream_t stream);
+
 /* Masked layout [LL]: A int8 [E][Mmax][K] with per-row scales sa
  * ([E][Mmax] or [E][Mmax][K/128]) and valid counts masked_m int32 [E]
  * (device).  Expert e computes rows [0, min(masked_m[e], Mmax)) with the

@@ -44,6 +44,7 @@ _SIGS = {
     "wq_moe_permute": (_I, [_P, _P, _I, _I, _I, _L, _P, _L, _P, _P, _P]),
     "wq_grouped_gemm_workspace_size": (_S, [_L, _I]),
     "wq_grouped_gemm_w8a8": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
+    "wq_grouped_gemm_w8a8_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _I, _P, _P, _P]),
     "wq_grouped_gemm_masked_workspace_size": (_S, [_I, _I]),
     "wq_grouped_gemm_w8a8_masked": (_I, [_P, _P, _P, _I, _I, _P, _P, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
     "wq_silu_mul_quant": (_I, [_P, _L, _L, _I, _P, _P, _P]),
