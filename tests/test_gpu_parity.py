@@ -156,7 +156,10 @@ def _gemm_case(seed, E, counts, N, K, scheme):
 @pytest.mark.parametrize("counts,N,K", [([3, 0, 130, 1, 257], 256, 384),
                                          ([0, 0, 5], 128, 128),
                                          ([700, 64, 129], 512, 1024),
-                                         ([300, 0, 1, 555], 768, 2304)])
+                                         ([300, 0, 1, 555], 768, 2304),
+                                         # few rows per expert: the 64-row token tiles
+                                         ([0, 1, 5, 16, 17, 63, 64, 65, 130, 3, 2, 0, 7, 9, 33, 40],
+                                          256, 512)])
 def test_grouped_gemm(scheme, acc, counts, N, K):
     E = len(counts)
     A, sa, W, sw, offs = _gemm_case(len(counts) + N + K, E, counts, N, K, scheme)

@@ -15,6 +15,7 @@ bool gemm_tc_supported(const GemmArgs &a);
 int launch_gemm_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
                     int32_t *redo, cudaStream_t st);
 bool gemm_tc2_supported(const GemmArgs &a);
+int gemm_tc2_tile_rows(const GemmArgs &a);
 }  // namespace wq
 
 using namespace wq;
@@ -111,9 +112,12 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
     // fast int32 engine; it raises *redo for any tile whose single-pass
     // float32 sums it cannot prove exact, and the chunked engine below then
     // recomputes the launch (it exits at once when *redo == 0)
-    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 256, a.R, w.t256, w.n256,
-                              w.redo, st));
-    WQ_TRY(launch_gemm_tc2(a, w.t256, w.n256, int(w.m256), w.redo, st));
+    const int rows = gemm_tc2_tile_rows(a);  // 64 (few rows per expert) or 256
+    Tile *t = rows == 64 ? w.t64 : w.t256;
+    int32_t *n = rows == 64 ? w.n64 : w.n256;
+    const int64_t m = rows == 64 ? w.m64 : w.m256;
+    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, rows, a.R, t, n, w.redo, st));
+    WQ_TRY(launch_gemm_tc2(a, t, n, int(m), w.redo, st));
     gate = w.redo;
   }
   if (gemm_tc_supported(a)) {

@@ -33,37 +33,58 @@ namespace {
 
 using namespace tc;
 
-constexpr int WM = 128, TN = 256, BK = 64;
-constexpr int S8 = 3, S16 = 3;
-constexpr int W8 = WM * BK, T8 = TN * BK;  // int8 bytes per stage
-constexpr int W16 = 2 * W8, T16 = 2 * T8;  // fp16 bytes per stage
-constexpr int ST8 = W8 + T8, ST16 = W16 + T16;
-constexpr int OFF_F16 = 0;
-constexpr int OFF_I8 = OFF_F16 + S16 * ST16;
-constexpr int OFF_BAR = OFF_I8 + S8 * ST8;
-constexpr int B_S8_FULL = 0, B_S8_EMPTY = S8, B_F16_FULL = 2 * S8, B_F16_EMPTY = 2 * S8 + S16,
-              B_ACC_FULL = 2 * S8 + 2 * S16,  // [2]
-    B_ACC_EMPTY = B_ACC_FULL + 2,             // [2]
-    B_NORM_READY = B_ACC_FULL + 4,            // [2]
-    B_NORM_FREE = B_ACC_FULL + 6,             // [2]
-    B_NORM_READ = B_ACC_FULL + 8,             // [2]
-    B_MMA_DONE = B_ACC_FULL + 10, NBAR = B_ACC_FULL + 11;
-constexpr int OFF_NORM = OFF_BAR + NBAR * 8;  // int32 [2 buffers][weights, tokens]
-constexpr int OFF_TMEM = OFF_NORM + 16;
-constexpr int OFF_ABORT = OFF_TMEM + 4;
-constexpr int SMEM_USED = OFF_ABORT + 4;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;
+constexpr int WM = 128, BK = 64;
 constexpr int NTHREADS = 448;
 constexpr int NCONV = 256;  // converter threads
 
+// Shared-memory plan of one instantiation: TN = most tokens per item (MMA N),
+// S8 / S16 = depths of the int8 staging ring and of the fp16 ring.  Large
+// TN suits many rows per expert (prefill); a small TN with a deep int8 ring
+// keeps enough weight bytes in flight when experts hold a few tokens each
+// (decode), where the GEMM streams weights from HBM.
+template <int TN, int S8, int S16>
+struct Plan {
+  static constexpr int W8 = WM * BK, T8 = TN * BK;  // int8 bytes per stage
+  static constexpr int W16 = 2 * W8, T16 = 2 * T8;  // fp16 bytes per stage
+  static constexpr int ST8 = W8 + T8, ST16 = W16 + T16;
+  static constexpr int OFF_F16 = 0;
+  static constexpr int OFF_I8 = OFF_F16 + S16 * ST16;
+  static constexpr int OFF_BAR = OFF_I8 + S8 * ST8;
+  static constexpr int B_S8_FULL = 0, B_S8_EMPTY = S8, B_F16_FULL = 2 * S8,
+                       B_F16_EMPTY = 2 * S8 + S16, B_ACC_FULL = 2 * S8 + 2 * S16,  // [2]
+      B_ACC_EMPTY = B_ACC_FULL + 2,                                                // [2]
+      B_NORM_READY = B_ACC_FULL + 4,                                               // [2]
+      B_NORM_FREE = B_ACC_FULL + 6,                                                // [2]
+      B_NORM_READ = B_ACC_FULL + 8,                                                // [2]
+      B_MMA_DONE = B_ACC_FULL + 10, NBAR = B_ACC_FULL + 11;
+  static constexpr int OFF_NORM = OFF_BAR + NBAR * 8;  // int32 [2 buffers][weights, tokens]
+  static constexpr int OFF_TMEM = OFF_NORM + 16;
+  static constexpr int OFF_ABORT = OFF_TMEM + 4;
+  static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
+  static constexpr int NJT = TN * 4 / NCONV;  // token 16-byte pieces per converter thread
+  static_assert(NJT >= 1 && TN * 4 == NJT * NCONV, "token tile must fill the converter threads");
+  static_assert(SMEM_BYTES <= 232448, "shared memory plan too large");
+};
+
 __device__ __forceinline__ int sq4(uint32_t w, int acc) { return __dp4a(int(w), int(w), acc); }
 
+template <int TN, int S8, int S16>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT16,
                     const __grid_constant__ CUtensorMap tmT64,
                     const __grid_constant__ CUtensorMap tmT256, const GemmArgs a,
                     const Tile *__restrict__ tiles, const int32_t *__restrict__ ntiles,
                     int32_t *__restrict__ redo) {
+  using P = Plan<TN, S8, S16>;
+  constexpr int W8 = P::W8, W16 = P::W16, ST8 = P::ST8, ST16 = P::ST16;
+  constexpr int OFF_F16 = P::OFF_F16, OFF_I8 = P::OFF_I8, OFF_BAR = P::OFF_BAR;
+  constexpr int B_S8_FULL = P::B_S8_FULL, B_S8_EMPTY = P::B_S8_EMPTY, B_F16_FULL = P::B_F16_FULL,
+                B_F16_EMPTY = P::B_F16_EMPTY, B_ACC_FULL = P::B_ACC_FULL,
+                B_ACC_EMPTY = P::B_ACC_EMPTY, B_NORM_READY = P::B_NORM_READY,
+                B_NORM_FREE = P::B_NORM_FREE, B_NORM_READ = P::B_NORM_READ,
+                B_MMA_DONE = P::B_MMA_DONE;
+  constexpr int OFF_NORM = P::OFF_NORM, OFF_TMEM = P::OFF_TMEM, OFF_ABORT = P::OFF_ABORT;
+  constexpr int NJT = P::NJT;
   extern __shared__ uint8_t smem_raw[];
   const int NB = int(a.N / WM);
   const int items = ntiles[0] * NB;
@@ -112,7 +133,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   };
   // token box height for a tile of `rows` tokens, and the MMA's N
   auto nmma_of = [](int rows) { return (rows + 15) & ~15; };
-  auto box_of = [](int nmma) { return nmma <= 16 ? 16 : (nmma <= 64 ? 64 : 256); };
+  auto box_of = [](int nmma) { return nmma <= 16 ? 16 : (nmma <= 64 || TN <= 64 ? 64 : 256); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -187,7 +208,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const Tile tl = tiles[it / NB];
       const int box = box_of(nmma_of(tl.rows));
       const int tchunks = box * 4;  // 16-byte pieces of the token tile
-      int nrm[6] = {0, 0, 0, 0, 0, 0};
+      int nrm[2 + NJT];
+#pragma unroll
+      for (int j = 0; j < 2 + NJT; ++j) nrm[j] = 0;
       for (int i = 0; i < KT; ++i, ++g) {
         const int s8 = g % S8, s16 = g % S16;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S8_FULL + s8), (g / S8) & 1, abort_flag))) {
@@ -196,9 +219,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           break;
         }
         const uint8_t *src = sm + OFF_I8 + s8 * ST8;
-        uint4 v[6];
+        uint4 v[2 + NJT];
 #pragma unroll
-        for (int j = 0; j < 6; ++j) {
+        for (int j = 0; j < 2 + NJT; ++j) {
           const int c = (j < 2 ? j : j - 2) * NCONV + t;
           v[j] = (j < 2 || c < tchunks)
                      ? *reinterpret_cast<const uint4 *>(src + (j < 2 ? 0 : W8) + c * 16)
@@ -214,7 +237,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         uint8_t *dst = sm + OFF_F16 + s16 * ST16;
 #pragma unroll
-        for (int j = 0; j < 6; ++j) {
+        for (int j = 0; j < 2 + NJT; ++j) {
           const int c = (j < 2 ? j : j - 2) * NCONV + t;
           if (j < 2 || c < tchunks) {
             const int row = c >> 2;
@@ -230,7 +253,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // squared norms: the 4 lanes 4m..4m+3 hold the 4 pieces of one row
       int wmax = 0, tmax = 0;
 #pragma unroll
-      for (int j = 0; j < 6; ++j) {
+      for (int j = 0; j < 2 + NJT; ++j) {
         int n2 = nrm[j];
         n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
         n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
@@ -336,25 +359,42 @@ bool gemm_tc2_supported(const GemmArgs &a) {
          a.R < (int64_t(1) << 31) && tma_available();
 }
 
-int launch_gemm_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
-                    int32_t *redo, cudaStream_t st) {
-  if (max_tiles <= 0) return WQ_OK;
+// Token-tile height the engine uses for this launch: 64 when experts hold few
+// rows on average (decode-like), else 256.
+int gemm_tc2_tile_rows(const GemmArgs &a) {
+  const int64_t rows = a.masked_m ? int64_t(a.E) * a.Mmax : a.R;
+  return rows <= int64_t(64) * a.E ? 64 : 256;
+}
+
+template <int TN, int S8, int S16>
+int launch_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
+               int32_t *redo, cudaStream_t st) {
+  using P = Plan<TN, S8, S16>;
   CUtensorMap mW, m16, m64, m256;
   if (!make_tma_2d_u8(&mW, a.W, int64_t(a.E) * a.N, a.K, BK, WM) ||
       !make_tma_2d_u8(&m16, a.A, a.R, a.K, BK, 16) || !make_tma_2d_u8(&m64, a.A, a.R, a.K, BK, 64) ||
-      !make_tma_2d_u8(&m256, a.A, a.R, a.K, BK, 256))
+      !make_tma_2d_u8(&m256, a.A, a.R, a.K, BK, TN > 64 ? 256 : 64))
     return WQ_ERR_LAUNCH;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(gemm_tc2_kernel<TN, S8, S16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES) != cudaSuccess)
       return WQ_ERR_LAUNCH;
     attr = true;
   }
   const int64_t max_items = int64_t(max_tiles) * (a.N / WM);
   const int grid = int(max_items < num_sms() ? max_items : num_sms());
-  gemm_tc2_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(mW, m16, m64, m256, a, tiles, ntiles, redo);
+  gemm_tc2_kernel<TN, S8, S16><<<grid, NTHREADS, P::SMEM_BYTES, st>>>(mW, m16, m64, m256, a, tiles,
+                                                                      ntiles, redo);
   return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+}
+
+// `tiles` must be built with gemm_tc2_tile_rows(a) rows per tile.
+int launch_gemm_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
+                    int32_t *redo, cudaStream_t st) {
+  if (max_tiles <= 0) return WQ_OK;
+  if (gemm_tc2_tile_rows(a) == 64) return launch_tc2<64, 8, 4>(a, tiles, ntiles, max_tiles, redo, st);
+  return launch_tc2<256, 3, 3>(a, tiles, ntiles, max_tiles, redo, st);
 }
 
 }  // namespace wq
