@@ -22,7 +22,8 @@
 // and [256,512)) let the epilogue of one item overlap the MMAs of the next.
 //   warp 0      TMA producer (weights 128 x 64, tokens box x 64 int8)
 //   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warps 2-9   converters: int8 -> fp16 (128-byte swizzled K-major) + norms
+//   warps 2-9   converters (two groups taking alternate K stages): int8 ->
+//               fp16 (128-byte swizzled K-major) + squared row norms
 //   warps 10-13 epilogue: dequant, bf16, coalesced stores (32 channels/warp)
 // Every wait is bounded (1 s); on expiry the kernel records WQ_ERR_TIMEOUT,
 // waits (bounded) for its own copies and MMAs, frees tensor memory and exits.
@@ -35,7 +36,8 @@ using namespace tc;
 
 constexpr int WM = 128, BK = 64;
 constexpr int NTHREADS = 448;
-constexpr int NCONV = 256;  // converter threads
+constexpr int NCONV = 256;  // converter threads: two groups of 128
+constexpr int GCONV = 128;  // threads of one converter group (its stages alternate with the other's)
 
 // Shared-memory plan of one instantiation: TN = most tokens per item (MMA N),
 // S8 / S16 = depths of the int8 staging ring and of the fp16 ring.  Large
@@ -57,12 +59,14 @@ struct Plan {
       B_NORM_FREE = B_ACC_FULL + 6,                                                // [2]
       B_NORM_READ = B_ACC_FULL + 8,                                                // [2]
       B_MMA_DONE = B_ACC_FULL + 10, NBAR = B_ACC_FULL + 11;
-  static constexpr int OFF_NORM = OFF_BAR + NBAR * 8;  // int32 [2 buffers][weights, tokens]
-  static constexpr int OFF_TMEM = OFF_NORM + 16;
+  // int32 [2 buffers][2 converter groups][weights, tokens]
+  static constexpr int OFF_NORM = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_TMEM = OFF_NORM + 32;
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
-  static constexpr int NJT = TN * 4 / NCONV;  // token 16-byte pieces per converter thread
-  static_assert(NJT >= 1 && TN * 4 == NJT * NCONV, "token tile must fill the converter threads");
+  static constexpr int NJW = WM * 4 / GCONV;  // weight 16-byte pieces per converter thread
+  static constexpr int NJT = TN * 4 / GCONV;  // token 16-byte pieces per converter thread
+  static_assert(NJT >= 1 && TN * 4 == NJT * GCONV, "token tile must fill a converter group");
   static_assert(SMEM_BYTES <= 232448, "shared memory plan too large");
 };
 
@@ -84,7 +88,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 B_NORM_FREE = P::B_NORM_FREE, B_NORM_READ = P::B_NORM_READ,
                 B_MMA_DONE = P::B_MMA_DONE;
   constexpr int OFF_NORM = P::OFF_NORM, OFF_TMEM = P::OFF_TMEM, OFF_ABORT = P::OFF_ABORT;
-  constexpr int NJT = P::NJT;
+  constexpr int NJW = P::NJW, NJT = P::NJT;
   extern __shared__ uint8_t smem_raw[];
   const int NB = int(a.N / WM);
   const int items = ntiles[0] * NB;
@@ -102,13 +106,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < 4; ++i) norm[i] = 0;
+    for (int i = 0; i < 8; ++i) norm[i] = 0;
     for (int s = 0; s < S8; ++s) {
       mbar_init(bar(B_S8_FULL + s), 1);
-      mbar_init(bar(B_S8_EMPTY + s), NCONV / 32);
+      mbar_init(bar(B_S8_EMPTY + s), GCONV / 32);
     }
     for (int s = 0; s < S16; ++s) {
-      mbar_init(bar(B_F16_FULL + s), NCONV / 32);
+      mbar_init(bar(B_F16_FULL + s), GCONV / 32);
       mbar_init(bar(B_F16_EMPTY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -201,17 +205,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp < 2 + NCONV / 32) {
     // ------------------------------------------------------------ converters
-    const int t = threadIdx.x - 64;  // 0..255
-    int g = 0, ii = 0;
+    // Two groups of four warps; group `grp` widens the stages of parity grp
+    // (K / 64 is even), so two stages are in flight through the converters.
+    const int grp = (warp - 2) >> 2;
+    const int t = threadIdx.x - 64 - grp * GCONV;  // 0..127 within the group
+    int gbase = 0, ii = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++ii) {
+    for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++ii, gbase += KT) {
       const Tile tl = tiles[it / NB];
       const int box = box_of(nmma_of(tl.rows));
       const int tchunks = box * 4;  // 16-byte pieces of the token tile
-      int nrm[2 + NJT];
+      int nrm[NJW + NJT];
 #pragma unroll
-      for (int j = 0; j < 2 + NJT; ++j) nrm[j] = 0;
-      for (int i = 0; i < KT; ++i, ++g) {
+      for (int j = 0; j < NJW + NJT; ++j) nrm[j] = 0;
+      for (int i = grp; i < KT; i += 2) {
+        const int g = gbase + i;
         const int s8 = g % S8, s16 = g % S16;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S8_FULL + s8), (g / S8) & 1, abort_flag))) {
           fail();
@@ -219,12 +227,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           break;
         }
         const uint8_t *src = sm + OFF_I8 + s8 * ST8;
-        uint4 v[2 + NJT];
+        uint4 v[NJW + NJT];
 #pragma unroll
-        for (int j = 0; j < 2 + NJT; ++j) {
-          const int c = (j < 2 ? j : j - 2) * NCONV + t;
-          v[j] = (j < 2 || c < tchunks)
-                     ? *reinterpret_cast<const uint4 *>(src + (j < 2 ? 0 : W8) + c * 16)
+        for (int j = 0; j < NJW + NJT; ++j) {
+          const int c = (j < NJW ? j : j - NJW) * GCONV + t;
+          v[j] = (j < NJW || c < tchunks)
+                     ? *reinterpret_cast<const uint4 *>(src + (j < NJW ? 0 : W8) + c * 16)
                      : make_uint4(0, 0, 0, 0);
         }
         __syncwarp();
@@ -237,11 +245,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         uint8_t *dst = sm + OFF_F16 + s16 * ST16;
 #pragma unroll
-        for (int j = 0; j < 2 + NJT; ++j) {
-          const int c = (j < 2 ? j : j - 2) * NCONV + t;
-          if (j < 2 || c < tchunks) {
+        for (int j = 0; j < NJW + NJT; ++j) {
+          const int c = (j < NJW ? j : j - NJW) * GCONV + t;
+          if (j < NJW || c < tchunks) {
             const int row = c >> 2;
-            store_f16_row_piece(dst + (j < 2 ? 0 : W16) + row * 128, row, c & 3, v[j]);
+            store_f16_row_piece(dst + (j < NJW ? 0 : W16) + row * 128, row, c & 3, v[j]);
             nrm[j] = sq4(v[j].w, sq4(v[j].z, sq4(v[j].y, sq4(v[j].x, nrm[j]))));
           }
         }
@@ -250,17 +258,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) mbar_arrive(bar(B_F16_FULL + s16));
       }
       if (!ok) break;
-      // squared norms: the 4 lanes 4m..4m+3 hold the 4 pieces of one row
+      // squared norms over this group's stages: the 4 lanes 4m..4m+3 hold the
+      // 4 pieces of one row; a row's full norm is at most the sum of the two
+      // groups' largest partial norms, which is what the epilogue checks
       int wmax = 0, tmax = 0;
 #pragma unroll
-      for (int j = 0; j < 2 + NJT; ++j) {
+      for (int j = 0; j < NJW + NJT; ++j) {
         int n2 = nrm[j];
         n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
         n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
-        if (j < 2) {
+        if (j < NJW) {
           wmax = max(wmax, n2);
         } else {
-          const int row = ((j - 2) * NCONV + t) >> 2;
+          const int row = ((j - NJW) * GCONV + t) >> 2;
           if (row < tl.rows) tmax = max(tmax, n2);
         }
       }
@@ -276,8 +286,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         break;
       }
       if (lane == 0) {
-        atomicMax(const_cast<int *>(norm + 2 * b), wmax);
-        atomicMax(const_cast<int *>(norm + 2 * b + 1), tmax);
+        atomicMax(const_cast<int *>(norm + 4 * b + 2 * grp), wmax);
+        atomicMax(const_cast<int *>(norm + 4 * b + 2 * grp + 1), tmax);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_NORM_READY + b));
@@ -296,15 +306,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         break;
       }
       tc_fence_after();
-      const long long nw = norm[2 * b], nt = norm[2 * b + 1];
+      const long long nw = (long long)norm[4 * b] + norm[4 * b + 2];
+      const long long nt = (long long)norm[4 * b + 1] + norm[4 * b + 3];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_NORM_READ + b));
       if (warp == 10 && lane == 0) {
         // once all four epilogue warps have read the norms, clear them for the
         // item after next and hand the slots back to the converters
         if (mbar_wait(bar(B_NORM_READ + b), par, abort_flag)) {
-          norm[2 * b] = 0;
-          norm[2 * b + 1] = 0;
+          for (int i = 0; i < 4; ++i) norm[4 * b + i] = 0;
           mbar_arrive(bar(B_NORM_FREE + b));
         } else {
           fail();
