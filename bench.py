@@ -112,9 +112,10 @@ class Layer:
     """Preallocated buffers and the staged C-ABI calls of one layer step."""
 
     STAGES = ["route", "quant", "align", "permute", "gemm1", "silu_mul_quant", "gemm2", "combine"]
-    # kernels per stage (align: histogram, scan, scatter; GEMMs: tile list + GEMM)
-    KERNELS = {"route": 1, "quant": 1, "align": 3, "permute": 1, "gemm1": 2, "silu_mul_quant": 1,
-               "gemm2": 2, "combine": 1}
+    # kernels per stage (align: histogram, scan, scatter; a GEMM: tile list, engine, tile
+    # list and gated exact recompute of the fast engines)
+    KERNELS = {"route": 1, "quant": 1, "align": 3, "permute": 1, "gemm1": 4, "silu_mul_quant": 1,
+               "gemm2": 4, "combine": 1}
 
     def __init__(self, wq, cfg, dev, weights):
         self.wq, self.lib, self.cfg, self.dev = wq, wq.lib(), cfg, dev
@@ -130,9 +131,15 @@ class Layer:
         self.sp, self.p2r = e(R, dt=torch.int32), e(R, dt=torch.int32)
         self.aws_n = self.lib.wq_moe_align_workspace_size(T, k, E)
         self.aws = e(max(self.aws_n, 1), dt=torch.uint8)
-        self.A, self.sa = e(R, H, dt=torch.int8), e(R * self.g1, dt=torch.float32)
+        # the one-call layer's choice: fp16-stored codes for the channel-wise
+        # int32 layer when both GEMM widths are multiples of 256
+        self.f16 = (cfg.scheme == "channel" and cfg.acc == "i32" and (2 * I) % 256 == 0
+                    and H % 256 == 0 and R > 64 * E)
+        cdt = torch.float16 if self.f16 else torch.int8
+        self.A, self.sa = e(R, H, dt=cdt), e(R * self.g1, dt=torch.float32)
+        self.anorm, self.hnorm = e(R, dt=torch.int32), e(R, dt=torch.int32)
         self.gu = e(R, 2 * I, dt=torch.bfloat16)
-        self.hq, self.sh = e(R, I, dt=torch.int8), e(R * self.g2, dt=torch.float32)
+        self.hq, self.sh = e(R, I, dt=cdt), e(R * self.g2, dt=torch.float32)
         self.y = e(R, H, dt=torch.bfloat16)
         self.out = e(T, H, dt=torch.bfloat16)
         self.gws_n = self.lib.wq_grouped_gemm_workspace_size(R, E)
@@ -162,19 +169,35 @@ class Layer:
         ok(L.wq_moe_align(P(self.ids), T, k, E, 1, P(self.counts), P(self.offsets), P(self.sp),
                           P(self.p2r), P(self.aws), self.aws_n, P(self.status), st), "align")
         rec(3)
-        ok(L.wq_moe_permute(P(self.q), P(self.s), self.g1, T, k, H, P(self.sp), R, P(self.A),
-                            P(self.sa), st), "permute")
-        rec(4)
-        ok(L.wq_grouped_gemm_w8a8(P(self.A), P(self.sa), P(self.W13), P(self.S13), P(self.offsets),
-                                  E, R, 2 * I, H, sc, ac, 0, P(self.gu), P(self.gws), self.gws_n,
-                                  P(self.status), st), "gemm1")
-        rec(5)
-        ok(L.wq_silu_mul_quant(P(self.gu), R, I, 128 if c.scheme == "block" else 0, P(self.hq),
-                               P(self.sh), st), "silu_mul_quant")
-        rec(6)
-        ok(L.wq_grouped_gemm_w8a8(P(self.hq), P(self.sh), P(self.W2), P(self.S2), P(self.offsets),
-                                  E, R, H, I, sc, ac, 0, P(self.y), P(self.gws), self.gws_n,
-                                  P(self.status), st), "gemm2")
+        if self.f16:
+            ok(L.wq_moe_permute_f16(P(self.q), P(self.s), 1, T, k, H, P(self.sp), R, P(self.A),
+                                    P(self.sa), P(self.anorm), st), "permute")
+            rec(4)
+            ok(L.wq_grouped_gemm_w8a8_f16codes(P(self.A), P(self.anorm), P(self.sa), P(self.W13),
+                                               P(self.S13), P(self.offsets), E, R, 2 * I, H, 0,
+                                               P(self.gu), P(self.gws), self.gws_n, P(self.status),
+                                               st), "gemm1")
+            rec(5)
+            ok(L.wq_silu_mul_quant_f16(P(self.gu), R, I, P(self.hq), P(self.sh), P(self.hnorm), st),
+               "silu_mul_quant")
+            rec(6)
+            ok(L.wq_grouped_gemm_w8a8_f16codes(P(self.hq), P(self.hnorm), P(self.sh), P(self.W2),
+                                               P(self.S2), P(self.offsets), E, R, H, I, 0, P(self.y),
+                                               P(self.gws), self.gws_n, P(self.status), st), "gemm2")
+        else:
+            ok(L.wq_moe_permute(P(self.q), P(self.s), self.g1, T, k, H, P(self.sp), R, P(self.A),
+                                P(self.sa), st), "permute")
+            rec(4)
+            ok(L.wq_grouped_gemm_w8a8(P(self.A), P(self.sa), P(self.W13), P(self.S13),
+                                      P(self.offsets), E, R, 2 * I, H, sc, ac, 0, P(self.gu),
+                                      P(self.gws), self.gws_n, P(self.status), st), "gemm1")
+            rec(5)
+            ok(L.wq_silu_mul_quant(P(self.gu), R, I, 128 if c.scheme == "block" else 0, P(self.hq),
+                                   P(self.sh), st), "silu_mul_quant")
+            rec(6)
+            ok(L.wq_grouped_gemm_w8a8(P(self.hq), P(self.sh), P(self.W2), P(self.S2),
+                                      P(self.offsets), E, R, H, I, sc, ac, 0, P(self.y),
+                                      P(self.gws), self.gws_n, P(self.status), st), "gemm2")
         rec(7)
         ok(L.wq_moe_combine(P(self.y), P(self.p2r), P(self.w), T, k, H, P(self.out), st), "combine")
         rec(8)

@@ -283,3 +283,57 @@ def test_layer_forward_masked():
     yb = bits(y)
     assert_bf16_equal(yb[valid], ref[valid], "masked layer")
     assert np.all(O.bf16_to_f32(yb[~valid]) == 5.0)
+
+
+# ---------------------------------------------------------------- fp16-stored codes
+def test_moe_permute_f16():
+    T, k, E, K = 200, 8, 64, 7168
+    rng = np.random.default_rng(21)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    q = rng.integers(-127, 128, (T, K), dtype=np.int8)
+    s = rng.random(T).astype(np.float32)
+    _, _, spo, _ = O.moe_align(ids, E, 4)
+    A16, sa, n2 = wq.moe_permute_f16(torch.from_numpy(q).to(DEV), torch.from_numpy(s).to(DEV),
+                                     torch.from_numpy(spo).to(DEV), k)
+    Ao, sao = O.moe_permute(q, s, spo, k)
+    assert np.array_equal(np_(A16).astype(np.int32), Ao.astype(np.int32))
+    assert np.array_equal(np_(sa), sao)
+    assert np.array_equal(np_(n2), (Ao.astype(np.int64) ** 2).sum(1))
+
+
+def test_silu_mul_quant_f16():
+    R, I = 70, 2048
+    g = torch.Generator().manual_seed(22)
+    gu = (torch.randn(R, 2 * I, generator=g) * 4).to(torch.bfloat16)
+    hq16, sh, n2 = wq.silu_mul_quant_f16(gu.to(DEV))
+    hqo, sho = O.silu_mul_quant(bits(gu), I, 0)
+    assert np.array_equal(np_(hq16).astype(np.int32), hqo.astype(np.int32))
+    assert np.array_equal(np_(sh), sho)
+    assert np.array_equal(np_(n2), (hqo.astype(np.int64) ** 2).sum(1))
+
+
+@pytest.mark.parametrize("extreme", [False, True])
+def test_grouped_gemm_f16codes(extreme):
+    """The CTA-pair engine (codes in +-40: the exactness check passes) and its
+    exact recompute (all-127 rows: the check fails), int32 and bf16 outputs."""
+    E, counts, N, K = 5, [3, 0, 270, 1, 513], 512, 2048
+    rng = np.random.default_rng(23)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    R = int(offs[-1])
+    lim = 127 if extreme else 40
+    A = rng.integers(-lim, lim + 1, (R, K), dtype=np.int8)
+    W = rng.integers(-lim, lim + 1, (E, N, K), dtype=np.int8)
+    if extreme:
+        A[:5] = 127
+        W[4, :3] = -127
+    sa = (rng.random(R) * 0.05).astype(np.float32)
+    sw = (rng.random((E, N)) * 1e-3).astype(np.float32)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    A16 = t(A).to(torch.float16)
+    n2 = t((A.astype(np.int64) ** 2).sum(1).astype(np.int32))
+    st = wq.new_status()
+    C = wq.grouped_gemm_w8a8_f16codes(A16, n2, t(sa), t(W), t(sw), t(offs), out_type="i32", status=st)
+    out = wq.grouped_gemm_w8a8_f16codes(A16, n2, t(sa), t(W), t(sw), t(offs), status=st)
+    assert int(st.item()) == 0
+    assert np.array_equal(np_(C), O.grouped_gemm_i32(A, W, offs))
+    assert_bf16_equal(bits(out), O.grouped_gemm_w8a8(A, sa, W, sw, offs), "f16 codes gemm")

@@ -45,6 +45,9 @@ _SIGS = {
     "wq_grouped_gemm_workspace_size": (_S, [_L, _I]),
     "wq_grouped_gemm_w8a8": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
     "wq_grouped_gemm_w8a8_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _I, _P, _P, _P]),
+    "wq_moe_permute_f16": (_I, [_P, _P, _I, _I, _I, _L, _P, _L, _P, _P, _P, _P]),
+    "wq_silu_mul_quant_f16": (_I, [_P, _L, _L, _P, _P, _P, _P]),
+    "wq_grouped_gemm_w8a8_f16codes": (_I, [_P, _P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _P, _P, _S, _P, _P]),
     "wq_grouped_gemm_masked_workspace_size": (_S, [_I, _I]),
     "wq_grouped_gemm_w8a8_masked": (_I, [_P, _P, _P, _I, _I, _P, _P, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
     "wq_silu_mul_quant": (_I, [_P, _L, _L, _I, _P, _P, _P]),
@@ -197,6 +200,58 @@ def moe_permute(q, s, sorted_pair, k):
     _check(lib().wq_moe_permute(_ptr(q), _ptr(s), groups, T, k, K, _ptr(sorted_pair), R, _ptr(A),
                                 _ptr(sa), _stream()), "wq_moe_permute")
     return A, sa
+
+
+def moe_permute_f16(q, s, sorted_pair, k):
+    """Permute into fp16-stored codes; returns (A16 as torch.float16, sa, norm2)."""
+    _dev(q, torch.int8, "q")
+    _dev(s, torch.float32, "s")
+    _dev(sorted_pair, torch.int32, "sorted_pair")
+    T, K = q.shape
+    groups = 1 if s.dim() == 1 else s.shape[1]
+    R = sorted_pair.numel()
+    A16 = torch.empty(R, K, dtype=torch.float16, device=q.device)
+    sa = torch.empty((R,) if s.dim() == 1 else (R, groups), dtype=torch.float32, device=q.device)
+    n2 = torch.empty(R, dtype=torch.int32, device=q.device)
+    _check(lib().wq_moe_permute_f16(_ptr(q), _ptr(s), groups, T, k, K, _ptr(sorted_pair), R,
+                                    _ptr(A16), _ptr(sa), _ptr(n2), _stream()), "wq_moe_permute_f16")
+    return A16, sa, n2
+
+
+def silu_mul_quant_f16(gu):
+    """SiLU-mul + per-row re-quantization into fp16-stored codes: (hq16, sh, norm2)."""
+    _dev(gu, torch.bfloat16, "gu")
+    R, I2 = gu.shape
+    I = I2 // 2
+    hq = torch.empty(R, I, dtype=torch.float16, device=gu.device)
+    sh = torch.empty(R, dtype=torch.float32, device=gu.device)
+    n2 = torch.empty(R, dtype=torch.int32, device=gu.device)
+    _check(lib().wq_silu_mul_quant_f16(_ptr(gu), R, I, _ptr(hq), _ptr(sh), _ptr(n2), _stream()),
+           "wq_silu_mul_quant_f16")
+    return hq, sh, n2
+
+
+def grouped_gemm_w8a8_f16codes(A16, a_norm2, sa, W, sw, offsets, out_type="bf16", out=None,
+                               status=None):
+    _dev(A16, torch.float16, "A16")
+    _dev(a_norm2, torch.int32, "a_norm2")
+    _dev(sa, torch.float32, "sa")
+    _dev(W, torch.int8, "W")
+    _dev(sw, torch.float32, "sw")
+    _dev(offsets, torch.int32, "offsets")
+    R, K = A16.shape
+    E, N, _ = W.shape
+    if out is None:
+        out = torch.empty(R, N, dtype=torch.bfloat16 if out_type == "bf16" else torch.int32,
+                          device=A16.device)
+    nws = lib().wq_grouped_gemm_workspace_size(R, E)
+    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=A16.device)
+    st = status if status is not None else new_status(A16.device)
+    _check(lib().wq_grouped_gemm_w8a8_f16codes(_ptr(A16), _ptr(a_norm2), _ptr(sa), _ptr(W), _ptr(sw),
+                                               _ptr(offsets), E, R, N, K, OUT[out_type], _ptr(out),
+                                               _ptr(ws), nws, _ptr(st), _stream()),
+           "wq_grouped_gemm_w8a8_f16codes")
+    return out
 
 
 # ---------------------------------------------------------------- GEMMs

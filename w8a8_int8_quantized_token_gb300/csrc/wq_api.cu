@@ -16,6 +16,9 @@ int launch_gemm_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles,
                     int32_t *redo, cudaStream_t st);
 bool gemm_tc2_supported(const GemmArgs &a);
 int gemm_tc2_tile_rows(const GemmArgs &a);
+int launch_gemm_tc4(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
+                    int32_t *redo, cudaStream_t st);
+bool gemm_tc4_supported(const GemmArgs &a);
 }  // namespace wq
 
 using namespace wq;
@@ -108,6 +111,17 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
   const bool masked = a.masked_m != nullptr;
   GemmWs w = carve_gemm_ws(a.ws, a.R, a.E, a.Mmax, masked);
   const int32_t *gate = nullptr;
+  if (a.A16 != nullptr) {
+    // fp16-stored codes: the CTA-pair engine, then the CUDA-core engine reading
+    // fp16 codes as its exact recompute (it exits at once when *redo == 0)
+    if (!gemm_tc4_supported(a)) return WQ_ERR_UNSUPPORTED;
+    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 256, a.R, w.t256, w.n256,
+                              w.redo, st));
+    WQ_TRY(launch_gemm_tc4(a, w.t256, w.n256, int(w.m256), w.redo, st));
+    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 64, a.R, w.t64, w.n64, nullptr,
+                              st));
+    return launch_gemm_simt(a, w.t64, w.n64, int(w.m64), w.redo, st);
+  }
   if (gemm_tc2_supported(a)) {
     // fast int32 engine; it raises *redo for any tile whose single-pass
     // float32 sums it cannot prove exact, and the chunked engine below then
@@ -255,7 +269,46 @@ int wq_grouped_gemm_w8a8(const int8_t *A, const float *sa, const int8_t *W, cons
   if (R >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;
   if (ws_bytes < gemm_ws_bytes(R, E, 0, false) || !ws) return WQ_ERR_WORKSPACE;
   WQ_TRY(check_device());
-  GemmArgs a{A, sa, W, sw, offsets, nullptr, 0, E, R, N, K, scheme, acc, out_type, out, ws, status};
+  GemmArgs a{A, nullptr, nullptr, sa, W, sw, offsets, nullptr, 0, E, R, N, K, scheme, acc, out_type, out, ws, status};
+  return launch_grouped_gemm(a, stream);
+}
+
+int wq_moe_permute_f16(const int8_t *q, const float *s, int groups, int T, int k, int64_t K,
+                       const int32_t *sorted_pair, int64_t R, uint16_t *A16, float *sa,
+                       int32_t *norm2, wq_stream_t stream) {
+  if (groups < 1 || T < 0 || k < 1 || K < 0 || R < 0) return WQ_ERR_INVALID_ARG;
+  if (R == 0) return WQ_OK;
+  if (!sorted_pair || !A16 || !sa || !norm2 || (T > 0 && (!q || !s))) return WQ_ERR_INVALID_ARG;
+  if (K % 16 || !al16(q) || !al16(A16)) return WQ_ERR_UNSUPPORTED;
+  WQ_TRY(check_device());
+  return launch_permute_f16(q, s, groups, k, K, sorted_pair, R, A16, sa, norm2, stream);
+}
+
+int wq_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, uint16_t *hq16, float *sh,
+                          int32_t *norm2, wq_stream_t stream) {
+  if (R < 0 || I < 0) return WQ_ERR_INVALID_ARG;
+  if (R == 0 || I == 0) return WQ_OK;
+  if (!gu || !hq16 || !sh || !norm2) return WQ_ERR_INVALID_ARG;
+  if (I % 8 || !al16(gu) || !al16(hq16)) return WQ_ERR_UNSUPPORTED;
+  WQ_TRY(check_device());
+  return launch_silu_mul_quant_f16(gu, R, I, nullptr, 0, hq16, sh, norm2, stream);
+}
+
+int wq_grouped_gemm_w8a8_f16codes(const uint16_t *A16, const int32_t *a_norm2, const float *sa,
+                                  const int8_t *W, const float *sw, const int32_t *offsets, int E,
+                                  int64_t R, int64_t N, int64_t K, int out_type, void *out,
+                                  void *ws, size_t ws_bytes, int32_t *status,
+                                  wq_stream_t stream) {
+  if (R < 0 || E > 4096) return WQ_ERR_INVALID_ARG;
+  if (R == 0) return WQ_OK;
+  WQ_TRY(check_gemm_common(W, sw, E, N, K, WQ_SCHEME_CHANNEL, WQ_ACC_I32, out_type, out));
+  if (!A16 || !a_norm2 || !sa || !offsets) return WQ_ERR_INVALID_ARG;
+  if (!al16(A16) || N % 256 || K > 65536) return WQ_ERR_UNSUPPORTED;
+  if (R >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;
+  if (ws_bytes < gemm_ws_bytes(R, E, 0, false) || !ws) return WQ_ERR_WORKSPACE;
+  WQ_TRY(check_device());
+  GemmArgs a{nullptr, A16, a_norm2, sa, W, sw, offsets, nullptr, 0, E, R, N, K, WQ_SCHEME_CHANNEL,
+             WQ_ACC_I32, out_type, out, ws, status};
   return launch_grouped_gemm(a, stream);
 }
 
@@ -277,7 +330,7 @@ int wq_grouped_gemm_w8a8_masked(const int8_t *A, const float *sa, const int32_t 
   if (R >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;
   if (ws_bytes < gemm_ws_bytes(R, E, Mmax, true) || !ws) return WQ_ERR_WORKSPACE;
   WQ_TRY(check_device());
-  GemmArgs a{A, sa, W, sw, nullptr, masked_m, Mmax, E, R, N, K, scheme, acc, out_type, out, ws,
+  GemmArgs a{A, nullptr, nullptr, sa, W, sw, nullptr, masked_m, Mmax, E, R, N, K, scheme, acc, out_type, out, ws,
              status};
   return launch_grouped_gemm(a, stream);
 }
@@ -315,11 +368,13 @@ struct FwdBufs {
   float *s;
   int32_t *counts, *offsets, *sorted_pair, *pair_to_row;
   void *align_ws;
-  int8_t *A;
+  int8_t *A;  // int8 codes, or fp16 codes (the buffer holds either)
   float *sa;
+  int32_t *anorm;
   uint16_t *gu;
-  int8_t *hq;
+  int8_t *hq;  // int8 codes, or fp16 codes
   float *sh;
+  int32_t *hnorm;
   uint16_t *y;
   void *gemm_ws;
   size_t gemm_ws_bytes;
@@ -340,11 +395,13 @@ size_t carve_forward(void *ws, int T, int H, int I, int E, int k, int scheme, Fw
   t.sorted_pair = c.take<int32_t>(R);
   t.pair_to_row = c.take<int32_t>(R);
   t.align_ws = c.take<char>(align_ws_bytes(T, k, E));
-  t.A = c.take<int8_t>(size_t(R) * H);
+  t.A = c.take<int8_t>(size_t(R) * H * 2);
   t.sa = c.take<float>(size_t(R) * g1);
+  t.anorm = c.take<int32_t>(size_t(R));
   t.gu = c.take<uint16_t>(size_t(R) * 2 * I);
-  t.hq = c.take<int8_t>(size_t(R) * I);
+  t.hq = c.take<int8_t>(size_t(R) * I * 2);
   t.sh = c.take<float>(size_t(R) * g2);
+  t.hnorm = c.take<int32_t>(size_t(R));
   t.y = c.take<uint16_t>(size_t(R) * H);
   t.gemm_ws_bytes = gemm_ws_bytes(R, E, 0, false);
   t.gemm_ws = c.take<char>(t.gemm_ws_bytes);
@@ -371,12 +428,34 @@ int run_forward(const uint16_t *x, const float *logits, const int8_t *W13, const
   WQ_TRY(launch_quant_rows(x, T, H, H, blk ? 128 : 0, b.q, b.s, st));
   WQ_TRY(launch_align(b.ids, T, k, E, 1, b.counts, b.offsets, b.sorted_pair, b.pair_to_row,
                       b.align_ws, status, st));
+  // channel-wise int32: activation codes travel as fp16 values with row norms
+  // (the CTA-pair GEMM engine); other modes and widths use int8 codes
+  GemmArgs probe{nullptr, reinterpret_cast<const uint16_t *>(b.A), b.anorm, b.sa, W13, sw13,
+                 b.offsets, nullptr, 0, E, R, int64_t(2) * I, H, scheme, acc, WQ_OUT_BF16, b.gu,
+                 b.gemm_ws, status};
+  // (with few rows per expert the GEMMs stream weights from HBM and the
+  // int8 path's 64-token engine with its deeper weight ring is faster)
+  const bool f16 = !blk && acc == WQ_ACC_I32 && (2 * I) % 256 == 0 && H % 256 == 0 &&
+                   R > int64_t(64) * E && gemm_tc4_supported(probe);
+  if (f16) {
+    uint16_t *A16 = reinterpret_cast<uint16_t *>(b.A);
+    uint16_t *hq16 = reinterpret_cast<uint16_t *>(b.hq);
+    WQ_TRY(launch_permute_f16(b.q, b.s, 1, k, H, b.sorted_pair, R, A16, b.sa, b.anorm, st));
+    GemmArgs f1{nullptr, A16, b.anorm, b.sa, W13, sw13, b.offsets, nullptr, 0, E, R,
+                int64_t(2) * I, H, scheme, acc, WQ_OUT_BF16, b.gu, b.gemm_ws, status};
+    WQ_TRY(launch_grouped_gemm(f1, st));
+    WQ_TRY(launch_silu_mul_quant_f16(b.gu, R, I, nullptr, 0, hq16, b.sh, b.hnorm, st));
+    GemmArgs f2{nullptr, hq16, b.hnorm, b.sh, W2, sw2, b.offsets, nullptr, 0, E, R, H, I, scheme,
+                acc, WQ_OUT_BF16, b.y, b.gemm_ws, status};
+    WQ_TRY(launch_grouped_gemm(f2, st));
+    return launch_combine(b.y, b.pair_to_row, b.w, T, k, H, out, st);
+  }
   WQ_TRY(launch_permute(b.q, b.s, blk ? H / 128 : 1, k, H, b.sorted_pair, R, b.A, b.sa, st));
-  GemmArgs g1{b.A, b.sa, W13, sw13, b.offsets, nullptr, 0, E, R, int64_t(2) * I, H, scheme, acc,
+  GemmArgs g1{b.A, nullptr, nullptr, b.sa, W13, sw13, b.offsets, nullptr, 0, E, R, int64_t(2) * I, H, scheme, acc,
               WQ_OUT_BF16, b.gu, b.gemm_ws, status};
   WQ_TRY(launch_grouped_gemm(g1, st));
   WQ_TRY(launch_silu_mul_quant(b.gu, R, I, blk ? 128 : 0, nullptr, 0, b.hq, b.sh, st));
-  GemmArgs g2{b.hq, b.sh, W2, sw2, b.offsets, nullptr, 0, E, R, H, I, scheme, acc,
+  GemmArgs g2{b.hq, nullptr, nullptr, b.sh, W2, sw2, b.offsets, nullptr, 0, E, R, H, I, scheme, acc,
               WQ_OUT_BF16, b.y, b.gemm_ws, status};
   WQ_TRY(launch_grouped_gemm(g2, st));
   return launch_combine(b.y, b.pair_to_row, b.w, T, k, H, out, st);
@@ -489,12 +568,12 @@ int wq_moe_forward_masked(const int8_t *a, const float *sa, const int32_t *maske
   if (!ws || !al16(ws) || ws_bytes < need) return WQ_ERR_WORKSPACE;
   WQ_TRY(check_device());
   const int64_t R = int64_t(E) * Mmax;
-  GemmArgs g1{a, sa, W13, sw13, nullptr, masked_m, Mmax, E, R, int64_t(2) * I, H, scheme, acc,
+  GemmArgs g1{a, nullptr, nullptr, sa, W13, sw13, nullptr, masked_m, Mmax, E, R, int64_t(2) * I, H, scheme, acc,
               WQ_OUT_BF16, gu, gws, status};
   WQ_TRY(launch_grouped_gemm(g1, stream));
   WQ_TRY(launch_silu_mul_quant(gu, R, I, scheme == WQ_SCHEME_BLOCK ? 128 : 0, masked_m, Mmax, hq,
                                sh, stream));
-  GemmArgs g2{hq, sh, W2, sw2, nullptr, masked_m, Mmax, E, R, H, I, scheme, acc, WQ_OUT_BF16, y,
+  GemmArgs g2{hq, nullptr, nullptr, sh, W2, sw2, nullptr, masked_m, Mmax, E, R, H, I, scheme, acc, WQ_OUT_BF16, y,
               gws, status};
   return launch_grouped_gemm(g2, stream);
 }

@@ -141,12 +141,20 @@ int launch_permute(const int8_t *q, const float *s, int groups, int k, int64_t K
 int launch_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group,
                           const int32_t *masked_m, int Mmax, int8_t *hq, float *sh,
                           cudaStream_t st);
+int launch_permute_f16(const int8_t *q, const float *s, int groups, int k, int64_t K,
+                       const int32_t *sorted_pair, int64_t R, uint16_t *A16, float *sa,
+                       int32_t *norm2, cudaStream_t st);
+int launch_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, const int32_t *masked_m,
+                              int Mmax, uint16_t *hq16, float *sh, int32_t *norm2,
+                              cudaStream_t st);
 int launch_combine(const uint16_t *y, const int32_t *pair_to_row, const float *w, int T, int k,
                    int64_t H, uint16_t *out, cudaStream_t st);
 
 // Grouped GEMM: segments come from offsets (contiguous) or masked_m (strided).
 struct GemmArgs {
-  const int8_t *A;
+  const int8_t *A;           // int8 codes [R][K], or nullptr when A16 is given
+  const uint16_t *A16;       // the same codes as fp16 values [R][K] (fast int32 engine)
+  const int32_t *a_norm2;    // squared L2 norm of each row of A16 (with A16)
   const float *sa;
   const int8_t *W;
   const float *sw;

@@ -3,6 +3,7 @@
 // re-quantization, and the weighted combine.  All are coalesced 16-byte
 // vector accesses with warp-shuffle reductions for the absolute maxima.
 #include "wq_common.cuh"
+#include "wq_tc.cuh"
 
 namespace wq {
 
@@ -252,6 +253,61 @@ __global__ void __launch_bounds__(128) permute_kernel(const int8_t *__restrict__
   for (int g = threadIdx.x; g < groups; g += blockDim.x) sa[r * groups + g] = s[tok * groups + g];
 }
 
+// Permute into fp16 codes: A16[r] holds the same integers as the int8 codes
+// (2 bytes each), plus the row's squared L2 norm (sum of code^2), the form the
+// fast int32 GEMM engine reads.  One CTA per destination row.
+__global__ void __launch_bounds__(128) permute_f16_kernel(const int8_t *__restrict__ q,
+                                                          const float *__restrict__ s, int groups,
+                                                          int k, int64_t K,
+                                                          const int32_t *__restrict__ sorted_pair,
+                                                          uint16_t *__restrict__ A16,
+                                                          float *__restrict__ sa,
+                                                          int32_t *__restrict__ norm2) {
+  __shared__ int red[4];
+  const int64_t r = blockIdx.x;
+  const int p = sorted_pair[r];
+  const int64_t nvec = K >> 4;  // 16 codes per piece
+  uint4 *dst = reinterpret_cast<uint4 *>(A16 + r * K);
+  if (p < 0) {
+    for (int64_t i = threadIdx.x; i < 2 * nvec; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
+    for (int g = threadIdx.x; g < groups; g += blockDim.x) sa[r * groups + g] = 0.0f;
+    if (threadIdx.x == 0) norm2[r] = 0;
+    return;
+  }
+  const int64_t tok = p / k;
+  const uint4 *src = reinterpret_cast<const uint4 *>(q + tok * K);
+  int acc = 0;
+  for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+    const uint4 v = __ldg(src + i);
+    uint4 o0, o1;
+    tc::s8x4_to_f16x4(v.x, o0.x, o0.y);
+    tc::s8x4_to_f16x4(v.y, o0.z, o0.w);
+    tc::s8x4_to_f16x4(v.z, o1.x, o1.y);
+    tc::s8x4_to_f16x4(v.w, o1.z, o1.w);
+    __stcs(dst + 2 * i, o0);
+    __stcs(dst + 2 * i + 1, o1);
+    acc = __dp4a(int(v.x), int(v.x), acc);
+    acc = __dp4a(int(v.y), int(v.y), acc);
+    acc = __dp4a(int(v.z), int(v.z), acc);
+    acc = __dp4a(int(v.w), int(v.w), acc);
+  }
+  for (int g = threadIdx.x; g < groups; g += blockDim.x) sa[r * groups + g] = s[tok * groups + g];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) norm2[r] = red[0] + red[1] + red[2] + red[3];
+}
+
+int launch_permute_f16(const int8_t *q, const float *s, int groups, int k, int64_t K,
+                       const int32_t *sorted_pair, int64_t R, uint16_t *A16, float *sa,
+                       int32_t *norm2, cudaStream_t st) {
+  if (R == 0) return WQ_OK;
+  if (R > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
+  permute_f16_kernel<<<unsigned(R), 128, 0, st>>>(q, s, groups, k, K, sorted_pair, A16, sa, norm2);
+  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+}
+
 int launch_permute(const int8_t *q, const float *s, int groups, int k, int64_t K,
                    const int32_t *sorted_pair, int64_t R, int8_t *A, float *sa, cudaStream_t st) {
   if (R == 0) return WQ_OK;
@@ -327,6 +383,94 @@ __global__ void __launch_bounds__(1024) silu_mul_quant_kernel(
       if (idx % GV == 0) sh[row * (nvec / GV) + idx / GV] = sc;
     }
   }
+}
+
+// SiLU-and-mul + per-row re-quantization writing fp16 codes and the row's
+// squared L2 norm (the fast int32 GEMM engine's input form); the arithmetic is
+// that of silu_mul_quant_kernel.
+template <int V>
+__global__ void __launch_bounds__(1024) silu_mul_quant_f16_kernel(
+    const uint16_t *__restrict__ gu, int64_t I, const int32_t *__restrict__ masked_m, int Mmax,
+    uint16_t *__restrict__ hq16, float *__restrict__ sh, int32_t *__restrict__ norm2) {
+  __shared__ float red[32];
+  __shared__ int redi[32];
+  const int64_t row = blockIdx.x;
+  if (masked_m != nullptr) {
+    const int e = int(row / Mmax), m = int(row % Mmax);
+    if (m >= masked_m[e]) return;  // whole CTA leaves together
+  }
+  const uint4 *g4 = reinterpret_cast<const uint4 *>(gu + row * 2 * I);
+  const uint4 *u4 = reinterpret_cast<const uint4 *>(gu + row * 2 * I + I);
+  const int nvec = int(I >> 3);
+  float h[V][8];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int idx = threadIdx.x + i * blockDim.x;
+    float ga[8], ua[8];
+    if (idx < nvec) {
+      unpack8(__ldcs(g4 + idx), ga);
+      unpack8(__ldcs(u4 + idx), ua);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        h[i][j] = __fmul_rn(silu(ga[j]), ua[j]);
+        amax = fmaxf(amax, fabsf(h[i][j]));
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) h[i][j] = 0.0f;
+    }
+  }
+  amax = block_max(amax, red);
+  const float sc = quant_scale(amax);
+  uint4 *dst = reinterpret_cast<uint4 *>(hq16 + row * I);
+  int n2 = 0;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int idx = threadIdx.x + i * blockDim.x;
+    if (idx < nvec) {
+      int c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = quant_code(h[i][j], sc);
+        n2 += c[j] * c[j];
+      }
+      uint4 o;
+      o.x = uint32_t(__half_as_ushort(__int2half_rn(c[0]))) | (uint32_t(__half_as_ushort(__int2half_rn(c[1]))) << 16);
+      o.y = uint32_t(__half_as_ushort(__int2half_rn(c[2]))) | (uint32_t(__half_as_ushort(__int2half_rn(c[3]))) << 16);
+      o.z = uint32_t(__half_as_ushort(__int2half_rn(c[4]))) | (uint32_t(__half_as_ushort(__int2half_rn(c[5]))) << 16);
+      o.w = uint32_t(__half_as_ushort(__int2half_rn(c[6]))) | (uint32_t(__half_as_ushort(__int2half_rn(c[7]))) << 16);
+      dst[idx] = o;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+  if (l == 0) redi[w] = n2;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int i = 0; i < nw; ++i) t += redi[i];
+    norm2[row] = t;
+    sh[row] = sc;
+  }
+}
+
+int launch_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, const int32_t *masked_m,
+                              int Mmax, uint16_t *hq16, float *sh, int32_t *norm2,
+                              cudaStream_t st) {
+  if (R == 0 || I == 0) return WQ_OK;
+  if (R > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
+  const int64_t nvec = I / 8;
+  auto rnd = [](int64_t t) { int v = int(((t + 31) / 32) * 32); return v < 32 ? 32 : v; };
+  if (nvec <= 1024) {
+    silu_mul_quant_f16_kernel<1><<<unsigned(R), rnd(nvec), 0, st>>>(gu, I, masked_m, Mmax, hq16, sh, norm2);
+  } else if (nvec <= 4096) {
+    silu_mul_quant_f16_kernel<4><<<unsigned(R), rnd((nvec + 3) / 4), 0, st>>>(gu, I, masked_m, Mmax, hq16, sh, norm2);
+  } else {
+    return WQ_ERR_UNSUPPORTED;
+  }
+  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
 }
 
 int launch_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group,

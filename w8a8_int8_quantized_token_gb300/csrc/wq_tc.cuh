@@ -76,6 +76,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// the same copy into the shared memory of every CTA in `mask` (same offset),
+// signalling each CTA's barrier at the offset of `bar`
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                               uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
+}
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -175,6 +185,26 @@ __device__ __forceinline__ void store_f16_row_piece(uint8_t *rowp, int row, int 
   *reinterpret_cast<uint4 *>(rowp + (((2 * part + 1) ^ sw) << 4)) = o1;
 }
 
+// ---- clusters ----
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// arrive (once) on the barrier at this offset in every CTA of `mask` when all
+// prior MMAs of this thread complete
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
                "r"(ncols)
@@ -191,6 +221,9 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 // host side: tensor-map encoder from the driver (no libcuda link needed)
 bool make_tma_2d_u8(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_k,
                     int box_rows);
+// 2-D 16-bit tensor [rows][K], box 64 x box_rows landing 128-byte swizzled
+bool make_tma_2d_b16_sw128(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K,
+                           int box_rows);
 bool tma_available();
 int num_sms();
 
