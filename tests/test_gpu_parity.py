@@ -312,11 +312,14 @@ def test_silu_mul_quant_f16():
     assert np.array_equal(np_(n2), (hqo.astype(np.int64) ** 2).sum(1))
 
 
+@pytest.mark.parametrize("K", [2048, 4096])
 @pytest.mark.parametrize("extreme", [False, True])
-def test_grouped_gemm_f16codes(extreme):
-    """The CTA-pair engine (codes in +-40: the exactness check passes) and its
-    exact recompute (all-127 rows: the check fails), int32 and bf16 outputs."""
-    E, counts, N, K = 5, [3, 0, 270, 1, 513], 512, 2048
+def test_grouped_gemm_f16codes(extreme, K):
+    """The CTA-pair engines (K 2048: shared-memory weights; K 4096: weights in
+    tensor memory, items above 256 tokens) with codes in +-40 (the exactness
+    check passes) and their exact recompute (all-127 rows: the check fails),
+    int32 and bf16 outputs."""
+    E, counts, N = 5, [3, 0, 270, 1, 513], 512
     rng = np.random.default_rng(23)
     offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     R = int(offs[-1])

@@ -19,6 +19,10 @@ int gemm_tc2_tile_rows(const GemmArgs &a);
 int launch_gemm_tc4(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
                     int32_t *redo, cudaStream_t st);
 bool gemm_tc4_supported(const GemmArgs &a);
+int launch_gemm_tc5(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
+                    int32_t *redo, cudaStream_t st);
+bool gemm_tc5_supported(const GemmArgs &a);
+int gemm_tc5_tile_rows();
 }  // namespace wq
 
 using namespace wq;
@@ -114,10 +118,20 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
   if (a.A16 != nullptr) {
     // fp16-stored codes: the CTA-pair engine, then the CUDA-core engine reading
     // fp16 codes as its exact recompute (it exits at once when *redo == 0)
-    if (!gemm_tc4_supported(a)) return WQ_ERR_UNSUPPORTED;
-    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 256, a.R, w.t256, w.n256,
-                              w.redo, st));
-    WQ_TRY(launch_gemm_tc4(a, w.t256, w.n256, int(w.m256), w.redo, st));
+    // long K: the tensor-memory-weights engine (one item per expert and
+    // weight block; its epilogue is not overlapped, a small cost per long
+    // item); short K: the double-buffered shared-memory engine
+    if (a.K >= 4096 && gemm_tc5_supported(a)) {
+      // token tiles of up to 384 rows (fit the 256-row list's capacity)
+      WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, gemm_tc5_tile_rows(), a.R,
+                                w.t256, w.n256, w.redo, st));
+      WQ_TRY(launch_gemm_tc5(a, w.t256, w.n256, int(w.m256), w.redo, st));
+    } else {
+      if (!gemm_tc4_supported(a)) return WQ_ERR_UNSUPPORTED;
+      WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 256, a.R, w.t256, w.n256,
+                                w.redo, st));
+      WQ_TRY(launch_gemm_tc4(a, w.t256, w.n256, int(w.m256), w.redo, st));
+    }
     WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 64, a.R, w.t64, w.n64, nullptr,
                               st));
     return launch_gemm_simt(a, w.t64, w.n64, int(w.m64), w.redo, st);
