@@ -132,8 +132,8 @@ class Layer:
         self.aws_n = self.lib.wq_moe_align_workspace_size(T, k, E)
         self.aws = e(max(self.aws_n, 1), dt=torch.uint8)
         # the one-call layer's choice: fp16-stored codes for the channel-wise
-        # int32 layer when both GEMM widths are multiples of 256
-        self.f16 = (cfg.scheme == "channel" and cfg.acc == "i32" and (2 * I) % 256 == 0
+        # layer when both GEMM widths are multiples of 256
+        self.f16 = (cfg.scheme == "channel" and (2 * I) % 256 == 0
                     and H % 256 == 0 and R > 64 * E)
         cdt = torch.float16 if self.f16 else torch.int8
         self.A, self.sa = e(R, H, dt=cdt), e(R * self.g1, dt=torch.float32)
@@ -174,7 +174,7 @@ class Layer:
                                     P(self.sa), P(self.anorm), st), "permute")
             rec(4)
             ok(L.wq_grouped_gemm_w8a8_f16codes(P(self.A), P(self.anorm), P(self.sa), P(self.W13),
-                                               P(self.S13), P(self.offsets), E, R, 2 * I, H, 0,
+                                               P(self.S13), P(self.offsets), E, R, 2 * I, H, ac, 0,
                                                P(self.gu), P(self.gws), self.gws_n, P(self.status),
                                                st), "gemm1")
             rec(5)
@@ -182,7 +182,7 @@ class Layer:
                "silu_mul_quant")
             rec(6)
             ok(L.wq_grouped_gemm_w8a8_f16codes(P(self.hq), P(self.hnorm), P(self.sh), P(self.W2),
-                                               P(self.S2), P(self.offsets), E, R, H, I, 0, P(self.y),
+                                               P(self.S2), P(self.offsets), E, R, H, I, ac, 0, P(self.y),
                                                P(self.gws), self.gws_n, P(self.status), st), "gemm2")
         else:
             ok(L.wq_moe_permute(P(self.q), P(self.s), self.g1, T, k, H, P(self.sp), R, P(self.A),

@@ -196,16 +196,17 @@ WQ_API int wq_grouped_gemm_w8a8_noalloc(const int8_t *A, const float *sa, const 
 /* ---------------------------------------------------------------------------
  * Activation codes stored as fp16 values ("fp16 codes"): the same integers in
  * [-127, 127] as the int8 codes, two bytes each, with each row's squared L2
- * norm (sum of code^2, int32).  This is the form the CTA-pair int32 GEMM
- * engine reads directly (TMA straight into the MMA layout); the one-call
- * layer uses it for the channel-wise scheme with the int32 accumulator.
+ * norm (sum of code^2, int32).  This is the form the CTA-pair GEMM engines
+ * read directly (TMA straight into the MMA layout); the one-call layer uses
+ * it for the channel-wise scheme with either accumulator.
  *
  * wq_moe_permute_f16: as wq_moe_permute, writing A16 uint16 (fp16 bits)
  *   [R][K] and norm2 int32 [R] (padding rows: zero codes, scale, norm).
  * wq_silu_mul_quant_f16: as wq_silu_mul_quant with one scale per row
  *   (group 0), writing hq16 (fp16 bits) [R][I] and norm2 int32 [R].
  * wq_grouped_gemm_w8a8_f16codes: as wq_grouped_gemm_w8a8 with the channel
- *   scheme and int32 accumulator, A given as fp16 codes with their row norms
+ *   scheme (acc WQ_ACC_I32 or WQ_ACC_F32; out_type WQ_OUT_I32 only with
+ *   WQ_ACC_I32), A given as fp16 codes with their row norms
  *   (a_norm2 must be the exact sums of squares: they decide whether the
  *   single-pass float32 sums are provably exact, else the launch is
  *   recomputed exactly).  Requirements: N % 256 == 0, K % 128 == 0,
@@ -218,7 +219,7 @@ WQ_API int wq_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, uint1
 WQ_API int wq_grouped_gemm_w8a8_f16codes(const uint16_t *A16, const int32_t *a_norm2,
                                          const float *sa, const int8_t *W, const float *sw,
                                          const int32_t *offsets, int E, int64_t R, int64_t N,
-                                         int64_t K, int out_type, void *out, void *ws,
+                                         int64_t K, int acc, int out_type, void *out, void *ws,
                                          size_t ws_bytes, int32_t *status, wq_stream_t stream);
 
 /* Masked layout [LL]: A int8 [E][Mmax][K] with per-row scales sa

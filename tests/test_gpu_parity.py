@@ -171,6 +171,27 @@ def test_grouped_gemm(scheme, acc, counts, N, K):
     assert_bf16_equal(bits(out), ref, f"gemm {scheme}/{acc}")
 
 
+@pytest.mark.parametrize("scheme,acc", [("channel", "i32"), ("channel", "f32"), ("block", "f32")])
+def test_grouped_gemm_few_tokens_per_expert(scheme, acc):
+    """Decode-like segments (0..16 rows, each size present) and small
+    remainders of larger segments: the small-token engine's tiles of 1..16
+    rows (token boxes 4, 8, 16); the channel-wise cases use a channel count
+    that leaves idle lanes in the last 256-channel block."""
+    counts = list(range(17)) + [33, 256 + 5, 128 + 16, 2 * 64 + 3]
+    E, N, K = len(counts), 384 if scheme == "channel" else 512, 1024
+    A, sa, W, sw, offs = _gemm_case(31, E, counts, N, K, scheme)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    st = wq.new_status()
+    out = wq.grouped_gemm_w8a8(t(A), t(sa), t(W), t(sw), t(offs), scheme, acc, status=st)
+    assert_bf16_equal(bits(out), O.grouped_gemm_w8a8(A, sa, W, sw, offs, scheme, acc),
+                      f"few-token gemm {scheme}/{acc}")
+    if scheme == "channel" and acc == "i32":
+        C = wq.grouped_gemm_w8a8(t(A), t(sa), t(W), t(sw), t(offs), "channel", "i32",
+                                 out_type="i32", status=st)
+        assert np.array_equal(np_(C), O.grouped_gemm_i32(A, W, offs))
+    assert int(st.item()) == 0
+
+
 def test_grouped_gemm_int32_accumulators_and_extremes():
     E, counts, N, K = 3, [200, 1, 77], 256, 7168
     A, sa, W, sw, offs = _gemm_case(9, E, counts, N, K, "channel")
@@ -186,6 +207,24 @@ def test_grouped_gemm_int32_accumulators_and_extremes():
     assert int(st.item()) == 0
     assert np.array_equal(np_(C), Co)
     assert Co[0, 0] == 127 * 127 * 7168 and Co[0, 1] == -127 * 127 * 7168
+
+
+def test_grouped_gemm_f32_accumulator_extremes():
+    """Float32-accumulator mode on rows whose sums exceed 2^24 (one of them
+    odd): the single-pass engine cannot prove these tiles exact and the
+    chunked recompute adds the 128-wide tile sums in order."""
+    E, counts, N, K = 3, [200, 1, 77], 256, 7168
+    A, sa, W, sw, offs = _gemm_case(10, E, counts, N, K, "channel")
+    A[0, :] = 127
+    W[0, 0, :] = 127
+    W[0, 0, 5] = 126
+    W[0, 1, :] = -127
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    st = wq.new_status()
+    out = wq.grouped_gemm_w8a8(t(A), t(sa), t(W), t(sw), t(offs), "channel", "f32", status=st)
+    assert int(st.item()) == 0
+    assert_bf16_equal(bits(out), O.grouped_gemm_w8a8(A, sa, W, sw, offs, "channel", "f32"),
+                      "gemm channel/f32 extremes")
 
 
 def test_grouped_gemm_leaves_rows_outside_segments():
@@ -318,7 +357,9 @@ def test_grouped_gemm_f16codes(extreme, K):
     """The CTA-pair engines (K 2048: shared-memory weights; K 4096: weights in
     tensor memory, items above 256 tokens) with codes in +-40 (the exactness
     check passes) and their exact recompute (all-127 rows: the check fails),
-    int32 and bf16 outputs."""
+    int32 and bf16 outputs, both accumulator modes.  In the extreme case
+    expert-0 rows sum to integers above 2^24 (one odd), so the exact
+    recompute runs and takes each accumulator mode's own steps."""
     E, counts, N = 5, [3, 0, 270, 1, 513], 512
     rng = np.random.default_rng(23)
     offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
@@ -329,6 +370,8 @@ def test_grouped_gemm_f16codes(extreme, K):
     if extreme:
         A[:5] = 127
         W[4, :3] = -127
+        W[0, :3] = 127
+        W[0, 2, 5] = 126
     sa = (rng.random(R) * 0.05).astype(np.float32)
     sw = (rng.random((E, N)) * 1e-3).astype(np.float32)
     t = lambda a: torch.from_numpy(a).to(DEV)
@@ -337,6 +380,9 @@ def test_grouped_gemm_f16codes(extreme, K):
     st = wq.new_status()
     C = wq.grouped_gemm_w8a8_f16codes(A16, n2, t(sa), t(W), t(sw), t(offs), out_type="i32", status=st)
     out = wq.grouped_gemm_w8a8_f16codes(A16, n2, t(sa), t(W), t(sw), t(offs), status=st)
+    out32 = wq.grouped_gemm_w8a8_f16codes(A16, n2, t(sa), t(W), t(sw), t(offs), acc="f32", status=st)
     assert int(st.item()) == 0
     assert np.array_equal(np_(C), O.grouped_gemm_i32(A, W, offs))
     assert_bf16_equal(bits(out), O.grouped_gemm_w8a8(A, sa, W, sw, offs), "f16 codes gemm")
+    assert_bf16_equal(bits(out32), O.grouped_gemm_w8a8(A, sa, W, sw, offs, "channel", "f32"),
+                      "f16 codes gemm, float32 accumulator")

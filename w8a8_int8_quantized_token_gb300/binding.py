@@ -47,7 +47,7 @@ _SIGS = {
     "wq_grouped_gemm_w8a8_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _I, _P, _P, _P]),
     "wq_moe_permute_f16": (_I, [_P, _P, _I, _I, _I, _L, _P, _L, _P, _P, _P, _P]),
     "wq_silu_mul_quant_f16": (_I, [_P, _L, _L, _P, _P, _P, _P]),
-    "wq_grouped_gemm_w8a8_f16codes": (_I, [_P, _P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _P, _P, _S, _P, _P]),
+    "wq_grouped_gemm_w8a8_f16codes": (_I, [_P, _P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _P, _P, _S, _P, _P]),
     "wq_grouped_gemm_masked_workspace_size": (_S, [_I, _I]),
     "wq_grouped_gemm_w8a8_masked": (_I, [_P, _P, _P, _I, _I, _P, _P, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
     "wq_silu_mul_quant": (_I, [_P, _L, _L, _I, _P, _P, _P]),
@@ -231,8 +231,8 @@ def silu_mul_quant_f16(gu):
     return hq, sh, n2
 
 
-def grouped_gemm_w8a8_f16codes(A16, a_norm2, sa, W, sw, offsets, out_type="bf16", out=None,
-                               status=None):
+def grouped_gemm_w8a8_f16codes(A16, a_norm2, sa, W, sw, offsets, acc="i32", out_type="bf16",
+                               out=None, status=None):
     _dev(A16, torch.float16, "A16")
     _dev(a_norm2, torch.int32, "a_norm2")
     _dev(sa, torch.float32, "sa")
@@ -248,7 +248,8 @@ def grouped_gemm_w8a8_f16codes(A16, a_norm2, sa, W, sw, offsets, out_type="bf16"
     ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=A16.device)
     st = status if status is not None else new_status(A16.device)
     _check(lib().wq_grouped_gemm_w8a8_f16codes(_ptr(A16), _ptr(a_norm2), _ptr(sa), _ptr(W), _ptr(sw),
-                                               _ptr(offsets), E, R, N, K, OUT[out_type], _ptr(out),
+                                               _ptr(offsets), E, R, N, K, ACC[acc], OUT[out_type],
+                                               _ptr(out),
                                                _ptr(ws), nws, _ptr(st), _stream()),
            "wq_grouped_gemm_w8a8_f16codes")
     return out

@@ -133,17 +133,24 @@ int launch_align(const int32_t *ids, int T, int k, int E, int pad_m, int32_t *co
 // ---------------------------------------------------------------------------
 // Tile list of the grouped GEMM.  Segment e: rows [offsets[e], offsets[e+1])
 // (contiguous layout) or [e*Mmax, e*Mmax + clamp(masked_m[e], 0, Mmax))
-// (masked layout).  Tiles are expert-major.  ntiles[0] = number written.
+// (masked layout).  A segment of len rows gives floor(len / BM) full tiles
+// and, for a remainder of rem rows, one more tile: in the small list when
+// 0 < rem <= small_max (a small list is given), else in the main list.
+// Lists are expert-major; ntiles[0] / nsmall[0] = numbers written.
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__restrict__ offsets,
                                                            const int32_t *__restrict__ masked_m,
                                                            int Mmax, int E, int BM, int64_t R,
                                                            Tile *__restrict__ tiles,
                                                            int32_t *__restrict__ ntiles,
-                                                           int32_t *__restrict__ zero_word) {
-  __shared__ int32_t part[1024];
+                                                           int32_t *__restrict__ zero_word,
+                                                           int small_max,
+                                                           Tile *__restrict__ small,
+                                                           int32_t *__restrict__ nsmall) {
+  __shared__ int32_t part[1024], part_s[1024];
   if (zero_word != nullptr && threadIdx.x == 0) *zero_word = 0;
   const int per = (E + blockDim.x - 1) / blockDim.x;
   const int e0 = threadIdx.x * per;
+  const bool split = small != nullptr && small_max > 0;
   auto seg = [&](int e, int &r0, int &len) {
     if (masked_m) {
       int m = masked_m[e];
@@ -159,41 +166,67 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
       len = int(b - a);
     }
   };
-  int local = 0;
+  // full tiles, whether the remainder goes to the small list, main-list tiles
+  auto plan = [&](int len, int &nfull, int &rem, bool &to_small) {
+    nfull = len / BM;
+    rem = len - nfull * BM;
+    to_small = split && rem > 0 && rem <= small_max;
+  };
+  int local = 0, local_s = 0;
   for (int e = e0; e < e0 + per && e < E; ++e) {
-    int r0, len;
+    int r0, len, nfull, rem;
+    bool ts;
     seg(e, r0, len);
-    local += (len + BM - 1) / BM;
+    plan(len, nfull, rem, ts);
+    local += nfull + ((rem > 0 && !ts) ? 1 : 0);
+    local_s += ts ? 1 : 0;
   }
   part[threadIdx.x] = local;
+  part_s[threadIdx.x] = local_s;
   __syncthreads();
   for (int o = 1; o < int(blockDim.x); o <<= 1) {
     const int v = threadIdx.x >= unsigned(o) ? part[threadIdx.x - o] : 0;
+    const int vs = threadIdx.x >= unsigned(o) ? part_s[threadIdx.x - o] : 0;
     __syncthreads();
     part[threadIdx.x] += v;
+    part_s[threadIdx.x] += vs;
     __syncthreads();
   }
-  int t = part[threadIdx.x] - local;
+  int t = part[threadIdx.x] - local, ts_i = part_s[threadIdx.x] - local_s;
   for (int e = e0; e < e0 + per && e < E; ++e) {
-    int r0, len;
+    int r0, len, nfull, rem;
+    bool ts;
     seg(e, r0, len);
-    for (int m = 0; m < len; m += BM) {
+    plan(len, nfull, rem, ts);
+    const int main_rows = ts ? nfull * BM : len;
+    for (int m = 0; m < main_rows; m += BM) {
       Tile tl;
       tl.expert = e;
       tl.row0 = r0 + m;
-      tl.rows = len - m < BM ? len - m : BM;
+      tl.rows = main_rows - m < BM ? main_rows - m : BM;
       tl.pad = 0;
       tiles[t++] = tl;
     }
+    if (ts) {
+      Tile tl;
+      tl.expert = e;
+      tl.row0 = r0 + nfull * BM;
+      tl.rows = rem;
+      tl.pad = 0;
+      small[ts_i++] = tl;
+    }
   }
-  if (threadIdx.x == blockDim.x - 1) ntiles[0] = part[threadIdx.x];
+  if (threadIdx.x == blockDim.x - 1) {
+    ntiles[0] = part[threadIdx.x];
+    if (split) nsmall[0] = part_s[threadIdx.x];
+  }
 }
 
 int launch_build_tiles(const int32_t *offsets, const int32_t *masked_m, int Mmax, int E, int BM,
                        int64_t R, Tile *tiles, int32_t *ntiles, int32_t *zero_word,
-                       cudaStream_t st) {
+                       cudaStream_t st, int small_max, Tile *small, int32_t *nsmall) {
   build_tiles_kernel<<<1, 1024, 0, st>>>(offsets, masked_m, Mmax, E, BM, R, tiles, ntiles,
-                                         zero_word);
+                                         zero_word, small_max, small, nsmall);
   return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
 }
 

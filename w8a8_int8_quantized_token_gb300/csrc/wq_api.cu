@@ -23,6 +23,10 @@ int launch_gemm_tc5(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles,
                     int32_t *redo, cudaStream_t st);
 bool gemm_tc5_supported(const GemmArgs &a);
 int gemm_tc5_tile_rows();
+int launch_gemm_small(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
+                      cudaStream_t st);
+bool gemm_small_supported(const GemmArgs &a);
+int gemm_small_max_rows();
 }  // namespace wq
 
 using namespace wq;
@@ -79,14 +83,15 @@ int64_t gemm_max_tiles(int64_t R, int E, int Mmax, bool masked, int BM) {
 
 namespace wq {
 
-// Workspace of one grouped GEMM: three tile lists (64-row tiles for the
+// Workspace of one grouped GEMM: four tile lists (64-row tiles for the
 // CUDA-core engine, 128-row tiles for the chunked tensor-core engine, 256-row
-// token tiles for the fast int32 engine), each with its count, and the flag
-// the fast engine raises when a tile needs the exact chunked recompute.
+// token tiles for the single-pass engines, and the small-token engine's
+// tiles: at most one per expert), each with its count, and the flag the
+// single-pass engines raise when a tile needs the exact recompute.
 struct GemmWs {
-  Tile *t64, *t128, *t256;
-  int32_t *n64, *n128, *n256, *redo;
-  int64_t m64, m128, m256;
+  Tile *t64, *t128, *t256, *tsm;
+  int32_t *n64, *n128, *n256, *nsm, *redo;
+  int64_t m64, m128, m256, msm;
   size_t bytes;
 };
 
@@ -102,6 +107,9 @@ GemmWs carve_gemm_ws(void *ws, int64_t R, int E, int Mmax, bool masked) {
   w.n128 = c.take<int32_t>(1);
   w.t256 = c.take<Tile>(size_t(w.m256));
   w.n256 = c.take<int32_t>(1);
+  w.msm = E;
+  w.tsm = c.take<Tile>(size_t(w.msm));
+  w.nsm = c.take<int32_t>(1);
   w.redo = c.take<int32_t>(1);
   w.bytes = c.used;
   return w;
@@ -136,21 +144,32 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
                               st));
     return launch_gemm_simt(a, w.t64, w.n64, int(w.m64), w.redo, st);
   }
+  // Segment remainders of at most 16 rows (all of a decode batch's experts,
+  // the ragged tail of larger ones) go to the small-token engine, which reads
+  // int8 weights without widening and is exact in every mode.
+  const bool small = gemm_small_supported(a);
+  const int small_max = small ? gemm_small_max_rows() : 0;
   if (gemm_tc2_supported(a)) {
-    // fast int32 engine; it raises *redo for any tile whose single-pass
-    // float32 sums it cannot prove exact, and the chunked engine below then
-    // recomputes the launch (it exits at once when *redo == 0)
+    // single-pass engine; it raises *redo for any tile whose float32 sums it
+    // cannot prove exact, and the chunked engine below then recomputes the
+    // whole launch (it exits at once when *redo == 0)
     const int rows = gemm_tc2_tile_rows(a);  // 64 (few rows per expert) or 256
     Tile *t = rows == 64 ? w.t64 : w.t256;
     int32_t *n = rows == 64 ? w.n64 : w.n256;
     const int64_t m = rows == 64 ? w.m64 : w.m256;
-    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, rows, a.R, t, n, w.redo, st));
+    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, rows, a.R, t, n, w.redo, st,
+                              small_max, w.tsm, w.nsm));
+    if (small) WQ_TRY(launch_gemm_small(a, w.tsm, w.nsm, int(w.msm), st));
     WQ_TRY(launch_gemm_tc2(a, t, n, int(m), w.redo, st));
     gate = w.redo;
   }
   if (gemm_tc_supported(a)) {
+    // as the gated recompute it covers every row; on its own it leaves the
+    // small remainders to the small-token engine
+    const bool split = small && gate == nullptr;
     WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 128, a.R, w.t128, w.n128,
-                              nullptr, st));
+                              nullptr, st, split ? small_max : 0, w.tsm, w.nsm));
+    if (split) WQ_TRY(launch_gemm_small(a, w.tsm, w.nsm, int(w.msm), st));
     return launch_gemm_tc(a, w.t128, w.n128, int(w.m128), gate, st);
   }
   WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 64, a.R, w.t64, w.n64, nullptr,
@@ -310,19 +329,19 @@ int wq_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, uint16_t *hq
 
 int wq_grouped_gemm_w8a8_f16codes(const uint16_t *A16, const int32_t *a_norm2, const float *sa,
                                   const int8_t *W, const float *sw, const int32_t *offsets, int E,
-                                  int64_t R, int64_t N, int64_t K, int out_type, void *out,
-                                  void *ws, size_t ws_bytes, int32_t *status,
+                                  int64_t R, int64_t N, int64_t K, int acc, int out_type,
+                                  void *out, void *ws, size_t ws_bytes, int32_t *status,
                                   wq_stream_t stream) {
   if (R < 0 || E > 4096) return WQ_ERR_INVALID_ARG;
   if (R == 0) return WQ_OK;
-  WQ_TRY(check_gemm_common(W, sw, E, N, K, WQ_SCHEME_CHANNEL, WQ_ACC_I32, out_type, out));
+  WQ_TRY(check_gemm_common(W, sw, E, N, K, WQ_SCHEME_CHANNEL, acc, out_type, out));
   if (!A16 || !a_norm2 || !sa || !offsets) return WQ_ERR_INVALID_ARG;
   if (!al16(A16) || N % 256 || K > 65536) return WQ_ERR_UNSUPPORTED;
   if (R >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;
   if (ws_bytes < gemm_ws_bytes(R, E, 0, false) || !ws) return WQ_ERR_WORKSPACE;
   WQ_TRY(check_device());
   GemmArgs a{nullptr, A16, a_norm2, sa, W, sw, offsets, nullptr, 0, E, R, N, K, WQ_SCHEME_CHANNEL,
-             WQ_ACC_I32, out_type, out, ws, status};
+             acc, out_type, out, ws, status};
   return launch_grouped_gemm(a, stream);
 }
 
@@ -442,14 +461,15 @@ int run_forward(const uint16_t *x, const float *logits, const int8_t *W13, const
   WQ_TRY(launch_quant_rows(x, T, H, H, blk ? 128 : 0, b.q, b.s, st));
   WQ_TRY(launch_align(b.ids, T, k, E, 1, b.counts, b.offsets, b.sorted_pair, b.pair_to_row,
                       b.align_ws, status, st));
-  // channel-wise int32: activation codes travel as fp16 values with row norms
-  // (the CTA-pair GEMM engine); other modes and widths use int8 codes
+  // channel-wise (either accumulator): activation codes travel as fp16 values
+  // with row norms (the CTA-pair GEMM engines); block-wise and other widths
+  // use int8 codes
   GemmArgs probe{nullptr, reinterpret_cast<const uint16_t *>(b.A), b.anorm, b.sa, W13, sw13,
                  b.offsets, nullptr, 0, E, R, int64_t(2) * I, H, scheme, acc, WQ_OUT_BF16, b.gu,
                  b.gemm_ws, status};
   // (with few rows per expert the GEMMs stream weights from HBM and the
   // int8 path's 64-token engine with its deeper weight ring is faster)
-  const bool f16 = !blk && acc == WQ_ACC_I32 && (2 * I) % 256 == 0 && H % 256 == 0 &&
+  const bool f16 = !blk && (2 * I) % 256 == 0 && H % 256 == 0 &&
                    R > int64_t(64) * E && gemm_tc4_supported(probe);
   if (f16) {
     uint16_t *A16 = reinterpret_cast<uint16_t *>(b.A);

@@ -170,9 +170,22 @@ struct GemmArgs {
   void *ws;
   int32_t *status;
 };
+// The single-pass float32 engines serve both channel-wise accumulator modes.
+// In the float32 mode the accumulator is the running sum, over 128-wide K
+// tiles in ascending order, of each tile's int32 partial product.  Every
+// prefix of that sum is an integer bounded by |a|*|w| (Cauchy-Schwarz); when
+// |a|^2*|w|^2 < 2^48 (the bound the engines prove before trusting a tile)
+// every conversion and addition is exact, the accumulator equals the int32
+// result, and the dequantization (acc*sa)*sw is the same expression in both
+// modes.  Tiles the bound does not cover go to the exact recompute, which
+// takes each mode's own steps.
+inline bool acc_modes_agree(const GemmArgs &a) {
+  return a.scheme == WQ_SCHEME_CHANNEL && (a.acc == WQ_ACC_I32 || a.acc == WQ_ACC_F32);
+}
 int launch_build_tiles(const int32_t *offsets, const int32_t *masked_m, int Mmax, int E, int BM,
                        int64_t R, Tile *tiles, int32_t *ntiles, int32_t *zero_word,
-                       cudaStream_t st);
+                       cudaStream_t st, int small_max = 0, Tile *small = nullptr,
+                       int32_t *nsmall = nullptr);
 size_t gemm_ws_bytes(int64_t R, int E, int Mmax, bool masked);
 int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st);
 }  // namespace wq

@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }  // namespace
 
 bool gemm_tc2_supported(const GemmArgs &a) {
-  return a.scheme == WQ_SCHEME_CHANNEL && a.acc == WQ_ACC_I32 && a.N % WM == 0 &&
+  return a.scheme == WQ_SCHEME_CHANNEL && acc_modes_agree(a) && a.N % WM == 0 &&
          a.K % BK == 0 && a.K <= 65536 && a.E * a.N < (int64_t(1) << 31) &&
          a.R < (int64_t(1) << 31) && tma_available();
 }

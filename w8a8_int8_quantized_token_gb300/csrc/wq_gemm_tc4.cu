@@ -349,7 +349,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 
 bool gemm_tc4_supported(const GemmArgs &a) {
   return a.A16 != nullptr && a.a_norm2 != nullptr && a.scheme == WQ_SCHEME_CHANNEL &&
-         a.acc == WQ_ACC_I32 && a.N % (2 * WM) == 0 && a.K % BK == 0 && a.K <= 65536 &&
+         acc_modes_agree(a) && a.N % (2 * WM) == 0 && a.K % BK == 0 && a.K <= 65536 &&
          a.E * a.N < (int64_t(1) << 31) && a.R < (int64_t(1) << 31) && tma_available() &&
          num_sms() >= 2;
 }

@@ -231,6 +231,8 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 // host side: tensor-map encoder from the driver (no libcuda link needed)
 bool make_tma_2d_u8(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_k,
                     int box_rows);
+// 2-D 8-bit tensor [rows][K], box 128 x box_rows landing 128-byte swizzled
+bool make_tma_2d_u8_sw128(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows);
 // 2-D 16-bit tensor [rows][K], box 64 x box_rows landing 128-byte swizzled
 bool make_tma_2d_b16_sw128(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K,
                            int box_rows);
