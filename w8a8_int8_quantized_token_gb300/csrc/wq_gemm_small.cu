@@ -92,6 +92,7 @@ __device__ __forceinline__ bool consume_item(const GemmArgs &a, const Tile &tl, 
         acc[t] = __dp4a(int(w.w), int(x.w), acc[t]);
       }
     }
+    fence_async_smem();  // these reads before the next copy into the slot
     __syncwarp();
     if (lane == 0) mbar_arrive(base + OFF_BAR + 8u * uint32_t(STAGES + s));
     if (blk) {

@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int j = 0; j < 12; ++j)
           v[j] = *reinterpret_cast<const uint4 *>(src + (j * 128 + t) * 16);
+        fence_async_smem();  // these reads before the next copy into the slot
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_S8_EMPTY + s8));
         if (!__all_sync(0xffffffffu,

@@ -235,6 +235,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                      ? *reinterpret_cast<const uint4 *>(src + (j < NJW ? 0 : W8) + c * 16)
                      : make_uint4(0, 0, 0, 0);
         }
+        fence_async_smem();  // these reads before the next copy into the slot
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_S8_EMPTY + s8));
         if (!__all_sync(0xffffffffu,

@@ -227,6 +227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int j = 0; j < NJW; ++j)
           v[j] = *reinterpret_cast<const uint4 *>(src + (j * GCONV + t) * 16);
+        fence_async_smem();  // these reads before the next copy into the slot
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_W8_EMPTY + sw));
         if (!__all_sync(0xffffffffu,

@@ -247,6 +247,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           for (int m = 0; m < 4; ++m)
             if (c == m) v[m] = x;
         }
+        fence_async_smem();  // these reads before the next copy into the slot
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_W8_EMPTY + sw));
         uint32_t f[32];

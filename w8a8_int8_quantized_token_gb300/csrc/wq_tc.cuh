@@ -86,6 +86,12 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
       : "memory");
 }
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy accesses (TMA copies, tcgen05.mma operand reads) that another
+// thread starts after a barrier hand-off.  Needed in both directions: after
+// writing data an MMA will read, and after reading a slot that TMA is about
+// to refill (without it a refill could land before the reads had taken
+// their data, an intermittent corruption seen on sm_103a).
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
