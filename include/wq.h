@@ -83,6 +83,12 @@ WQ_API int wq_init(int device);
 /* Static text for a status code (never NULL). */
 WQ_API const char *wq_status_string(int code);
 
+/* Number of kernels this library has enqueued in the process so far (all
+ * devices and threads; monotone).  Accounting only: a caller differences it
+ * around a region to count the library's launches there.  The pages have no
+ * counterpart. */
+WQ_API uint64_t wq_kernel_launches(void);
+
 /* ---------------------------------------------------------------------------
  * Online activation quantization [MT] (and offline weight quantization).
  *

@@ -45,6 +45,30 @@ def test_quantize_zero_and_constant_rows():
     assert np.all(np_(q)[1] == -127) and np.all(np_(q)[0] == 0)
 
 
+def test_quantize_exact_half_integer_quotients():
+    """Rows whose scale is a power of two (absmax = 127 * 2^j) so that x / s
+    is exactly every half-integer in (-127, 127) and every integer: the codes
+    of the half-integers take the ties-to-even rule through the
+    exact-quotient branch."""
+    K = 512
+    rows = []
+    for j in (-3, 0, 2):
+        h = (np.arange(-127, 127) + 0.5) * 2.0 ** j
+        n = np.arange(-127, 128) * 2.0 ** j
+        rows.append(np.resize(np.concatenate([[127 * 2.0 ** j], h, n]), K))
+    x = torch.tensor(np.stack(rows), dtype=torch.float32)
+    assert torch.equal(x.to(torch.bfloat16).float(), x)  # exact in bf16
+    x = x.to(torch.bfloat16)
+    q, s = wq.quantize_per_token(x.to(DEV))
+    qo, so = O.quantize_per_token(bits(x))
+    assert np.array_equal(np_(s), so) and np.all(so == 2.0 ** np.array([-3, 0, 2], np.float32))
+    assert np.array_equal(np_(q), qo)
+    assert qo[1, 1 + 127] == 0 and qo[1, 1 + 128] == 2  # 0.5 -> 0, 1.5 -> 2
+    qg, sg = wq.quantize_per_token_group(x.to(DEV), 128)
+    qgo, sgo = O.quantize_per_token_group(bits(x), 128)
+    assert np.array_equal(np_(qg), qgo) and np.array_equal(np_(sg), sgo)
+
+
 @pytest.mark.parametrize("group", [32, 64, 128, 256])
 def test_quantize_per_token_group(group):
     x = synth.activations(19, 1024, True, seed=group)

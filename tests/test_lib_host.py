@@ -41,6 +41,15 @@ def test_status_strings(lib):
     assert lib.wq_status_string(99) == b"unknown status"
 
 
+def test_launch_counter_ignores_rejected_calls(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)
+    n0 = lib.wq_kernel_launches()
+    assert lib.wq_route_topk(fake, 4, 8, 9, fake, fake, None) == -1
+    assert lib.wq_quantize_per_token(fake, 4, 12, 12, fake, fake, None) == -2
+    assert lib.wq_kernel_launches() == n0
+
+
 def test_workspace_sizes(lib):
     # forward workspace holds at least A, GU, y of the prefill shape
     T, H, I, E, k = 8192, 7168, 2048, 256, 8

@@ -35,6 +35,7 @@ _S = _c.c_size_t
 _SIGS = {
     "wq_init": (_I, [_I]),
     "wq_status_string": (_c.c_char_p, [_I]),
+    "wq_kernel_launches": (_c.c_uint64, []),
     "wq_quantize_per_token": (_I, [_P, _L, _L, _L, _P, _P, _P]),
     "wq_quantize_per_token_group": (_I, [_P, _L, _L, _L, _I, _P, _P, _P]),
     "wq_quantize_weight_block": (_I, [_P, _L, _L, _P, _P, _P]),

@@ -127,7 +127,7 @@ int launch_align(const int32_t *ids, int T, int k, int E, int pad_m, int32_t *co
   if (chunks > 0) {
     align_scatter_kernel<<<chunks, 32, smem, st>>>(ids, P, E, hist, sorted_pair, pair_to_row);
   }
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  return launched(chunks > 0 ? 3 : 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -227,7 +227,7 @@ int launch_build_tiles(const int32_t *offsets, const int32_t *masked_m, int Mmax
                        cudaStream_t st, int small_max, Tile *small, int32_t *nsmall) {
   build_tiles_kernel<<<1, 1024, 0, st>>>(offsets, masked_m, Mmax, E, BM, R, tiles, ntiles,
                                          zero_word, small_max, small, nsmall);
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  return launched(1);
 }
 
 }  // namespace wq

@@ -1,6 +1,7 @@
 // C ABI of libwq.so: host-side argument checks, workspace carving and the
 // composition of the layer's steps on one stream.  Declarations and the
 // contract of every entry point are in include/wq.h.
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 
@@ -82,6 +83,13 @@ int64_t gemm_max_tiles(int64_t R, int E, int Mmax, bool masked, int BM) {
 }  // namespace
 
 namespace wq {
+
+std::atomic<uint64_t> g_launches{0};
+
+int launched(int n) {
+  g_launches.fetch_add(uint64_t(n), std::memory_order_relaxed);
+  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+}
 
 // Workspace of one grouped GEMM: four tile lists (64-row tiles for the
 // CUDA-core engine, 128-row tiles for the chunked tensor-core engine, 256-row
@@ -187,6 +195,8 @@ int wq_init(int device) {
   if (cudaSetDevice(device) != cudaSuccess) return WQ_ERR_DEVICE;
   return check_device();
 }
+
+uint64_t wq_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char *wq_status_string(int code) {
   switch (code) {

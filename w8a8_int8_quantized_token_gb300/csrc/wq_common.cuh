@@ -82,16 +82,39 @@ __device__ __forceinline__ float quant_scale(float amax) {
   return __fdiv_rn(fmaxf(amax, 1e-10f), 127.0f);
 }
 
-// One code: clamp(rint(x / s), -127, 127).
-__device__ __forceinline__ int quant_code(float x, float s) {
-  float q = rintf(__fdiv_rn(x, s));
-  q = fminf(fmaxf(q, -127.0f), 127.0f);
-  return __float2int_rn(q);
+// One code clamp(rint(x / s), -127, 127), x / s the correctly rounded
+// quotient, given rs = __frcp_rn(s) (the correctly rounded reciprocal).
+//  * The clamp never binds for finite x: |x| <= amax and s = RN(amax / 127)
+//    >= (amax / 127)(1 - 2^-24), so |x / s| <= 127 (1 + 2^-23) and rint gives
+//    at most 127 in magnitude.
+//  * Only the side of a half-integer on which the quotient falls matters:
+//    y = RN(x * rs) = (x / s)(1 + e), |e| <= 2^-23 + 2^-48, lies within
+//    1.52e-5 of x / s, which lies within 3.9e-6 (half an ulp below 128) of
+//    RN(x / s).  When y is 2^-15 (3.05e-5) or farther from every
+//    half-integer, y and RN(x / s) sit strictly inside the same interval
+//    between half-integers and round to the same integer; the rare y nearer
+//    than that take the exact quotient.
+//  * Adding 1.5 * 2^23 rounds a float of magnitude below 2^22 to an integer
+//    (to nearest, ties to even) held in the low mantissa bits, so the low
+//    byte of the sum is the two's-complement code; subtracting it back gives
+//    rint(y) exactly, and y - rint(y) is exact (Sterbenz) for |y| <= 128.
+// Returns the sum's bits: the code is the low byte.
+__device__ __forceinline__ uint32_t quant_bits(float x, float s, float rs) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  const float y = __fmul_rn(x, rs);
+  float t = __fadd_rn(y, kRound);
+  if (fabsf(__fsub_rn(y, __fsub_rn(t, kRound))) >= 0.499969482421875f)  // 0.5 - 2^-15
+    t = __fadd_rn(__fdiv_rn(x, s), kRound);
+  return __float_as_uint(t);
+}
+// The same code as an int in [-127, 127].
+__device__ __forceinline__ int quant_code(float x, float s, float rs) {
+  return int(quant_bits(x, s, rs) << 24) >> 24;
 }
 
-__device__ __forceinline__ uint32_t pack_s8x4(int a, int b, int c, int d) {
-  return (uint32_t(a) & 0xffu) | ((uint32_t(b) & 0xffu) << 8) | ((uint32_t(c) & 0xffu) << 16) |
-         ((uint32_t(d) & 0xffu) << 24);
+// Low bytes of four words -> one word (a in byte 0).
+__device__ __forceinline__ uint32_t pack_s8x4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
 }
 
 __device__ __forceinline__ void set_status(int32_t *status, int code) {
@@ -127,6 +150,9 @@ struct Tile {
 
 // Launchers implemented in the kernel translation units (host side).
 namespace wq {
+// Adds n to the process-wide count of kernels the library has enqueued and
+// returns WQ_OK if the last launch was accepted, else WQ_ERR_LAUNCH.
+int launched(int n);
 int launch_quant_rows(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group, int8_t *q,
                       float *s, cudaStream_t st);
 int launch_quant_weight_block(const uint16_t *w, int64_t N, int64_t K, int8_t *q, float *s,

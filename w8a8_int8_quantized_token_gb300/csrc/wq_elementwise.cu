@@ -8,10 +8,14 @@
 namespace wq {
 
 // ---------------------------------------------------------------------------
-// Per-token quantization: one CTA per row, the row held in registers.
+// Per-token and per-token-group quantization: one CTA per row, the row held
+// in registers (V 16-byte vectors per thread, issued together), one scale
+// per row (GV == 0: block-wide absmax) or per group of GV vectors (the GV
+// consecutive lanes owning a group reduce with xor shuffles).
 // (Meituan INT8 DeepSeek R1 article, 量化技术的探索: online per-token
-// activation quantization of the channel-wise scheme.)
-template <int V>
+// activation quantization of the channel-wise scheme, per-token-group
+// quantization of the block-wise scheme.)
+template <int V, int GV>
 __global__ void __launch_bounds__(1024) quant_row_kernel(const uint16_t *__restrict__ x, int64_t K,
                                                          int64_t ldx, int8_t *__restrict__ q,
                                                          float *__restrict__ s) {
@@ -20,102 +24,100 @@ __global__ void __launch_bounds__(1024) quant_row_kernel(const uint16_t *__restr
   const uint4 *xr = reinterpret_cast<const uint4 *>(x + row * ldx);
   const int nvec = int(K >> 3);
   uint4 v[V];
-  float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < V; ++i) {
     const int idx = threadIdx.x + i * blockDim.x;
+    if (idx < nvec) v[i] = __ldcs(xr + idx);
+  }
+  float a[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int idx = threadIdx.x + i * blockDim.x;
+    a[i] = 0.0f;
     if (idx < nvec) {
-      v[i] = __ldcs(xr + idx);
       float f[8];
       unpack8(v[i], f);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+      for (int j = 0; j < 8; ++j) a[i] = fmaxf(a[i], fabsf(f[j]));
     }
   }
-  amax = block_max(amax, red);
-  const float sc = quant_scale(amax);
   uint2 *qr = reinterpret_cast<uint2 *>(q + row * K);
+  if constexpr (GV == 0) {
+    float amax = a[0];
 #pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int idx = threadIdx.x + i * blockDim.x;
-    if (idx < nvec) {
-      float f[8];
-      unpack8(v[i], f);
-      uint2 o;
-      o.x = pack_s8x4(quant_code(f[0], sc), quant_code(f[1], sc), quant_code(f[2], sc),
-                      quant_code(f[3], sc));
-      o.y = pack_s8x4(quant_code(f[4], sc), quant_code(f[5], sc), quant_code(f[6], sc),
-                      quant_code(f[7], sc));
-      qr[idx] = o;
+    for (int i = 1; i < V; ++i) amax = fmaxf(amax, a[i]);
+    amax = block_max(amax, red);
+    const float sc = quant_scale(amax);
+    const float rs = __frcp_rn(sc);
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int idx = threadIdx.x + i * blockDim.x;
+      if (idx < nvec) {
+        float f[8];
+        unpack8(v[i], f);
+        uint2 o;
+        o.x = pack_s8x4(quant_bits(f[0], sc, rs), quant_bits(f[1], sc, rs),
+                        quant_bits(f[2], sc, rs), quant_bits(f[3], sc, rs));
+        o.y = pack_s8x4(quant_bits(f[4], sc, rs), quant_bits(f[5], sc, rs),
+                        quant_bits(f[6], sc, rs), quant_bits(f[7], sc, rs));
+        qr[idx] = o;
+      }
     }
-  }
-  if (threadIdx.x == 0) s[row] = sc;
-}
-
-// Per-token-group quantization: each thread owns 8 consecutive elements; the
-// GV = group/8 lanes of one group reduce with xor shuffles (the block-wise
-// scheme's per-token-group activation quantization).
-template <int GV>
-__global__ void __launch_bounds__(256) quant_group_kernel(const uint16_t *__restrict__ x, int64_t T,
-                                                          int64_t K, int64_t ldx,
-                                                          int8_t *__restrict__ q,
-                                                          float *__restrict__ s) {
-  const int64_t vpr = K >> 3;  // vectors per row
-  const int64_t total = T * vpr;
-  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx - threadIdx.x % 32 < total;
-       idx += stride) {
-    const bool live = idx < total;
-    const int64_t row = live ? idx / vpr : 0;
-    const int64_t vec = live ? idx - row * vpr : 0;
-    float f[8];
-    float amax = 0.0f;
-    if (live) {
-      const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(x + row * ldx) + vec);
-      unpack8(v, f);
+    if (threadIdx.x == 0) s[row] = sc;
+  } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
-    }
+    for (int i = 0; i < V; ++i) {
+      const int idx = threadIdx.x + i * blockDim.x;
+      float am = a[i];
 #pragma unroll
-    for (int o = GV / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (live) {
-      const float sc = quant_scale(amax);
-      uint2 o;
-      o.x = pack_s8x4(quant_code(f[0], sc), quant_code(f[1], sc), quant_code(f[2], sc),
-                      quant_code(f[3], sc));
-      o.y = pack_s8x4(quant_code(f[4], sc), quant_code(f[5], sc), quant_code(f[6], sc),
-                      quant_code(f[7], sc));
-      reinterpret_cast<uint2 *>(q + row * K)[vec] = o;
-      if (vec % GV == 0) s[row * (vpr / GV) + vec / GV] = sc;
+      for (int o = GV / 2; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      if (idx < nvec) {
+        const float sc = quant_scale(am);
+        const float rs = __frcp_rn(sc);
+        float f[8];
+        unpack8(v[i], f);
+        uint2 o;
+        o.x = pack_s8x4(quant_bits(f[0], sc, rs), quant_bits(f[1], sc, rs),
+                        quant_bits(f[2], sc, rs), quant_bits(f[3], sc, rs));
+        o.y = pack_s8x4(quant_bits(f[4], sc, rs), quant_bits(f[5], sc, rs),
+                        quant_bits(f[6], sc, rs), quant_bits(f[7], sc, rs));
+        qr[idx] = o;
+        if (idx % GV == 0) s[row * (nvec / GV) + idx / GV] = sc;
+      }
     }
   }
 }
 
+template <int V>
+int launch_quant_v(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group, int8_t *q,
+                   float *s, cudaStream_t st) {
+  const int64_t nvec = K / 8;
+  int threads = int((nvec + V - 1) / V);
+  threads = ((threads + 31) / 32) * 32;
+  switch (group) {
+    case 0: quant_row_kernel<V, 0><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s); break;
+    case 32: quant_row_kernel<V, 4><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s); break;
+    case 64: quant_row_kernel<V, 8><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s); break;
+    case 128: quant_row_kernel<V, 16><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s); break;
+    case 256: quant_row_kernel<V, 32><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s); break;
+    default: return WQ_ERR_UNSUPPORTED;
+  }
+  return launched(1);
+}
+
+// Rows up to 2048 vectors (K <= 16384) take two vectors per thread (the
+// fastest split measured on 7168-wide rows: 40.7 us for 8192 rows, against
+// 45 us with 8 per thread and 41 us with 4); longer rows up to 8 per
+// thread.  Warps are whole, so the group shuffles always see full warps, and
+// a group (GV consecutive vectors, K % group == 0) never straddles the row end.
 int launch_quant_rows(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group, int8_t *q,
                       float *s, cudaStream_t st) {
   if (T == 0 || K == 0) return WQ_OK;
-  if (group == 0) {
-    const int64_t nvec = K / 8;
-    constexpr int V = 8;
-    if (nvec > int64_t(V) * 1024 || T > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
-    int threads = int((nvec + V - 1) / V);
-    threads = ((threads + 31) / 32) * 32;
-    if (threads < 128) threads = nvec >= 128 ? 128 : 32;
-    if (threads > 1024) threads = 1024;
-    quant_row_kernel<V><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s);
-  } else {
-    const int64_t total = T * (K / 8);
-    int64_t blocks = (total + 255) / 256;
-    if (blocks > 152 * 64) blocks = 152 * 64;
-    switch (group) {
-      case 32: quant_group_kernel<4><<<unsigned(blocks), 256, 0, st>>>(x, T, K, ldx, q, s); break;
-      case 64: quant_group_kernel<8><<<unsigned(blocks), 256, 0, st>>>(x, T, K, ldx, q, s); break;
-      case 128: quant_group_kernel<16><<<unsigned(blocks), 256, 0, st>>>(x, T, K, ldx, q, s); break;
-      case 256: quant_group_kernel<32><<<unsigned(blocks), 256, 0, st>>>(x, T, K, ldx, q, s); break;
-      default: return WQ_ERR_UNSUPPORTED;
-    }
-  }
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  const int64_t nvec = K / 8;
+  if (nvec > 8 * 1024 || T > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
+  if (nvec <= 2 * 1024) return launch_quant_v<2>(x, T, K, ldx, group, q, s, st);
+  if (nvec <= 4 * 1024) return launch_quant_v<4>(x, T, K, ldx, group, q, s, st);
+  return launch_quant_v<8>(x, T, K, ldx, group, q, s, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -141,6 +143,7 @@ __global__ void __launch_bounds__(256) quant_wblock_kernel(const uint16_t *__res
   }
   amax = block_max(amax, red);
   const float sc = quant_scale(amax);
+  const float rs = __frcp_rn(sc);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = threadIdx.x + i * 256;
@@ -148,10 +151,10 @@ __global__ void __launch_bounds__(256) quant_wblock_kernel(const uint16_t *__res
     float f[8];
     unpack8(v[i], f);
     uint2 o;
-    o.x = pack_s8x4(quant_code(f[0], sc), quant_code(f[1], sc), quant_code(f[2], sc),
-                    quant_code(f[3], sc));
-    o.y = pack_s8x4(quant_code(f[4], sc), quant_code(f[5], sc), quant_code(f[6], sc),
-                    quant_code(f[7], sc));
+    o.x = pack_s8x4(quant_bits(f[0], sc, rs), quant_bits(f[1], sc, rs), quant_bits(f[2], sc, rs),
+                    quant_bits(f[3], sc, rs));
+    o.y = pack_s8x4(quant_bits(f[4], sc, rs), quant_bits(f[5], sc, rs), quant_bits(f[6], sc, rs),
+                    quant_bits(f[7], sc, rs));
     reinterpret_cast<uint2 *>(q + (nb * 128 + r) * K + kb * 128)[c] = o;
   }
   if (threadIdx.x == 0) s[nb * kb_n + kb] = sc;
@@ -163,7 +166,7 @@ int launch_quant_weight_block(const uint16_t *w, int64_t N, int64_t K, int8_t *q
   if (blocks == 0) return WQ_OK;
   if (blocks > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
   quant_wblock_kernel<<<unsigned(blocks), 256, 0, st>>>(w, K, q, s);
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  return launched(1);
 }
 
 // ---------------------------------------------------------------------------
@@ -227,7 +230,7 @@ int launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *
   else if (nper <= 8) route_kernel<8><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
   else if (nper <= 16) route_kernel<16><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
   else route_kernel<32><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  return launched(1);
 }
 
 // ---------------------------------------------------------------------------
@@ -305,7 +308,7 @@ int launch_permute_f16(const int8_t *q, const float *s, int groups, int k, int64
   if (R == 0) return WQ_OK;
   if (R > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
   permute_f16_kernel<<<unsigned(R), 128, 0, st>>>(q, s, groups, k, K, sorted_pair, A16, sa, norm2);
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  return launched(1);
 }
 
 int launch_permute(const int8_t *q, const float *s, int groups, int k, int64_t K,
@@ -313,7 +316,7 @@ int launch_permute(const int8_t *q, const float *s, int groups, int k, int64_t K
   if (R == 0) return WQ_OK;
   if (R > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
   permute_kernel<<<unsigned(R), 128, 0, st>>>(q, s, groups, k, K, sorted_pair, A, sa);
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  return launched(1);
 }
 
 // ---------------------------------------------------------------------------
@@ -353,16 +356,17 @@ __global__ void __launch_bounds__(1024) silu_mul_quant_kernel(
   if constexpr (GV == 0) {
     amax = block_max(amax, red);
     const float sc = quant_scale(amax);
+    const float rs = __frcp_rn(sc);
     uint2 *dst = reinterpret_cast<uint2 *>(hq + row * I);
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int idx = threadIdx.x + i * blockDim.x;
       if (idx < nvec) {
         uint2 o;
-        o.x = pack_s8x4(quant_code(h[i][0], sc), quant_code(h[i][1], sc), quant_code(h[i][2], sc),
-                        quant_code(h[i][3], sc));
-        o.y = pack_s8x4(quant_code(h[i][4], sc), quant_code(h[i][5], sc), quant_code(h[i][6], sc),
-                        quant_code(h[i][7], sc));
+        o.x = pack_s8x4(quant_bits(h[i][0], sc, rs), quant_bits(h[i][1], sc, rs), quant_bits(h[i][2], sc, rs),
+                        quant_bits(h[i][3], sc, rs));
+        o.y = pack_s8x4(quant_bits(h[i][4], sc, rs), quant_bits(h[i][5], sc, rs), quant_bits(h[i][6], sc, rs),
+                        quant_bits(h[i][7], sc, rs));
         dst[idx] = o;
       }
     }
@@ -374,11 +378,12 @@ __global__ void __launch_bounds__(1024) silu_mul_quant_kernel(
     for (int o = GV / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     if (idx < nvec) {
       const float sc = quant_scale(amax);
+      const float rs = __frcp_rn(sc);
       uint2 o;
-      o.x = pack_s8x4(quant_code(h[0][0], sc), quant_code(h[0][1], sc), quant_code(h[0][2], sc),
-                      quant_code(h[0][3], sc));
-      o.y = pack_s8x4(quant_code(h[0][4], sc), quant_code(h[0][5], sc), quant_code(h[0][6], sc),
-                      quant_code(h[0][7], sc));
+      o.x = pack_s8x4(quant_bits(h[0][0], sc, rs), quant_bits(h[0][1], sc, rs), quant_bits(h[0][2], sc, rs),
+                      quant_bits(h[0][3], sc, rs));
+      o.y = pack_s8x4(quant_bits(h[0][4], sc, rs), quant_bits(h[0][5], sc, rs), quant_bits(h[0][6], sc, rs),
+                      quant_bits(h[0][7], sc, rs));
       reinterpret_cast<uint2 *>(hq + row * I)[idx] = o;
       if (idx % GV == 0) sh[row * (nvec / GV) + idx / GV] = sc;
     }
@@ -423,6 +428,7 @@ __global__ void __launch_bounds__(1024) silu_mul_quant_f16_kernel(
   }
   amax = block_max(amax, red);
   const float sc = quant_scale(amax);
+  const float rs = __frcp_rn(sc);
   uint4 *dst = reinterpret_cast<uint4 *>(hq16 + row * I);
   int n2 = 0;
 #pragma unroll
@@ -432,7 +438,7 @@ __global__ void __launch_bounds__(1024) silu_mul_quant_f16_kernel(
       int c[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        c[j] = quant_code(h[i][j], sc);
+        c[j] = quant_code(h[i][j], sc, rs);
         n2 += c[j] * c[j];
       }
       uint4 o;
@@ -470,7 +476,7 @@ int launch_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, const in
   } else {
     return WQ_ERR_UNSUPPORTED;
   }
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  return launched(1);
 }
 
 int launch_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group,
@@ -499,7 +505,7 @@ int launch_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group,
       default: return WQ_ERR_UNSUPPORTED;
     }
   }
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  return launched(1);
 }
 
 // ---------------------------------------------------------------------------
@@ -536,7 +542,7 @@ int launch_combine(const uint16_t *y, const int32_t *pair_to_row, const float *w
                    int64_t H, uint16_t *out, cudaStream_t st) {
   if (T == 0 || H == 0) return WQ_OK;
   combine_kernel<<<unsigned(T), 128, 0, st>>>(y, pair_to_row, w, k, H, out);
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  return launched(1);
 }
 
 }  // namespace wq

@@ -161,7 +161,7 @@ int launch_gemm_simt(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles
   const unsigned grid = unsigned(max_items < cap ? max_items : cap);
   if (a.A16 != nullptr) gemm_simt_kernel<true><<<grid, 256, 0, st>>>(a, tiles, ntiles, gate);
   else gemm_simt_kernel<false><<<grid, 256, 0, st>>>(a, tiles, ntiles, gate);
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  return launched(1);
 }
 
 }  // namespace wq

@@ -251,7 +251,7 @@ int launch_gemm_small(const GemmArgs &a, const Tile *tiles, const int32_t *ntile
   const int64_t max_items = int64_t(max_tiles) * ((a.N + WN - 1) / WN);
   const int grid = int(max_items < num_sms() ? max_items : num_sms());
   gemm_small_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(mW, m4, m8, m16, a, tiles, ntiles);
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  return launched(1);
 }
 
 }  // namespace wq

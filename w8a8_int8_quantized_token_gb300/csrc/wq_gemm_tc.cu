@@ -332,7 +332,7 @@ int launch_gemm_tc(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, 
   const int64_t max_items = int64_t(max_tiles) * (a.N / BN);
   const int grid = int(max_items < num_sms() ? max_items : num_sms());
   gemm_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(mA, mW, a, tiles, ntiles, gate, chunk_stages);
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  return launched(1);
 }
 
 }  // namespace wq

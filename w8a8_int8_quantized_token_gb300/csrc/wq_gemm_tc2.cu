@@ -397,7 +397,7 @@ int launch_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int 
   const int grid = int(max_items < num_sms() ? max_items : num_sms());
   gemm_tc2_kernel<TN, S8, S16><<<grid, NTHREADS, P::SMEM_BYTES, st>>>(mW, m16, m64, m256, a, tiles,
                                                                       ntiles, redo);
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  return launched(1);
 }
 
 // `tiles` must be built with gemm_tc2_tile_rows(a) rows per tile.

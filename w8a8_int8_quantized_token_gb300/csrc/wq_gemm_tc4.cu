@@ -389,7 +389,7 @@ int launch_gemm_tc4(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles,
   const int pairs = int(max_items < pairs_resident ? max_items : pairs_resident);
   gemm_tc4_kernel<<<2 * pairs, NTHREADS, SMEM_BYTES, st>>>(mW, m8, m32, m128, a, tiles, ntiles,
                                                           redo);
-  return cudaPeekAtLastError() == cudaSuccess ? WQ_OK : WQ_ERR_LAUNCH;
+  return launched(1);
 }
 
 }  // namespace wq
