@@ -51,7 +51,20 @@ def layer_ops(T, H, I, k):
 # summaries under profiles/ give the commands).  A figure holds only for the
 # kernel source it was measured on: it is reported while that file's SHA-256
 # matches, else the traffic is null.
-TRAFFIC = {}
+_TC5 = {"kernel": "gemm_tc5_kernel", "file": "wq_gemm_tc5.cu",
+        "sha256": "d589c6a016304e83eff5afd41c5a01191e0e69804715673dc4ec6b6c3d6b1c46",
+        "bytes": 8 * (1.080670e9 + 62.923264e6),
+        "how": "ncu capture of GEMM1 at 1024 tokens / 32 experts (same 256 rows per expert), "
+               "dram read+write x 8 experts ratio (profiles/gemm_tc5_tc4_reduced_prefill.md)"}
+TRAFFIC = {
+    "prefill": _TC5,
+    "prefill_f32": _TC5,
+    "decode": {"kernel": "gemm_small_kernel", "file": "wq_gemm_small.cu",
+               "sha256": "e53537d8fa0b3b99d98faf1a3cf1183a0faa56d97eb8a556f491ad0c06afdbdc",
+               "bytes": 8 * (941.189888e6 + 4.634624e6),
+               "how": "ncu capture of GEMM1 at 16 tokens / 32 experts (same 4 rows per expert), "
+                      "dram read+write x 8 experts ratio (profiles/gemm_small_reduced_decode.md)"},
+}
 
 
 def measured_traffic(cfg_name):
