@@ -192,9 +192,9 @@ class Layer:
         self.sp, self.p2r = e(R, dt=torch.int32), e(R, dt=torch.int32)
         self.aws_n = self.lib.wq_moe_align_workspace_size(T, k, E)
         self.aws = e(max(self.aws_n, 1), dt=torch.uint8)
-        # the one-call layer's choice: fp16-stored codes for the channel-wise
-        # layer when both GEMM widths are multiples of 256
-        self.f16 = (cfg.scheme == "channel" and (2 * I) % 256 == 0
+        # the one-call layer's choice: fp16-stored codes when both GEMM widths
+        # are multiples of 256 and experts hold many rows
+        self.f16 = ((2 * I) % 256 == 0
                     and H % 256 == 0 and R > 64 * E)
         cdt = torch.float16 if self.f16 else torch.int8
         self.A, self.sa = e(R, H, dt=cdt), e(R * self.g1, dt=torch.float32)
@@ -231,20 +231,21 @@ class Layer:
                           P(self.p2r), P(self.aws), self.aws_n, P(self.status), st), "align")
         rec(3)
         if self.f16:
-            ok(L.wq_moe_permute_f16(P(self.q), P(self.s), 1, T, k, H, P(self.sp), R, P(self.A),
+            ok(L.wq_moe_permute_f16(P(self.q), P(self.s), self.g1, T, k, H, P(self.sp), R, P(self.A),
                                     P(self.sa), P(self.anorm), st), "permute")
             rec(4)
             ok(L.wq_grouped_gemm_w8a8_f16codes(P(self.A), P(self.anorm), P(self.sa), P(self.W13),
-                                               P(self.S13), P(self.offsets), E, R, 2 * I, H, ac, 0,
-                                               P(self.gu), P(self.gws), self.gws_n, P(self.status),
-                                               st), "gemm1")
+                                               P(self.S13), P(self.offsets), E, R, 2 * I, H, sc, ac,
+                                               0, P(self.gu), P(self.gws), self.gws_n,
+                                               P(self.status), st), "gemm1")
             rec(5)
-            ok(L.wq_silu_mul_quant_f16(P(self.gu), R, I, P(self.hq), P(self.sh), P(self.hnorm), st),
-               "silu_mul_quant")
+            ok(L.wq_silu_mul_quant_f16(P(self.gu), R, I, 128 if c.scheme == "block" else 0,
+                                       P(self.hq), P(self.sh), P(self.hnorm), st), "silu_mul_quant")
             rec(6)
             ok(L.wq_grouped_gemm_w8a8_f16codes(P(self.hq), P(self.hnorm), P(self.sh), P(self.W2),
-                                               P(self.S2), P(self.offsets), E, R, H, I, ac, 0, P(self.y),
-                                               P(self.gws), self.gws_n, P(self.status), st), "gemm2")
+                                               P(self.S2), P(self.offsets), E, R, H, I, sc, ac, 0,
+                                               P(self.y), P(self.gws), self.gws_n, P(self.status),
+                                               st), "gemm2")
         else:
             ok(L.wq_moe_permute(P(self.q), P(self.s), self.g1, T, k, H, P(self.sp), R, P(self.A),
                                 P(self.sa), st), "permute")

@@ -204,29 +204,34 @@ WQ_API int wq_grouped_gemm_w8a8_noalloc(const int8_t *A, const float *sa, const 
  * [-127, 127] as the int8 codes, two bytes each, with each row's squared L2
  * norm (sum of code^2, int32).  This is the form the CTA-pair GEMM engines
  * read directly (TMA straight into the MMA layout); the one-call layer uses
- * it for the channel-wise scheme with either accumulator.
+ * it when experts hold many rows and both GEMM widths are multiples of 256.
  *
  * wq_moe_permute_f16: as wq_moe_permute, writing A16 uint16 (fp16 bits)
  *   [R][K] and norm2 int32 [R] (padding rows: zero codes, scale, norm).
- * wq_silu_mul_quant_f16: as wq_silu_mul_quant with one scale per row
- *   (group 0), writing hq16 (fp16 bits) [R][I] and norm2 int32 [R].
- * wq_grouped_gemm_w8a8_f16codes: as wq_grouped_gemm_w8a8 with the channel
- *   scheme (acc WQ_ACC_I32 or WQ_ACC_F32; out_type WQ_OUT_I32 only with
- *   WQ_ACC_I32), A given as fp16 codes with their row norms
- *   (a_norm2 must be the exact sums of squares: they decide whether the
- *   single-pass float32 sums are provably exact, else the launch is
- *   recomputed exactly).  Requirements: N % 256 == 0, K % 128 == 0,
- *   K <= 65536.  Workspace: wq_grouped_gemm_workspace_size(R, E). */
+ * wq_silu_mul_quant_f16: as wq_silu_mul_quant (group 0: one scale per row;
+ *   32/64/128/256: per-group scales, sh [R][I/group]), writing hq16 (fp16
+ *   bits) [R][I]; with group 0 also norm2 int32 [R] (with a group, norm2 is
+ *   not written and may be NULL).
+ * wq_grouped_gemm_w8a8_f16codes: as wq_grouped_gemm_w8a8 with A given as
+ *   fp16 codes.  Channel scheme (acc WQ_ACC_I32 or WQ_ACC_F32; out_type
+ *   WQ_OUT_I32 only with WQ_ACC_I32): a_norm2 must be the exact row sums of
+ *   squares (they decide whether the single-pass float32 sums are provably
+ *   exact, else the launch is recomputed exactly).  Block scheme (sa
+ *   [R][K/128], sw [E][N/128][K/128], bf16 output): a_norm2 is not read and
+ *   may be NULL; every 128-wide K block's sum is exact in float32.
+ *   Requirements: N % 256 == 0, K % 128 == 0, K <= 65536.
+ *   Workspace: wq_grouped_gemm_workspace_size(R, E). */
 WQ_API int wq_moe_permute_f16(const int8_t *q, const float *s, int groups, int T, int k, int64_t K,
                               const int32_t *sorted_pair, int64_t R, uint16_t *A16, float *sa,
                               int32_t *norm2, wq_stream_t stream);
-WQ_API int wq_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, uint16_t *hq16,
-                                 float *sh, int32_t *norm2, wq_stream_t stream);
+WQ_API int wq_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, int group,
+                                 uint16_t *hq16, float *sh, int32_t *norm2, wq_stream_t stream);
 WQ_API int wq_grouped_gemm_w8a8_f16codes(const uint16_t *A16, const int32_t *a_norm2,
                                          const float *sa, const int8_t *W, const float *sw,
                                          const int32_t *offsets, int E, int64_t R, int64_t N,
-                                         int64_t K, int acc, int out_type, void *out, void *ws,
-                                         size_t ws_bytes, int32_t *status, wq_stream_t stream);
+                                         int64_t K, int scheme, int acc, int out_type, void *out,
+                                         void *ws, size_t ws_bytes, int32_t *status,
+                                         wq_stream_t stream);
 
 /* Masked layout [LL]: A int8 [E][Mmax][K] with per-row scales sa
  * ([E][Mmax] or [E][Mmax][K/128]) and valid counts masked_m int32 [E]

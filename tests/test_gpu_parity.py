@@ -307,6 +307,8 @@ def _layer_case(cfg):
     synth.small_config("small_i32", T=150, H=384, I=256, E=6, k=3),
     synth.small_config("small_f32", T=97, H=512, I=256, E=7, k=2, acc="f32"),
     synth.small_config("small_block", T=130, H=384, I=256, E=5, k=3, scheme="block", acc="f32"),
+    # widths multiples of 256 and many rows per expert: the fp16-code block engine
+    synth.small_config("small_block_f16", T=300, H=512, I=256, E=4, k=2, scheme="block", acc="f32"),
     synth.small_config("hot", T=300, H=256, I=128, E=4, k=1),
 ], ids=lambda c: c.name)
 def test_layer_forward(cfg):
@@ -349,12 +351,13 @@ def test_layer_forward_masked():
 
 
 # ---------------------------------------------------------------- fp16-stored codes
-def test_moe_permute_f16():
+@pytest.mark.parametrize("groups", [1, 56])
+def test_moe_permute_f16(groups):
     T, k, E, K = 200, 8, 64, 7168
     rng = np.random.default_rng(21)
     ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
     q = rng.integers(-127, 128, (T, K), dtype=np.int8)
-    s = rng.random(T).astype(np.float32)
+    s = rng.random(T).astype(np.float32) if groups == 1 else rng.random((T, groups)).astype(np.float32)
     _, _, spo, _ = O.moe_align(ids, E, 4)
     A16, sa, n2 = wq.moe_permute_f16(torch.from_numpy(q).to(DEV), torch.from_numpy(s).to(DEV),
                                      torch.from_numpy(spo).to(DEV), k)
@@ -364,15 +367,43 @@ def test_moe_permute_f16():
     assert np.array_equal(np_(n2), (Ao.astype(np.int64) ** 2).sum(1))
 
 
-def test_silu_mul_quant_f16():
+@pytest.mark.parametrize("group", [0, 32, 128])
+def test_silu_mul_quant_f16(group):
     R, I = 70, 2048
     g = torch.Generator().manual_seed(22)
     gu = (torch.randn(R, 2 * I, generator=g) * 4).to(torch.bfloat16)
-    hq16, sh, n2 = wq.silu_mul_quant_f16(gu.to(DEV))
-    hqo, sho = O.silu_mul_quant(bits(gu), I, 0)
+    hq16, sh, n2 = wq.silu_mul_quant_f16(gu.to(DEV), group)
+    hqo, sho = O.silu_mul_quant(bits(gu), I, group)
     assert np.array_equal(np_(hq16).astype(np.int32), hqo.astype(np.int32))
-    assert np.array_equal(np_(sh), sho)
-    assert np.array_equal(np_(n2), (hqo.astype(np.int64) ** 2).sum(1))
+    assert np.array_equal(np_(sh).reshape(sho.shape), sho)
+    if group == 0:
+        assert np.array_equal(np_(n2), (hqo.astype(np.int64) ** 2).sum(1))
+
+
+@pytest.mark.parametrize("K", [384, 2048])
+def test_grouped_gemm_f16codes_block(K):
+    """The block-wise CTA-pair engine (token tiles of up to 160 rows, per-K-
+    block drains of a float32 running sum): segments around the tile size
+    (0, 1, 16, 17, 159, 160, 161, 330 rows) against the oracle's block GEMM."""
+    counts = [3, 0, 160, 1, 161, 330, 16, 17, 159]
+    E, N = len(counts), 512
+    rng = np.random.default_rng(29)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    R = int(offs[-1])
+    A = rng.integers(-127, 128, (R, K), dtype=np.int8)
+    W = rng.integers(-127, 128, (E, N, K), dtype=np.int8)
+    A[:3] = 127
+    W[0, :2] = -127
+    sa = (rng.random((R, K // 128)) * 0.05).astype(np.float32)
+    sw = (rng.random((E, N // 128, K // 128)) * 1e-3).astype(np.float32)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    st = wq.new_status()
+    out = torch.full((R, N), 5.0, dtype=torch.bfloat16, device=DEV)
+    wq.grouped_gemm_w8a8_f16codes(t(A).to(torch.float16), None, t(sa), t(W), t(sw), t(offs),
+                                  acc="f32", out=out, status=st, scheme="block")
+    assert int(st.item()) == 0
+    assert_bf16_equal(bits(out), O.grouped_gemm_w8a8(A, sa, W, sw, offs, "block", "f32"),
+                      "f16 codes block gemm")
 
 
 @pytest.mark.parametrize("K", [2048, 4096])

@@ -47,8 +47,8 @@ _SIGS = {
     "wq_grouped_gemm_w8a8": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
     "wq_grouped_gemm_w8a8_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _I, _P, _P, _P]),
     "wq_moe_permute_f16": (_I, [_P, _P, _I, _I, _I, _L, _P, _L, _P, _P, _P, _P]),
-    "wq_silu_mul_quant_f16": (_I, [_P, _L, _L, _P, _P, _P, _P]),
-    "wq_grouped_gemm_w8a8_f16codes": (_I, [_P, _P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _P, _P, _S, _P, _P]),
+    "wq_silu_mul_quant_f16": (_I, [_P, _L, _L, _I, _P, _P, _P, _P]),
+    "wq_grouped_gemm_w8a8_f16codes": (_I, [_P, _P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
     "wq_grouped_gemm_masked_workspace_size": (_S, [_I, _I]),
     "wq_grouped_gemm_w8a8_masked": (_I, [_P, _P, _P, _I, _I, _P, _P, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
     "wq_silu_mul_quant": (_I, [_P, _L, _L, _I, _P, _P, _P]),
@@ -219,23 +219,26 @@ def moe_permute_f16(q, s, sorted_pair, k):
     return A16, sa, n2
 
 
-def silu_mul_quant_f16(gu):
-    """SiLU-mul + per-row re-quantization into fp16-stored codes: (hq16, sh, norm2)."""
+def silu_mul_quant_f16(gu, group=0):
+    """SiLU-mul + re-quantization into fp16-stored codes: (hq16, sh, norm2);
+    with a group, sh is [R, I/group] and norm2 is None."""
     _dev(gu, torch.bfloat16, "gu")
     R, I2 = gu.shape
     I = I2 // 2
     hq = torch.empty(R, I, dtype=torch.float16, device=gu.device)
-    sh = torch.empty(R, dtype=torch.float32, device=gu.device)
-    n2 = torch.empty(R, dtype=torch.int32, device=gu.device)
-    _check(lib().wq_silu_mul_quant_f16(_ptr(gu), R, I, _ptr(hq), _ptr(sh), _ptr(n2), _stream()),
+    sh = torch.empty(R, I // group if group else 1, dtype=torch.float32, device=gu.device)
+    n2 = torch.empty(R, dtype=torch.int32, device=gu.device) if group == 0 else None
+    _check(lib().wq_silu_mul_quant_f16(_ptr(gu), R, I, group, _ptr(hq), _ptr(sh),
+                                       _ptr(n2) if n2 is not None else None, _stream()),
            "wq_silu_mul_quant_f16")
-    return hq, sh, n2
+    return hq, (sh.view(R) if group == 0 else sh), n2
 
 
 def grouped_gemm_w8a8_f16codes(A16, a_norm2, sa, W, sw, offsets, acc="i32", out_type="bf16",
-                               out=None, status=None):
+                               out=None, status=None, scheme="channel"):
     _dev(A16, torch.float16, "A16")
-    _dev(a_norm2, torch.int32, "a_norm2")
+    if a_norm2 is not None:
+        _dev(a_norm2, torch.int32, "a_norm2")
     _dev(sa, torch.float32, "sa")
     _dev(W, torch.int8, "W")
     _dev(sw, torch.float32, "sw")
@@ -248,8 +251,10 @@ def grouped_gemm_w8a8_f16codes(A16, a_norm2, sa, W, sw, offsets, acc="i32", out_
     nws = lib().wq_grouped_gemm_workspace_size(R, E)
     ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=A16.device)
     st = status if status is not None else new_status(A16.device)
-    _check(lib().wq_grouped_gemm_w8a8_f16codes(_ptr(A16), _ptr(a_norm2), _ptr(sa), _ptr(W), _ptr(sw),
-                                               _ptr(offsets), E, R, N, K, ACC[acc], OUT[out_type],
+    _check(lib().wq_grouped_gemm_w8a8_f16codes(_ptr(A16), _ptr(a_norm2) if a_norm2 is not None else None,
+                                               _ptr(sa), _ptr(W), _ptr(sw),
+                                               _ptr(offsets), E, R, N, K, SCHEME[scheme], ACC[acc],
+                                               OUT[out_type],
                                                _ptr(out),
                                                _ptr(ws), nws, _ptr(st), _stream()),
            "wq_grouped_gemm_w8a8_f16codes")

@@ -26,6 +26,10 @@ bool gemm_tc5_supported(const GemmArgs &a);
 int gemm_tc5_tile_rows();
 int launch_gemm_small(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
                       cudaStream_t st);
+int launch_gemm_tc6(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
+                    cudaStream_t st);
+bool gemm_tc6_supported(const GemmArgs &a);
+int gemm_tc6_tile_rows();
 bool gemm_small_supported(const GemmArgs &a);
 int gemm_small_max_rows();
 }  // namespace wq
@@ -131,6 +135,14 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
   const bool masked = a.masked_m != nullptr;
   GemmWs w = carve_gemm_ws(a.ws, a.R, a.E, a.Mmax, masked);
   const int32_t *gate = nullptr;
+  if (a.A16 != nullptr && a.scheme == WQ_SCHEME_BLOCK) {
+    // block-wise on fp16 codes: every K block's sum is exact in float32, so
+    // the CTA-pair block engine needs no check and no recompute
+    if (!gemm_tc6_supported(a)) return WQ_ERR_UNSUPPORTED;
+    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, gemm_tc6_tile_rows(), a.R,
+                              w.t128, w.n128, nullptr, st));
+    return launch_gemm_tc6(a, w.t128, w.n128, int(w.m128), st);
+  }
   if (a.A16 != nullptr) {
     // fp16-stored codes: the CTA-pair engine, then the CUDA-core engine reading
     // fp16 codes as its exact recompute (it exits at once when *redo == 0)
@@ -327,30 +339,32 @@ int wq_moe_permute_f16(const int8_t *q, const float *s, int groups, int T, int k
   return launch_permute_f16(q, s, groups, k, K, sorted_pair, R, A16, sa, norm2, stream);
 }
 
-int wq_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, uint16_t *hq16, float *sh,
-                          int32_t *norm2, wq_stream_t stream) {
+int wq_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, int group, uint16_t *hq16,
+                          float *sh, int32_t *norm2, wq_stream_t stream) {
   if (R < 0 || I < 0) return WQ_ERR_INVALID_ARG;
+  if (group != 0 && !group_ok(group)) return WQ_ERR_UNSUPPORTED;
   if (R == 0 || I == 0) return WQ_OK;
-  if (!gu || !hq16 || !sh || !norm2) return WQ_ERR_INVALID_ARG;
-  if (I % 8 || !al16(gu) || !al16(hq16)) return WQ_ERR_UNSUPPORTED;
+  if (!gu || !hq16 || !sh || (group == 0 && !norm2)) return WQ_ERR_INVALID_ARG;
+  if (I % 8 || (group && I % group) || !al16(gu) || !al16(hq16)) return WQ_ERR_UNSUPPORTED;
   WQ_TRY(check_device());
-  return launch_silu_mul_quant_f16(gu, R, I, nullptr, 0, hq16, sh, norm2, stream);
+  return launch_silu_mul_quant_f16(gu, R, I, group, nullptr, 0, hq16, sh, norm2, stream);
 }
 
 int wq_grouped_gemm_w8a8_f16codes(const uint16_t *A16, const int32_t *a_norm2, const float *sa,
                                   const int8_t *W, const float *sw, const int32_t *offsets, int E,
-                                  int64_t R, int64_t N, int64_t K, int acc, int out_type,
-                                  void *out, void *ws, size_t ws_bytes, int32_t *status,
-                                  wq_stream_t stream) {
+                                  int64_t R, int64_t N, int64_t K, int scheme, int acc,
+                                  int out_type, void *out, void *ws, size_t ws_bytes,
+                                  int32_t *status, wq_stream_t stream) {
   if (R < 0 || E > 4096) return WQ_ERR_INVALID_ARG;
   if (R == 0) return WQ_OK;
-  WQ_TRY(check_gemm_common(W, sw, E, N, K, WQ_SCHEME_CHANNEL, acc, out_type, out));
-  if (!A16 || !a_norm2 || !sa || !offsets) return WQ_ERR_INVALID_ARG;
-  if (!al16(A16) || N % 256 || K > 65536) return WQ_ERR_UNSUPPORTED;
+  WQ_TRY(check_gemm_common(W, sw, E, N, K, scheme, acc, out_type, out));
+  const bool blk = scheme == WQ_SCHEME_BLOCK;
+  if (!A16 || (!blk && !a_norm2) || !sa || !offsets) return WQ_ERR_INVALID_ARG;
+  if (!al16(A16) || N % 256 || K > 65536 || (blk && K % 128)) return WQ_ERR_UNSUPPORTED;
   if (R >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;
   if (ws_bytes < gemm_ws_bytes(R, E, 0, false) || !ws) return WQ_ERR_WORKSPACE;
   WQ_TRY(check_device());
-  GemmArgs a{nullptr, A16, a_norm2, sa, W, sw, offsets, nullptr, 0, E, R, N, K, WQ_SCHEME_CHANNEL,
+  GemmArgs a{nullptr, A16, a_norm2, sa, W, sw, offsets, nullptr, 0, E, R, N, K, scheme,
              acc, out_type, out, ws, status};
   return launch_grouped_gemm(a, stream);
 }
@@ -471,24 +485,26 @@ int run_forward(const uint16_t *x, const float *logits, const int8_t *W13, const
   WQ_TRY(launch_quant_rows(x, T, H, H, blk ? 128 : 0, b.q, b.s, st));
   WQ_TRY(launch_align(b.ids, T, k, E, 1, b.counts, b.offsets, b.sorted_pair, b.pair_to_row,
                       b.align_ws, status, st));
-  // channel-wise (either accumulator): activation codes travel as fp16 values
-  // with row norms (the CTA-pair GEMM engines); block-wise and other widths
-  // use int8 codes
+  // with many rows per expert and widths that are multiples of 256 the
+  // activation codes travel as fp16 values (the CTA-pair GEMM engines; row
+  // norms for the channel-wise exactness check); otherwise int8 codes
   GemmArgs probe{nullptr, reinterpret_cast<const uint16_t *>(b.A), b.anorm, b.sa, W13, sw13,
                  b.offsets, nullptr, 0, E, R, int64_t(2) * I, H, scheme, acc, WQ_OUT_BF16, b.gu,
                  b.gemm_ws, status};
   // (with few rows per expert the GEMMs stream weights from HBM and the
   // int8 path's 64-token engine with its deeper weight ring is faster)
-  const bool f16 = !blk && (2 * I) % 256 == 0 && H % 256 == 0 &&
-                   R > int64_t(64) * E && gemm_tc4_supported(probe);
+  const bool f16 = (2 * I) % 256 == 0 && H % 256 == 0 && R > int64_t(64) * E &&
+                   (blk ? gemm_tc6_supported(probe) : gemm_tc4_supported(probe));
   if (f16) {
     uint16_t *A16 = reinterpret_cast<uint16_t *>(b.A);
     uint16_t *hq16 = reinterpret_cast<uint16_t *>(b.hq);
-    WQ_TRY(launch_permute_f16(b.q, b.s, 1, k, H, b.sorted_pair, R, A16, b.sa, b.anorm, st));
+    WQ_TRY(launch_permute_f16(b.q, b.s, blk ? H / 128 : 1, k, H, b.sorted_pair, R, A16, b.sa,
+                              b.anorm, st));
     GemmArgs f1{nullptr, A16, b.anorm, b.sa, W13, sw13, b.offsets, nullptr, 0, E, R,
                 int64_t(2) * I, H, scheme, acc, WQ_OUT_BF16, b.gu, b.gemm_ws, status};
     WQ_TRY(launch_grouped_gemm(f1, st));
-    WQ_TRY(launch_silu_mul_quant_f16(b.gu, R, I, nullptr, 0, hq16, b.sh, b.hnorm, st));
+    WQ_TRY(launch_silu_mul_quant_f16(b.gu, R, I, blk ? 128 : 0, nullptr, 0, hq16, b.sh, b.hnorm,
+                                     st));
     GemmArgs f2{nullptr, hq16, b.hnorm, b.sh, W2, sw2, b.offsets, nullptr, 0, E, R, H, I, scheme,
                 acc, WQ_OUT_BF16, b.y, b.gemm_ws, status};
     WQ_TRY(launch_grouped_gemm(f2, st));

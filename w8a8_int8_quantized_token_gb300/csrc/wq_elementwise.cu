@@ -321,10 +321,12 @@ int launch_permute(const int8_t *q, const float *s, int groups, int k, int64_t K
 
 // ---------------------------------------------------------------------------
 // SiLU-and-mul + re-quantization: one CTA per row, V vector pairs per thread.
-template <int V, int GV>  // GV = 0: one scale per row; else lanes per group
+// F16: write the codes as fp16 values (group mode only).
+template <int V, int GV, bool F16 = false>  // GV = 0: one scale per row; else lanes per group
 __global__ void __launch_bounds__(1024) silu_mul_quant_kernel(
     const uint16_t *__restrict__ gu, int64_t I, const int32_t *__restrict__ masked_m, int Mmax,
-    int8_t *__restrict__ hq, float *__restrict__ sh) {
+    void *__restrict__ hq_out, float *__restrict__ sh) {
+  int8_t *hq = static_cast<int8_t *>(hq_out);
   __shared__ float red[32];
   const int64_t row = blockIdx.x;
   if (masked_m != nullptr) {
@@ -384,7 +386,14 @@ __global__ void __launch_bounds__(1024) silu_mul_quant_kernel(
                       quant_bits(h[0][3], sc, rs));
       o.y = pack_s8x4(quant_bits(h[0][4], sc, rs), quant_bits(h[0][5], sc, rs), quant_bits(h[0][6], sc, rs),
                       quant_bits(h[0][7], sc, rs));
-      reinterpret_cast<uint2 *>(hq + row * I)[idx] = o;
+      if constexpr (F16) {
+        uint4 w;  // the same codes as fp16 values (exact)
+        tc::s8x4_to_f16x4(o.x, w.x, w.y);
+        tc::s8x4_to_f16x4(o.y, w.z, w.w);
+        reinterpret_cast<uint4 *>(static_cast<uint16_t *>(hq_out) + row * I)[idx] = w;
+      } else {
+        reinterpret_cast<uint2 *>(hq + row * I)[idx] = o;
+      }
       if (idx % GV == 0) sh[row * (nvec / GV) + idx / GV] = sc;
     }
   }
@@ -462,13 +471,25 @@ __global__ void __launch_bounds__(1024) silu_mul_quant_f16_kernel(
   }
 }
 
-int launch_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, const int32_t *masked_m,
-                              int Mmax, uint16_t *hq16, float *sh, int32_t *norm2,
-                              cudaStream_t st) {
+int launch_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, int group,
+                              const int32_t *masked_m, int Mmax, uint16_t *hq16, float *sh,
+                              int32_t *norm2, cudaStream_t st) {
   if (R == 0 || I == 0) return WQ_OK;
   if (R > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
   const int64_t nvec = I / 8;
   auto rnd = [](int64_t t) { int v = int(((t + 31) / 32) * 32); return v < 32 ? 32 : v; };
+  if (group != 0) {  // per-group scales, fp16 codes, no norms
+    if (nvec > 1024) return WQ_ERR_UNSUPPORTED;
+    const int th = rnd(nvec);
+    switch (group) {
+      case 32: silu_mul_quant_kernel<1, 4, true><<<unsigned(R), th, 0, st>>>(gu, I, masked_m, Mmax, hq16, sh); break;
+      case 64: silu_mul_quant_kernel<1, 8, true><<<unsigned(R), th, 0, st>>>(gu, I, masked_m, Mmax, hq16, sh); break;
+      case 128: silu_mul_quant_kernel<1, 16, true><<<unsigned(R), th, 0, st>>>(gu, I, masked_m, Mmax, hq16, sh); break;
+      case 256: silu_mul_quant_kernel<1, 32, true><<<unsigned(R), th, 0, st>>>(gu, I, masked_m, Mmax, hq16, sh); break;
+      default: return WQ_ERR_UNSUPPORTED;
+    }
+    return launched(1);
+  }
   if (nvec <= 1024) {
     silu_mul_quant_f16_kernel<1><<<unsigned(R), rnd(nvec), 0, st>>>(gu, I, masked_m, Mmax, hq16, sh, norm2);
   } else if (nvec <= 4096) {
