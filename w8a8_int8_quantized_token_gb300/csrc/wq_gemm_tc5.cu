@@ -182,7 +182,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       for (int ip = pair; ip < items && ok; ip += npairs, ++ii) {
         const Tile tl = tiles[ip / NBP];
         const int nm = nmma_of(tl.rows);
-        const int n0 = nm < 256 ? nm : 256, n1 = nm - n0;
+        // above 256 tokens: two MMAs of balanced widths (multiples of 16, so
+        // the second token block starts on an 8-row swizzle group)
+        const int n0 = nm <= 256 ? nm : ((nm / 2 + 15) & ~15), n1 = nm - n0;
         const uint32_t idesc0 = idesc_f16(WM, n0), idesc1 = idesc_f16(WM, n1 > 0 ? n1 : 16);
         if (!mbar_wait(bar(B_ACC_EMPTY), (ii & 1) ^ 1, abort_flag)) {
           fail();
@@ -205,7 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           if (n1 > 0) {
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-              mma_f16_ts(tmem + 256u, wt + 8u * kk, sdesc(t0 + 256u * 128u + 32u * kk), idesc1,
+              mma_f16_ts(tmem + uint32_t(n0), wt + 8u * kk, sdesc(t0 + uint32_t(n0) * 128u + 32u * kk), idesc1,
                          (i | kk) ? 1u : 0u);
           }
           mma_commit(bar(B_WT_EMPTY + swt));
