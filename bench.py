@@ -426,18 +426,97 @@ def run_masked(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+# dense W8A8 linear workloads ("Norm Linear"): (tokens, K, N) of DeepSeek-V3's
+# dense-MLP gate_up projection (hidden 7168 -> 2 x 18432) at prefill
+LINEAR = {"linear": (8192, 7168, 36864)}
+
+
+def run_linear(args, name):
+    """The dense W8A8 linear: quantize x per token, INT8 GEMM with its
+    dequantization (wq_linear_w8a8).  One step = one call."""
+    from w8a8_int8_quantized_token_gb300 import binding as wq
+    from w8a8_int8_quantized_token_gb300 import build_lib
+    T, K, N = LINEAR[name]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build_lib.build()
+    wq.init(0)
+    g = torch.Generator(device=dev).manual_seed(0)
+    x = torch.randn(T, K, generator=g, device=dev).to(torch.bfloat16)
+    w = (torch.randn(N, K, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    Wq, sw = wq.quantize_weight(w, "channel")
+    del w
+    out = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
+    ws = wq.linear_workspace(T, K, N, "channel", dev)
+    st = wq.new_status(dev)
+    step = lambda xx: wq.linear_w8a8(xx, Wq, sw, "channel", "i32", out=out, ws=ws, status=st)
+    for _ in range(args.warmup):
+        step(x)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize()
+        n0 = wq.lib().wq_kernel_launches()
+        e0.record()
+        for _ in range(args.steps):
+            step(x)
+        e1.record()
+        launches = wq.lib().wq_kernel_launches() - n0
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    # end to end: the input from pinned host memory, the output back
+    xh = x.cpu().pin_memory()
+    outh = torch.empty(T, N, dtype=torch.bfloat16, pin_memory=True)
+    xd = torch.empty_like(x)
+    for _ in range(args.warmup):
+        xd.copy_(xh, non_blocking=True); step(xd); outh.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.steps):
+        xd.copy_(xh, non_blocking=True); step(xd); outh.copy_(out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    flops = 2.0 * T * N * K
+    peaks, src = load_peaks()
+    tf = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    ach = flops / (ms / 1e3) / 1e12
+    line = {"metric": METRIC, "value": ach, "unit": "TOPS", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {"workload": f"dense W8A8 INT8 linear (DeepSeek-V3 dense-MLP gate_up shape), "
+                                   f"channel-wise, int32 accumulator: {T} tokens, K {K}, N {N}",
+                       "l2": "inputs larger than L2 (264 MB of int8 weights, 117 MB of "
+                             "activations, 604 MB of output per step)",
+                       "parallelism": "single"},
+            "gpu_launches": launches,
+            "roofline": {"bound": "tensor", "kernel": "wq_linear_w8a8 (quantize + INT8 GEMM)",
+                         "achieved": ach, "peak": tf, "unit": "TFLOP/s", "frac": ach / tf,
+                         "traffic": None, "flops": flops,
+                         "peak_source": f"{src} bf16 sustained (fp16 tcgen05 kind::f16)"},
+            "e2e": {"value": flops / (e2e_ms / 1e3) / 1e12, "unit": "TOPS",
+                    "h2d_bytes_per_step": T * K * 2, "d2h_bytes_per_step": T * N * 2,
+                    "ms_per_step": e2e_ms},
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", default="prefill", choices=list(synth.CONFIGS))
+    ap.add_argument("--config", default="prefill", choices=list(synth.CONFIGS) + list(LINEAR))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling)")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (profiling)")
     args = ap.parse_args()
+    if args.config in LINEAR:
+        run_linear(args, args.config)
+        return
     cfg = synth.CONFIGS[args.config]
     if args.tokens or args.experts:
         import dataclasses

@@ -302,6 +302,23 @@ WQ_API int wq_moe_forward_masked(const int8_t *a, const float *sa, const int32_t
                           const float *sw2, int H, int I, int scheme, int acc, uint16_t *y,
                           void *ws, size_t ws_bytes, int32_t *status, wq_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Dense W8A8 INT8 linear [CW] (Modifications, "Norm Linear": the model's
+ * non-MoE linear layers run as a w8a8 INT8 GEMM).  out = dequant(quant(x)
+ * W^T): the activation quantization of the scheme (per token, or per token
+ * per 128-group for the block scheme), the INT8 GEMM and its dequantization
+ * exactly as wq_grouped_gemm_w8a8 with one expert.
+ *   x bf16 [T][K] (leading dimension ldx), W int8 [N][K], sw float [N]
+ *   (channel) or [N/128][K/128] (block), out bf16 [T][N] contiguous.
+ * Requirements: K % 128 == 0, N % 128 == 0, K <= 65536, ldx % 8 == 0, x, W
+ * and out 16-byte aligned.  T == 0 enqueues nothing.
+ * Workspace: wq_linear_w8a8_workspace_size(T, K, N, scheme) (0: the shape is
+ * not supported).  Device-side errors go to *status (may be NULL). */
+WQ_API size_t wq_linear_w8a8_workspace_size(int64_t T, int64_t K, int64_t N, int scheme);
+WQ_API int wq_linear_w8a8(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, const int8_t *W,
+                          const float *sw, int64_t N, int scheme, int acc, uint16_t *out, void *ws,
+                          size_t ws_bytes, int32_t *status, wq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

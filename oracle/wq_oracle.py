@@ -446,3 +446,18 @@ def moe_forward_masked(a_q, a_s, masked_m, W13, S13, W2, S2, scheme="channel", a
         hq, sh = silu_mul_quant(gu, I, 0 if scheme == "channel" else 128)
         y[e, :m] = f32_to_bf16(gemm_dequant(hq, sh, W2[e], S2[e], scheme, acc))
     return y, valid
+
+
+def linear_w8a8(x_bits: np.ndarray, w: np.ndarray, sw: np.ndarray, scheme: str = "channel",
+                acc: str = "i32") -> np.ndarray:
+    """Dense W8A8 INT8 linear ("Norm Linear" in [Feature] DeepSeek V3/R1 INT8
+    Quantization (channel-wise), Modifications: the non-MoE linears run as a
+    w8a8 INT8 GEMM).  The activation quantization of the scheme (per token,
+    or per token per 128-group), then the INT8 GEMM with its dequantization
+    (gemm_dequant), rounded to bf16.  x_bits bf16 bits [T, K]; w int8 [N, K];
+    sw [N] or [N/128, K/128].  Returns bf16 bits [T, N]."""
+    if scheme == "channel":
+        q, s = quantize_per_token(x_bits)
+    else:
+        q, s = quantize_per_token_group(x_bits, KTILE)
+    return f32_to_bf16(gemm_dequant(q, s, w, sw, scheme, acc))

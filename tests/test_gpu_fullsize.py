@@ -187,3 +187,26 @@ def test_layer_repeatable(name):
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), first.view(torch.int16)), f"run {i + 1} differs"
     assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("T", [8192, 128])
+def test_linear_full_size(T):
+    """The dense W8A8 linear at a DeepSeek-V3 dense-MLP gate_up shape (K
+    7168, N 36864): sampled rows against the oracle's linear on the same
+    weights."""
+    K, N = 7168, 36864
+    g = torch.Generator(device=DEV).manual_seed(3)
+    x = torch.randn(T, K, generator=g, device=DEV).to(torch.bfloat16)
+    w = (torch.randn(N, K, generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    Wq, sw = wq.quantize_weight(w, "channel")
+    del w
+    st = wq.new_status()
+    out = wq.linear_w8a8(x, Wq, sw, "channel", "i32", status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rows = sorted({0, T - 1, T // 3})
+    ref = O.linear_w8a8(bits(x[rows]), np_(Wq), np_(sw), "channel", "i32")
+    got = bits(out[rows])
+    max_abs, rel = tolerance_report(got, ref)
+    assert max_abs <= 2e-2 and rel <= 1e-2
+    assert_bf16_equal(got, ref, f"linear T{T} sampled rows {rows}")

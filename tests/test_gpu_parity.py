@@ -441,3 +441,27 @@ def test_grouped_gemm_f16codes(extreme, K):
     assert_bf16_equal(bits(out), O.grouped_gemm_w8a8(A, sa, W, sw, offs), "f16 codes gemm")
     assert_bf16_equal(bits(out32), O.grouped_gemm_w8a8(A, sa, W, sw, offs, "channel", "f32"),
                       "f16 codes gemm, float32 accumulator")
+
+
+# ---------------------------------------------------------------- dense linear
+@pytest.mark.parametrize("T,K,N,scheme,acc", [
+    (5, 256, 256, "channel", "i32"),      # few rows: the small-token engine
+    (70, 384, 384, "channel", "i32"),     # N not a multiple of 256: int8 codes
+    (300, 512, 512, "channel", "i32"),    # fp16 codes, shared-memory pair engine
+    (300, 512, 512, "channel", "f32"),
+    (300, 4096, 512, "channel", "i32"),   # fp16 codes, tensor-memory weights
+    (300, 512, 512, "block", "f32"),      # fp16 codes, block-wise pair engine
+    (40, 256, 384, "block", "f32"),       # int8 codes, block-wise
+])
+def test_linear_w8a8(T, K, N, scheme, acc):
+    rng = np.random.default_rng(T + K + N)
+    g = torch.Generator().manual_seed(T + N)
+    x = (torch.randn(T, K, generator=g) * 2).to(torch.bfloat16)
+    w = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16)
+    Wq, sw = wq.quantize_weight(w.to(DEV), scheme)
+    out = wq.linear_w8a8(x.to(DEV), Wq, sw, scheme, acc)
+    torch.cuda.synchronize()
+    ref = O.linear_w8a8(bits(x), np_(Wq), np_(sw), scheme, acc)
+    max_abs, rel = tolerance_report(bits(out), ref)
+    assert max_abs <= 2e-2 and rel <= 1e-2
+    assert_bf16_equal(bits(out), ref, f"linear {scheme}/{acc} T{T} K{K} N{N}")

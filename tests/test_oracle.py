@@ -475,3 +475,58 @@ def test_masked_layout_matches_per_expert_layer():
         hq, sh = O.silu_mul_quant(gu, cfg.I)
         ye = O.grouped_gemm_w8a8(hq, sh, W2[e:e + 1], S2[e:e + 1], np.array([0, m]))
         assert np.array_equal(y[e, :m], ye)
+
+
+def test_linear_hand_worked():
+    """A dense W8A8 linear worked by hand: x = [2, -1, 0.5, 0, ...] gives
+    s = 2/127 and codes [127, -64 (-63.5, tie to even), 32 (31.75), 0, ...];
+    channel codes [1, 2, 3, 0, ...] and [-1, 0, 4, 0, ...] with scales 0.5
+    and 0.25 give C = 95 and 1, and v = (C * s) * sw rounded to float32 at
+    each step, then to bf16."""
+    from fractions import Fraction
+    K = 128
+    x = np.zeros((1, K), np.float32)
+    x[0, :3] = [2.0, -1.0, 0.5]
+    xb = O.f32_to_bf16(x)
+    w = np.zeros((2, K), np.int8)
+    w[0, :3] = [1, 2, 3]
+    w[1, :3] = [-1, 0, 4]
+    sw = np.array([0.5, 0.25], np.float32)
+    got = O.bf16_to_f32(O.linear_w8a8(xb, w, sw, "channel", "i32"))[0]
+    s = np.float32(2.0) / np.float32(127.0)
+    q = [127, -64, 32]
+    C = [sum(qi * wi for qi, wi in zip(q, (1, 2, 3))), sum(qi * wi for qi, wi in zip(q, (-1, 0, 4)))]
+    assert C == [95, 1]
+
+    want = []
+    for c, swc in zip(C, sw):
+        p = np.float32(float(Fraction(c) * Fraction(float(s))))
+        want.append(np.float32(float(Fraction(float(p)) * Fraction(float(swc)))))
+    want_bf = O.bf16_to_f32(O.f32_to_bf16(np.array(want, np.float32)))
+    assert np.array_equal(got, want_bf), (got, want_bf)
+    assert abs(float(got[0]) - 95 * 2 / 127 * 0.5) < 0.01 and abs(float(got[1]) - 2 / 127 * 0.25) < 1e-4
+
+
+def test_linear_is_single_expert_grouped_gemm_on_quantized_rows():
+    """The linear equals the oracle's grouped GEMM with one expert on the
+    rows' own quantization, both schemes, and the float64 dequantized
+    product within the float32 rounding bound."""
+    rng = np.random.default_rng(17)
+    T, K, N = 9, 256, 384
+    x = (rng.standard_normal((T, K)) * 3).astype(np.float32)
+    xb = O.f32_to_bf16(x)
+    w = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    sw = (rng.random(N) * 1e-2).astype(np.float32)
+    q, s = O.quantize_per_token(xb)
+    got = O.linear_w8a8(xb, w, sw, "channel", "i32")
+    assert np.array_equal(got, O.grouped_gemm_w8a8(q, s, w[None], sw[None], np.array([0, T]),
+                                                   "channel", "i32"))
+    ref = (q.astype(np.float64) * s[:, None].astype(np.float64)) @ (
+        w.astype(np.float64) * sw[:, None].astype(np.float64)).T
+    assert np.allclose(O.bf16_to_f32(got), ref, rtol=2 ** -7, atol=1e-6)
+    swb = (rng.random((N // 128, K // 128)) * 1e-2).astype(np.float32)
+    qb, sb = O.quantize_per_token_group(xb, 128)
+    gotb = O.linear_w8a8(xb, w, swb, "block", "f32")
+    assert np.array_equal(gotb, O.grouped_gemm_w8a8(qb, sb, w[None], swb[None], np.array([0, T]),
+                                                    "block", "f32"))
+

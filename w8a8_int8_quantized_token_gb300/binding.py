@@ -58,6 +58,8 @@ _SIGS = {
     "wq_moe_forward_host_workspace_size": (_S, [_I, _I, _I, _I, _I, _I]),
     "wq_moe_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _S, _P, _P]),
     "wq_moe_forward_masked_workspace_size": (_S, [_I, _I, _I, _I, _I]),
+    "wq_linear_w8a8_workspace_size": (_S, [_L, _L, _L, _I]),
+    "wq_linear_w8a8": (_I, [_P, _L, _L, _L, _P, _P, _L, _I, _I, _P, _P, _S, _P, _P]),
     "wq_moe_forward_masked": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _S, _P, _P]),
 }
 
@@ -400,3 +402,31 @@ def moe_forward_masked(a, sa, masked_m, W13, sw13, W2, sw2, scheme="channel", ac
                                        ACC[acc], _ptr(y), _ptr(ws), ws.numel(), _ptr(st),
                                        _stream()), "wq_moe_forward_masked")
     return y
+
+
+# ---------------------------------------------------------------- dense linear
+def linear_workspace(T, K, N, scheme, device):
+    n = lib().wq_linear_w8a8_workspace_size(T, K, N, SCHEME[scheme])
+    if n == 0:
+        raise WQError(f"linear shape T={T} K={K} N={N} ({scheme}) is not supported")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def linear_w8a8(x, W, sw, scheme="channel", acc="i32", out=None, ws=None, status=None):
+    """Dense W8A8 INT8 linear: quantize x (bf16 [T, K]) and multiply by the
+    int8 weights W [N, K] with their scales; bf16 [T, N]."""
+    _dev(x, torch.bfloat16, "x")
+    _dev(W, torch.int8, "W")
+    _dev(sw, torch.float32, "sw")
+    T, K = x.shape
+    N = W.shape[0]
+    if out is None:
+        out = torch.empty(T, N, dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = linear_workspace(T, K, N, scheme, x.device)
+    st = status if status is not None else new_status(x.device)
+    _check(lib().wq_linear_w8a8(_ptr(x), T, K, x.stride(0), _ptr(W), _ptr(sw), N, SCHEME[scheme],
+                                ACC[acc], _ptr(out), _ptr(ws), ws.numel(), _ptr(st), _stream()),
+           "wq_linear_w8a8")
+    return out
+

@@ -582,6 +582,88 @@ int wq_moe_forward_host(const uint16_t *x_host, const float *logits_host, const 
 }
 
 // ---------------------------------------------------------------------------
+// Dense W8A8 linear ("Norm Linear")
+
+namespace {
+
+struct LinBufs {
+  int32_t *offsets;
+  void *q;  // int8 codes, or the same codes as fp16
+  float *s;
+  int32_t *norm;
+  void *gws;
+  size_t gws_bytes;
+};
+
+size_t carve_linear(void *ws, int64_t T, int64_t K, int scheme, LinBufs *b) {
+  Carver c(ws);
+  LinBufs t;
+  const int64_t g = scheme == WQ_SCHEME_BLOCK ? K / 128 : 1;
+  t.offsets = c.take<int32_t>(2);
+  t.q = c.take<uint16_t>(size_t(T) * K);
+  t.s = c.take<float>(size_t(T) * g);
+  t.norm = c.take<int32_t>(size_t(T));
+  t.gws_bytes = gemm_ws_bytes(T, 1, 0, false);
+  t.gws = c.take<char>(t.gws_bytes);
+  if (b) *b = t;
+  return c.used;
+}
+
+__global__ void linear_offsets_kernel(int32_t *offsets, int32_t T) {
+  offsets[0] = 0;
+  offsets[1] = T;
+}
+
+int check_linear_shape(int64_t T, int64_t K, int64_t N, int scheme, int acc) {
+  if (T < 0 || K <= 0 || N <= 0) return WQ_ERR_INVALID_ARG;
+  if (scheme != WQ_SCHEME_CHANNEL && scheme != WQ_SCHEME_BLOCK) return WQ_ERR_INVALID_ARG;
+  if (acc != WQ_ACC_I32 && acc != WQ_ACC_F32) return WQ_ERR_INVALID_ARG;
+  if (K % 128 || N % 128 || K > 65536) return WQ_ERR_UNSUPPORTED;
+  if (T >= (int64_t(1) << 31) / 2) return WQ_ERR_UNSUPPORTED;
+  return WQ_OK;
+}
+
+}  // namespace
+
+size_t wq_linear_w8a8_workspace_size(int64_t T, int64_t K, int64_t N, int scheme) {
+  if (check_linear_shape(T, K, N, scheme, WQ_ACC_I32) != WQ_OK) return 0;
+  return carve_linear(nullptr, T, K, scheme, nullptr);
+}
+
+int wq_linear_w8a8(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, const int8_t *W,
+                   const float *sw, int64_t N, int scheme, int acc, uint16_t *out, void *ws,
+                   size_t ws_bytes, int32_t *status, wq_stream_t stream) {
+  WQ_TRY(check_linear_shape(T, K, N, scheme, acc));
+  if (ldx < K) return WQ_ERR_INVALID_ARG;
+  if (T == 0) return WQ_OK;
+  if (!x || !W || !sw || !out) return WQ_ERR_INVALID_ARG;
+  if (ldx % 8 || !al16(x) || !al16(W) || !al16(out)) return WQ_ERR_UNSUPPORTED;
+  LinBufs b;
+  const size_t need = carve_linear(ws, T, K, scheme, &b);
+  if (!ws || !al16(ws) || ws_bytes < need) return WQ_ERR_WORKSPACE;
+  WQ_TRY(check_device());
+  const bool blk = scheme == WQ_SCHEME_BLOCK;
+  linear_offsets_kernel<<<1, 1, 0, stream>>>(b.offsets, int32_t(T));
+  WQ_TRY(launched(1));
+  // many rows and N a multiple of 256: fp16 codes for the CTA-pair engines
+  // (the quantizer writes them directly, with row norms for the channel-wise
+  // exactness check); otherwise int8 codes (few rows: the small-token engine)
+  GemmArgs probe{nullptr, static_cast<const uint16_t *>(b.q), b.norm, b.s, W, sw, b.offsets,
+                 nullptr, 0, 1, T, N, K, scheme, acc, WQ_OUT_BF16, out, b.gws, status};
+  const bool f16 = N % 256 == 0 && T > 64 &&
+                   (blk ? gemm_tc6_supported(probe) : gemm_tc4_supported(probe));
+  if (f16) {
+    WQ_TRY(launch_quant_rows_f16(x, T, K, ldx, blk ? 128 : 0, static_cast<uint16_t *>(b.q), b.s,
+                                 b.norm, stream));
+    return launch_grouped_gemm(probe, stream);
+  }
+  WQ_TRY(launch_quant_rows(x, T, K, ldx, blk ? 128 : 0, static_cast<int8_t *>(b.q), b.s, stream));
+  GemmArgs g{static_cast<const int8_t *>(b.q), nullptr, nullptr, b.s, W, sw, b.offsets, nullptr, 0,
+             1, T, N, K, scheme, acc, WQ_OUT_BF16, out, b.gws, status};
+  return launch_grouped_gemm(g, stream);
+}
+
+// ---------------------------------------------------------------------------
 // Masked layout
 
 namespace {

@@ -155,6 +155,9 @@ namespace wq {
 int launched(int n);
 int launch_quant_rows(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group, int8_t *q,
                       float *s, cudaStream_t st);
+// the same quantization writing fp16 codes (and, with group 0, row norms)
+int launch_quant_rows_f16(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group,
+                          uint16_t *q16, float *s, int32_t *norm2, cudaStream_t st);
 int launch_quant_weight_block(const uint16_t *w, int64_t N, int64_t K, int8_t *q, float *s,
                               cudaStream_t st);
 int launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w, cudaStream_t st);

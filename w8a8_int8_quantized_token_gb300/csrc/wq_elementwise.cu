@@ -14,12 +14,28 @@ namespace wq {
 // consecutive lanes owning a group reduce with xor shuffles).
 // (Meituan INT8 DeepSeek R1 article, 量化技术的探索: online per-token
 // activation quantization of the channel-wise scheme, per-token-group
-// quantization of the block-wise scheme.)
-template <int V, int GV>
+// quantization of the block-wise scheme.)  F16: the codes are written as
+// fp16 values (the CTA-pair GEMM engines' input form), and with one scale
+// per row also the row's squared norm.
+template <int V, int GV, bool F16 = false>
 __global__ void __launch_bounds__(1024) quant_row_kernel(const uint16_t *__restrict__ x, int64_t K,
-                                                         int64_t ldx, int8_t *__restrict__ q,
-                                                         float *__restrict__ s) {
+                                                         int64_t ldx, void *__restrict__ q_out,
+                                                         float *__restrict__ s,
+                                                         int32_t *__restrict__ norm2 = nullptr) {
   __shared__ float red[32];
+  __shared__ int redi[32];
+  int8_t *q = static_cast<int8_t *>(q_out);
+  // one vector of 8 codes: int8 bytes, or fp16 values (exact)
+  auto store8 = [&](int64_t row, int idx, uint2 o) {
+    if constexpr (F16) {
+      uint4 w;
+      tc::s8x4_to_f16x4(o.x, w.x, w.y);
+      tc::s8x4_to_f16x4(o.y, w.z, w.w);
+      reinterpret_cast<uint4 *>(static_cast<uint16_t *>(q_out) + row * K)[idx] = w;
+    } else {
+      reinterpret_cast<uint2 *>(q + row * K)[idx] = o;
+    }
+  };
   const int64_t row = blockIdx.x;
   const uint4 *xr = reinterpret_cast<const uint4 *>(x + row * ldx);
   const int nvec = int(K >> 3);
@@ -41,7 +57,6 @@ __global__ void __launch_bounds__(1024) quant_row_kernel(const uint16_t *__restr
       for (int j = 0; j < 8; ++j) a[i] = fmaxf(a[i], fabsf(f[j]));
     }
   }
-  uint2 *qr = reinterpret_cast<uint2 *>(q + row * K);
   if constexpr (GV == 0) {
     float amax = a[0];
 #pragma unroll
@@ -49,6 +64,7 @@ __global__ void __launch_bounds__(1024) quant_row_kernel(const uint16_t *__restr
     amax = block_max(amax, red);
     const float sc = quant_scale(amax);
     const float rs = __frcp_rn(sc);
+    int n2 = 0;
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int idx = threadIdx.x + i * blockDim.x;
@@ -60,7 +76,20 @@ __global__ void __launch_bounds__(1024) quant_row_kernel(const uint16_t *__restr
                         quant_bits(f[2], sc, rs), quant_bits(f[3], sc, rs));
         o.y = pack_s8x4(quant_bits(f[4], sc, rs), quant_bits(f[5], sc, rs),
                         quant_bits(f[6], sc, rs), quant_bits(f[7], sc, rs));
-        qr[idx] = o;
+        store8(row, idx, o);
+        if constexpr (F16) n2 = __dp4a(int(o.y), int(o.y), __dp4a(int(o.x), int(o.x), n2));
+      }
+    }
+    if constexpr (F16) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+      const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+      if (l == 0) redi[w] = n2;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int t = 0;
+        for (int k = 0; k < nw; ++k) t += redi[k];
+        norm2[row] = t;
       }
     }
     if (threadIdx.x == 0) s[row] = sc;
@@ -81,28 +110,39 @@ __global__ void __launch_bounds__(1024) quant_row_kernel(const uint16_t *__restr
                         quant_bits(f[2], sc, rs), quant_bits(f[3], sc, rs));
         o.y = pack_s8x4(quant_bits(f[4], sc, rs), quant_bits(f[5], sc, rs),
                         quant_bits(f[6], sc, rs), quant_bits(f[7], sc, rs));
-        qr[idx] = o;
+        store8(row, idx, o);
         if (idx % GV == 0) s[row * (nvec / GV) + idx / GV] = sc;
       }
     }
   }
 }
 
-template <int V>
-int launch_quant_v(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group, int8_t *q,
-                   float *s, cudaStream_t st) {
+template <int V, bool F16>
+int launch_quant_v(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group, void *q,
+                   float *s, int32_t *norm2, cudaStream_t st) {
   const int64_t nvec = K / 8;
   int threads = int((nvec + V - 1) / V);
   threads = ((threads + 31) / 32) * 32;
   switch (group) {
-    case 0: quant_row_kernel<V, 0><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s); break;
-    case 32: quant_row_kernel<V, 4><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s); break;
-    case 64: quant_row_kernel<V, 8><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s); break;
-    case 128: quant_row_kernel<V, 16><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s); break;
-    case 256: quant_row_kernel<V, 32><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s); break;
+    case 0: quant_row_kernel<V, 0, F16><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s, norm2); break;
+    case 32: quant_row_kernel<V, 4, F16><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s, norm2); break;
+    case 64: quant_row_kernel<V, 8, F16><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s, norm2); break;
+    case 128: quant_row_kernel<V, 16, F16><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s, norm2); break;
+    case 256: quant_row_kernel<V, 32, F16><<<unsigned(T), threads, 0, st>>>(x, K, ldx, q, s, norm2); break;
     default: return WQ_ERR_UNSUPPORTED;
   }
   return launched(1);
+}
+
+template <bool F16>
+int launch_quant_rows_t(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group, void *q,
+                        float *s, int32_t *norm2, cudaStream_t st) {
+  if (T == 0 || K == 0) return WQ_OK;
+  const int64_t nvec = K / 8;
+  if (nvec > 8 * 1024 || T > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
+  if (nvec <= 2 * 1024) return launch_quant_v<2, F16>(x, T, K, ldx, group, q, s, norm2, st);
+  if (nvec <= 4 * 1024) return launch_quant_v<4, F16>(x, T, K, ldx, group, q, s, norm2, st);
+  return launch_quant_v<8, F16>(x, T, K, ldx, group, q, s, norm2, st);
 }
 
 // Rows up to 2048 vectors (K <= 16384) take two vectors per thread (the
@@ -112,12 +152,12 @@ int launch_quant_v(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int gro
 // a group (GV consecutive vectors, K % group == 0) never straddles the row end.
 int launch_quant_rows(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group, int8_t *q,
                       float *s, cudaStream_t st) {
-  if (T == 0 || K == 0) return WQ_OK;
-  const int64_t nvec = K / 8;
-  if (nvec > 8 * 1024 || T > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
-  if (nvec <= 2 * 1024) return launch_quant_v<2>(x, T, K, ldx, group, q, s, st);
-  if (nvec <= 4 * 1024) return launch_quant_v<4>(x, T, K, ldx, group, q, s, st);
-  return launch_quant_v<8>(x, T, K, ldx, group, q, s, st);
+  return launch_quant_rows_t<false>(x, T, K, ldx, group, q, s, nullptr, st);
+}
+
+int launch_quant_rows_f16(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group,
+                          uint16_t *q16, float *s, int32_t *norm2, cudaStream_t st) {
+  return launch_quant_rows_t<true>(x, T, K, ldx, group, q16, s, norm2, st);
 }
 
 // ---------------------------------------------------------------------------
