@@ -502,12 +502,75 @@ def run_linear(args, name):
     print(json.dumps(line), flush=True)
 
 
+def run_convert(args):
+    """Offline FP8 -> BF16 -> INT8 conversion of all 256 experts' weights of
+    the DeepSeek-V3 MoE layer (W13 [256*4096, 7168] and W2 [256*7168, 2048]
+    stacked, FP8 e4m3 with [128,128] block scales) to channel-wise INT8.  One
+    step = both conversions.  HBM bound: each weight byte is read once (FP8)
+    and written once (INT8)."""
+    from w8a8_int8_quantized_token_gb300 import binding as wq
+    from w8a8_int8_quantized_token_gb300 import build_lib
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build_lib.build()
+    wq.init(0)
+    E, H, I = 256, 7168, 2048
+    mats = []
+    for (N, K) in ((2 * I, H), (H, I)):
+        w8 = torch.empty(E * N, K, dtype=torch.uint8, device=dev)
+        s8 = torch.empty(E * N // 128, K // 128, dtype=torch.float32, device=dev)
+        for e in range(E):
+            a, b = synth.fp8_block_weights(N, K, seed=1_000 + e + (0 if K == H else E), device=dev)
+            w8[e * N:(e + 1) * N] = a
+            s8[e * N // 128:(e + 1) * N // 128] = b
+        q = torch.empty(E * N, K, dtype=torch.int8, device=dev)
+        s = torch.empty(E * N, dtype=torch.float32, device=dev)
+        mats.append((w8, s8, q, s))
+    torch.cuda.synchronize()
+
+    def step():
+        for w8, s8, q, s in mats:
+            wq.convert_fp8_weights(w8, s8, "channel", q_out=q, s_out=s)
+    for _ in range(args.warmup):
+        step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize()
+        n0 = wq.lib().wq_kernel_launches()
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        launches = wq.lib().wq_kernel_launches() - n0
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    nbytes = sum(w8.numel() + s8.numel() * 4 + q.numel() + s.numel() * 4 for w8, s8, q, s in mats)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peaks, src = load_peaks()
+    line = {"metric": "FP8 -> BF16 -> INT8 weight conversion throughput", "value": gbs,
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8->int8", "data": "synthetic",
+            "config": {"workload": "DeepSeek-V3 MoE layer weights, 256 experts (W13 + W2, 11.3 G "
+                                   "weights), FP8 e4m3 with [128,128] scales -> channel-wise INT8",
+                       "l2": "inputs larger than L2 (11.3 GB read, 11.3 GB written per step)",
+                       "parallelism": "single"},
+            "gpu_launches": launches,
+            "roofline": {"bound": "hbm", "kernel": "convert_fp8_row_kernel", "achieved": gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": None, "algorithmic_bytes": nbytes,
+                         "peak_source": f"{src} HBM copy bandwidth"},
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--config", default="prefill", choices=list(synth.CONFIGS) + list(LINEAR))
+    ap.add_argument("--config", default="prefill",
+                    choices=list(synth.CONFIGS) + list(LINEAR) + ["convert"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -516,6 +579,9 @@ def main():
     args = ap.parse_args()
     if args.config in LINEAR:
         run_linear(args, args.config)
+        return
+    if args.config == "convert":
+        run_convert(args)
         return
     cfg = synth.CONFIGS[args.config]
     if args.tokens or args.experts:

@@ -109,6 +109,19 @@ WQ_API int wq_quantize_per_token(const uint16_t *x, int64_t T, int64_t K, int64_
 WQ_API int wq_quantize_per_token_group(const uint16_t *x, int64_t T, int64_t K, int64_t ldx,
                                 int group, int8_t *q, float *s, wq_stream_t stream);
 
+/* Offline FP8 -> BF16 -> INT8 weight conversion [MT] (量化技术的探索: the
+ * released weights are FP8; they are dequantized to BF16, then quantized to
+ * INT8 per [128,128] block or per output channel).  w8: FP8 e4m3 bytes
+ * [N][K] (no infinities; NaN bytes give unspecified codes); s8: float one
+ * scale per [128,128] block [N/128][K/128].  Each value is (e4m3 value *
+ * block scale) rounded to float32 then to bf16, and the bf16 matrix is
+ * quantized by the rule above: scheme WQ_SCHEME_CHANNEL -> q int8 [N][K],
+ * s float [N]; WQ_SCHEME_BLOCK -> s float [N/128][K/128].  The bf16 values
+ * never reach memory.  Requirements: N % 128 == 0, K % 128 == 0 (channel:
+ * K <= 16384), w8 and q 16-byte aligned. */
+WQ_API int wq_convert_fp8_weights(const uint8_t *w8, const float *s8, int64_t N, int64_t K,
+                                  int scheme, int8_t *q, float *s, wq_stream_t stream);
+
 /* Offline [128,128] block weight quantization [MT]: w bf16 [N][K] ->
  * q int8 [N][K], s float [N/128][K/128]; the rule above over each block.
  * Requirements: N % 128 == 0, K % 128 == 0, w 16-byte aligned. */

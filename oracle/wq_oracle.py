@@ -461,3 +461,40 @@ def linear_w8a8(x_bits: np.ndarray, w: np.ndarray, sw: np.ndarray, scheme: str =
     else:
         q, s = quantize_per_token_group(x_bits, KTILE)
     return f32_to_bf16(gemm_dequant(q, s, w, sw, scheme, acc))
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) block-scaled weights -> BF16 -> INT8 (offline conversion)
+# ---------------------------------------------------------------------------
+def e4m3_to_f32(b: np.ndarray) -> np.ndarray:
+    """The value of FP8 e4m3 bytes (1 sign, 4 exponent bits with bias 7, 3
+    mantissa bits; no infinities, S.1111.111 is NaN): exponent field 0 gives
+    (m / 8) * 2^-6, otherwise (1 + m / 8) * 2^(e - 7).  Every value is exact
+    in float32."""
+    b = b.astype(np.uint8)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = ((b >> 3) & 0xF).astype(np.int64)
+    m = (b & 0x7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return (sign * mag).astype(np.float32)
+
+
+def dequant_fp8_block(w8: np.ndarray, s8: np.ndarray, block: int = 128) -> np.ndarray:
+    """FP8 weights [N, K] with one float32 scale per [128, 128] block
+    ([N/128, K/128]) to BF16, the first step of the conversion in the Meituan
+    INT8 article (量化技术的探索: the released FP8 weights are dequantized to
+    BF16 before INT8 quantization).  Reading: the product value * scale is
+    one float32 multiplication rounded to nearest, then rounded to bf16.
+    Returns bf16 bits [N, K]."""
+    N, K = w8.shape
+    sc = np.repeat(np.repeat(s8.astype(np.float32), block, axis=0), block, axis=1)[:N, :K]
+    return f32_to_bf16((e4m3_to_f32(w8) * sc).astype(np.float32))
+
+
+def convert_fp8_weights(w8: np.ndarray, s8: np.ndarray, scheme: str):
+    """FP8 -> BF16 -> INT8: dequantize (dequant_fp8_block), then the INT8
+    weight quantization of the scheme (per output channel, or per [128,128]
+    block).  Returns (int8 codes [N, K], scales)."""
+    bf = dequant_fp8_block(w8, s8)
+    return quantize_weight_channel(bf) if scheme == "channel" else quantize_weight_block(bf)

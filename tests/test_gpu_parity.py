@@ -465,3 +465,17 @@ def test_linear_w8a8(T, K, N, scheme, acc):
     max_abs, rel = tolerance_report(bits(out), ref)
     assert max_abs <= 2e-2 and rel <= 1e-2
     assert_bf16_equal(bits(out), ref, f"linear {scheme}/{acc} T{T} K{K} N{N}")
+
+
+# ---------------------------------------------------------------- FP8 -> INT8 weights
+@pytest.mark.parametrize("scheme", ["channel", "block"])
+@pytest.mark.parametrize("N,K", [(128, 128), (384, 1024), (256, 7168)])
+def test_convert_fp8_weights(scheme, N, K):
+    w8, s8 = synth.fp8_block_weights(N, K, seed=N + K)
+    w8[0, :17] = torch.arange(17, dtype=torch.uint8)       # zero and subnormal bytes
+    w8[1, :8] = torch.tensor([0x7E, 0xFE, 0x38, 0xB8, 0x08, 0x88, 0x01, 0x81], dtype=torch.uint8)
+    q, s = wq.convert_fp8_weights(w8.to(DEV), s8.to(DEV), scheme)
+    qo, so = O.convert_fp8_weights(w8.numpy(), s8.numpy(), scheme)
+    assert np.array_equal(np_(q), qo)
+    assert np.array_equal(np_(s), so)
+

@@ -530,3 +530,42 @@ def test_linear_is_single_expert_grouped_gemm_on_quantized_rows():
     assert np.array_equal(gotb, O.grouped_gemm_w8a8(qb, sb, w[None], swb[None], np.array([0, T]),
                                                     "block", "f32"))
 
+
+
+def test_e4m3_decode_matches_torch_and_fixed_points():
+    """Every one of the 256 e4m3 bytes decodes to torch's float8_e4m3fn value
+    (a library conversion), and fixed points of the format hold: 0x38 = 1,
+    0x7e = 448 (largest), 0x01 = 2^-9 (smallest subnormal), 0x08 = 2^-6,
+    0x7f is NaN."""
+    b = np.arange(256, dtype=np.uint8)
+    got = O.e4m3_to_f32(b)
+    want = torch.from_numpy(b).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    assert got[0x38] == 1.0 and got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+    assert got[0x08] == 2.0 ** -6 and got[0xB8] == -1.0 and np.isnan(got[0x7F])
+
+
+def test_fp8_dequant_and_conversion():
+    """Dequantization = the byte's value times its block's scale, rounded to
+    float32 then bf16 (checked against float64 products); the conversion's
+    codes then follow the INT8 weight rules (a block whose bf16 values are
+    already n * s quantizes back to n exactly)."""
+    rng = np.random.default_rng(41)
+    N, K = 256, 384
+    w8 = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    w8[(w8 & 0x7F) == 0x7F] = 0x10  # no NaN bytes
+    s8 = (rng.random((N // 128, K // 128)) * 1e-2 + 1e-4).astype(np.float32)
+    bf = O.bf16_to_f32(O.dequant_fp8_block(w8, s8))
+    v64 = O.e4m3_to_f32(w8).astype(np.float64) * np.repeat(np.repeat(s8, 128, 0), 128, 1)
+    assert np.all(np.abs(bf - v64) <= np.abs(v64) * 2.0 ** -8 + 1e-30)
+    q, s = O.convert_fp8_weights(w8, s8, "channel")
+    q2, s2 = O.quantize_weight_channel(O.dequant_fp8_block(w8, s8))
+    assert np.array_equal(q, q2) and np.array_equal(s, s2)
+    # power-of-two block scale and codes of a single magnitude: values n * s
+    w8b = np.full((128, 128), 0x38, np.uint8)  # 1.0 everywhere
+    w8b[:, ::2] = 0xB8  # -1.0
+    qb, sb = O.convert_fp8_weights(w8b, np.array([[0.25]], np.float32), "block")
+    assert sb[0, 0] == np.float32(np.float32(0.25) / np.float32(127.0))
+    assert np.all(np.abs(qb) == 127)

@@ -39,6 +39,7 @@ _SIGS = {
     "wq_quantize_per_token": (_I, [_P, _L, _L, _L, _P, _P, _P]),
     "wq_quantize_per_token_group": (_I, [_P, _L, _L, _L, _I, _P, _P, _P]),
     "wq_quantize_weight_block": (_I, [_P, _L, _L, _P, _P, _P]),
+    "wq_convert_fp8_weights": (_I, [_P, _P, _L, _L, _I, _P, _P, _P]),
     "wq_route_topk": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "wq_moe_align_workspace_size": (_S, [_I, _I, _I]),
     "wq_moe_align": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P, _P]),
@@ -142,6 +143,23 @@ def quantize_weight_block(w):
     s = torch.empty(N // 128, K // 128, dtype=torch.float32, device=w.device)
     _check(lib().wq_quantize_weight_block(_ptr(w), N, K, _ptr(q), _ptr(s), _stream()),
            "wq_quantize_weight_block")
+    return q, s
+
+
+def convert_fp8_weights(w8, s8, scheme: str, q_out=None, s_out=None):
+    """FP8 e4m3 weights (uint8 [N, K] bytes) with [N/128, K/128] block
+    scales -> bf16 -> int8 codes and scales of the scheme."""
+    _dev(w8, torch.uint8, "w8")
+    _dev(s8, torch.float32, "s8")
+    N, K = w8.shape
+    q = q_out if q_out is not None else torch.empty(N, K, dtype=torch.int8, device=w8.device)
+    if s_out is not None:
+        s = s_out
+    else:
+        shape = (N,) if scheme == "channel" else (N // 128, K // 128)
+        s = torch.empty(shape, dtype=torch.float32, device=w8.device)
+    _check(lib().wq_convert_fp8_weights(_ptr(w8), _ptr(s8), N, K, SCHEME[scheme], _ptr(q), _ptr(s),
+                                        _stream()), "wq_convert_fp8_weights")
     return q, s
 
 

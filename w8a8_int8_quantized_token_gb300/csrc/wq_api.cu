@@ -245,6 +245,17 @@ int wq_quantize_per_token_group(const uint16_t *x, int64_t T, int64_t K, int64_t
   return launch_quant_rows(x, T, K, ldx, group, q, s, stream);
 }
 
+int wq_convert_fp8_weights(const uint8_t *w8, const float *s8, int64_t N, int64_t K, int scheme,
+                           int8_t *q, float *s, wq_stream_t stream) {
+  if (N < 0 || K < 0) return WQ_ERR_INVALID_ARG;
+  if (scheme != WQ_SCHEME_CHANNEL && scheme != WQ_SCHEME_BLOCK) return WQ_ERR_INVALID_ARG;
+  if (N == 0 || K == 0) return WQ_OK;
+  if (!w8 || !s8 || !q || !s) return WQ_ERR_INVALID_ARG;
+  if (N % 128 || K % 128 || !al16(w8) || !al16(q)) return WQ_ERR_UNSUPPORTED;
+  WQ_TRY(check_device());
+  return launch_convert_fp8(w8, s8, N, K, scheme, q, s, stream);
+}
+
 int wq_quantize_weight_block(const uint16_t *w, int64_t N, int64_t K, int8_t *q, float *s,
                              wq_stream_t stream) {
   if (N < 0 || K < 0) return WQ_ERR_INVALID_ARG;

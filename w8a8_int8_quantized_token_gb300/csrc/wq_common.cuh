@@ -158,6 +158,10 @@ int launch_quant_rows(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int 
 // the same quantization writing fp16 codes (and, with group 0, row norms)
 int launch_quant_rows_f16(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group,
                           uint16_t *q16, float *s, int32_t *norm2, cudaStream_t st);
+// FP8 e4m3 weights [N][K] with [N/128][K/128] float32 block scales -> bf16
+// (in registers) -> int8 codes with per-row (channel) or per-block scales
+int launch_convert_fp8(const uint8_t *w8, const float *s8, int64_t N, int64_t K, int scheme,
+                       int8_t *q, float *s, cudaStream_t st);
 int launch_quant_weight_block(const uint16_t *w, int64_t N, int64_t K, int8_t *q, float *s,
                               cudaStream_t st);
 int launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w, cudaStream_t st);

@@ -161,6 +161,121 @@ int launch_quant_rows_f16(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, 
 }
 
 // ---------------------------------------------------------------------------
+// FP8 (e4m3, one float32 scale per [128,128] block) -> BF16 -> INT8 weight
+// conversion (Meituan INT8 article, 量化技术的探索: DeepSeek releases FP8
+// weights only, so they are dequantized to BF16 and then quantized to INT8,
+// per [128,128] block or per output channel).  Both steps in one pass: the
+// bf16 values live only in registers.
+
+// Two e4m3 bytes (sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+// infinities) -> their exact values: every e4m3 value is an fp16 value, so
+// the hardware conversion to fp16 pairs is exact (byte 0 -> low half).
+__device__ __forceinline__ void e4m3x2_values(uint32_t two, float &lo, float &hi) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(uint16_t(two)));
+  lo = __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFFu)));
+  hi = __half2float(__ushort_as_half(uint16_t(h2 >> 16)));
+}
+
+// 16 e4m3 bytes times one block scale, each rounded to float32 then bf16
+__device__ __forceinline__ void fp8x16_to_bf16(const uint4 &w, float sc, float (&f)[16]) {
+  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float v[4];
+    e4m3x2_values(words[i] & 0xFFFFu, v[0], v[1]);
+    e4m3x2_values(words[i] >> 16, v[2], v[3]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) f[4 * i + j] = bf16_to_f(f_to_bf16(__fmul_rn(v[j], sc)));
+  }
+}
+
+__device__ __forceinline__ uint4 codes16(const float (&f)[16], float sc, float rs) {
+  uint4 o;
+  o.x = pack_s8x4(quant_bits(f[0], sc, rs), quant_bits(f[1], sc, rs), quant_bits(f[2], sc, rs),
+                  quant_bits(f[3], sc, rs));
+  o.y = pack_s8x4(quant_bits(f[4], sc, rs), quant_bits(f[5], sc, rs), quant_bits(f[6], sc, rs),
+                  quant_bits(f[7], sc, rs));
+  o.z = pack_s8x4(quant_bits(f[8], sc, rs), quant_bits(f[9], sc, rs), quant_bits(f[10], sc, rs),
+                  quant_bits(f[11], sc, rs));
+  o.w = pack_s8x4(quant_bits(f[12], sc, rs), quant_bits(f[13], sc, rs), quant_bits(f[14], sc, rs),
+                  quant_bits(f[15], sc, rs));
+  return o;
+}
+
+// channel-wise: one CTA per output row (K/16 threads, 16 bytes each)
+__global__ void __launch_bounds__(1024) convert_fp8_row_kernel(const uint8_t *__restrict__ w8,
+                                                               const float *__restrict__ s8,
+                                                               int64_t K, int8_t *__restrict__ q,
+                                                               float *__restrict__ s) {
+  __shared__ float red[32];
+  const int64_t row = blockIdx.x;
+  const int c = threadIdx.x;  // 16-byte piece of the row
+  const int nchunk = int(K >> 4);
+  float f[16];
+  float amax = 0.0f;
+  if (c < nchunk) {
+    const uint4 w = __ldcs(reinterpret_cast<const uint4 *>(w8 + row * K) + c);
+    const float sc = s8[(row >> 7) * (K >> 7) + (c >> 3)];
+    fp8x16_to_bf16(w, sc, f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  }
+  amax = block_max(amax, red);
+  const float sc = quant_scale(amax);
+  const float rs = __frcp_rn(sc);
+  if (c < nchunk) reinterpret_cast<uint4 *>(q + row * K)[c] = codes16(f, sc, rs);
+  if (threadIdx.x == 0) s[row] = sc;
+}
+
+// block-wise: one CTA of 256 threads per [128,128] block, 4 pieces each
+__global__ void __launch_bounds__(256) convert_fp8_block_kernel(const uint8_t *__restrict__ w8,
+                                                                const float *__restrict__ s8,
+                                                                int64_t K, int8_t *__restrict__ q,
+                                                                float *__restrict__ s) {
+  __shared__ float red[32];
+  const int64_t kb_n = K >> 7;
+  const int64_t nb = blockIdx.x / kb_n, kb = blockIdx.x % kb_n;
+  const float sc8 = s8[nb * kb_n + kb];
+  float f[4][16];
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int p = threadIdx.x + 256 * j;  // piece: row p / 8, 16-byte column p % 8
+    const int64_t r = nb * 128 + (p >> 3), col = kb * 128 + (p & 7) * 16;
+    const uint4 w = __ldcs(reinterpret_cast<const uint4 *>(w8 + r * K + col));
+    fp8x16_to_bf16(w, sc8, f[j]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[j][i]));
+  }
+  amax = block_max(amax, red);
+  const float sc = quant_scale(amax);
+  const float rs = __frcp_rn(sc);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int p = threadIdx.x + 256 * j;
+    const int64_t r = nb * 128 + (p >> 3), col = kb * 128 + (p & 7) * 16;
+    *reinterpret_cast<uint4 *>(q + r * K + col) = codes16(f[j], sc, rs);
+  }
+  if (threadIdx.x == 0) s[nb * kb_n + kb] = sc;
+}
+
+int launch_convert_fp8(const uint8_t *w8, const float *s8, int64_t N, int64_t K, int scheme,
+                       int8_t *q, float *s, cudaStream_t st) {
+  if (N == 0 || K == 0) return WQ_OK;
+  if (scheme == WQ_SCHEME_CHANNEL) {
+    if (K / 16 > 1024 || N > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
+    const int threads = int(((K / 16 + 31) / 32) * 32);
+    convert_fp8_row_kernel<<<unsigned(N), threads, 0, st>>>(w8, s8, K, q, s);
+  } else {
+    const int64_t blocks = (N / 128) * (K / 128);
+    if (blocks > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
+    convert_fp8_block_kernel<<<unsigned(blocks), 256, 0, st>>>(w8, s8, K, q, s);
+  }
+  return launched(1);
+}
+
+// ---------------------------------------------------------------------------
 // [128,128] block weight quantization: one CTA of 256 threads per block,
 // 8 vectors (64 elements) per thread held in registers.
 __global__ void __launch_bounds__(256) quant_wblock_kernel(const uint16_t *__restrict__ w, int64_t K,

@@ -129,3 +129,18 @@ def small_config(name: str = "small", T=40, H=384, I=256, E=6, k=3, scheme="chan
                  acc="i32", outliers=True, seed=1) -> LayerConfig:
     """A parity-test shape that spans several 128-row/128-col tiles with ragged tails."""
     return LayerConfig(name, T, H, I, E, k, scheme, acc, outliers, seed)
+
+
+def fp8_block_weights(N: int, K: int, seed: int, device="cpu"):
+    """Weights in the FP8 release format DeepSeek-V3/R1 ships: bf16 N(0, 0.02)
+    draws, one float32 scale per [128, 128] block (block absmax / 448, the
+    e4m3 maximum) and the e4m3 bytes of weight / scale (torch's float8 cast).
+    Returns (uint8 bytes [N, K], float32 scales [N/128, K/128])."""
+    g = _gen(device, seed)
+    w = (torch.randn(N, K, generator=g, device=device) * 0.02).to(torch.bfloat16).float()
+    blocks = w.view(N // 128, 128, K // 128, 128)
+    s8 = blocks.abs().amax(dim=(1, 3)) / 448.0
+    s8 = torch.where(s8 > 0, s8, torch.ones_like(s8))
+    q = (blocks / s8[:, None, :, None]).view(N, K).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8), s8.contiguous()
+
