@@ -36,44 +36,82 @@ __global__ void __launch_bounds__(kAlignChunk) align_hist_kernel(const int32_t *
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[int64_t(blockIdx.x) * E + e] = cnt[e];
 }
 
-// 2) one CTA: column prefix over chunks, padded counts, exclusive scan over
-//    experts -> offsets; hist[c][e] becomes the first row of chunk c's pairs
-//    of expert e.
+// 2) one CTA. Warps own contiguous chunk ranges, lanes own experts, so
+//    every access to hist is a coalesced row piece. Per tile of 128
+//    experts: the warps' sums, their exclusive scan down the 32 warps in
+//    shared memory (-> counts), then each warp rewrites its rows with the
+//    running prefix. Then the padded counts are scanned over experts
+//    (-> offsets) and added to every row: hist[c][e] becomes the first row
+//    of chunk c's pairs of expert e.
 __global__ void __launch_bounds__(1024) align_scan_kernel(int32_t *__restrict__ hist, int chunks,
                                                           int E, int pad_m,
                                                           int32_t *__restrict__ counts,
                                                           int32_t *__restrict__ offsets) {
-  __shared__ int32_t part[1024];
+  constexpr int TE = 128, J = TE / 32;
+  __shared__ int32_t part[32][TE];
+  __shared__ int32_t scan[1024];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per_warp = (chunks + 31) / 32;
+  const int c0 = min(chunks, warp * per_warp), c1 = min(chunks, c0 + per_warp);
+  for (int eb = 0; eb < E; eb += TE) {
+    int acc[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) acc[j] = 0;
+    for (int c = c0; c < c1; ++c) {
+      const int32_t *row = hist + int64_t(c) * E + eb;
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+        if (eb + lane + 32 * j < E) acc[j] += row[lane + 32 * j];
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) part[warp][lane + 32 * j] = acc[j];
+    __syncthreads();
+    if (threadIdx.x < TE) {
+      int run = 0;
+      for (int w = 0; w < 32; ++w) {
+        const int v = part[w][threadIdx.x];
+        part[w][threadIdx.x] = run;
+        run += v;
+      }
+      if (eb + int(threadIdx.x) < E) counts[eb + threadIdx.x] = run;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < J; ++j) acc[j] = part[warp][lane + 32 * j];
+    for (int c = c0; c < c1; ++c) {
+      int32_t *row = hist + int64_t(c) * E + eb;
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+        if (eb + lane + 32 * j < E) {
+          const int v = row[lane + 32 * j];
+          row[lane + 32 * j] = acc[j];
+          acc[j] += v;
+        }
+    }
+    __syncthreads();  // part is reused by the next tile
+  }
+  // padded counts of this thread's experts, block-wide exclusive scan
   const int per = (E + blockDim.x - 1) / blockDim.x;
   const int e0 = threadIdx.x * per;
   int local = 0;
-  for (int e = e0; e < e0 + per && e < E; ++e) {
-    int run = 0;
-    for (int c = 0; c < chunks; ++c) {
-      const int v = hist[int64_t(c) * E + e];
-      hist[int64_t(c) * E + e] = run;
-      run += v;
-    }
-    counts[e] = run;
-    local += (run + pad_m - 1) / pad_m * pad_m;
-  }
-  part[threadIdx.x] = local;
+  for (int e = e0; e < e0 + per && e < E; ++e) local += (counts[e] + pad_m - 1) / pad_m * pad_m;
+  scan[threadIdx.x] = local;
   __syncthreads();
-  // inclusive Hillis-Steele scan over the block
-  for (int o = 1; o < int(blockDim.x); o <<= 1) {
-    const int v = threadIdx.x >= unsigned(o) ? part[threadIdx.x - o] : 0;
+  for (int o = 1; o < int(blockDim.x); o <<= 1) {  // inclusive Hillis-Steele scan
+    const int v = threadIdx.x >= unsigned(o) ? scan[threadIdx.x - o] : 0;
     __syncthreads();
-    part[threadIdx.x] += v;
+    scan[threadIdx.x] += v;
     __syncthreads();
   }
-  int base = part[threadIdx.x] - local;
+  int base = scan[threadIdx.x] - local;
   for (int e = e0; e < e0 + per && e < E; ++e) {
     offsets[e] = base;
-    for (int c = 0; c < chunks; ++c) hist[int64_t(c) * E + e] += base;
-    const int cnt = counts[e];
-    base += (cnt + pad_m - 1) / pad_m * pad_m;
+    base += (counts[e] + pad_m - 1) / pad_m * pad_m;
   }
-  if (threadIdx.x == blockDim.x - 1) offsets[E] = part[threadIdx.x];
+  if (threadIdx.x == blockDim.x - 1) offsets[E] = scan[threadIdx.x];
+  __syncthreads();
+  for (int c = c0; c < c1; ++c)
+    for (int e = lane; e < E; e += 32) hist[int64_t(c) * E + e] += offsets[e];
 }
 
 // 3) one warp per chunk walks its pairs in order, 32 at a time; a pair's row
