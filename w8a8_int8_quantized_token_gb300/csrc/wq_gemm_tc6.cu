@@ -283,7 +283,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const int b = gk & 1;
         // column scales sa[col][kb] * sw[kb] (0 past the tile's rows)
 #pragma unroll
-        for (int m = 0; m < NG; ++m) scal[32 * (half + 2 * m) + lane] = __fmul_rn(sap[m], swv);
+        for (int m = 0; m < NG; ++m)
+          if (32 * (half + 2 * m) < TN) scal[32 * (half + 2 * m) + lane] = __fmul_rn(sap[m], swv);
         if (kb + 1 < KB) {
           swv = swp[kb + 1];
 #pragma unroll
