@@ -52,8 +52,8 @@ def layer_ops(T, H, I, k):
 # kernel source it was measured on: it is reported while that file's SHA-256
 # matches, else the traffic is null.
 _TC5 = {"kernel": "gemm_tc5_kernel", "file": "wq_gemm_tc5.cu",
-        "sha256": "b8045b0fac1158f44842497e3b0449042cd70ef544a03f047423ed4166a12126",
-        "bytes": 8 * (1.080620e9 + 62.663168e6),
+        "sha256": "be4b94c601fcad1b269a7dcec9bfbe7318794275217113123ce3f5e0bad01a11",
+        "bytes": 8 * (1.080667e9 + 62.903808e6),
         "how": "ncu capture of GEMM1 at 1024 tokens / 32 experts (same 256 rows per expert), "
                "dram read+write x 8 experts ratio (profiles/gemm_tc5_tc4_reduced_prefill.md)"}
 TRAFFIC = {

@@ -284,6 +284,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       for (int j = lane; j < tl.rows; j += 32) tmax = max(tmax, a.a_norm2[int64_t(tl.row0) + j]);
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+      // the item's token scales (lane j of group p holds token 32p + j) and
+      // this thread's weight scale, loaded while the item's MMAs still run
+      constexpr int NGRP = TN / 32;
+      const int64_t n = int64_t(wb) * WM + q * 32 + lane;  // this thread's output channel
+      const float swn = a.sw[int64_t(tl.expert) * a.N + n];
+      float sal[NGRP];
+#pragma unroll
+      for (int p = 0; p < NGRP; ++p)
+        sal[p] = p * 32 + lane < tl.rows ? a.sa[int64_t(tl.row0) + p * 32 + lane] : 0.0f;
       if (!__all_sync(0xffffffffu, mbar_wait<500>(bar(B_ACC_FULL + b), par, abort_flag)) ||
           !__all_sync(0xffffffffu, mbar_wait(bar(B_NORM_READY + b), par, abort_flag))) {
         fail();
@@ -305,15 +314,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
       }
       if (nw * (long long)tmax >= (1ll << 48) && q == 0 && lane == 0) atomicExch(redo, 1);
-      const int64_t n = int64_t(wb) * WM + q * 32 + lane;  // this thread's output channel
-      const float swn = a.sw[int64_t(tl.expert) * a.N + n];
       const int nmma = nmma_of(tl.rows);
       const uint32_t taddr = tmem + (uint32_t(q * 32) << 16) + uint32_t(b) * 256u;
-      for (int p = 0; p * 32 < nmma; ++p) {
+#pragma unroll 1
+      for (int p = 0; p < NGRP; ++p) {
+        if (p * 32 >= nmma) break;
         uint32_t v[32];
         tmem_ld32(taddr + 32u * p, v);
         const int tok0 = p * 32;
-        const float sal = (tok0 + lane < tl.rows) ? a.sa[int64_t(tl.row0) + tok0 + lane] : 0.0f;
+        float sp = sal[0];  // sal[p] without a dynamic register index
+#pragma unroll
+        for (int m = 1; m < NGRP; ++m) sp = p == m ? sal[m] : sp;
         tmem_wait_ld();
         const int lim = min(32, tl.rows - tok0);
         if (a.out_type == WQ_OUT_I32) {
@@ -325,7 +336,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           uint16_t *o = static_cast<uint16_t *>(a.out) + (int64_t(tl.row0) + tok0) * a.N + n;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float s = __shfl_sync(0xffffffffu, sal, j);
+            const float s = __shfl_sync(0xffffffffu, sp, j);
             if (j < lim)
               o[int64_t(j) * a.N] = f_to_bf16(__fmul_rn(__fmul_rn(__uint_as_float(v[j]), s), swn));
           }

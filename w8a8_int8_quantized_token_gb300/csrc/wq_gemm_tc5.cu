@@ -27,7 +27,9 @@
 //   warp 1      TMEM allocator and MMA issuer (one thread)
 //   warps 2-9   converters, two groups of four taking alternate K stages:
 //               one weight row per thread, int8 -> fp16 -> TMEM
-//   warps 10-13 epilogue: dequant, bf16, coalesced stores (32 channels/warp)
+//   warps 10-21 epilogue: dequant, bf16, coalesced stores (32 channels/warp);
+//               three warps per lane quarter take every third 32-token group,
+//               so the single accumulator is drained three times faster
 // Every wait is bounded (1 s); on expiry the kernel records WQ_ERR_TIMEOUT,
 // waits (bounded) for its own copies and MMAs, frees tensor memory and exits.
 #include "wq_tc.cuh"
@@ -62,7 +64,9 @@ constexpr int OFF_ABORT = OFF_TMEM + 4;
 constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory plan too large");
 static_assert((TB % 1024) == 0 && (W8B % 1024) == 0, "stage alignment");
-constexpr int NTHREADS = 448;
+constexpr int NEPI = 12;             // epilogue warps (three per tensor-memory lane quarter)
+constexpr int NTHREADS = (10 + NEPI) * 32;
+constexpr int NGRP = TNMAX / 32;     // 32-token groups of the largest item
 
 __device__ __forceinline__ int sq4(uint32_t w, int acc) { return __dp4a(int(w), int(w), acc); }
 
@@ -106,11 +110,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(B_T_EMPTY + s), 2);  // MMA completions of both CTAs
     }
     mbar_init(bar(B_ACC_FULL), 1);
-    mbar_init(bar(B_ACC_EMPTY), 4);
+    mbar_init(bar(B_ACC_EMPTY), NEPI);
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(B_NORM_READY + b), 8);  // both converter groups
       mbar_init(bar(B_NORM_FREE + b), 1);
-      mbar_init(bar(B_NORM_READ + b), 4);
+      mbar_init(bar(B_NORM_READ + b), NEPI);
     }
     mbar_init(bar(B_MMA_DONE), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -299,6 +303,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       for (int j = lane; j < tl.rows; j += 32) tmax = max(tmax, a.a_norm2[int64_t(tl.row0) + j]);
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+      // the item's token scales (lane j of group p holds token 32p + j) and
+      // this thread's weight scale, loaded while the item's MMAs still run
+      const int64_t n = int64_t(wb) * WM + q * 32 + lane;  // this thread's output channel
+      const float swn = a.sw[int64_t(tl.expert) * a.N + n];
+      float sal[NGRP];
+#pragma unroll
+      for (int p = 0; p < NGRP; ++p)
+        sal[p] = p * 32 + lane < tl.rows ? a.sa[int64_t(tl.row0) + p * 32 + lane] : 0.0f;
       if (!__all_sync(0xffffffffu, mbar_wait<500>(bar(B_ACC_FULL), ii & 1, abort_flag)) ||
           !__all_sync(0xffffffffu, mbar_wait(bar(B_NORM_READY + b), par, abort_flag))) {
         fail();
@@ -310,7 +322,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_NORM_READ + b));
       if (warp == 10 && lane == 0) {
-        // once all four epilogue warps have read the norm, clear it for the
+        // once every epilogue warp has read the norm, clear it for the
         // item after next and hand the slot back to the converters
         if (mbar_wait(bar(B_NORM_READ + b), par, abort_flag)) {
           norm[2 * b] = 0;
@@ -321,15 +333,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
       }
       if (nw * (long long)tmax >= (1ll << 48) && q == 0 && lane == 0) atomicExch(redo, 1);
-      const int64_t n = int64_t(wb) * WM + q * 32 + lane;  // this thread's output channel
-      const float swn = a.sw[int64_t(tl.expert) * a.N + n];
       const int nm = nmma_of(tl.rows);
       const uint32_t taddr = tmem + (uint32_t(q * 32) << 16);
-      for (int p = 0; p * 32 < nm; ++p) {
+#pragma unroll 1
+      for (int p = (warp - 10) >> 2; p < NGRP; p += NEPI / 4) {
+        if (p * 32 >= nm) break;
         uint32_t v[32];
         tmem_ld32(taddr + 32u * p, v);
         const int tok0 = p * 32;
-        const float sal = (tok0 + lane < tl.rows) ? a.sa[int64_t(tl.row0) + tok0 + lane] : 0.0f;
+        float sp = sal[0];  // sal[p] without a dynamic register index
+#pragma unroll
+        for (int m = 1; m < NGRP; ++m) sp = p == m ? sal[m] : sp;
         tmem_wait_ld();
         const int lim = min(32, tl.rows - tok0);
         if (a.out_type == WQ_OUT_I32) {
@@ -341,7 +355,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           uint16_t *o = static_cast<uint16_t *>(a.out) + (int64_t(tl.row0) + tok0) * a.N + n;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float s = __shfl_sync(0xffffffffu, sal, j);
+            const float s = __shfl_sync(0xffffffffu, sp, j);
             if (j < lim)
               o[int64_t(j) * a.N] = f_to_bf16(__fmul_rn(__fmul_rn(__uint_as_float(v[j]), s), swn));
           }
