@@ -23,7 +23,10 @@
 // one expert (two MMAs per K step beyond 256), so an expert is one item per
 // weight block and its weight tile is widened once.  Tensor memory: columns
 // [0, 384) the accumulator, [384, 512) four 32-column weight stages.
-//   warp 0      TMA producer (int8 weights; half of each token tile, multicast)
+//   warp 0      TMA producer of the int8 weights
+//   warp 22     TMA producer of the tokens (half of each stage, multicast);
+//               separate from the weight producer so neither ring's wait
+//               holds back the other's copies
 //   warp 1      TMEM allocator and MMA issuer (one thread)
 //   warps 2-9   converters, two groups of four taking alternate K stages:
 //               one weight row per thread, int8 -> fp16 -> TMEM
@@ -46,13 +49,17 @@ constexpr int WT_COL = ACC_COLS;     // first tensor-memory column of the weight
 constexpr int NWT = 4;               // weight stages in tensor memory (32 columns each)
 constexpr int SW8 = 4;               // int8 weight staging ring (shared memory)
 constexpr int ST = 4;                // token slots (shared memory)
+// a K stage's weight columns and token slot are released together: one
+// commit per stage, multicast to both CTAs' token-empty barriers, which the
+// converters wait on as well
+static_assert(NWT == ST, "a weight stage is released with its token slot");
 constexpr int W8B = WM * BK;         // int8 weight stage bytes
 constexpr int TB = TNMAX * BK * 2;   // token slot bytes (fp16)
 constexpr int OFF_T = 0;
 constexpr int OFF_W8 = OFF_T + ST * TB;
 constexpr int OFF_BAR = OFF_W8 + SW8 * W8B;
-constexpr int B_W8_FULL = 0, B_W8_EMPTY = SW8, B_WT_FULL = 2 * SW8, B_WT_EMPTY = 2 * SW8 + NWT,
-              B_T_FULL = 2 * SW8 + 2 * NWT, B_T_EMPTY = B_T_FULL + ST,
+constexpr int B_W8_FULL = 0, B_W8_EMPTY = SW8, B_WT_FULL = 2 * SW8,
+              B_T_FULL = 2 * SW8 + NWT, B_T_EMPTY = B_T_FULL + ST,
               B_ACC_FULL = B_T_EMPTY + ST, B_ACC_EMPTY = B_ACC_FULL + 1,
               B_NORM_READY = B_ACC_FULL + 2,  // [2]
     B_NORM_FREE = B_ACC_FULL + 4,             // [2]
@@ -65,7 +72,8 @@ constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory plan too large");
 static_assert((TB % 1024) == 0 && (W8B % 1024) == 0, "stage alignment");
 constexpr int NEPI = 12;             // epilogue warps (three per tensor-memory lane quarter)
-constexpr int NTHREADS = (10 + NEPI) * 32;
+constexpr int WARP_TOK = 10 + NEPI;  // token producer
+constexpr int NTHREADS = (11 + NEPI) * 32;
 constexpr int NGRP = TNMAX / 32;     // 32-token groups of the largest item
 
 __device__ __forceinline__ int sq4(uint32_t w, int acc) { return __dp4a(int(w), int(w), acc); }
@@ -103,7 +111,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     }
     for (int s = 0; s < NWT; ++s) {
       mbar_init(bar(B_WT_FULL + s), 4);
-      mbar_init(bar(B_WT_EMPTY + s), 1);
     }
     for (int s = 0; s < ST; ++s) {
       mbar_init(bar(B_T_FULL + s), 1);   // local expect_tx; bytes from both CTAs' copies
@@ -137,21 +144,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ weight producer
     if (lane == 0) {
-      int g = 0, gw = 0, gt = 0;  // stage counter; weight / token stages issued
+      int g = 0, gw = 0;
       bool ok = true;
       for (int ip = pair; ip < items && ok; ip += npairs) {
         const Tile tl = tiles[ip / NBP];
         const int wb = (ip % NBP) * 2 + int(rank);
-        const int box = box_of(nmma_of(tl.rows));
-        const CUtensorMap *tmT =
-            box == 8 ? &tmT8 : (box == 32 ? &tmT32 : (box == 128 ? &tmT128 : &tmT192));
-        const uint32_t ttx = uint32_t(2 * box * BK * 2);
         const int wrow = int(int64_t(tl.expert) * a.N + int64_t(wb) * WM);
-        const int trow = tl.row0 + int(rank) * box;
         for (int i = 0; i < KT; ++i, ++g) {
-          const int sw = g % SW8, stt = g % ST;
+          const int sw = g % SW8;
           if (!mbar_wait<200>(bar(B_W8_EMPTY + sw), ((g / SW8) & 1) ^ 1, abort_flag)) {
             fail();
             ok = false;
@@ -160,6 +162,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           mbar_expect_tx(bar(B_W8_FULL + sw), W8B);
           tma_load_2d(base + OFF_W8 + uint32_t(sw) * W8B, &tmW, i * BK, wrow, bar(B_W8_FULL + sw));
           gw = g + 1;
+        }
+      }
+      if (!ok) {
+        for (int j = gw > SW8 ? gw - SW8 : 0; j < gw; ++j)
+          mbar_wait_bounded(bar(B_W8_FULL + j % SW8), (j / SW8) & 1);
+      }
+    }
+  } else if (warp == WARP_TOK) {
+    // ------------------------------------------------------------ token producer
+    if (lane == 0) {
+      int g = 0, gt = 0;
+      bool ok = true;
+      for (int ip = pair; ip < items && ok; ip += npairs) {
+        const Tile tl = tiles[ip / NBP];
+        const int box = box_of(nmma_of(tl.rows));
+        const CUtensorMap *tmT =
+            box == 8 ? &tmT8 : (box == 32 ? &tmT32 : (box == 128 ? &tmT128 : &tmT192));
+        const uint32_t ttx = uint32_t(2 * box * BK * 2);
+        const int trow = tl.row0 + int(rank) * box;
+        for (int i = 0; i < KT; ++i, ++g) {
+          const int stt = g % ST;
           if (!mbar_wait<200>(bar(B_T_EMPTY + stt), ((g / ST) & 1) ^ 1, abort_flag)) {
             fail();
             ok = false;
@@ -171,9 +194,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           gt = g + 1;
         }
       }
-      if (!ok) {  // let copies already in flight land before the CTA goes away
-        for (int j = gw > SW8 ? gw - SW8 : 0; j < gw; ++j)
-          mbar_wait_bounded(bar(B_W8_FULL + j % SW8), (j / SW8) & 1);
+      if (!ok) {
         for (int j = gt > ST ? gt - ST : 0; j < gt; ++j)
           mbar_wait_bounded(bar(B_T_FULL + j % ST), (j / ST) & 1);
       }
@@ -214,7 +235,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
               mma_f16_ts(tmem + uint32_t(n0), wt + 8u * kk, sdesc(t0 + uint32_t(n0) * 128u + 32u * kk), idesc1,
                          (i | kk) ? 1u : 0u);
           }
-          mma_commit(bar(B_WT_EMPTY + swt));
           mma_commit_mc(bar(B_T_EMPTY + stt), 3);
         }
         if (ok) mma_commit(bar(B_ACC_FULL));
@@ -266,7 +286,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           nrm = sq4(v[m].w, sq4(v[m].z, sq4(v[m].y, sq4(v[m].x, nrm))));
         }
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(bar(B_WT_EMPTY + swt), ((g / NWT) & 1) ^ 1, abort_flag))) {
+                        mbar_wait(bar(B_T_EMPTY + swt), ((g / NWT) & 1) ^ 1, abort_flag))) {
           fail();
           ok = false;
           break;
@@ -291,7 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_NORM_READY + b));
     }
-  } else {
+  } else if (warp < WARP_TOK) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // tensor-memory lane quarter of this warp
     int ii = 0;
