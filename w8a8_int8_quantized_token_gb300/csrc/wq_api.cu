@@ -146,10 +146,12 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
   if (a.A16 != nullptr) {
     // fp16-stored codes: the CTA-pair engine, then the CUDA-core engine reading
     // fp16 codes as its exact recompute (it exits at once when *redo == 0)
-    // long K: the tensor-memory-weights engine (one item per expert and
-    // weight block; its epilogue is not overlapped, a small cost per long
-    // item); short K: the double-buffered shared-memory engine
-    if (a.K >= 4096 && gemm_tc5_supported(a)) {
+    // K >= 1024: the tensor-memory-weights engine (one item of up to 384
+    // tokens per expert and weight block, so an expert a little above 256
+    // rows streams its weights once; its drain is not overlapped with the
+    // next item's MMAs but takes twelve warps); shorter K: the double-buffered
+    // shared-memory engine
+    if (a.K >= 1024 && gemm_tc5_supported(a)) {
       // token tiles of up to 384 rows (fit the 256-row list's capacity)
       WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, gemm_tc5_tile_rows(), a.R,
                                 w.t256, w.n256, w.redo, st));

@@ -20,7 +20,14 @@
 // the other: it scales the chunk column by column and adds it to a running
 // sum held in tensor memory (columns [320, 480)), and after the last K block
 // writes bf16.
-//   warp 0      TMA producer (weights; half the tokens, multicast)
+//   warp 0      TMA producer of the int8 weights
+//   warp 14     TMA producer of the tokens (half of each stage, multicast);
+//               the two producers wait on separate rings, so weight copies
+//               run up to SW8 stages ahead of the converters whatever the
+//               token ring holds
+// A K stage's widened weights and token slot are released together: one
+// commit per stage, multicast to both CTAs' token-empty barriers, which the
+// converters wait on as well (the two rings have the same depth).
 //   warp 1      TMEM allocator and MMA issuer (one thread)
 //   warps 2-5   converters: int8 weights -> fp16 (128-byte swizzled K-major)
 //   warps 6-13  epilogue (two per tensor-memory lane quarter, alternate
@@ -36,7 +43,8 @@ namespace {
 using namespace tc;
 
 constexpr int WM = 128, TN = 160, BK = 64;
-constexpr int SW8 = 4, SW16 = 3, ST = 5;        // ring depths: int8 W, fp16 W, fp16 tokens
+constexpr int SW8 = 8, SW16 = 4, ST = 4;        // ring depths: int8 W, fp16 W, fp16 tokens
+static_assert(SW16 == ST, "a widened-weight slot is released with its token slot");
 constexpr int W8B = WM * BK, W16B = 2 * W8B;    // weight stage bytes
 constexpr int TB = TN * BK * 2;                 // token stage bytes (fp16)
 constexpr int CH0 = 0, CH1 = TN, RUN = 2 * TN;  // tensor-memory columns: chunks, running sum
@@ -46,8 +54,8 @@ constexpr int OFF_W8 = OFF_W16 + SW16 * W16B;
 constexpr int NEPI = 8;                         // epilogue warps
 constexpr int OFF_SC = OFF_W8 + SW8 * W8B;      // float [NEPI][TN] column scales
 constexpr int OFF_BAR = OFF_SC + NEPI * TN * 4;
-constexpr int B_W8_FULL = 0, B_W8_EMPTY = SW8, B_W16_FULL = 2 * SW8, B_W16_EMPTY = 2 * SW8 + SW16,
-              B_T_FULL = 2 * SW8 + 2 * SW16, B_T_EMPTY = B_T_FULL + ST,
+constexpr int B_W8_FULL = 0, B_W8_EMPTY = SW8, B_W16_FULL = 2 * SW8,
+              B_T_FULL = 2 * SW8 + SW16, B_T_EMPTY = B_T_FULL + ST,
               B_ACC_FULL = B_T_EMPTY + ST,  // [2]
     B_ACC_EMPTY = B_ACC_FULL + 2,           // [2]
     B_MMA_DONE = B_ACC_FULL + 4, NBAR = B_ACC_FULL + 5;
@@ -57,7 +65,8 @@ constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
 static_assert(TB % 1024 == 0 && OFF_W16 % 1024 == 0 && OFF_W8 % 1024 == 0, "swizzle alignment");
 static_assert(RUN + TN <= 512, "tensor memory plan");
 static_assert(SMEM_BYTES <= 232448, "shared memory plan too large");
-constexpr int NTHREADS = 448;
+constexpr int NTHREADS = 480;
+constexpr int WARP_TOK = 14;            // token producer
 constexpr int GCONV = 128;              // threads of one converter group
 constexpr int NJW = WM * 4 / GCONV;     // weight 16-byte pieces per converter thread
 
@@ -105,7 +114,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     }
     for (int s = 0; s < SW16; ++s) {
       mbar_init(bar(B_W16_FULL + s), GCONV / 32);
-      mbar_init(bar(B_W16_EMPTY + s), 1);
     }
     for (int s = 0; s < ST; ++s) {
       mbar_init(bar(B_T_FULL + s), 1);   // local expect_tx; bytes from both CTAs' copies
@@ -134,20 +142,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   auto box_of = [](int nmma) { return nmma <= 16 ? 8 : (nmma <= 64 ? 32 : 80); };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ weight producer
     if (lane == 0) {
-      int g = 0, gw = 0, gt = 0;  // stage counter; weight / token stages issued
+      int g = 0, gw = 0;  // stage counter; weight stages issued
       bool ok = true;
       for (int ip = pair; ip < items && ok; ip += npairs) {
         const Tile tl = tiles[ip / NBP];
         const int wb = (ip % NBP) * 2 + int(rank);
-        const int box = box_of(nmma_of(tl.rows));
-        const CUtensorMap *tmT = box == 8 ? &tmT8 : (box == 32 ? &tmT32 : &tmT80);
-        const uint32_t ttx = uint32_t(2 * box * BK * 2);
         const int wrow = int(int64_t(tl.expert) * a.N + int64_t(wb) * WM);
-        const int trow = tl.row0 + int(rank) * box;
         for (int i = 0; i < KT; ++i, ++g) {
-          const int sw = g % SW8, stt = g % ST;
+          const int sw = g % SW8;
           if (!mbar_wait<200>(bar(B_W8_EMPTY + sw), ((g / SW8) & 1) ^ 1, abort_flag)) {
             fail();
             ok = false;
@@ -156,6 +160,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           mbar_expect_tx(bar(B_W8_FULL + sw), W8B);
           tma_load_2d(base + OFF_W8 + uint32_t(sw) * W8B, &tmW, i * BK, wrow, bar(B_W8_FULL + sw));
           gw = g + 1;
+        }
+      }
+      if (!ok) {  // let copies already in flight land before the CTA goes away
+        for (int j = gw > SW8 ? gw - SW8 : 0; j < gw; ++j)
+          mbar_wait_bounded(bar(B_W8_FULL + j % SW8), (j / SW8) & 1);
+      }
+    }
+  } else if (warp == WARP_TOK) {
+    // ------------------------------------------------------------ token producer
+    if (lane == 0) {
+      int g = 0, gt = 0;  // stage counter; token stages issued
+      bool ok = true;
+      for (int ip = pair; ip < items && ok; ip += npairs) {
+        const Tile tl = tiles[ip / NBP];
+        const int box = box_of(nmma_of(tl.rows));
+        const CUtensorMap *tmT = box == 8 ? &tmT8 : (box == 32 ? &tmT32 : &tmT80);
+        const uint32_t ttx = uint32_t(2 * box * BK * 2);
+        const int trow = tl.row0 + int(rank) * box;
+        for (int i = 0; i < KT; ++i, ++g) {
+          const int stt = g % ST;
           if (!mbar_wait<200>(bar(B_T_EMPTY + stt), ((g / ST) & 1) ^ 1, abort_flag)) {
             fail();
             ok = false;
@@ -167,9 +191,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           gt = g + 1;
         }
       }
-      if (!ok) {  // let copies already in flight land before the CTA goes away
-        for (int j = gw > SW8 ? gw - SW8 : 0; j < gw; ++j)
-          mbar_wait_bounded(bar(B_W8_FULL + j % SW8), (j / SW8) & 1);
+      if (!ok) {
         for (int j = gt > ST ? gt - ST : 0; j < gt; ++j)
           mbar_wait_bounded(bar(B_T_FULL + j % ST), (j / ST) & 1);
       }
@@ -204,7 +226,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
               mma_f16(d, sdesc(w0 + 32u * kk), sdesc(t0 + 32u * kk), idesc, (h | kk) ? 1u : 0u);
-            mma_commit(bar(B_W16_EMPTY + s16));
             mma_commit_mc(bar(B_T_EMPTY + stt), 3);
           }
           if (ok) mma_commit(bar(B_ACC_FULL + b));
@@ -236,7 +257,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_W8_EMPTY + sw));
         if (!__all_sync(0xffffffffu,
-                        mbar_wait<1000>(bar(B_W16_EMPTY + s16), ((g / SW16) & 1) ^ 1, abort_flag))) {
+                        mbar_wait<1000>(bar(B_T_EMPTY + s16), ((g / SW16) & 1) ^ 1, abort_flag))) {
           fail();
           ok = false;
           break;
@@ -253,7 +274,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         if (lane == 0) mbar_arrive(bar(B_W16_FULL + s16));
       }
     }
-  } else {
+  } else if (warp < 6 + NEPI) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;          // tensor-memory lane quarter of this warp
     const int half = (warp - 6) >> 2;  // which alternate 32-column groups it drains
