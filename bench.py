@@ -52,10 +52,10 @@ def layer_ops(T, H, I, k):
 # kernel source it was measured on: it is reported while that file's SHA-256
 # matches, else the traffic is null.
 _TC5 = {"kernel": "gemm_tc5_kernel", "file": "wq_gemm_tc5.cu",
-        "sha256": "be4b94c601fcad1b269a7dcec9bfbe7318794275217113123ce3f5e0bad01a11",
-        "bytes": 8 * (1.080667e9 + 62.903808e6),
+        "sha256": "c2c90d59701dbab23dc5fc5ec6bb50b51931a084064dd986e7c509c6e58f0815",
+        "bytes": 8 * (1.080453e9 + 62.256384e6),
         "how": "ncu capture of GEMM1 at 1024 tokens / 32 experts (same 256 rows per expert), "
-               "dram read+write x 8 experts ratio (profiles/gemm_tc5_tc4_reduced_prefill.md)"}
+               "dram read+write x 8 experts ratio (profiles/gemm_tc5_reduced_prefill.md)"}
 TRAFFIC = {
     "prefill": _TC5,
     "prefill_f32": _TC5,
