@@ -23,7 +23,7 @@ bool gemm_tc4_supported(const GemmArgs &a);
 int launch_gemm_tc5(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
                     int32_t *redo, cudaStream_t st);
 bool gemm_tc5_supported(const GemmArgs &a);
-int gemm_tc5_tile_rows();
+int gemm_tc5_tile_rows(const GemmArgs &a);
 int launch_gemm_small(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
                       cudaStream_t st);
 int launch_gemm_tc6(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
@@ -146,14 +146,14 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
   if (a.A16 != nullptr) {
     // fp16-stored codes: the CTA-pair engine, then the CUDA-core engine reading
     // fp16 codes as its exact recompute (it exits at once when *redo == 0)
-    // K >= 1024: the tensor-memory-weights engine (one item of up to 384
-    // tokens per expert and weight block, so an expert a little above 256
+    // K >= 1024: the tensor-memory-weights engine (one item of up to 320 or
+    // 384 tokens per expert and weight block, so an expert a little above 256
     // rows streams its weights once; its drain is not overlapped with the
     // next item's MMAs but takes twelve warps); shorter K: the double-buffered
     // shared-memory engine
     if (a.K >= 1024 && gemm_tc5_supported(a)) {
-      // token tiles of up to 384 rows (fit the 256-row list's capacity)
-      WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, gemm_tc5_tile_rows(), a.R,
+      // token tiles of up to 320 or 384 rows (fit the 256-row list's capacity)
+      WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, gemm_tc5_tile_rows(a), a.R,
                                 w.t256, w.n256, w.redo, st));
       WQ_TRY(launch_gemm_tc5(a, w.t256, w.n256, int(w.m256), w.redo, st));
     } else {
