@@ -52,8 +52,8 @@ def layer_ops(T, H, I, k):
 # kernel source it was measured on: it is reported while that file's SHA-256
 # matches, else the traffic is null.
 _TC5 = {"kernel": "gemm_tc5_kernel", "file": "wq_gemm_tc5.cu",
-        "sha256": "c2c90d59701dbab23dc5fc5ec6bb50b51931a084064dd986e7c509c6e58f0815",
-        "bytes": 8 * (1.080453e9 + 62.256384e6),
+        "sha256": "0371ec48d23b80f7e62d1618579bb7c963acd55212b87399377995b7a4a796b1",
+        "bytes": 8 * (1.077663e9 + 62.478848e6),
         "how": "ncu capture of GEMM1 at 1024 tokens / 32 experts (same 256 rows per expert), "
                "dram read+write x 8 experts ratio (profiles/gemm_tc5_reduced_prefill.md)"}
 TRAFFIC = {

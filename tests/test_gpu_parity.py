@@ -406,16 +406,23 @@ def test_grouped_gemm_f16codes_block(K):
                       "f16 codes block gemm")
 
 
-@pytest.mark.parametrize("K", [2048, 4096])
+@pytest.mark.parametrize("K,counts", [
+    (512, [3, 0, 270, 1, 513]),    # K < 1024: shared-memory-weights pair engine
+    (2048, [3, 0, 270, 1, 513]),   # tensor-memory weights, 320-token items with
+    (4096, [3, 0, 270, 1, 513]),   #   output boxes (513 rows split at 320)
+    (2048, [700, 5, 400]),         # experts average > 320 rows: 384-token items,
+])                                 #   direct stores (700 rows split at 384)
 @pytest.mark.parametrize("extreme", [False, True])
-def test_grouped_gemm_f16codes(extreme, K):
-    """The CTA-pair engines (K 2048: shared-memory weights; K 4096: weights in
-    tensor memory, items above 256 tokens) with codes in +-40 (the exactness
-    check passes) and their exact recompute (all-127 rows: the check fails),
-    int32 and bf16 outputs, both accumulator modes.  In the extreme case
-    expert-0 rows sum to integers above 2^24 (one odd), so the exact
-    recompute runs and takes each accumulator mode's own steps."""
-    E, counts, N = 5, [3, 0, 270, 1, 513], 512
+def test_grouped_gemm_f16codes(extreme, K, counts):
+    """The CTA-pair engines (K < 1024: shared-memory weights; K >= 1024:
+    weights in tensor memory, two MMAs for items above 256 tokens, 320-token
+    items with shared-memory output boxes or 384-token items with direct
+    stores) with codes in +-40 (the exactness check passes) and their exact
+    recompute (all-127 rows: the check fails), int32 and bf16 outputs, both
+    accumulator modes.  In the extreme case expert-0 rows sum to integers
+    above 2^24 (one odd), so the exact recompute runs and takes each
+    accumulator mode's own steps."""
+    E, N = len(counts), 512
     rng = np.random.default_rng(23)
     offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     R = int(offs[-1])
@@ -424,7 +431,7 @@ def test_grouped_gemm_f16codes(extreme, K):
     W = rng.integers(-lim, lim + 1, (E, N, K), dtype=np.int8)
     if extreme:
         A[:5] = 127
-        W[4, :3] = -127
+        W[E - 1, :3] = -127
         W[0, :3] = 127
         W[0, 2, 5] = 126
     sa = (rng.random(R) * 0.05).astype(np.float32)
