@@ -39,6 +39,47 @@ SCHEME = {"channel": 0, "block": 1}
 ACC = {"i32": 0, "f32": 1}
 
 
+class Replicas:
+    """One process per GPU, each running an independent replica of the layer
+    (no data-path collective: the layer is not sharded here).  Rendezvous from
+    the launcher's RANK / WORLD_SIZE / LOCAL_RANK / MASTER_* variables, a
+    barrier on both sides of the timed region, and the slowest rank's time;
+    the reported value is all ranks' work over that time."""
+
+    def __init__(self, backend="nccl", device=None):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.device = device
+        if self.world > 1:
+            import torch.distributed as dist
+            if backend == "nccl":
+                dist.init_process_group(backend, device_id=device)
+            else:
+                dist.init_process_group(backend)
+
+    def barrier(self):
+        if self.world > 1:
+            torch.distributed.barrier()
+
+    def max(self, value):
+        """The largest `value` over the ranks (every rank gets it)."""
+        if self.world == 1:
+            return float(value)
+        t = torch.tensor([float(value)], dtype=torch.float64, device=self.device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    def total_rate(self, units_per_rank, seconds):
+        """Whole-job throughput: the units every rank processed over the
+        slowest rank's time."""
+        return self.world * units_per_rank / seconds
+
+    def close(self):
+        if self.world > 1:
+            torch.distributed.destroy_process_group()
+
+
 def layer_ops(T, H, I, k):
     """Algorithmic integer ops of one layer step: 2 per multiply-add of the
     two GEMMs over the T*k routed (token, expert) pairs."""
@@ -595,14 +636,11 @@ def main():
         run_masked(args, cfg)
         return
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
+    reps_ = Replicas("nccl", dev)
+    world, rank = reps_.world, reps_.rank
     from w8a8_int8_quantized_token_gb300 import binding as wq
     from w8a8_int8_quantized_token_gb300 import build_lib
     build_lib.build()
@@ -626,8 +664,7 @@ def main():
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def barrier():
-        if world > 1:
-            torch.distributed.barrier()
+        reps_.barrier()
         torch.cuda.synchronize()
 
     with ClockSampler(local) as clk:
@@ -641,11 +678,7 @@ def main():
         launches = wq.lib().wq_kernel_launches() - n0
         torch.cuda.nvtx.range_pop()
         barrier()
-    total_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reps_.max(start.elapsed_time(end))
     stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]))
                 for j, s in enumerate(Layer.STAGES)}
     if int(layer.status.item()) != 0:
@@ -653,8 +686,8 @@ def main():
 
     ms = total_ms / args.steps
     ops = layer_ops(cfg.T, cfg.H, cfg.I, cfg.k)
-    tops = world * ops / (ms / 1e3) / 1e12
-    tok_s = world * cfg.T / (ms / 1e3)
+    tops = reps_.total_rate(ops, ms / 1e3) / 1e12
+    tok_s = reps_.total_rate(cfg.T, ms / 1e3)
 
     # end to end: host activations in, host output back, through the one-call API
     xh, lh = x.cpu().pin_memory(), logits.cpu().pin_memory()
@@ -669,11 +702,7 @@ def main():
         wq.moe_forward_host(xh, lh, *weights, cfg.k, cfg.scheme, cfg.acc, out_host=outh, ws=hws)
     e1.record()
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reps_.max(e0.elapsed_time(e1) / args.steps)
     if not torch.equal(outh.view(torch.int16), ref.cpu().view(torch.int16)):
         raise RuntimeError("host-buffer layer differs from the device one")
 
@@ -693,7 +722,7 @@ def main():
             "tokens_per_s": tok_s, "stages_ms": stage_ms,
             "gpu_launches": launches,
             "roofline": roofline,
-            "e2e": {"value": world * ops / (e2e_ms / 1e3) / 1e12, "unit": "TOPS",
+            "e2e": {"value": reps_.total_rate(ops, e2e_ms / 1e3) / 1e12, "unit": "TOPS",
                     "h2d_bytes_per_step": cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4,
                     "d2h_bytes_per_step": cfg.T * cfg.H * 2, "ms_per_step": e2e_ms},
             "clocks": clk.summary()}
@@ -710,8 +739,7 @@ def main():
                                           f"workload, full layer, run {reps} times ({dt:.1f} s)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    reps_.close()
 
 
 if __name__ == "__main__":
