@@ -97,6 +97,54 @@ def test_invalid_arguments_rejected_on_host(lib):
                                     None, 0, None, None) == 0
 
 
+def test_newer_entry_points_reject_bad_arguments_on_host(lib):
+    """The dense linear, the FP8 weight converter and the fp16-code entries
+    check their arguments on the host, before touching a device."""
+    fake = 4096  # never dereferenced: argument checks fail first
+    big = 1 << 30
+    # dense linear: negative T, bad scheme, K not a multiple of 128, ldx < K
+    assert lib.wq_linear_w8a8(fake, -1, 128, 128, fake, fake, 256, 0, 0, fake, fake, big, None,
+                              None) == -1
+    assert lib.wq_linear_w8a8(fake, 4, 128, 128, fake, fake, 256, 7, 0, fake, fake, big, None,
+                              None) == -1
+    assert lib.wq_linear_w8a8(fake, 4, 100, 100, fake, fake, 256, 0, 0, fake, fake, big, None,
+                              None) == -2
+    assert lib.wq_linear_w8a8(fake, 4, 128, 64, fake, fake, 256, 0, 0, fake, fake, big, None,
+                              None) == -1
+    # ... a workspace smaller than its size function says; no rows is a no-op
+    need = lib.wq_linear_w8a8_workspace_size(4, 128, 256, 0)
+    assert need > 0 and lib.wq_linear_w8a8_workspace_size(4, 100, 256, 0) == 0
+    assert lib.wq_linear_w8a8(fake, 4, 128, 128, fake, fake, 256, 0, 0, fake, fake, need - 1,
+                              None, None) == -5
+    assert lib.wq_linear_w8a8(None, 0, 128, 128, None, None, 256, 0, 0, None, None, 0, None,
+                              None) == 0
+    # FP8 weight converter: negative size, bad scheme, sizes off the 128 grid
+    assert lib.wq_convert_fp8_weights(fake, fake, -1, 128, 0, fake, fake, None) == -1
+    assert lib.wq_convert_fp8_weights(fake, fake, 128, 128, 5, fake, fake, None) == -1
+    assert lib.wq_convert_fp8_weights(fake, fake, 100, 128, 0, fake, fake, None) == -2
+    assert lib.wq_convert_fp8_weights(None, None, 0, 128, 1, None, None, None) == 0
+    # SiLU-mul-quant to fp16 codes: negative rows, unsupported group, missing
+    # norms for per-row scales, width not a multiple of 8
+    assert lib.wq_silu_mul_quant_f16(fake, -1, 128, 0, fake, fake, fake, None) == -1
+    assert lib.wq_silu_mul_quant_f16(fake, 4, 128, 100, fake, fake, fake, None) == -2
+    assert lib.wq_silu_mul_quant_f16(fake, 4, 128, 0, fake, fake, None, None) == -1
+    assert lib.wq_silu_mul_quant_f16(fake, 4, 12, 0, fake, fake, fake, None) == -2
+    assert lib.wq_silu_mul_quant_f16(None, 0, 128, 0, None, None, None, None) == 0
+    # fp16-code grouped GEMM: negative rows, missing norms (channel-wise),
+    # N not a multiple of 256, workspace too small
+    gemm = lambda n2, R, N, ws: lib.wq_grouped_gemm_w8a8_f16codes(
+        fake, n2, fake, fake, fake, fake, 4, R, N, 128, 0, 0, 0, fake, fake, ws, None, None)
+    assert gemm(fake, -1, 256, big) == -1
+    assert gemm(None, 16, 256, big) == -1
+    assert gemm(fake, 16, 128, big) == -2
+    assert gemm(fake, 16, 256, 1) == -5
+    assert gemm(None, 0, 256, 0) == 0
+    # fp16 permute: no groups, rows not a multiple of 16 codes
+    assert lib.wq_moe_permute_f16(fake, fake, 0, 4, 2, 128, fake, 8, fake, fake, fake, None) == -1
+    assert lib.wq_moe_permute_f16(fake, fake, 1, 4, 2, 8, fake, 8, fake, fake, fake, None) == -2
+    assert lib.wq_moe_permute_f16(None, None, 1, 0, 2, 128, None, 0, None, None, None, None) == 0
+
+
 def test_no_device_is_reported(lib):
     # this check runs where no GPU is visible; on a GPU machine device 10**6 does not exist
     assert lib.wq_init(10 ** 6) == -3
