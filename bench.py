@@ -2,17 +2,21 @@
 
 One step = the whole hot path on one batch: route -> quantize -> align ->
 permute -> GEMM1 (gate_up) -> SiLU-mul + re-quantize -> GEMM2 (down) ->
-combine, each a call into libwq.so's C ABI on one stream.  Weights (11.3 GB
-of int8) and the step's activations are resident in HBM before the timed
-region; CUDA events between the stages give per-kernel times inside the
-timed region.  The e2e figure runs the same layer through
-wq_moe_forward_host with pinned host activations, copies included.
+combine.  Weights (11.3 GB of int8) and the step's activations are resident
+in HBM before the timed region.  `value` times the one-call layer
+(wq_moe_forward) over K steps; a second timed pass runs the same steps as
+separate C-ABI calls with CUDA events between them for the per-stage times
+and the rooflines; `e2e` runs the layer through wq_moe_forward_host with
+pinned host activations, copies included.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config prefill]
+  python bench.py [--steps K] [--warmup W] [--config prefill]
   python bench.py --impl reference   # the CPU oracle on a bounded sample
 
-Under torchrun each rank runs an independent replica on its own GPU (the
-layer's experts are not sharded here; value = all ranks' work / max time).
+One GPU only: the GEMM engines share token tiles between the two CTAs of a
+cluster through TMA multicast, which this build keeps to one-GPU runs, so a
+launch with WORLD_SIZE > 1 (or --gpus > 1) is refused before the library is
+loaded.  The reference arm (CPU only) runs on rank 0 and the other ranks
+exit without work.
 """
 from __future__ import annotations
 
@@ -39,47 +43,6 @@ SCHEME = {"channel": 0, "block": 1}
 ACC = {"i32": 0, "f32": 1}
 
 
-class Replicas:
-    """One process per GPU, each running an independent replica of the layer
-    (no data-path collective: the layer is not sharded here).  Rendezvous from
-    the launcher's RANK / WORLD_SIZE / LOCAL_RANK / MASTER_* variables, a
-    barrier on both sides of the timed region, and the slowest rank's time;
-    the reported value is all ranks' work over that time."""
-
-    def __init__(self, backend="nccl", device=None):
-        self.world = int(os.environ.get("WORLD_SIZE", "1"))
-        self.rank = int(os.environ.get("RANK", "0"))
-        self.local = int(os.environ.get("LOCAL_RANK", "0"))
-        self.device = device
-        if self.world > 1:
-            import torch.distributed as dist
-            if backend == "nccl":
-                dist.init_process_group(backend, device_id=device)
-            else:
-                dist.init_process_group(backend)
-
-    def barrier(self):
-        if self.world > 1:
-            torch.distributed.barrier()
-
-    def max(self, value):
-        """The largest `value` over the ranks (every rank gets it)."""
-        if self.world == 1:
-            return float(value)
-        t = torch.tensor([float(value)], dtype=torch.float64, device=self.device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
-
-    def total_rate(self, units_per_rank, seconds):
-        """Whole-job throughput: the units every rank processed over the
-        slowest rank's time."""
-        return self.world * units_per_rank / seconds
-
-    def close(self):
-        if self.world > 1:
-            torch.distributed.destroy_process_group()
-
-
 def layer_ops(T, H, I, k):
     """Algorithmic integer ops of one layer step: 2 per multiply-add of the
     two GEMMs over the T*k routed (token, expert) pairs."""
@@ -88,15 +51,14 @@ def layer_ops(T, H, I, k):
 
 # DRAM traffic per launch of GEMM1's main kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum of one ncu capture on a reduced workload with the same
-# rows per expert, scaled to the full launch by the expert count; the profile
-# summaries under profiles/ give the commands).  A figure holds only for the
-# kernel source it was measured on: it is reported while that file's SHA-256
-# matches, else the traffic is null.
+# rows per expert, scaled to the full launch by the expert count).  A figure
+# holds only for the kernel source it was measured on: it is reported while
+# that file's SHA-256 matches, else the traffic is null.
 _TC5 = {"kernel": "gemm_tc5_kernel", "file": "wq_gemm_tc5.cu",
         "sha256": "0371ec48d23b80f7e62d1618579bb7c963acd55212b87399377995b7a4a796b1",
         "bytes": 8 * (1.077663e9 + 62.478848e6),
         "how": "ncu capture of GEMM1 at 1024 tokens / 32 experts (same 256 rows per expert), "
-               "dram read+write x 8 experts ratio (profiles/gemm_tc5_reduced_prefill.md)"}
+               "dram read+write scaled by the expert count (x 8)"}
 TRAFFIC = {
     "prefill": _TC5,
     "prefill_f32": _TC5,
@@ -104,7 +66,7 @@ TRAFFIC = {
                "sha256": "e53537d8fa0b3b99d98faf1a3cf1183a0faa56d97eb8a556f491ad0c06afdbdc",
                "bytes": 8 * (941.189888e6 + 4.634624e6),
                "how": "ncu capture of GEMM1 at 16 tokens / 32 experts (same 4 rows per expert), "
-                      "dram read+write x 8 experts ratio (profiles/gemm_small_reduced_decode.md)"},
+                      "dram read+write scaled by the expert count (x 8)"},
 }
 
 
@@ -119,35 +81,84 @@ def measured_traffic(cfg_name):
     return t
 
 
-def gemm1_roofline(peaks, src, g1_ms, rows, touched, H, I, scheme, code_bytes, traffic):
-    """Roofline of the gate_up GEMM: algorithmic flops 2*rows*2I*H and bytes
-    (touched experts' int8 weights and scales, the activation codes and
+def tensor_peak(peaks, clocks):
+    """The measured bf16 dense rate that applies to kernels timed in this run.
+
+    The peaks file holds a burst figure (cuBLAS timed alone) and a sustained
+    one (a seconds-long loop under the power cap, at a lower SM clock).  A
+    kernel timed inside a short step runs at the burst condition when the SM
+    clock sampled during the timed region stayed at its maximum with no power
+    cap; otherwise the sustained figure applies.  Without clock samples the
+    burst figure (the larger, so the smaller fraction) is taken."""
+    burst = peaks["bf16_tflops"]
+    sus = peaks.get("bf16_tflops_sustained", burst)
+    mhz, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    capped = "sw_power_cap" in clocks.get("reasons", [])
+    if mhz is None or not mx:
+        return burst, "burst (no clock samples)"
+    if mhz >= 0.97 * mx and not capped:
+        return burst, "burst (SM clock at its maximum, no power cap, during the timed region)"
+    return sus, "sustained (SM clock below its maximum or power-capped during the timed region)"
+
+
+def gemm_roofline(peaks, src, clocks, ms, rows, touched, N, K, scheme, code_bytes, traffic,
+                  kernel):
+    """Roofline of one grouped GEMM launch: algorithmic flops 2*rows*N*K and
+    bytes (touched experts' int8 weights and scales, the activation codes and
     scales, the bf16 output), bound by whichever of the measured bf16 dense
     rate (tcgen05 kind::f16 runs at it) and the measured HBM copy bandwidth
     the arithmetic intensity reaches first."""
-    N, K = 2 * I, H
     blk = scheme == "block"
     flops = 2.0 * rows * N * K
     nbytes = (touched * N * K + touched * ((N // 128) * (K // 128) if blk else N) * 4
               + rows * K * code_bytes + rows * (K // 128 if blk else 1) * 4 + rows * N * 2)
-    tf = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    tf, which = tensor_peak(peaks, clocks)
     bw = peaks["hbm_gbs"]
-    sec = g1_ms / 1e3
+    sec = ms / 1e3
     if flops / nbytes >= tf * 1e12 / (bw * 1e9):
         r = {"bound": "tensor", "achieved": flops / sec / 1e12, "peak": tf, "unit": "TFLOP/s",
-             "peak_source": f"{src} bf16 sustained (fp16 tcgen05 kind::f16 runs at the bf16 rate; "
-                            f"sm_103a has no kind::i8)"}
+             "peak_source": f"{src} bf16 dense, {which} (fp16 tcgen05 kind::f16 runs at the bf16 "
+                            f"rate; sm_103a has no kind::i8)"}
     else:
         r = {"bound": "hbm", "achieved": nbytes / sec / 1e9, "peak": bw, "unit": "GB/s",
              "peak_source": f"{src} HBM copy bandwidth"}
     r["frac"] = r["achieved"] / r["peak"]
-    r["kernel"] = "grouped_gemm_w8a8 gate_up (GEMM1)"
+    r["kernel"] = kernel
+    r["ms"] = ms
     r["traffic"] = traffic["bytes"] if traffic else None
     if traffic:
         r["traffic_source"] = traffic["how"]
     r["algorithmic_bytes"] = nbytes
     r["flops"] = flops
     return r
+
+
+def gemm1_roofline(peaks, src, g1_ms, rows, touched, H, I, scheme, code_bytes, traffic,
+                   clocks=None):
+    """The gate_up GEMM (N = 2I, K = H)."""
+    return gemm_roofline(peaks, src, clocks or {}, g1_ms, rows, touched, 2 * I, H, scheme,
+                         code_bytes, traffic, "grouped_gemm_w8a8 gate_up (GEMM1)")
+
+
+def layer_bytes(T, H, I, E_touched, k, scheme, E):
+    """Minimal bytes of one layer step: the touched experts' int8 weights and
+    scales, the bf16 activations in and out, the float32 router logits."""
+    blk = scheme == "block"
+    w = E_touched * (2 * I * H + H * I)
+    sc = E_touched * (((2 * I // 128) * (H // 128) + (H // 128) * (I // 128)) if blk
+                      else (2 * I + H)) * 4
+    return w + sc + T * H * 2 + T * E * 4 + T * H * 2
+
+
+def layer_roofline(peaks, clocks, ms, ops, nbytes):
+    """The layer against its floor max(ops / tensor peak, bytes / HBM)."""
+    tf, which = tensor_peak(peaks, clocks)
+    bw = peaks["hbm_gbs"]
+    t_ops, t_bytes = ops / (tf * 1e12), nbytes / (bw * 1e9)
+    floor = max(t_ops, t_bytes)
+    return {"bound": "tensor" if t_ops >= t_bytes else "hbm", "floor_ms": floor * 1e3,
+            "ms": ms, "frac": floor * 1e3 / ms, "ops": ops, "bytes": nbytes,
+            "tensor_peak_tflops": tf, "hbm_gbs": bw, "peak_choice": which}
 
 
 def load_peaks():
@@ -434,27 +445,31 @@ def run_masked(args, cfg):
         e1.record()
         launches = wq.lib().wq_kernel_launches() - n0
         torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
-    gu = torch.empty(E, Mmax, 2 * I, dtype=torch.bfloat16, device=dev)
-    g1 = lambda: wq.grouped_gemm_w8a8_masked(a, sa, mmd, weights[0], weights[1], cfg.scheme, cfg.acc,
-                                             out=gu, status=st)
-    for _ in range(args.warmup):
-        g1()
-    torch.cuda.synchronize()
-    e0.record()
-    for _ in range(args.steps):
-        g1()
-    e1.record()
-    torch.cuda.synchronize()
-    g1_ms = e0.elapsed_time(e1) / args.steps
+        ms = e0.elapsed_time(e1) / args.steps
+        gu = torch.empty(E, Mmax, 2 * I, dtype=torch.bfloat16, device=dev)
+        g1 = lambda: wq.grouped_gemm_w8a8_masked(a, sa, mmd, weights[0], weights[1], cfg.scheme,
+                                                 cfg.acc, out=gu, status=st)
+        for _ in range(args.warmup):
+            g1()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            g1()
+        e1.record()
+        torch.cuda.synchronize()
+        g1_ms = e0.elapsed_time(e1) / args.steps
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())}")
+    clocks = clk.summary()
     rows = int(mm.sum())
     ops = 2.0 * rows * 3 * H * I
     peaks, src = load_peaks()
-    roofline = gemm1_roofline(peaks, src, g1_ms, rows, int((mm > 0).sum()), H, I, cfg.scheme, 1,
-                              measured_traffic(cfg.name))
-    roofline["kernel"] = "grouped_gemm_w8a8_masked gate_up (GEMM1)"
+    touched = int((mm > 0).sum())
+    roofline = gemm_roofline(peaks, src, clocks, g1_ms, rows, touched, 2 * I, H, cfg.scheme, 1,
+                             measured_traffic(cfg.name), "grouped_gemm_w8a8_masked gate_up (GEMM1)")
+    # minimal bytes: touched experts' weights and scales, valid rows' codes and
+    # scales in, bf16 outputs of the valid rows
+    nbytes = touched * (3 * H * I + (2 * I + H) * 4) + rows * (H + 4) + rows * H * 2
     line = {"metric": METRIC, "value": ops / (ms / 1e3) / 1e12, "unit": "TOPS", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
@@ -463,7 +478,8 @@ def run_masked(args, cfg):
                        "parallelism": "single"},
             "tokens_per_s": rows / (ms / 1e3), "gemm1_ms": g1_ms, "gpu_launches": launches,
             "roofline": roofline,
-            "clocks": clk.summary()}
+            "layer_roofline": layer_roofline(peaks, clocks, ms, ops, nbytes),
+            "clocks": clocks}
     print(json.dumps(line), flush=True)
 
 
@@ -521,7 +537,8 @@ def run_linear(args, name):
         raise RuntimeError(f"device status {int(st.item())}")
     flops = 2.0 * T * N * K
     peaks, src = load_peaks()
-    tf = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    clocks = clk.summary()
+    tf, which = tensor_peak(peaks, clocks)
     ach = flops / (ms / 1e3) / 1e12
     line = {"metric": METRIC, "value": ach, "unit": "TOPS", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -535,7 +552,7 @@ def run_linear(args, name):
             "roofline": {"bound": "tensor", "kernel": "wq_linear_w8a8 (quantize + INT8 GEMM)",
                          "achieved": ach, "peak": tf, "unit": "TFLOP/s", "frac": ach / tf,
                          "traffic": None, "flops": flops,
-                         "peak_source": f"{src} bf16 sustained (fp16 tcgen05 kind::f16)"},
+                         "peak_source": f"{src} bf16 dense, {which} (fp16 tcgen05 kind::f16)"},
             "e2e": {"value": flops / (e2e_ms / 1e3) / 1e12, "unit": "TOPS",
                     "h2d_bytes_per_step": T * K * 2, "d2h_bytes_per_step": T * N * 2,
                     "ms_per_step": e2e_ms},
@@ -605,6 +622,18 @@ def run_convert(args):
     print(json.dumps(line), flush=True)
 
 
+def one_gpu_only(args):
+    """Refuse a multi-GPU launch of our arm before the library is loaded: the
+    pair GEMM engines' token loads are TMA multicasts between the two CTAs of
+    a cluster, kept to one-GPU runs."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1 or args.gpus > 1:
+        print(f"bench.py: refused: {max(world, args.gpus)} GPUs requested; this build runs the "
+              f"layer on one GPU only (its GEMM engines use TMA multicast within a cluster, "
+              f"which it keeps to one-GPU runs)", file=sys.stderr, flush=True)
+        sys.exit(2)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -618,76 +647,97 @@ def main():
     ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiling)")
     ap.add_argument("--experts", type=int, default=0, help="override the expert count (profiling)")
     args = ap.parse_args()
+    cfg = synth.CONFIGS.get(args.config)
+    if cfg is not None and (args.tokens or args.experts):
+        import dataclasses
+        cfg = dataclasses.replace(cfg, name=cfg.name + "-reduced", T=args.tokens or cfg.T,
+                                  E=args.experts or cfg.E)
+    if args.impl == "reference":
+        if cfg is None:
+            print(json.dumps({"impl": "reference", "unavailable": "the CPU oracle arm covers the "
+                              "MoE layer configurations only"}), flush=True)
+            return
+        run_reference(args, cfg)
+        return
+    one_gpu_only(args)
     if args.config in LINEAR:
         run_linear(args, args.config)
         return
     if args.config == "convert":
         run_convert(args)
         return
-    cfg = synth.CONFIGS[args.config]
-    if args.tokens or args.experts:
-        import dataclasses
-        cfg = dataclasses.replace(cfg, name=cfg.name + "-reduced", T=args.tokens or cfg.T,
-                                  E=args.experts or cfg.E)
-    if args.impl == "reference":
-        run_reference(args, cfg)
-        return
     if cfg.masked:
         run_masked(args, cfg)
         return
+    run_layer(args, cfg)
 
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dev = torch.device("cuda", local)
+
+def run_layer(args, cfg):
+    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    reps_ = Replicas("nccl", dev)
-    world, rank = reps_.world, reps_.rank
     from w8a8_int8_quantized_token_gb300 import binding as wq
     from w8a8_int8_quantized_token_gb300 import build_lib
     build_lib.build()
-    wq.init(local)
+    wq.init(0)
 
     weights = make_weights(wq, cfg, dev)
     x, logits = synth.layer_inputs(cfg, device=dev)
     layer = Layer(wq, cfg, dev, weights)
+    fws = wq.forward_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.scheme, dev)
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+    fst = wq.new_status(dev)
+    fwd = lambda: wq.moe_forward(x, logits, *weights, cfg.k, cfg.scheme, cfg.acc, out=out, ws=fws,
+                                 status=fst)
 
     # the staged calls reproduce the one-call layer exactly
-    ref = wq.moe_forward(x, logits, *weights, cfg.k, cfg.scheme, cfg.acc)
+    ref = fwd().clone()
     got = layer.step(x, logits)
     torch.cuda.synchronize()
     if not torch.equal(ref.view(torch.int16), got.view(torch.int16)):
         raise RuntimeError("staged step differs from wq_moe_forward")
 
     for _ in range(args.warmup):
+        fwd()
         layer.step(x, logits)
     nst = len(Layer.STAGES)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
-    def barrier():
-        reps_.barrier()
+    with ClockSampler(0) as clk:
+        # timed region 1: the one-call layer, K steps (the headline value)
         torch.cuda.synchronize()
-
-    with ClockSampler(local) as clk:
-        barrier()
         torch.cuda.nvtx.range_push("timed")
         n0 = wq.lib().wq_kernel_launches()
+        start.record()
+        for _ in range(args.steps):
+            fwd()
+        end.record()
+        launches = wq.lib().wq_kernel_launches() - n0
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        total_ms = start.elapsed_time(end)
+        # timed region 2: the same steps as separate calls, events between stages
+        torch.cuda.nvtx.range_push("staged")
         start.record()
         for i in range(args.steps):
             layer.step(x, logits, evs[i])
         end.record()
-        launches = wq.lib().wq_kernel_launches() - n0
         torch.cuda.nvtx.range_pop()
-        barrier()
-    total_ms = reps_.max(start.elapsed_time(end))
+        torch.cuda.synchronize()
+        staged_ms = start.elapsed_time(end) / args.steps
     stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]))
                 for j, s in enumerate(Layer.STAGES)}
-    if int(layer.status.item()) != 0:
-        raise RuntimeError(f"device status {int(layer.status.item())}")
+    for st in (layer.status, fst):
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())}")
+    if not torch.equal(out.view(torch.int16), ref.view(torch.int16)):
+        raise RuntimeError("timed steps changed the layer output")
+    clocks = clk.summary()
 
     ms = total_ms / args.steps
     ops = layer_ops(cfg.T, cfg.H, cfg.I, cfg.k)
-    tops = reps_.total_rate(ops, ms / 1e3) / 1e12
-    tok_s = reps_.total_rate(cfg.T, ms / 1e3)
+    tops = ops / (ms / 1e3) / 1e12
+    tok_s = cfg.T / (ms / 1e3)
 
     # end to end: host activations in, host output back, through the one-call API
     xh, lh = x.cpu().pin_memory(), logits.cpu().pin_memory()
@@ -695,22 +745,28 @@ def main():
     hws = wq.forward_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.scheme, dev, host=True)
     for _ in range(args.warmup):
         wq.moe_forward_host(xh, lh, *weights, cfg.k, cfg.scheme, cfg.acc, out_host=outh, ws=hws)
-    barrier()
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(args.steps):
         wq.moe_forward_host(xh, lh, *weights, cfg.k, cfg.scheme, cfg.acc, out_host=outh, ws=hws)
     e1.record()
-    barrier()
-    e2e_ms = reps_.max(e0.elapsed_time(e1) / args.steps)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
     if not torch.equal(outh.view(torch.int16), ref.cpu().view(torch.int16)):
         raise RuntimeError("host-buffer layer differs from the device one")
 
     peaks, src = load_peaks()
     touched = int((layer.counts > 0).sum().item())
-    roofline = gemm1_roofline(peaks, src, stage_ms["gemm1"], cfg.T * cfg.k, touched, cfg.H, cfg.I,
-                              cfg.scheme, 2 if layer.f16 else 1, measured_traffic(cfg.name))
-    line = {"metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+    cb = 2 if layer.f16 else 1
+    R = cfg.T * cfg.k
+    roofline = gemm_roofline(peaks, src, clocks, stage_ms["gemm1"], R, touched, 2 * cfg.I, cfg.H,
+                             cfg.scheme, cb, measured_traffic(cfg.name),
+                             "grouped_gemm_w8a8 gate_up (GEMM1)")
+    roof2 = gemm_roofline(peaks, src, clocks, stage_ms["gemm2"], R, touched, cfg.H, cfg.I,
+                          cfg.scheme, cb, None, "grouped_gemm_w8a8 down (GEMM2)")
+    nbytes = layer_bytes(cfg.T, cfg.H, cfg.I, touched, cfg.k, cfg.scheme, cfg.E)
+    line = {"metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int8", "data": "synthetic",
             "config": {"workload": workload_name(cfg), "tokens": cfg.T, "hidden": cfg.H,
@@ -718,15 +774,17 @@ def main():
                        "scheme": cfg.scheme, "accumulator": cfg.acc,
                        "l2": "inputs larger than L2: 11.3 GB of int8 weights and ~2 GB of "
                              "activations are streamed every step",
-                       "parallelism": "replicas" if world > 1 else "single"},
-            "tokens_per_s": tok_s, "stages_ms": stage_ms,
+                       "parallelism": "single"},
+            "tokens_per_s": tok_s, "stages_ms": stage_ms, "staged_ms_per_step": staged_ms,
             "gpu_launches": launches,
             "roofline": roofline,
-            "e2e": {"value": reps_.total_rate(ops, e2e_ms / 1e3) / 1e12, "unit": "TOPS",
+            "roofline_gemm2": roof2,
+            "layer_roofline": layer_roofline(peaks, clocks, ms, ops, nbytes),
+            "e2e": {"value": ops / (e2e_ms / 1e3) / 1e12, "unit": "TOPS",
                     "h2d_bytes_per_step": cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4,
                     "d2h_bytes_per_step": cfg.T * cfg.H * 2, "ms_per_step": e2e_ms},
-            "clocks": clk.summary()}
-    if rank == 0 and not args.no_cpu_baseline:
+            "clocks": clocks}
+    if not args.no_cpu_baseline:
         run, sops, cores = oracle_sample(cfg, args.cpu_tokens, dev)
         # the same sample again and again until at least 10 s of CPU work
         reps, dt = 0, 0.0
@@ -737,9 +795,7 @@ def main():
                                 "kind": "oracle", "tokens_per_s": reps * args.cpu_tokens / dt,
                                 "sample": f"first {args.cpu_tokens} of {cfg.T} tokens of the same "
                                           f"workload, full layer, run {reps} times ({dt:.1f} s)"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    reps_.close()
+    print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

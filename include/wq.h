@@ -202,10 +202,11 @@ WQ_API int wq_grouped_gemm_w8a8(const int8_t *A, const float *sa, const int8_t *
  * WQ_NOALLOC_SCRATCH_BYTES that every GPU loading libwq.so holds until the
  * process exits; the first call on a device looks up that array's address
  * (cudaGetSymbolAddress) with the device current.  All calls on a device
- * share the array; calls that overlap on the GPU race on it.  A problem whose
- * scratch need (wq_grouped_gemm_workspace_size(R, E)) exceeds the array
- * returns WQ_ERR_UNSUPPORTED before any work is enqueued.  Nothing is
- * allocated. */
+ * share the array; calls that overlap on the GPU race on it.  Arguments are
+ * checked first, exactly as wq_grouped_gemm_w8a8 checks them (same codes);
+ * then a problem whose scratch need (wq_grouped_gemm_workspace_size(R, E))
+ * exceeds the array returns WQ_ERR_UNSUPPORTED before any work is enqueued.
+ * Nothing is allocated. */
 #define WQ_NOALLOC_SCRATCH_BYTES (256 * 1024)
 WQ_API int wq_grouped_gemm_w8a8_noalloc(const int8_t *A, const float *sa, const int8_t *W,
                                         const float *sw, const int32_t *offsets, int E, int64_t R,

@@ -5,10 +5,15 @@ Inputs are drawn on the GPU (the weights one expert at a time) and quantized
 by the library.  Compared with the oracle:
   * in full: routing ids and weights, activation codes and scales, expert
     counts/offsets, the stable permutation and its inverse;
-  * on sampled tokens, evaluated by the oracle one token at a time with its
-    own quantization of those experts' bf16 weights: the int8 weights of the
-    touched experts, the int32 accumulators of GEMM1 and the final bf16
-    outputs (exactly, and against the stated tolerance)."""
+  * GEMM1's int32 accumulators of eight whole expert segments, on the engine
+    the layer uses, against the oracle's exact integer matmul;
+  * the final bf16 outputs of 64 sampled tokens (exactly, and against the
+    stated tolerance), evaluated by the oracle from its own quantization of
+    the touched experts' bf16 weights (whose int8 codes and scales are
+    checked against the library's too)."""
+import concurrent.futures as cf
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -43,13 +48,31 @@ def gpu_weights(cfg):
     return W13, S13, W2, S2
 
 
-def oracle_expert(cfg, e, cache):
-    """The oracle's own quantization of expert e's bf16 weights (drawn by the
-    same seeded generator on the GPU, copied to the host)."""
-    if e not in cache:
-        w13, w2 = synth.expert_weights(cfg, e, device=DEV)
-        cache[e] = O.quantize_weights(bits(w13), bits(w2), cfg.scheme)
-    return cache[e]
+# The oracle's own quantization of experts' bf16 weights, kept across the
+# configurations that share them (decode, prefill and prefill_f32 draw the
+# same channel-wise weights); one scheme at a time to bound host memory.
+_ORACLE_W = {"key": None, "experts": {}}
+
+
+def oracle_experts(cfg, experts):
+    """{e: (q13, s13, q2, s2)}: each expert's bf16 weights drawn by the same
+    seeded generator on the GPU, copied to the host and quantized by the
+    oracle (numpy, a thread pool over experts)."""
+    key = (cfg.scheme, cfg.seed, cfg.H, cfg.I)
+    if _ORACLE_W["key"] != key:
+        _ORACLE_W["key"], _ORACLE_W["experts"] = key, {}
+    cache = _ORACLE_W["experts"]
+    todo = sorted(set(int(e) for e in experts) - set(cache))
+    for i in range(0, len(todo), 32):
+        chunk = todo[i:i + 32]
+        host = []
+        for e in chunk:
+            w13, w2 = synth.expert_weights(cfg, e, device=DEV)
+            host.append((bits(w13), bits(w2)))
+        with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            res = list(ex.map(lambda hw: O.quantize_weights(hw[0], hw[1], cfg.scheme), host))
+        cache.update(zip(chunk, res))
+    return {int(e): cache[int(e)] for e in experts}
 
 
 def check_expert_weights(gpu_w, oq, e):
@@ -59,23 +82,38 @@ def check_expert_weights(gpu_w, oq, e):
     assert np.array_equal(np_(W2[e]), q2) and np.array_equal(np_(S2[e]), s2)
 
 
-def token_output(cfg, x_row_bits, ids, w, oq_of):
-    """Oracle value of one token: its k experts evaluated directly."""
+def sampled_outputs(cfg, qo, so, io, wo, toks, oq):
+    """Oracle outputs of the sampled tokens.  Each (token, slot) pair goes
+    through its expert's GEMM1 -> SiLU-mul + re-quantize -> GEMM2 (the rows of
+    one expert evaluated together: every step is row by row), then each
+    token's k results are combined in slot order."""
     grp = 0 if cfg.scheme == "channel" else 128
-    if cfg.scheme == "channel":
-        q, s = O.quantize_per_token(x_row_bits[None])
-    else:
-        q, s = O.quantize_per_token_group(x_row_bits[None], 128)
-    acc = np.zeros(cfg.H, np.float32)
-    gemm1_i32 = []
-    for j, e in enumerate(ids):
-        q13, s13, q2, s2 = oq_of(int(e))
-        gemm1_i32.append(O.int_matmul(q, q13)[0])
+    pairs = {}
+    for t in toks:
+        for j in range(cfg.k):
+            pairs.setdefault(int(io[t, j]), []).append((t, j))
+
+    def run(e):
+        rows = pairs[e]
+        q = qo[[t for t, _ in rows]]
+        s = so[[t for t, _ in rows]]
+        q13, s13, q2, s2 = oq[e]
         gu = O.f32_to_bf16(O.gemm_dequant(q, s, q13, s13, cfg.scheme, cfg.acc))
         hq, sh = O.silu_mul_quant(gu, cfg.I, grp)
-        y = O.f32_to_bf16(O.gemm_dequant(hq, sh, q2, s2, cfg.scheme, cfg.acc))
-        acc = acc + w[j] * O.bf16_to_f32(y[0])
-    return O.f32_to_bf16(acc), gemm1_i32
+        return e, O.gemm_dequant(hq, sh, q2, s2, cfg.scheme, cfg.acc)
+
+    y = {}
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        for e, ye in ex.map(run, sorted(pairs)):
+            for (t, j), row in zip(pairs[e], O.f32_to_bf16(ye)):
+                y[t, j] = row
+    out = []
+    for t in toks:
+        acc = np.zeros(cfg.H, np.float32)
+        for j in range(cfg.k):
+            acc = acc + wo[t, j] * O.bf16_to_f32(y[t, j])
+        out.append(O.f32_to_bf16(acc))
+    return np.stack(out)
 
 
 @pytest.mark.parametrize("name", ["decode", "prefill", "prefill_f32", "block"])
@@ -105,32 +143,47 @@ def test_layer_full_size(name):
     assert np.array_equal(np_(c), co) and np.array_equal(np_(off), offo)
     assert np.array_equal(np_(sp), spo) and np.array_equal(np_(p2r), p2ro)
 
-    # GEMM1 int32 accumulators of the permuted rows (channel, int32 mode)
-    A, sa = wq.moe_permute(q, s, sp, cfg.k)
-    gemm1_raw = None
-    if cfg.scheme == "channel" and cfg.acc == "i32":
-        gemm1_raw = wq.grouped_gemm_w8a8(A, sa, gw[0], gw[1], off, "channel", "i32", out_type="i32")
-
-    # final outputs of sampled tokens, evaluated token by token by the oracle
+    # GEMM1's int32 accumulators (channel, int32 mode) for eight whole expert
+    # segments, on the engine the layer uses: fp16 codes when experts hold
+    # many rows (the CTA-pair engine), int8 codes otherwise
     rng = np.random.default_rng(11)
-    toks = sorted({0, cfg.T - 1, *rng.choice(cfg.T, 2, replace=False).tolist()})
-    cache = {}
-    ob = bits(out)
-    got, want = [], []
-    for t in toks:
-        for e in io[t]:
-            check_expert_weights(gw, oracle_expert(cfg, int(e), cache), int(e))
-        ref, g1 = token_output(cfg, xb[t], io[t], wo[t], lambda e: oracle_expert(cfg, e, cache))
-        got.append(ob[t])
-        want.append(ref)
-        if gemm1_raw is not None:
-            for j in range(cfg.k):
-                row = int(p2ro[t * cfg.k + j])
-                assert np.array_equal(np_(gemm1_raw[row]), g1[j].astype(np.int32)), (t, j)
-    got, want = np.stack(got), np.stack(want)
+    if cfg.scheme == "channel" and cfg.acc == "i32":
+        R = cfg.T * cfg.k
+        if R > 64 * cfg.E:
+            A16, sa16, n2 = wq.moe_permute_f16(q, s, sp, cfg.k)
+            raw = wq.grouped_gemm_w8a8_f16codes(A16, n2, sa16, gw[0], gw[1], off, out_type="i32")
+        else:
+            A, sa = wq.moe_permute(q, s, sp, cfg.k)
+            raw = wq.grouped_gemm_w8a8(A, sa, gw[0], gw[1], off, "channel", "i32", out_type="i32")
+        raw = np_(raw)
+        Ao, _ = O.moe_permute(qo, so, spo, cfg.k)
+        nz = np.flatnonzero(co)
+        ends = {int(nz[np.argmax(co[nz])]), int(nz[np.argmin(co[nz])])}
+        rest = np.array([e for e in nz if int(e) not in ends])
+        segs = sorted(ends | set(rng.choice(rest, 8 - len(ends), replace=False).tolist()))
+        oq = oracle_experts(cfg, segs)
+        nrows = 0
+        for e in segs:
+            r0, r1 = int(offo[e]), int(offo[e + 1])
+            check_expert_weights(gw, oq[e], e)
+            want = O.int_matmul(Ao[r0:r1], oq[e][0]).astype(np.int32)
+            assert np.array_equal(raw[r0:r1], want), f"GEMM1 int32, expert {e} rows {r0}:{r1}"
+            nrows += r1 - r0
+        assert len(segs) >= 8 and nrows >= (1500 if R > 64 * cfg.E else 20)
+
+    # final outputs of 64 tokens spread over the batch (and so over the
+    # experts), evaluated by the oracle from its own weight quantization
+    toks = sorted({0, cfg.T - 1, *rng.choice(cfg.T, 62, replace=False).tolist()})[:64]
+    experts = sorted(set(io[toks].reshape(-1).tolist()))
+    oq = oracle_experts(cfg, experts)
+    for e in experts:
+        check_expert_weights(gw, oq[e], e)
+    want = sampled_outputs(cfg, qo, so, io, wo, toks, oq)
+    got = bits(out)[toks]
+    assert len(toks) == 64
     max_abs, rel = tolerance_report(got, want)
     assert max_abs <= 2e-2 and rel <= 1e-2, (max_abs, rel)
-    assert_bf16_equal(got, want, f"{name} sampled tokens {toks}")
+    assert_bf16_equal(got, want, f"{name}: 64 sampled tokens over {len(experts)} experts")
 
 
 def test_masked_full_size():
@@ -150,20 +203,21 @@ def test_masked_full_size():
     # rows at or past the counts stay untouched
     for e in range(E):
         assert np.all(O.bf16_to_f32(yb[e, mm[e]:]) == 3.0)
-    # sampled valid rows, evaluated by the oracle one row at a time
+    # valid rows of every expert (all of them up to 24, else 24 sampled with
+    # the first and the last), evaluated by the oracle expert by expert
     rng = np.random.default_rng(5)
-    experts = sorted({int(np.argmax(mm)), int(np.argmin(mm)), *rng.choice(E, 2, replace=False).tolist()})
-    cache = {}
+    experts = [e for e in range(E) if mm[e] > 0]
+    oq = oracle_experts(cfg, experts)
     got, want = [], []
     for e in experts:
-        oq = oracle_expert(cfg, e, cache)
-        check_expert_weights(gw, oq, e)
-        rows = sorted({0, int(mm[e]) - 1})
+        check_expert_weights(gw, oq[e], e)
+        m = int(mm[e])
+        rows = list(range(m)) if m <= 24 else sorted({0, m - 1, *rng.choice(m, 22, replace=False).tolist()})
         xr = bits(xm[e, rows])
         q, s = O.quantize_per_token(xr)
-        gu = O.f32_to_bf16(O.gemm_dequant(q, s, oq[0], oq[1], "channel", "i32"))
+        gu = O.f32_to_bf16(O.gemm_dequant(q, s, oq[e][0], oq[e][1], "channel", "i32"))
         hq, sh = O.silu_mul_quant(gu, cfg.I)
-        ref = O.f32_to_bf16(O.gemm_dequant(hq, sh, oq[2], oq[3], "channel", "i32"))
+        ref = O.f32_to_bf16(O.gemm_dequant(hq, sh, oq[e][2], oq[e][3], "channel", "i32"))
         got.append(yb[e, rows])
         want.append(ref)
     got, want = np.concatenate(got), np.concatenate(want)

@@ -450,6 +450,69 @@ def test_grouped_gemm_f16codes(extreme, K, counts):
                       "f16 codes gemm, float32 accumulator")
 
 
+def _redo_flag(ws):
+    """The exact-recompute flag a single-pass engine raises when a tile fails
+    its exactness check: the last 256-byte piece of the grouped GEMM's
+    workspace (the tile lists and their counts come first)."""
+    return int(ws[-256:-252].view(torch.int32).item())
+
+
+# K, engine: the single-pass engines on the exactness check's edge.  The rows
+# are all +-127 and the channels all +-127 but for one 126, so
+# max||a||^2 * max||w||^2 = (K*127^2) * (K*127^2) stays below 2^48 (the check
+# passes and the single pass is trusted) while the sums reach odd integers in
+# [2^23, 2^24): 127*127*(K-1) + 127*126.  A tensor pipe that dropped a low
+# bit while adding a product to a partial sum near 2^24 would fail here.
+@pytest.mark.parametrize("K,engine", [(1024, "tc5"), (768, "tc4"), (1024, "tc2")])
+def test_single_pass_odd_sums_near_2_24(K, engine):
+    counts = [40, 300, 3, 129]  # ragged token tiles, and a remainder of 3 rows
+    E, N = len(counts), 512
+    rng = np.random.default_rng(K + len(engine))
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    R = int(offs[-1])
+    sgn = lambda *shape: np.where(rng.random(shape) < 0.5, -1, 1)
+    A = (127 * sgn(R, K)).astype(np.int8)
+    A[offs[:-1]] = 127                         # each expert's first row: all +127
+    W = (127 * sgn(E, N, K)).astype(np.int8)
+    W[:, 0, :] = 127
+    W[:, 1, :] = 127
+    W[:, 1, 5] = 126                           # 127^2 (K-1) + 127*126: odd
+    W[:, 2, :] = -127
+    W[:, 2, K - 1] = -126
+    n2a = (A.astype(np.int64) ** 2).sum(1)
+    n2w = (W.astype(np.int64) ** 2).sum(2)
+    assert int(n2a.max()) * int(n2w.max()) < 2 ** 48  # the engines' check passes
+    sa = (rng.random(R) * 0.05).astype(np.float32)
+    sw = (rng.random((E, N)) * 1e-3).astype(np.float32)
+    Co = O.grouped_gemm_i32(A, W, offs)
+    edge = Co[offs[:-1], 1]
+    assert np.all(edge == 127 * 127 * (K - 1) + 127 * 126) and np.all(edge % 2 == 1)
+    assert np.all((edge >= 2 ** 23) & (edge < 2 ** 24))
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    st = wq.new_status()
+    nws = wq.lib().wq_grouped_gemm_workspace_size(R, E)
+    outs = {}
+    for acc, out_type in (("i32", "i32"), ("i32", "bf16"), ("f32", "bf16")):
+        ws = torch.zeros(nws, dtype=torch.uint8, device=DEV)
+        if engine == "tc2":
+            outs[acc, out_type] = wq.grouped_gemm_w8a8(t(A), t(sa), t(W), t(sw), t(offs), "channel", acc,
+                                                       out_type, status=st, ws=ws)
+        else:
+            A16 = t(A).to(torch.float16)
+            outs[acc, out_type] = wq.grouped_gemm_w8a8_f16codes(
+                A16, t(n2a.astype(np.int32)), t(sa), t(W), t(sw), t(offs), acc=acc, out_type=out_type,
+                status=st, ws=ws)
+        torch.cuda.synchronize()
+        assert _redo_flag(ws) == 0, "the exactness check failed: the recompute ran instead"
+    assert int(st.item()) == 0
+    assert np.array_equal(np_(outs["i32", "i32"]), Co)
+    assert_bf16_equal(bits(outs["i32", "bf16"]), O.grouped_gemm_w8a8(A, sa, W, sw, offs),
+                      f"{engine} K{K} int32 accumulator")
+    assert_bf16_equal(bits(outs["f32", "bf16"]),
+                      O.grouped_gemm_w8a8(A, sa, W, sw, offs, "channel", "f32"),
+                      f"{engine} K{K} float32 accumulator")
+
+
 # ---------------------------------------------------------------- dense linear
 @pytest.mark.parametrize("T,K,N,scheme,acc", [
     (5, 256, 256, "channel", "i32"),      # few rows: the small-token engine

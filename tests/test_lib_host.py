@@ -148,3 +148,15 @@ def test_newer_entry_points_reject_bad_arguments_on_host(lib):
 def test_no_device_is_reported(lib):
     # this check runs where no GPU is visible; on a GPU machine device 10**6 does not exist
     assert lib.wq_init(10 ** 6) == -3
+
+
+def test_noalloc_entry_checks_arguments_before_its_scratch_limit(lib):
+    """The allocation-free grouped GEMM rejects the calls the workspace entry
+    rejects, with the same codes, before it compares the problem with its
+    static scratch array."""
+    fake = ctypes.c_void_p(4096)  # never dereferenced
+    for E, R, scheme, want in ((5000, 4_000_000, 0, -1), (5000, 100, 0, -1), (256, 4_000_000, 7, -1),
+                               (256, 4_000_000, 0, -2)):
+        rc = lib.wq_grouped_gemm_w8a8_noalloc(fake, fake, fake, fake, fake, E, R, 4096, 7168, scheme,
+                                              0, 0, fake, None, None)
+        assert rc == want, (E, R, scheme, rc)

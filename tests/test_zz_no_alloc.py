@@ -72,3 +72,17 @@ def test_noalloc_refuses_problems_beyond_its_scratch():
     rc = lib.wq_grouped_gemm_w8a8_noalloc(fake, fake, fake, fake, fake, 256, R, 4096, 7168, 0, 0, 0,
                                           fake, None, None)
     assert rc == -2
+
+
+def test_noalloc_rejects_bad_arguments_like_the_workspace_entry():
+    """The same argument checks, with the same codes, come before the scratch
+    limit: E > 4096 and a bad scheme are invalid arguments even when the
+    problem would also be too large for the scratch array."""
+    lib = wq.lib()
+    fake = ctypes.c_void_p(4096)  # never dereferenced: argument checks fail first
+    for E, R, scheme in ((5000, 4_000_000, 0), (5000, 100, 0), (256, 4_000_000, 7)):
+        ws_rc = lib.wq_grouped_gemm_w8a8(fake, fake, fake, fake, fake, E, R, 4096, 7168, scheme, 0,
+                                         0, fake, fake, 1 << 40, None, None)
+        na_rc = lib.wq_grouped_gemm_w8a8_noalloc(fake, fake, fake, fake, fake, E, R, 4096, 7168,
+                                                 scheme, 0, 0, fake, None, None)
+        assert ws_rc == na_rc == -1, (E, R, scheme, ws_rc, na_rc)

@@ -70,9 +70,14 @@ def exported_names():
 
 
 def lib():
-    """Load libwq.so (once).  Raises if it has not been built."""
+    """Load libwq.so (once).  Raises if it has not been built, or if this
+    process is one rank of a multi-process launch (WORLD_SIZE > 1): the
+    library's pair GEMM engines share token tiles between the two CTAs of a
+    cluster through TMA multicast, which it supports in one-GPU runs only."""
     global _lib
     if _lib is None:
+        if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+            raise WQError("libwq.so serves one-GPU runs only; WORLD_SIZE > 1 is refused")
         if not os.path.exists(LIB_PATH):
             raise WQError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
         h = ctypes.CDLL(LIB_PATH)
@@ -255,7 +260,7 @@ def silu_mul_quant_f16(gu, group=0):
 
 
 def grouped_gemm_w8a8_f16codes(A16, a_norm2, sa, W, sw, offsets, acc="i32", out_type="bf16",
-                               out=None, status=None, scheme="channel"):
+                               out=None, status=None, scheme="channel", ws=None):
     _dev(A16, torch.float16, "A16")
     if a_norm2 is not None:
         _dev(a_norm2, torch.int32, "a_norm2")
@@ -269,7 +274,8 @@ def grouped_gemm_w8a8_f16codes(A16, a_norm2, sa, W, sw, offsets, acc="i32", out_
         out = torch.empty(R, N, dtype=torch.bfloat16 if out_type == "bf16" else torch.int32,
                           device=A16.device)
     nws = lib().wq_grouped_gemm_workspace_size(R, E)
-    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=A16.device)
+    if ws is None:
+        ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=A16.device)
     st = status if status is not None else new_status(A16.device)
     _check(lib().wq_grouped_gemm_w8a8_f16codes(_ptr(A16), _ptr(a_norm2) if a_norm2 is not None else None,
                                                _ptr(sa), _ptr(W), _ptr(sw),
@@ -283,7 +289,7 @@ def grouped_gemm_w8a8_f16codes(A16, a_norm2, sa, W, sw, offsets, acc="i32", out_
 
 # ---------------------------------------------------------------- GEMMs
 def grouped_gemm_w8a8(A, sa, W, sw, offsets, scheme="channel", acc="i32", out_type="bf16",
-                      out=None, status=None):
+                      out=None, status=None, ws=None):
     _dev(A, torch.int8, "A")
     _dev(sa, torch.float32, "sa")
     _dev(W, torch.int8, "W")
@@ -297,7 +303,8 @@ def grouped_gemm_w8a8(A, sa, W, sw, offsets, scheme="channel", acc="i32", out_ty
         out = torch.empty(R, N, dtype=torch.bfloat16 if out_type == "bf16" else torch.int32,
                           device=A.device)
     nws = lib().wq_grouped_gemm_workspace_size(R, E)
-    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=A.device)
+    if ws is None:
+        ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=A.device)
     st = status if status is not None else new_status(A.device)
     _check(lib().wq_grouped_gemm_w8a8(_ptr(A), _ptr(sa), _ptr(W), _ptr(sw), _ptr(offsets), E, R, N,
                                       K, SCHEME[scheme], ACC[acc], OUT[out_type], _ptr(out),

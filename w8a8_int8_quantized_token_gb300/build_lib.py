@@ -3,11 +3,20 @@
 Each translation unit compiles in parallel; the link step makes the shared
 library next to this file.  Float contraction is disabled (-fmad=false) and
 no fast-math flag is used: the kernels' float arithmetic is IEEE round to
-nearest, operation by operation."""
+nearest, operation by operation.
+
+Reuse of earlier objects is keyed on content, not on file times: every
+object and the library carry a stamp, the SHA-256 of the sources and headers
+they depend on, the compiler flags, the nvcc version and the host machine.
+A tree copied to another machine (whose files keep or lose their times) is
+therefore always rebuilt from its own sources, and a stale object can never
+be linked."""
 from __future__ import annotations
 
 import concurrent.futures as cf
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -17,6 +26,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libwq.so")
+LIB_STAMP = os.path.join(BUILD, "libwq.so.stamp")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC",
@@ -34,37 +44,79 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _deps():
+def headers():
     hdrs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     hdrs += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
-    return max(os.path.getmtime(h) for h in hdrs)
+    return sorted(hdrs)
 
 
-def _compile(src: str, hdr_mtime: float, extra) -> str:
+def _nvcc_version(exe: str) -> str:
+    r = subprocess.run([exe, "--version"], capture_output=True, text=True)
+    return r.stdout.strip()
+
+
+def _digest(paths, extra: str) -> str:
+    h = hashlib.sha256(extra.encode())
+    for p in paths:
+        h.update(os.path.basename(p).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _stamp_ok(stamp_path: str, target: str, digest: str) -> bool:
+    if not (os.path.exists(target) and os.path.exists(stamp_path)):
+        return False
+    with open(stamp_path) as f:
+        return f.read().strip() == digest
+
+
+def _write_stamp(stamp_path: str, digest: str) -> None:
+    with open(stamp_path, "w") as f:
+        f.write(digest + "\n")
+
+
+def _compile(src: str, key: str, extra) -> tuple:
+    """Compile one translation unit unless its stamped object matches `key`
+    (sources, headers, flags, toolchain).  Returns (object, compiled?)."""
     obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-    if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), hdr_mtime):
-        return obj
+    stamp = obj + ".stamp"
+    digest = _digest([src], key + "|" + " ".join(extra))
+    if _stamp_ok(stamp, obj, digest):
+        return obj, False
     cmd = [nvcc(), *ARCH, *NVFLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
-    return obj
+    _write_stamp(stamp, digest)
+    return obj, True
 
 
 def build(verbose: bool = False, extra=()) -> str:
-    """Compile (if stale) and link libwq.so; returns its path."""
+    """Compile every translation unit whose content stamp is stale, link
+    libwq.so when any object changed, and return the library's path."""
     os.makedirs(BUILD, exist_ok=True)
+    exe = nvcc()
     srcs = sources()
-    hm = _deps()
+    # the common key: every header, the flags, the compiler and the machine
+    key = _digest(headers(), "|".join([*ARCH, *NVFLAGS, _nvcc_version(exe), platform.machine()]))
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, hm, list(extra)), srcs))
-    if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        cmd = [nvcc(), *ARCH, "-shared", "-o", LIB, *objs]
+        res = list(ex.map(lambda s: _compile(s, key, list(extra)), srcs))
+    objs = [o for o, _ in res]
+    compiled = sum(1 for _, c in res if c)
+    lib_digest = _digest(objs, "link|" + " ".join(ARCH))
+    if not _stamp_ok(LIB_STAMP, LIB, lib_digest):
+        cmd = [exe, *ARCH, "-shared", "-o", LIB, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        _write_stamp(LIB_STAMP, lib_digest)
+        linked = True
+    else:
+        linked = False
     if verbose:
-        print(f"built {LIB}", file=sys.stderr)
+        print(f"built {LIB} ({compiled} of {len(srcs)} units compiled, "
+              f"{'linked' if linked else 'link up to date'}, {platform.machine()})", file=sys.stderr)
     return LIB
 
 

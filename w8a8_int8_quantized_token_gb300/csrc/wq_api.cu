@@ -325,16 +325,34 @@ size_t wq_grouped_gemm_workspace_size(int64_t R, int E) {
   return gemm_ws_bytes(R, E, 0, false);
 }
 
-int wq_grouped_gemm_w8a8(const int8_t *A, const float *sa, const int8_t *W, const float *sw,
-                         const int32_t *offsets, int E, int64_t R, int64_t N, int64_t K,
-                         int scheme, int acc, int out_type, void *out, void *ws, size_t ws_bytes,
-                         int32_t *status, wq_stream_t stream) {
+}  // extern "C"
+
+namespace wq {
+// The host-side argument checks of the grouped GEMM on int8 codes, shared by
+// the workspace entry point and the allocation-free one (which must reject
+// the same calls with the same codes).  WQ_OK with R == 0 means "nothing to
+// do".
+int check_grouped_gemm_args(const int8_t *A, const float *sa, const int8_t *W, const float *sw,
+                            const int32_t *offsets, int E, int64_t R, int64_t N, int64_t K,
+                            int scheme, int acc, int out_type, const void *out) {
   if (R < 0 || E > 4096) return WQ_ERR_INVALID_ARG;
   if (R == 0) return WQ_OK;
   WQ_TRY(check_gemm_common(W, sw, E, N, K, scheme, acc, out_type, out));
   if (!A || !sa || !offsets) return WQ_ERR_INVALID_ARG;
   if (!al16(A)) return WQ_ERR_UNSUPPORTED;
   if (R >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;
+  return WQ_OK;
+}
+}  // namespace wq
+
+extern "C" {
+
+int wq_grouped_gemm_w8a8(const int8_t *A, const float *sa, const int8_t *W, const float *sw,
+                         const int32_t *offsets, int E, int64_t R, int64_t N, int64_t K,
+                         int scheme, int acc, int out_type, void *out, void *ws, size_t ws_bytes,
+                         int32_t *status, wq_stream_t stream) {
+  WQ_TRY(check_grouped_gemm_args(A, sa, W, sw, offsets, E, R, N, K, scheme, acc, out_type, out));
+  if (R == 0) return WQ_OK;
   if (ws_bytes < gemm_ws_bytes(R, E, 0, false) || !ws) return WQ_ERR_WORKSPACE;
   WQ_TRY(check_device());
   GemmArgs a{A, nullptr, nullptr, sa, W, sw, offsets, nullptr, 0, E, R, N, K, scheme, acc, out_type, out, ws, status};

@@ -11,33 +11,43 @@
 // The array is a module global: every GPU that loads libwq.so holds
 // WQ_NOALLOC_SCRATCH_BYTES of it until the process exits.  Its device address
 // is looked up once per device, on the first call made with that device
-// current.  All calls on a device share the one array and it keeps the last
+// current, and cached in an atomic slot per device (host threads that make
+// their first calls at the same time each look it up and store the same
+// value).  All calls on a device share the one array and it keeps the last
 // call's contents: each call rewrites the tile lists and counts and zeroes
 // the recompute flag before its kernels read them, and calls whose kernels
 // overlap on the GPU (different streams or threads) race on it.
+#include <atomic>
+
 #include "wq_common.cuh"
+
+namespace wq {
+int check_grouped_gemm_args(const int8_t *A, const float *sa, const int8_t *W, const float *sw,
+                            const int32_t *offsets, int E, int64_t R, int64_t N, int64_t K,
+                            int scheme, int acc, int out_type, const void *out);
+}
 
 namespace {
 
 __device__ __align__(256) unsigned char g_gemm_scratch[WQ_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices];  // device address of g_gemm_scratch, per device
+std::atomic<void *> g_scratch_addr[kMaxDevices];  // device address of g_gemm_scratch, per device
 
 // Device address of the scratch array on the current device (looked up on
 // the first call for that device).
 int scratch_address(void **out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return WQ_ERR_DEVICE;
-  if (g_scratch_addr[dev] == nullptr) {
-    void *p = nullptr;
+  void *p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
     if (cudaGetSymbolAddress(&p, g_gemm_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return WQ_ERR_LAUNCH;
     }
-    g_scratch_addr[dev] = p;
+    g_scratch_addr[dev].store(p, std::memory_order_release);
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return WQ_OK;
 }
 
@@ -48,7 +58,11 @@ extern "C" int wq_grouped_gemm_w8a8_noalloc(const int8_t *A, const float *sa, co
                                             int64_t R, int64_t N, int64_t K, int scheme, int acc,
                                             int out_type, void *out, int32_t *status,
                                             wq_stream_t stream) {
-  if (R < 0 || E < 1) return WQ_ERR_INVALID_ARG;
+  // the workspace entry point's argument checks first, so both reject a bad
+  // call with the same code; then the scratch limit
+  const int arg = wq::check_grouped_gemm_args(A, sa, W, sw, offsets, E, R, N, K, scheme, acc,
+                                              out_type, out);
+  if (arg != WQ_OK) return arg;
   if (R == 0) return WQ_OK;
   const size_t need = wq_grouped_gemm_workspace_size(R, E);
   if (need == 0 || need > size_t(WQ_NOALLOC_SCRATCH_BYTES)) return WQ_ERR_UNSUPPORTED;
