@@ -350,6 +350,58 @@ def test_layer_forward_masked():
     assert np.all(O.bf16_to_f32(yb[~valid]) == 5.0)
 
 
+@pytest.mark.parametrize("group", [0, 128])
+@pytest.mark.parametrize("f16", [False, True])
+def test_silu_mul_quant_every_bf16_gate(group, f16):
+    """Every finite bf16 gate value g (65280 patterns: both signs, subnormals,
+    zeros, the largest) through SiLU-mul + re-quantization: the kernel looks
+    silu(g) up in a table for g in [2^-24, 17) and (-89, -2^-24] and takes
+    the formula elsewhere; codes and scales must equal the oracle's.  The
+    patterns are sorted by magnitude so the values sharing a row (or a
+    128-group) are alike and their codes carry information; |u| < 1 keeps
+    every product finite."""
+    I = 2048
+    b = np.arange(65536, dtype=np.uint32)
+    finite = (b & 0x7F80) != 0x7F80
+    pats = b[finite].astype(np.uint16)
+    pats = pats[np.argsort(O.bf16_to_f32(pats).astype(np.float64) ** 2, kind="stable")]
+    R = (pats.size + I - 1) // I
+    g = np.zeros(R * I, np.uint16)
+    g[:pats.size] = pats
+    rng = np.random.default_rng(31)
+    u = O.f32_to_bf16((rng.random(R * I) * 1.8 - 0.9).astype(np.float32))
+    gu = np.concatenate([g.reshape(R, I), u.reshape(R, I)], axis=1)
+    gut = torch.from_numpy(gu.view(np.int16)).view(torch.bfloat16).to(DEV)
+    hqo, sho = O.silu_mul_quant(gu, I, group)
+    if f16:
+        hq, sh, n2 = wq.silu_mul_quant_f16(gut, group)
+        assert np.array_equal(np_(hq).astype(np.int32), hqo.astype(np.int32))
+        if group == 0:
+            assert np.array_equal(np_(n2), (hqo.astype(np.int64) ** 2).sum(1))
+    else:
+        hq, sh = wq.silu_mul_quant(gut, group)
+        assert np.array_equal(np_(hq), hqo)
+    assert np.array_equal(np_(sh).reshape(sho.shape), sho)
+
+
+@pytest.mark.parametrize("R,I,group", [(1, 8, 0), (3, 24, 0), (2, 256, 32), (40, 1024, 64),
+                                       (17, 2048, 256), (5, 4096, 0), (4, 4096, 128)])
+def test_silu_mul_quant_shapes(R, I, group):
+    """Row widths around the table kernel's per-lane vector counts (1 to 8
+    vectors of 8 per lane, partly filled last vectors), every group size, and
+    rows too wide for it (I = 4096: the block-per-row kernels)."""
+    g = torch.Generator().manual_seed(R * 7 + I)
+    gu = (torch.randn(R, 2 * I, generator=g) * 3).to(torch.bfloat16)
+    hq, sh = wq.silu_mul_quant(gu.to(DEV), group)
+    hqo, sho = O.silu_mul_quant(bits(gu), I, group)
+    assert np.array_equal(np_(hq), hqo)
+    assert np.array_equal(np_(sh).reshape(sho.shape), sho)
+    if group in (0, 32, 128):
+        hq16, sh16, n2 = wq.silu_mul_quant_f16(gu.to(DEV), group)
+        assert np.array_equal(np_(hq16).astype(np.int32), hqo.astype(np.int32))
+        assert np.array_equal(np_(sh16).reshape(sho.shape), sho)
+
+
 # ---------------------------------------------------------------- fp16-stored codes
 @pytest.mark.parametrize("groups", [1, 56])
 def test_moe_permute_f16(groups):

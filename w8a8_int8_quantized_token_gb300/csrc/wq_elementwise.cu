@@ -626,12 +626,181 @@ __global__ void __launch_bounds__(1024) silu_mul_quant_f16_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// SiLU-and-mul + re-quantization, table form (rows of at most 2048 outputs).
+// The gate value g is a bf16 number, so silu(g) takes one of finitely many
+// values.  Each CTA first tabulates silu(g) in shared memory for every bf16
+// g whose magnitude lies in [2^-24, 17) (g > 0) or [2^-24, 89) (g < 0),
+// computing each entry with silu() itself, so a lookup returns exactly what
+// the formula returns; any other g (smaller, larger, non-finite) takes the
+// formula directly.  Outside those ranges silu is trivial anyway (g / 2, g,
+// or -0), and a GEMM output rarely lands there, so the branch is almost
+// never taken.  Then one warp per row (persistent CTAs loop over rows):
+// 8-element vectors v = i*32 + lane (each warp access is 512 contiguous
+// bytes), h = silu(g) * u, the row's or each group's absolute maximum by
+// xor shuffles, the codes (int8, or the same integers as fp16 with the
+// row's squared norm), the scale.
+namespace silu_tab {
+constexpr uint32_t kLo = 0x3380u;        // bf16 bits of 2^-24
+constexpr uint32_t kPosHi = 0x4188u;     // bf16 bits of 17
+constexpr uint32_t kNegHi = 0x42B2u;     // bf16 bits of 89
+constexpr int kPos = int(kPosHi - kLo);  // entries for g > 0
+constexpr int kNeg = int(kNegHi - kLo);  // entries for g < 0
+constexpr int kSize = kPos + kNeg;
+constexpr int kBytes = kSize * 4;
+}  // namespace silu_tab
+
+__device__ __forceinline__ void silu_table_fill(float *tab) {
+  using namespace silu_tab;
+  for (int i = threadIdx.x; i < kSize; i += blockDim.x) {
+    const uint32_t b = i < kPos ? kLo + uint32_t(i) : (0x8000u | (kLo + uint32_t(i - kPos)));
+    tab[i] = silu(bf16_to_f(uint16_t(b)));
+  }
+}
+
+// silu(g) of the bf16 pattern b (value g): the table entry, or the formula
+__device__ __forceinline__ float silu_lookup(uint32_t b, float g, const float *tab) {
+  using namespace silu_tab;
+  const bool neg = (b & 0x8000u) != 0;
+  const uint32_t k = (b & 0x7fffu) - kLo;  // wraps (large) below 2^-24
+  if (k < (neg ? uint32_t(kNeg) : uint32_t(kPos))) return tab[neg ? k + uint32_t(kPos) : k];
+  return silu(g);
+}
+
+// VPL vectors of 8 per lane (rows up to 256 * VPL outputs); GV lanes per
+// quantization group (0: one scale per row); F16: fp16 codes (with the row's
+// squared norm when GV == 0).
+template <int VPL, int GV, bool F16>
+__global__ void __launch_bounds__(512, 1) silu_mul_quant_tab_kernel(
+    const uint16_t *__restrict__ gu, int64_t R, int64_t I, const int32_t *__restrict__ masked_m,
+    int Mmax, void *__restrict__ hq_out, float *__restrict__ sh, int32_t *__restrict__ norm2) {
+  extern __shared__ float tab[];
+  silu_table_fill(tab);
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int nvec = int(I >> 3);
+  const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t row = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); row < R;
+       row += nwarps) {
+    if (masked_m != nullptr && int(row % Mmax) >= masked_m[row / Mmax]) continue;  // warp-uniform
+    const uint4 *g4 = reinterpret_cast<const uint4 *>(gu + row * 2 * I);
+    const uint4 *u4 = reinterpret_cast<const uint4 *>(gu + row * 2 * I + I);
+    uint4 gv[VPL], uv[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int v = i * 32 + lane;
+      gv[i] = v < nvec ? __ldcs(g4 + v) : make_uint4(0, 0, 0, 0);
+      uv[i] = v < nvec ? __ldcs(u4 + v) : make_uint4(0, 0, 0, 0);
+    }
+    float h[VPL][8], am[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const uint32_t gw[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
+      const uint32_t uw[4] = {uv[i].x, uv[i].y, uv[i].z, uv[i].w};
+      am[i] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        h[i][2 * j] = __fmul_rn(silu_lookup(gw[j] & 0xffffu, bf16_lo(gw[j]), tab), bf16_lo(uw[j]));
+        h[i][2 * j + 1] = __fmul_rn(silu_lookup(gw[j] >> 16, bf16_hi(gw[j]), tab), bf16_hi(uw[j]));
+        am[i] = fmaxf(am[i], fabsf(h[i][2 * j]));
+        am[i] = fmaxf(am[i], fabsf(h[i][2 * j + 1]));
+      }
+    }
+    float sc = 0.0f, rs = 0.0f;
+    if constexpr (GV == 0) {
+      float a = am[0];
+#pragma unroll
+      for (int i = 1; i < VPL; ++i) a = fmaxf(a, am[i]);
+      sc = quant_scale(warp_max(a));
+      rs = __frcp_rn(sc);
+    }
+    int n2 = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int v = i * 32 + lane;
+      if constexpr (GV != 0) {
+        float a = am[i];
+#pragma unroll
+        for (int o = GV / 2; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        sc = quant_scale(a);
+        rs = __frcp_rn(sc);
+      }
+      if (v < nvec) {
+        const uint32_t lo = pack_s8x4(quant_bits(h[i][0], sc, rs), quant_bits(h[i][1], sc, rs),
+                                      quant_bits(h[i][2], sc, rs), quant_bits(h[i][3], sc, rs));
+        const uint32_t hi = pack_s8x4(quant_bits(h[i][4], sc, rs), quant_bits(h[i][5], sc, rs),
+                                      quant_bits(h[i][6], sc, rs), quant_bits(h[i][7], sc, rs));
+        if constexpr (F16) {
+          uint4 w;  // the same integers as fp16 values (exact)
+          tc::s8x4_to_f16x4(lo, w.x, w.y);
+          tc::s8x4_to_f16x4(hi, w.z, w.w);
+          reinterpret_cast<uint4 *>(static_cast<uint16_t *>(hq_out) + row * I)[v] = w;
+          n2 = __dp4a(int(hi), int(hi), __dp4a(int(lo), int(lo), n2));
+        } else {
+          reinterpret_cast<uint2 *>(static_cast<int8_t *>(hq_out) + row * I)[v] = make_uint2(lo, hi);
+        }
+        if constexpr (GV != 0) {
+          if (lane % GV == 0) sh[row * (nvec / GV) + v / GV] = sc;
+        }
+      }
+    }
+    if constexpr (GV == 0) {
+      if constexpr (F16) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+        if (lane == 0) norm2[row] = n2;
+      }
+      if (lane == 0) sh[row] = sc;
+    }
+  }
+}
+
+// The table kernel for rows of at most 2048 outputs; returns WQ_ERR_UNSUPPORTED
+// for wider rows (the callers then take the block-per-row kernels).
+template <bool F16>
+int launch_silu_tab(const uint16_t *gu, int64_t R, int64_t I, int group, const int32_t *masked_m,
+                    int Mmax, void *hq, float *sh, int32_t *norm2, cudaStream_t st) {
+  const int64_t nvec = I / 8;
+  if (nvec > 256) return WQ_ERR_UNSUPPORTED;
+  // one CTA of 16 warps per SM (the table fits the default 48 KB of shared
+  // memory), fewer for short launches
+  const int64_t rows_per_cta = 16;
+  int64_t grid = (R + rows_per_cta - 1) / rows_per_cta;
+  const int64_t cap = int64_t(num_sms());
+  if (grid > cap) grid = cap;
+  const size_t smem = silu_tab::kBytes;
+#define WQ_SILU_TAB(VPL, GV) \
+  silu_mul_quant_tab_kernel<VPL, GV, F16><<<unsigned(grid), 512, smem, st>>>(gu, R, I, masked_m, Mmax, hq, sh, norm2)
+#define WQ_SILU_TAB_G(VPL)                         \
+  switch (group) {                                 \
+    case 0: WQ_SILU_TAB(VPL, 0); break;            \
+    case 32: WQ_SILU_TAB(VPL, 4); break;           \
+    case 64: WQ_SILU_TAB(VPL, 8); break;           \
+    case 128: WQ_SILU_TAB(VPL, 16); break;         \
+    case 256: WQ_SILU_TAB(VPL, 32); break;         \
+    default: return WQ_ERR_UNSUPPORTED;            \
+  }
+  if (nvec <= 32) {
+    WQ_SILU_TAB_G(1)
+  } else if (nvec <= 64) {
+    WQ_SILU_TAB_G(2)
+  } else if (nvec <= 128) {
+    WQ_SILU_TAB_G(4)
+  } else {
+    WQ_SILU_TAB_G(8)
+  }
+#undef WQ_SILU_TAB_G
+#undef WQ_SILU_TAB
+  return launched(1);
+}
+
 int launch_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, int group,
                               const int32_t *masked_m, int Mmax, uint16_t *hq16, float *sh,
                               int32_t *norm2, cudaStream_t st) {
   if (R == 0 || I == 0) return WQ_OK;
   if (R > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
   const int64_t nvec = I / 8;
+  if (nvec <= 256) return launch_silu_tab<true>(gu, R, I, group, masked_m, Mmax, hq16, sh, norm2, st);
   auto rnd = [](int64_t t) { int v = int(((t + 31) / 32) * 32); return v < 32 ? 32 : v; };
   if (group != 0) {  // per-group scales, fp16 codes, no norms
     if (nvec > 1024) return WQ_ERR_UNSUPPORTED;
@@ -661,6 +830,7 @@ int launch_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group,
   if (R == 0 || I == 0) return WQ_OK;
   if (R > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
   const int64_t nvec = I / 8;
+  if (nvec <= 256) return launch_silu_tab<false>(gu, R, I, group, masked_m, Mmax, hq, sh, nullptr, st);
   auto rnd = [](int64_t t) { int v = int(((t + 31) / 32) * 32); return v < 32 ? 32 : v; };
   if (group == 0) {
     if (nvec <= 1024) {
