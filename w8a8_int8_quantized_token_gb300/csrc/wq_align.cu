@@ -3,7 +3,8 @@
 // (token, slot) pairs by expert.  Deterministic: a counting sort whose ranks
 // come from ordered scans and warp match masks, never from atomic order.
 //
-// Also the grouped GEMM's tile list: per expert segment, ceil(rows/BM) tiles.
+// Also the grouped GEMM's tile list: per expert segment, ceil(rows/BM)
+// tiles, longest first.
 #include "wq_common.cuh"
 
 namespace wq {
@@ -174,7 +175,14 @@ int launch_align(const int32_t *ids, int T, int k, int E, int pad_m, int32_t *co
 // (masked layout).  A segment of len rows gives floor(len / BM) full tiles
 // and, for a remainder of rem rows, one more tile: in the small list when
 // 0 < rem <= small_max (a small list is given), else in the main list.
-// Lists are expert-major; ntiles[0] / nsmall[0] = numbers written.
+// The main list is ordered longest first, so that persistent engines that
+// hand items out in order finish with their shortest ones: the full tiles
+// (BM rows) in expert order, then the partial tiles by row count,
+// descending (equal counts in arbitrary order: the tiles write disjoint
+// rows, so the order changes no result).  ntiles[0] / nsmall[0] = numbers
+// written.
+constexpr int kMaxTileRows = 384;
+
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__restrict__ offsets,
                                                            const int32_t *__restrict__ masked_m,
                                                            int Mmax, int E, int BM, int64_t R,
@@ -185,7 +193,9 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
                                                            Tile *__restrict__ small,
                                                            int32_t *__restrict__ nsmall) {
   __shared__ int32_t part[1024], part_s[1024];
+  __shared__ int32_t hist[kMaxTileRows + 1];  // partial main tiles by row count, then cursors
   if (zero_word != nullptr && threadIdx.x == 0) *zero_word = 0;
+  for (int i = threadIdx.x; i <= kMaxTileRows; i += blockDim.x) hist[i] = 0;
   const int per = (E + blockDim.x - 1) / blockDim.x;
   const int e0 = threadIdx.x * per;
   const bool split = small != nullptr && small_max > 0;
@@ -204,19 +214,21 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
       len = int(b - a);
     }
   };
-  // full tiles, whether the remainder goes to the small list, main-list tiles
+  // full tiles, the remainder, and whether it goes to the small list
   auto plan = [&](int len, int &nfull, int &rem, bool &to_small) {
     nfull = len / BM;
     rem = len - nfull * BM;
     to_small = split && rem > 0 && rem <= small_max;
   };
+  __syncthreads();
   int local = 0, local_s = 0;
   for (int e = e0; e < e0 + per && e < E; ++e) {
     int r0, len, nfull, rem;
     bool ts;
     seg(e, r0, len);
     plan(len, nfull, rem, ts);
-    local += nfull + ((rem > 0 && !ts) ? 1 : 0);
+    local += nfull;
+    if (rem > 0 && !ts) atomicAdd(&hist[rem], 1);
     local_s += ts ? 1 : 0;
   }
   part[threadIdx.x] = local;
@@ -230,39 +242,49 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
     part_s[threadIdx.x] += vs;
     __syncthreads();
   }
+  const int nfull_total = part[blockDim.x - 1];
+  if (threadIdx.x == 0) {
+    // first position of the partial tiles of each row count, longest first
+    int pos = nfull_total;
+    for (int r = BM - 1; r >= 1; --r) {
+      const int c = hist[r];
+      hist[r] = pos;
+      pos += c;
+    }
+    ntiles[0] = pos;
+    if (split) nsmall[0] = part_s[blockDim.x - 1];
+  }
+  __syncthreads();
   int t = part[threadIdx.x] - local, ts_i = part_s[threadIdx.x] - local_s;
   for (int e = e0; e < e0 + per && e < E; ++e) {
     int r0, len, nfull, rem;
     bool ts;
     seg(e, r0, len);
     plan(len, nfull, rem, ts);
-    const int main_rows = ts ? nfull * BM : len;
-    for (int m = 0; m < main_rows; m += BM) {
+    for (int m = 0; m < nfull; ++m) {
       Tile tl;
       tl.expert = e;
-      tl.row0 = r0 + m;
-      tl.rows = main_rows - m < BM ? main_rows - m : BM;
+      tl.row0 = r0 + m * BM;
+      tl.rows = BM;
       tl.pad = 0;
       tiles[t++] = tl;
     }
-    if (ts) {
+    if (rem > 0) {
       Tile tl;
       tl.expert = e;
       tl.row0 = r0 + nfull * BM;
       tl.rows = rem;
       tl.pad = 0;
-      small[ts_i++] = tl;
+      if (ts) small[ts_i++] = tl;
+      else tiles[atomicAdd(&hist[rem], 1)] = tl;
     }
-  }
-  if (threadIdx.x == blockDim.x - 1) {
-    ntiles[0] = part[threadIdx.x];
-    if (split) nsmall[0] = part_s[threadIdx.x];
   }
 }
 
 int launch_build_tiles(const int32_t *offsets, const int32_t *masked_m, int Mmax, int E, int BM,
                        int64_t R, Tile *tiles, int32_t *ntiles, int32_t *zero_word,
                        cudaStream_t st, int small_max, Tile *small, int32_t *nsmall) {
+  if (BM < 1 || BM > kMaxTileRows) return WQ_ERR_UNSUPPORTED;
   build_tiles_kernel<<<1, 1024, 0, st>>>(offsets, masked_m, Mmax, E, BM, R, tiles, ntiles,
                                          zero_word, small_max, small, nsmall);
   return launched(1);

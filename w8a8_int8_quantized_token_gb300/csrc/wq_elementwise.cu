@@ -389,26 +389,39 @@ int launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *
 }
 
 // ---------------------------------------------------------------------------
-// Permute (ep_scatter): one CTA per destination row, 16-byte copies.
-__global__ void __launch_bounds__(128) permute_kernel(const int8_t *__restrict__ q,
-                                                      const float *__restrict__ s, int groups,
-                                                      int k, int64_t K,
-                                                      const int32_t *__restrict__ sorted_pair,
-                                                      int8_t *__restrict__ A,
-                                                      float *__restrict__ sa) {
-  const int64_t r = blockIdx.x;
+// Permute (ep_scatter): one warp per destination row, 16-byte pieces; each
+// lane issues all its loads of a batch (the token's codes, usually L2
+// resident since a token is read by k rows) before its streaming stores.
+constexpr int kPermWarps = 8;  // rows per CTA
+constexpr int kPermBatch = 8;  // 16-byte pieces in flight per lane
+
+__global__ void __launch_bounds__(32 * kPermWarps) permute_kernel(
+    const int8_t *__restrict__ q, const float *__restrict__ s, int groups, int k, int64_t K,
+    const int32_t *__restrict__ sorted_pair, int64_t R, int8_t *__restrict__ A,
+    float *__restrict__ sa) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = int64_t(blockIdx.x) * kPermWarps + (threadIdx.x >> 5);
+  if (r >= R) return;
   const int p = sorted_pair[r];
   const int64_t nvec = K >> 4;
   uint4 *dst = reinterpret_cast<uint4 *>(A + r * K);
   if (p < 0) {
-    for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) dst[i] = make_uint4(0, 0, 0, 0);
-    for (int g = threadIdx.x; g < groups; g += blockDim.x) sa[r * groups + g] = 0.0f;
+    for (int64_t i = lane; i < nvec; i += 32) __stcs(dst + i, make_uint4(0, 0, 0, 0));
+    for (int g = lane; g < groups; g += 32) sa[r * groups + g] = 0.0f;
     return;
   }
   const int64_t tok = p / k;
   const uint4 *src = reinterpret_cast<const uint4 *>(q + tok * K);
-  for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) __stcs(dst + i, __ldg(src + i));
-  for (int g = threadIdx.x; g < groups; g += blockDim.x) sa[r * groups + g] = s[tok * groups + g];
+  for (int64_t i0 = lane; i0 < nvec; i0 += 32 * kPermBatch) {
+    uint4 v[kPermBatch];
+#pragma unroll
+    for (int u = 0; u < kPermBatch; ++u)
+      if (i0 + 32 * u < nvec) v[u] = __ldg(src + i0 + 32 * u);
+#pragma unroll
+    for (int u = 0; u < kPermBatch; ++u)
+      if (i0 + 32 * u < nvec) __stcs(dst + i0 + 32 * u, v[u]);
+  }
+  for (int g = lane; g < groups; g += 32) sa[r * groups + g] = s[tok * groups + g];
 }
 
 // Permute into fp16 codes: A16[r] holds the same integers as the int8 codes
@@ -470,7 +483,9 @@ int launch_permute(const int8_t *q, const float *s, int groups, int k, int64_t K
                    const int32_t *sorted_pair, int64_t R, int8_t *A, float *sa, cudaStream_t st) {
   if (R == 0) return WQ_OK;
   if (R > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
-  permute_kernel<<<unsigned(R), 128, 0, st>>>(q, s, groups, k, K, sorted_pair, A, sa);
+  const int64_t ctas = (R + kPermWarps - 1) / kPermWarps;
+  permute_kernel<<<unsigned(ctas), 32 * kPermWarps, 0, st>>>(q, s, groups, k, K, sorted_pair, R, A,
+                                                             sa);
   return launched(1);
 }
 
@@ -658,13 +673,31 @@ __device__ __forceinline__ void silu_table_fill(float *tab) {
   }
 }
 
-// silu(g) of the bf16 pattern b (value g): the table entry, or the formula
-__device__ __forceinline__ float silu_lookup(uint32_t b, float g, const float *tab) {
+// Table index of the bf16 pattern b, or -1 when b lies outside the table
+__device__ __forceinline__ int silu_index(uint32_t b) {
   using namespace silu_tab;
   const bool neg = (b & 0x8000u) != 0;
   const uint32_t k = (b & 0x7fffu) - kLo;  // wraps (large) below 2^-24
-  if (k < (neg ? uint32_t(kNeg) : uint32_t(kPos))) return tab[neg ? k + uint32_t(kPos) : k];
-  return silu(g);
+  return k < (neg ? uint32_t(kNeg) : uint32_t(kPos)) ? int(neg ? k + uint32_t(kPos) : k) : -1;
+}
+
+// silu of the eight bf16 gate values in w[0..3] (low half first): table
+// lookups (an out-of-table value reads entry 0 and is marked), then, only if
+// some lane of the warp has a marked value, the formula for those values
+__device__ __forceinline__ void silu8(const uint32_t (&w)[4], const float *tab, float (&sv)[8]) {
+  uint32_t miss = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t b = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
+    const int idx = silu_index(b);
+    miss |= idx < 0 ? 1u << j : 0u;
+    sv[j] = tab[idx < 0 ? 0 : idx];
+  }
+  if (__any_sync(0xffffffffu, miss != 0)) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (miss >> j & 1u) sv[j] = silu((j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]));
+  }
 }
 
 // VPL vectors of 8 per lane (rows up to 256 * VPL outputs); GV lanes per
@@ -697,11 +730,13 @@ __global__ void __launch_bounds__(512, 1) silu_mul_quant_tab_kernel(
     for (int i = 0; i < VPL; ++i) {
       const uint32_t gw[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
       const uint32_t uw[4] = {uv[i].x, uv[i].y, uv[i].z, uv[i].w};
+      float sv[8];
+      silu8(gw, tab, sv);
       am[i] = 0.0f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        h[i][2 * j] = __fmul_rn(silu_lookup(gw[j] & 0xffffu, bf16_lo(gw[j]), tab), bf16_lo(uw[j]));
-        h[i][2 * j + 1] = __fmul_rn(silu_lookup(gw[j] >> 16, bf16_hi(gw[j]), tab), bf16_hi(uw[j]));
+        h[i][2 * j] = __fmul_rn(sv[2 * j], bf16_lo(uw[j]));
+        h[i][2 * j + 1] = __fmul_rn(sv[2 * j + 1], bf16_hi(uw[j]));
         am[i] = fmaxf(am[i], fabsf(h[i][2 * j]));
         am[i] = fmaxf(am[i], fabsf(h[i][2 * j + 1]));
       }

@@ -203,8 +203,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const uint32_t d = tmem + uint32_t(b) * 256u;
         for (int i = 0; i < KT; ++i, ++g) {
           const int s16 = g % SW16, stt = g % ST;
-          if (!mbar_wait(bar(B_W16_FULL + s16), (g / SW16) & 1, abort_flag) ||
-              !mbar_wait(bar(B_T_FULL + stt), (g / ST) & 1, abort_flag)) {
+          // weights widened and tokens landed (the converters wait for both)
+          if (!mbar_wait(bar(B_W16_FULL + s16), (g / SW16) & 1, abort_flag)) {
             fail();
             ok = false;
             break;
@@ -264,6 +264,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           nrm[j] = sq4(v[j].w, sq4(v[j].z, sq4(v[j].y, sq4(v[j].x, nrm[j]))));
         }
         fence_async_smem();
+        // the stage's token slot has landed too: the MMA issuer then checks a
+        // single barrier per stage
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_T_FULL + s16), (g / ST) & 1, abort_flag))) {
+          fail();
+          ok = false;
+          break;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_W16_FULL + s16));
       }

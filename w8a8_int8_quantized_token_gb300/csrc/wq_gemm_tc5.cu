@@ -30,7 +30,9 @@
 //               holds back the other's copies
 //   warp 1      TMEM allocator and MMA issuer (one thread)
 //   warps 2-9   converters, two groups of four taking alternate K stages:
-//               one weight row per thread, int8 -> fp16 -> TMEM
+//               one weight row per thread, int8 -> fp16 -> TMEM; a stage is
+//               signalled ready once its token slot has landed as well, so
+//               the MMA issuer waits on one barrier per stage
 //   warps 10-21 epilogue: dequant, bf16; three triples of four warps (one
 //               per lane quarter) take every third 32-token group, so the
 //               single accumulator is drained three times faster.  In the
@@ -74,6 +76,7 @@ struct Tc5Plan {
   static constexpr int W8B = WM * BK;        // int8 weight stage bytes
   static constexpr int TB = TNMAX * BK * 2;  // token slot bytes (fp16)
   static constexpr int TBOX = TNMAX / 2;     // token rows each CTA loads for the widest items
+  static_assert(TBOX % 8 == 0 && TBOX <= 256, "token box heights");
   static constexpr int OUTB = 32 * WM * 2;   // one bf16 output box: 32 tokens x 128 channels
   static constexpr int OFF_T = 0;
   static constexpr int OFF_W8 = OFF_T + ST * TB;
@@ -100,12 +103,19 @@ struct Tc5Plan {
 
 __device__ __forceinline__ int sq4(uint32_t w, int acc) { return __dp4a(int(w), int(w), acc); }
 
+// Token tensor maps, one per box height 8, 16, ..., TN / 2: each CTA of a
+// pair loads exactly half of an item's rows rounded up to the MMA's
+// 16-token granularity, so no L2 bandwidth goes to rows the MMA skips.
+template <int TN>
+struct TokenMaps {
+  static constexpr int N = TN / 16;  // box heights 8 * (i + 1)
+  CUtensorMap m[N];
+};
+
 template <int TN, bool BOX>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
-    gemm_tc5_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT8,
-                    const __grid_constant__ CUtensorMap tmT32,
-                    const __grid_constant__ CUtensorMap tmT128,
-                    const __grid_constant__ CUtensorMap tmTbig,
+    gemm_tc5_kernel(const __grid_constant__ CUtensorMap tmW,
+                    const __grid_constant__ TokenMaps<TN> tmT,
                     const __grid_constant__ CUtensorMap tmO, const GemmArgs a,
                     const Tile *__restrict__ tiles, const int32_t *__restrict__ ntiles,
                     int32_t *__restrict__ redo) {
@@ -163,17 +173,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     set_status(a.status, WQ_ERR_TIMEOUT);
   };
   auto nmma_of = [](int rows) { return (rows + 15) & ~15; };
-  // token rows each CTA of the pair loads for an item of nmma tokens
-  auto box_of = [](int nmma) {
-    return nmma <= 16 ? 8 : (nmma <= 64 ? 32 : (nmma <= 256 ? 128 : P::TBOX));
-  };
+  // The pair's r-th item: rounds of npairs items, alternate rounds walked in
+  // reverse, over the longest-first tile list, so the shortest items fill
+  // the last round (every role walks the same sequence).
+  auto item_at = [&](int r) { return r * npairs + ((r & 1) ? npairs - 1 - pair : pair); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ weight producer
     if (lane == 0) {
       int g = 0, gw = 0;
       bool ok = true;
-      for (int ip = pair; ip < items && ok; ip += npairs) {
+      for (int r = 0, ip = pair; ip < items && ok; ip = item_at(++r)) {
         const Tile tl = tiles[ip / NBP];
         const int wb = (ip % NBP) * 2 + int(rank);
         const int wrow = int(int64_t(tl.expert) * a.N + int64_t(wb) * WM);
@@ -199,11 +209,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       int g = 0, gt = 0;
       bool ok = true;
-      for (int ip = pair; ip < items && ok; ip += npairs) {
+      for (int r = 0, ip = pair; ip < items && ok; ip = item_at(++r)) {
         const Tile tl = tiles[ip / NBP];
-        const int box = box_of(nmma_of(tl.rows));
-        const CUtensorMap *tmT =
-            box == 8 ? &tmT8 : (box == 32 ? &tmT32 : (box == 128 ? &tmT128 : &tmTbig));
+        const int box = nmma_of(tl.rows) / 2;  // this CTA's half: a multiple of 8 rows
+        const CUtensorMap *tmap = &tmT.m[box / 8 - 1];
         const uint32_t ttx = uint32_t(2 * box * BK * 2);
         const int trow = tl.row0 + int(rank) * box;
         for (int i = 0; i < KT; ++i, ++g) {
@@ -214,7 +223,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             break;
           }
           mbar_expect_tx(bar(P::B_T_FULL + stt), ttx);
-          tma_load_2d_mc(base + P::OFF_T + uint32_t(stt) * P::TB + rank * uint32_t(box * BK * 2), tmT,
+          tma_load_2d_mc(base + P::OFF_T + uint32_t(stt) * P::TB + rank * uint32_t(box * BK * 2), tmap,
                          i * BK, trow, bar(P::B_T_FULL + stt), 3);
           gt = g + 1;
         }
@@ -230,9 +239,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       int g = 0, ii = 0;
       bool ok = true;
       Tile next = tiles[pair / NBP];  // the next item's tile, loaded an item ahead
-      for (int ip = pair; ip < items && ok; ip += npairs, ++ii) {
+      for (int ip = pair; ip < items && ok; ip = item_at(++ii)) {
         const Tile tl = next;
-        if (ip + npairs < items) next = tiles[(ip + npairs) / NBP];
+        if (item_at(ii + 1) < items) next = tiles[item_at(ii + 1) / NBP];
         const int nm = nmma_of(tl.rows);
         // above 256 tokens: two MMAs of balanced widths (multiples of 16, so
         // the second token block starts on an 8-row swizzle group)
@@ -244,8 +253,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
         for (int i = 0; i < KT; ++i, ++g) {
           const int swt = g % P::NWT, stt = g % P::ST;
-          if (!mbar_wait(bar(P::B_WT_FULL + swt), (g / P::NWT) & 1, abort_flag) ||
-              !mbar_wait(bar(P::B_T_FULL + stt), (g / P::ST) & 1, abort_flag)) {
+          // weights widened and tokens landed (the converters wait for both)
+          if (!mbar_wait(bar(P::B_WT_FULL + swt), (g / P::NWT) & 1, abort_flag)) {
             fail();
             ok = false;
             break;
@@ -280,7 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     const uint32_t tlane = uint32_t(q * 32) << 16;
     int gbase = 0, ii = 0;
     bool ok = true;
-    for (int ip = pair; ip < items && ok; ip += npairs, ++ii, gbase += KT) {
+    for (int ip = pair; ip < items && ok; ip = item_at(++ii), gbase += KT) {
       int nrm = 0;
       for (int i = grp; i < KT; i += 2) {
         const int g = gbase + i;
@@ -321,6 +330,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         tmem_st32(tmem + tlane + uint32_t(P::WT_COL + swt * 32), f);
         tmem_wait_st();
         tc_fence_before();
+        // the stage's token slot has landed too: the MMA issuer then checks
+        // a single barrier per stage (it is the pipeline's critical thread;
+        // the converters run stages ahead of it)
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(P::B_T_FULL + swt), (g / P::ST) & 1, abort_flag))) {
+          fail();
+          ok = false;
+          break;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(P::B_WT_FULL + swt));
       }
@@ -346,7 +363,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     uint16_t *box = reinterpret_cast<uint16_t *>(sm + P::OFF_OUT + trip * P::OUTB);
     const uint32_t box_s = base + P::OFF_OUT + uint32_t(trip) * P::OUTB;
     int ii = 0;
-    for (int ip = pair; ip < items; ip += npairs, ++ii) {
+    for (int ip = pair; ip < items; ip = item_at(++ii)) {
       const Tile tl = tiles[ip / NBP];
       const int wb = (ip % NBP) * 2 + int(rank);
       const int b = ii & 1, par = (ii >> 1) & 1;
@@ -468,16 +485,15 @@ template <int TN, bool BOX>
 static int launch_tc5(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
                       int32_t *redo, cudaStream_t st) {
   using P = Tc5Plan<TN, BOX>;
-  CUtensorMap mW, m8, m32, m128, mbig, mO;
+  CUtensorMap mW, mO;
+  TokenMaps<TN> mT;
   // the output box map: bf16 [R][N]; the direct-store plan and int32 output
   // never use it (the same rows read as 16-bit values stay inside the buffer)
   if (!make_tma_2d_u8(&mW, a.W, int64_t(a.E) * a.N, a.K, BK, WM) ||
-      !make_tma_2d_b16_sw128(&m8, a.A16, a.R, a.K, 8) ||
-      !make_tma_2d_b16_sw128(&m32, a.A16, a.R, a.K, 32) ||
-      !make_tma_2d_b16_sw128(&m128, a.A16, a.R, a.K, 128) ||
-      !make_tma_2d_b16_sw128(&mbig, a.A16, a.R, a.K, P::TBOX) ||
       !make_tma_2d_b16(&mO, a.out, a.R, a.N, WM, 32))
     return WQ_ERR_LAUNCH;
+  for (int i = 0; i < TokenMaps<TN>::N; ++i)
+    if (!make_tma_2d_b16_sw128(&mT.m[i], a.A16, a.R, a.K, 8 * (i + 1))) return WQ_ERR_LAUNCH;
   static bool attr = false;
   static int pairs_resident = 0;
   if (!attr) {
@@ -500,8 +516,8 @@ static int launch_tc5(const GemmArgs &a, const Tile *tiles, const int32_t *ntile
   }
   const int64_t max_items = int64_t(max_tiles) * (a.N / (2 * WM));
   const int pairs = int(max_items < pairs_resident ? max_items : pairs_resident);
-  gemm_tc5_kernel<TN, BOX><<<2 * pairs, NTHREADS, P::SMEM_BYTES, st>>>(mW, m8, m32, m128, mbig, mO,
-                                                                      a, tiles, ntiles, redo);
+  gemm_tc5_kernel<TN, BOX><<<2 * pairs, NTHREADS, P::SMEM_BYTES, st>>>(mW, mT, mO, a, tiles,
+                                                                      ntiles, redo);
   return launched(1);
 }
 
