@@ -92,8 +92,12 @@ struct Tc5Plan {
   static constexpr int OFF_NORM = OFF_BAR + NBAR * 8;  // int32 [2 buffers][2 converter groups]
   static constexpr int OFF_TMEM = OFF_NORM + 16;
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
-  static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
   static constexpr int NGRP = TNMAX / 32;  // 32-token groups of the largest item
+  static constexpr int GPT = (NGRP + NTRIP - 1) / NTRIP;  // groups per triple
+  // BOX plan: each triple's token scales of its groups, [triple][item parity][GPT * 32]
+  static constexpr int OFF_TSC = (OFF_ABORT + 4 + 15) & ~15;
+  static constexpr int TSC_BYTES = BOX ? NTRIP * 2 * GPT * 32 * 4 : 0;
+  static constexpr int SMEM_BYTES = OFF_TSC + TSC_BYTES + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory plan too large");
   static_assert((TB % 1024) == 0 && (W8B % 1024) == 0 && (OUTB % 1024) == 0 &&
                     (TBOX * BK * 2) % 1024 == 0,
@@ -371,14 +375,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       for (int j = lane; j < tl.rows; j += 32) tmax = max(tmax, a.a_norm2[int64_t(tl.row0) + j]);
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-      // the item's token scales (lane j of group p holds token 32p + j) and
-      // this thread's weight scale, loaded while the item's MMAs still run
+      // the item's token scales and this thread's weight scale, loaded while
+      // the item's MMAs still run.  BOX plan: each thread of the triple puts
+      // one token scale of the triple's groups into shared memory (published
+      // by the triple's barrier below) and the drain reads them as
+      // broadcasts; otherwise lane j of register sal[p] holds token 32p + j.
       const int64_t n = int64_t(wb) * WM + q * 32 + lane;  // this thread's output channel
       const float swn = a.sw[int64_t(tl.expert) * a.N + n];
-      float sal[P::NGRP];
+      float sal[BOX ? 1 : P::NGRP];
+      float *tsc = reinterpret_cast<float *>(sm + P::OFF_TSC) + (trip * 2 + (ii & 1)) * P::GPT * 32;
+      if constexpr (BOX) {
+        const int tok = (trip + NTRIP * q) * 32 + lane;  // group trip + NTRIP*q, token lane
+        if (q < P::GPT) tsc[q * 32 + lane] = tok < tl.rows ? a.sa[int64_t(tl.row0) + tok] : 0.0f;
+      } else {
 #pragma unroll
-      for (int p = 0; p < P::NGRP; ++p)
-        sal[p] = p * 32 + lane < tl.rows ? a.sa[int64_t(tl.row0) + p * 32 + lane] : 0.0f;
+        for (int p = 0; p < P::NGRP; ++p)
+          sal[p] = p * 32 + lane < tl.rows ? a.sa[int64_t(tl.row0) + p * 32 + lane] : 0.0f;
+      }
       bool okw = __all_sync(0xffffffffu, mbar_wait<500>(bar(P::B_ACC_FULL), ii & 1, abort_flag));
       if (okw) okw = __all_sync(0xffffffffu, mbar_wait(bar(P::B_NORM_READY + b), par, abort_flag));
       // the four warps of a triple take one decision (every one of them
@@ -413,10 +426,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         tmem_ld32(taddr + 32u * p, v);
         const int tok0 = p * 32;
         float sp = sal[0];  // sal[p] without a dynamic register index
+        if constexpr (!BOX) {
 #pragma unroll
-        for (int m = 1; m < P::NGRP; ++m) sp = p == m ? sal[m] : sp;
+          for (int m = 1; m < P::NGRP; ++m) sp = p == m ? sal[m] : sp;
+        }
         tmem_wait_ld();
         const int lim = min(32, tl.rows - tok0);
+        if constexpr (BOX) {
+          if (a.out_type != WQ_OUT_I32) {
+            // (v * sa) * sw for token pairs in packed products, rounded to
+            // bf16 pairs; the group's token scales are shared-memory broadcasts
+            const float *ts = tsc + ((p - trip) / NTRIP) * 32;
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 s2 = *reinterpret_cast<const float2 *>(ts + 2 * i);
+              float x0 = __uint_as_float(v[2 * i]), x1 = __uint_as_float(v[2 * i + 1]);
+              fmul2(x0, x1, s2.x, s2.y);
+              fmul2(x0, x1, swn, swn);
+              pk[i] = bf16x2_rn(x0, x1);
+            }
+            if (lim < 32) {
+              uint16_t *o = static_cast<uint16_t *>(a.out) + (int64_t(tl.row0) + tok0) * a.N + n;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < lim) o[int64_t(j) * a.N] = uint16_t(pk[j >> 1] >> ((j & 1) * 16));
+            } else {
+              // a full group: the triple writes its 32 x 128 box, the leader
+              // stores it once every warp has written and fenced its part
+              if (leader) bulk_wait_read_all();  // the previous box has been read out
+              named_sync(1 + trip, 128);
+              uint16_t *col = box + q * 32 + lane;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) col[j * WM] = uint16_t(pk[j >> 1] >> ((j & 1) * 16));
+              fence_async_smem();
+              named_sync(1 + trip, 128);
+              if (leader) {
+                tma_store_2d(&tmO, box_s, wb * WM, tl.row0 + tok0);
+                bulk_commit();
+              }
+            }
+            continue;
+          }
+        }
         if (a.out_type == WQ_OUT_I32) {
           int32_t *o = static_cast<int32_t *>(a.out) + (int64_t(tl.row0) + tok0) * a.N + n;
 #pragma unroll

@@ -201,6 +201,21 @@ __device__ __forceinline__ void store_f16_row_piece(uint8_t *rowp, int row, int 
   *reinterpret_cast<uint4 *>(rowp + (((2 * part + 1) ^ sw) << 4)) = o1;
 }
 
+// Two float32 products in one packed instruction, each rounded to nearest
+// even exactly as a scalar multiply is (no fusion: nothing is added).
+__device__ __forceinline__ void fmul2(float &x0, float &x1, float y0, float y1) {
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%0, %1};\n mov.b64 b, {%2, %3};\n"
+      " mul.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+      : "+f"(x0), "+f"(x1)
+      : "f"(y0), "f"(y1));
+}
+// Two floats -> a bf16 pair (round to nearest even each): lo in bits 0-15
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // ---- clusters ----
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
