@@ -247,6 +247,17 @@ WQ_API int wq_grouped_gemm_w8a8_f16codes(const uint16_t *A16, const int32_t *a_n
                                          void *ws, size_t ws_bytes, int32_t *status,
                                          wq_stream_t stream);
 
+/* Per-token quantization into fp16 codes with row norms (the rule of
+ * wq_quantize_per_token, Meituan INT8 DeepSeek R1 article, 量化技术的探索:
+ * online per-token activation quantization): codes as fp16 bits q16 [T][K]
+ * (row pitch K), s float32 [T] and norm2 int32 [T] = sum of code^2 of each
+ * row, the input form of wq_grouped_gemm_w8a8_f16codes (a dense W8A8 linear
+ * with one expert reads it directly).
+ * Requirements: K % 8 == 0, ldx % 8 == 0, K <= 65536, 16-byte aligned x and
+ * q16. */
+WQ_API int wq_quantize_per_token_f16(const uint16_t *x, int64_t T, int64_t K, int64_t ldx,
+                                     uint16_t *q16, float *s, int32_t *norm2, wq_stream_t stream);
+
 /* Masked layout [LL]: A int8 [E][Mmax][K] with per-row scales sa
  * ([E][Mmax] or [E][Mmax][K/128]) and valid counts masked_m int32 [E]
  * (device).  Expert e computes rows [0, min(masked_m[e], Mmax)) with the

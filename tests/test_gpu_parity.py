@@ -310,6 +310,10 @@ def _layer_case(cfg):
     # widths multiples of 256 and many rows per expert: the fp16-code block engine
     synth.small_config("small_block_f16", T=300, H=512, I=256, E=4, k=2, scheme="block", acc="f32"),
     synth.small_config("hot", T=300, H=256, I=128, E=4, k=1),
+    # K >= 1024 with many rows per expert: GEMM1 on the tensor-memory-weights
+    # pair engine within a small layer
+    synth.small_config("small_k1024", T=300, H=1024, I=256, E=4, k=2),
+    synth.small_config("small_k2048_f32", T=260, H=2048, I=256, E=3, k=2, acc="f32"),
 ], ids=lambda c: c.name)
 def test_layer_forward(cfg):
     x, lg, w, ow = _layer_case(cfg)
@@ -563,6 +567,18 @@ def test_single_pass_odd_sums_near_2_24(K, engine):
     assert_bf16_equal(bits(outs["f32", "bf16"]),
                       O.grouped_gemm_w8a8(A, sa, W, sw, offs, "channel", "f32"),
                       f"{engine} K{K} float32 accumulator")
+
+
+def test_quantize_per_token_f16():
+    """fp16-code quantization: the per-token codes, scales and squared row
+    norms of the oracle (codes compared as the integers they hold)."""
+    x = synth.activations(70, 7168, True, seed=41)
+    x[3] = 0  # a zero row: zero codes, norm 0
+    q16, s, n2 = wq.quantize_per_token_f16(x.to(DEV))
+    qo, so = O.quantize_per_token(bits(x))
+    assert np.array_equal(np_(q16).astype(np.int32), qo.astype(np.int32))
+    assert np.array_equal(np_(s), so)
+    assert np.array_equal(np_(n2), (qo.astype(np.int64) ** 2).sum(1))
 
 
 # ---------------------------------------------------------------- dense linear

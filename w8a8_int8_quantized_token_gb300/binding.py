@@ -50,6 +50,7 @@ _SIGS = {
     "wq_moe_permute_f16": (_I, [_P, _P, _I, _I, _I, _L, _P, _L, _P, _P, _P, _P]),
     "wq_silu_mul_quant_f16": (_I, [_P, _L, _L, _I, _P, _P, _P, _P]),
     "wq_grouped_gemm_w8a8_f16codes": (_I, [_P, _P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
+    "wq_quantize_per_token_f16": (_I, [_P, _L, _L, _L, _P, _P, _P, _P]),
     "wq_grouped_gemm_masked_workspace_size": (_S, [_I, _I]),
     "wq_grouped_gemm_w8a8_masked": (_I, [_P, _P, _P, _I, _I, _P, _P, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
     "wq_silu_mul_quant": (_I, [_P, _L, _L, _I, _P, _P, _P]),
@@ -285,6 +286,18 @@ def grouped_gemm_w8a8_f16codes(A16, a_norm2, sa, W, sw, offsets, acc="i32", out_
                                                _ptr(ws), nws, _ptr(st), _stream()),
            "wq_grouped_gemm_w8a8_f16codes")
     return out
+
+
+def quantize_per_token_f16(x):
+    """Per-token quantization into fp16 codes: (q16 fp16 [T, K], s [T], norm2 [T])."""
+    _dev(x, torch.bfloat16, "x")
+    T, K = x.shape
+    q16 = torch.empty(T, K, dtype=torch.float16, device=x.device)
+    s = torch.empty(T, dtype=torch.float32, device=x.device)
+    n2 = torch.empty(T, dtype=torch.int32, device=x.device)
+    _check(lib().wq_quantize_per_token_f16(_ptr(x), T, K, K, _ptr(q16), _ptr(s), _ptr(n2), _stream()),
+           "wq_quantize_per_token_f16")
+    return q16, s, n2
 
 
 # ---------------------------------------------------------------- GEMMs

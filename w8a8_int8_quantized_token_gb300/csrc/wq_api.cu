@@ -400,6 +400,17 @@ int wq_grouped_gemm_w8a8_f16codes(const uint16_t *A16, const int32_t *a_norm2, c
   return launch_grouped_gemm(a, stream);
 }
 
+int wq_quantize_per_token_f16(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, uint16_t *q16,
+                              float *s, int32_t *norm2, wq_stream_t stream) {
+  if (T < 0 || K < 0 || ldx < K) return WQ_ERR_INVALID_ARG;
+  if (T == 0 || K == 0) return WQ_OK;
+  if (!x || !q16 || !s || !norm2) return WQ_ERR_INVALID_ARG;
+  if (K % 8 || ldx % 8 || !al16(x) || !al16(q16)) return WQ_ERR_UNSUPPORTED;
+  if (K > 65536) return WQ_ERR_UNSUPPORTED;  // squared norms stay below 2^31
+  WQ_TRY(check_device());
+  return launch_quant_rows_f16(x, T, K, ldx, 0, q16, s, norm2, stream);
+}
+
 size_t wq_grouped_gemm_masked_workspace_size(int E, int Mmax) {
   if (E < 1 || Mmax < 0) return 0;
   return gemm_ws_bytes(int64_t(E) * Mmax, E, Mmax, true);
