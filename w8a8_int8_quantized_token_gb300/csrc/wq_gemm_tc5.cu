@@ -51,10 +51,12 @@ namespace {
 using namespace tc;
 
 constexpr int WM = 128, BK = 64;
-constexpr int NEPI = 12;             // epilogue warps (three per tensor-memory lane quarter)
-constexpr int NTRIP = NEPI / 4;      // epilogue triples
-constexpr int WARP_TOK = 10 + NEPI;  // token producer
-constexpr int NTHREADS = (11 + NEPI) * 32;
+constexpr int NCG = 2;                 // converter groups (four warps each), alternate K stages
+constexpr int NEPI = 12;               // epilogue warps (three per tensor-memory lane quarter)
+constexpr int NTRIP = NEPI / 4;        // epilogue triples
+constexpr int WARP_EPI = 2 + 4 * NCG;  // first epilogue warp
+constexpr int WARP_TOK = WARP_EPI + NEPI;  // token producer
+constexpr int NTHREADS = (WARP_TOK + 1) * 32;
 
 // Shared- and tensor-memory plan of one instantiation.  TN = most tokens of
 // one item (accumulator columns); BOX = full output groups leave through a
@@ -89,11 +91,13 @@ struct Tc5Plan {
       B_NORM_FREE = B_ACC_FULL + 4,                    // [2]
       B_NORM_READ = B_ACC_FULL + 6,                    // [2]
       B_MMA_DONE = B_ACC_FULL + 8, NBAR = B_ACC_FULL + 9;
-  static constexpr int OFF_NORM = OFF_BAR + NBAR * 8;  // int32 [2 buffers][2 converter groups]
-  static constexpr int OFF_TMEM = OFF_NORM + 16;
+  static constexpr int OFF_NORM = OFF_BAR + NBAR * 8;  // int32 [2 buffers][NCG converter groups]
+  static constexpr int OFF_TMEM = OFF_NORM + 8 * NCG;
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int NGRP = TNMAX / 32;  // 32-token groups of the largest item
   static constexpr int GPT = (NGRP + NTRIP - 1) / NTRIP;  // groups per triple
+  // each thread of a triple stages one token scale of one of its groups
+  static_assert(!BOX || GPT <= 4, "a triple's token scales fit its four warps");
   // BOX plan: each triple's token scales of its groups, [triple][item parity][GPT * 32]
   static constexpr int OFF_TSC = (OFF_ABORT + 4 + 15) & ~15;
   static constexpr int TSC_BYTES = BOX ? NTRIP * 2 * GPT * 32 * 4 : 0;
@@ -143,7 +147,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < 4; ++i) norm[i] = 0;
+    for (int i = 0; i < 2 * NCG; ++i) norm[i] = 0;
     for (int s = 0; s < P::SW8; ++s) {
       mbar_init(bar(P::B_W8_FULL + s), 1);
       mbar_init(bar(P::B_W8_EMPTY + s), 4);
@@ -158,7 +162,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     mbar_init(bar(P::B_ACC_FULL), 1);
     mbar_init(bar(P::B_ACC_EMPTY), NEPI);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(P::B_NORM_READY + b), 8);  // both converter groups
+      mbar_init(bar(P::B_NORM_READY + b), 4 * NCG);  // every converter warp
       mbar_init(bar(P::B_NORM_FREE + b), 1);
       mbar_init(bar(P::B_NORM_READ + b), NEPI);
     }
@@ -282,7 +286,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       mma_commit(bar(P::B_MMA_DONE));
       mbar_wait_bounded(bar(P::B_MMA_DONE), 0);
     }
-  } else if (warp < 10) {
+  } else if (warp < WARP_EPI) {
     // ------------------------------------------------------------ converters
     // thread = weight row (its tensor-memory lane); group `grp` takes the K
     // stages of parity grp; the 16-byte pieces of a row are read in a
@@ -295,7 +299,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     bool ok = true;
     for (int ip = pair; ip < items && ok; ip = item_at(++ii), gbase += KT) {
       int nrm = 0;
-      for (int i = grp; i < KT; i += 2) {
+      for (int i = grp; i < KT; i += NCG) {
         const int g = gbase + i;
         const int sw = g % P::SW8, swt = g % P::NWT;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(P::B_W8_FULL + sw), (g / P::SW8) & 1, abort_flag))) {
@@ -355,14 +359,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         fail();
         break;
       }
-      if (lane == 0) atomicMax(const_cast<int *>(norm + 2 * b + grp), wmax);
+      if (lane == 0) atomicMax(const_cast<int *>(norm + NCG * b + grp), wmax);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(P::B_NORM_READY + b));
     }
   } else if (warp < WARP_TOK) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;              // tensor-memory lane quarter of this warp
-    const int trip = (warp - 10) >> 2;   // triple: 32-token groups trip, trip + NTRIP, ...
+    const int trip = (warp - WARP_EPI) >> 2;  // triple: 32-token groups trip, trip + NTRIP, ...
     const bool leader = q == 0 && lane == 0;  // issues the triple's box stores
     uint16_t *box = reinterpret_cast<uint16_t *>(sm + P::OFF_OUT + trip * P::OUTB);
     const uint32_t box_s = base + P::OFF_OUT + uint32_t(trip) * P::OUTB;
@@ -402,15 +406,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       }
       tc_fence_after();
       // a row's norm is at most the sum of the groups' largest partial norms
-      const long long nw = (long long)norm[2 * b] + norm[2 * b + 1];
+      long long nw = 0;
+#pragma unroll
+      for (int c = 0; c < NCG; ++c) nw += norm[NCG * b + c];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(P::B_NORM_READ + b));
-      if (warp == 10 && lane == 0) {
+      if (warp == WARP_EPI && lane == 0) {
         // once every epilogue warp has read the norm, clear it for the
         // item after next and hand the slot back to the converters
         if (mbar_wait(bar(P::B_NORM_READ + b), par, abort_flag)) {
-          norm[2 * b] = 0;
-          norm[2 * b + 1] = 0;
+          for (int c = 0; c < NCG; ++c) norm[NCG * b + c] = 0;
           mbar_arrive(bar(P::B_NORM_FREE + b));
         } else {
           fail();

@@ -47,23 +47,25 @@ constexpr int SW8 = 8, SW16 = 4, ST = 4;        // ring depths: int8 W, fp16 W, 
 static_assert(SW16 == ST, "a widened-weight slot is released with its token slot");
 constexpr int W8B = WM * BK, W16B = 2 * W8B;    // weight stage bytes
 constexpr int TB = TN * BK * 2;                 // token stage bytes (fp16)
-constexpr int CH0 = 0, CH1 = TN, RUN = 2 * TN;  // tensor-memory columns: chunks, running sum
+constexpr int NCH = 3;                          // chunk accumulators (tensor-memory columns [0, 3*TN))
+constexpr int EPI_COLS = TN / 2;                // token columns each epilogue warp owns
 constexpr int OFF_T = 0;
 constexpr int OFF_W16 = OFF_T + ST * TB;
 constexpr int OFF_W8 = OFF_W16 + SW16 * W16B;
 constexpr int NEPI = 8;                         // epilogue warps
-constexpr int OFF_SC = OFF_W8 + SW8 * W8B;      // float [NEPI][TN] column scales
-constexpr int OFF_BAR = OFF_SC + NEPI * TN * 4;
+constexpr int OFF_SC = OFF_W8 + SW8 * W8B;      // float [NEPI][EPI_COLS] column scales
+constexpr int OFF_BAR = OFF_SC + NEPI * EPI_COLS * 4;
 constexpr int B_W8_FULL = 0, B_W8_EMPTY = SW8, B_W16_FULL = 2 * SW8,
               B_T_FULL = 2 * SW8 + SW16, B_T_EMPTY = B_T_FULL + ST,
-              B_ACC_FULL = B_T_EMPTY + ST,  // [2]
-    B_ACC_EMPTY = B_ACC_FULL + 2,           // [2]
-    B_MMA_DONE = B_ACC_FULL + 4, NBAR = B_ACC_FULL + 5;
+              B_ACC_FULL = B_T_EMPTY + ST,  // [NCH]
+    B_ACC_EMPTY = B_ACC_FULL + NCH,         // [NCH]
+    B_MMA_DONE = B_ACC_FULL + 2 * NCH, NBAR = B_ACC_FULL + 2 * NCH + 1;
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 4;
 constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
 static_assert(TB % 1024 == 0 && OFF_W16 % 1024 == 0 && OFF_W8 % 1024 == 0, "swizzle alignment");
-static_assert(RUN + TN <= 512, "tensor memory plan");
+static_assert(NCH * TN <= 512, "tensor memory plan");
+static_assert(EPI_COLS % 16 == 0 && NEPI == 8, "each epilogue warp owns 16-column pieces");
 static_assert(SMEM_BYTES <= 232448, "shared memory plan too large");
 constexpr int NTHREADS = 480;
 constexpr int WARP_TOK = 14;            // token producer
@@ -119,7 +121,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(B_T_FULL + s), 1);   // local expect_tx; bytes from both CTAs' copies
       mbar_init(bar(B_T_EMPTY + s), 2);  // MMA completions of both CTAs
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NCH; ++b) {
       mbar_init(bar(B_ACC_FULL + b), 1);
       mbar_init(bar(B_ACC_EMPTY + b), NEPI);
     }
@@ -205,13 +207,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         const Tile tl = tiles[ip / NBP];
         const uint32_t idesc = idesc_f16(WM, nmma_of(tl.rows));
         for (int kb = 0; kb < KB && ok; ++kb, ++gk) {
-          const int b = gk & 1;
-          if (!mbar_wait<1000>(bar(B_ACC_EMPTY + b), ((gk >> 1) & 1) ^ 1, abort_flag)) {
+          const int b = gk % NCH;
+          if (!mbar_wait<1000>(bar(B_ACC_EMPTY + b), ((gk / NCH) & 1) ^ 1, abort_flag)) {
             fail();
             ok = false;
             break;
           }
-          const uint32_t d = tmem + uint32_t(b ? CH1 : CH0);
+          const uint32_t d = tmem + uint32_t(b * TN);
           for (int h = 0; h < 2; ++h, ++g) {
             const int s16 = g % SW16, stt = g % ST;
             if (!mbar_wait<1000>(bar(B_W16_FULL + s16), (g / SW16) & 1, abort_flag) ||
@@ -276,10 +278,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp < 6 + NEPI) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;          // tensor-memory lane quarter of this warp
-    const int half = (warp - 6) >> 2;  // which alternate 32-column groups it drains
-    float *scal = reinterpret_cast<float *>(sm + OFF_SC) + (warp - 6) * TN;
+    // Warp (q, h) owns token columns [h * EPI_COLS, (h + 1) * EPI_COLS) of
+    // tensor-memory lane quarter q (this thread: one output channel) for the
+    // whole item and keeps their running sums in registers: per K block one
+    // tensor-memory load, one product and one sum per element, no round trip
+    // of the sum through tensor memory.  The block's column scales
+    // sa[tok][kb] * sw[kb] are staged in this warp's shared-memory row and
+    // read back as broadcasts.
+    const int q = warp & 3;            // tensor-memory lane quarter of this warp
+    const int h = (warp - 6) >> 2;     // which half of the chunk's columns it owns
+    const int c0 = h * EPI_COLS;       // first owned column
+    float *scal = reinterpret_cast<float *>(sm + OFF_SC) + (warp - 6) * EPI_COLS;
     const uint32_t tq = tmem + (uint32_t(q * 32) << 16);
+    constexpr int NSC = (EPI_COLS + 31) / 32;  // owned columns per lane when staging scales
     int gk = 0;
     bool ok = true;
     for (int ip = pair; ip < items && ok; ip += npairs) {
@@ -287,82 +298,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       const int wb = (ip % NBP) * 2 + int(rank);  // this CTA's weight block = scale block row
       const int64_t n = int64_t(wb) * WM + q * 32 + lane;  // this thread's output channel
       const float *swp = a.sw + (int64_t(tl.expert) * (a.N / 128) + wb) * KB;
-      const int nmma = nmma_of(tl.rows);
-      const int ngrp = (nmma + 31) / 32;
-      // token scales of this K block for the columns this lane stages
-      // token and weight scales of the next K block, loaded one block ahead;
-      // this warp stages only the columns of its own groups (p = half + 2m)
-      constexpr int NG = (TN / 32 + 1) / 2;
-      float sap[NG];
+      // token scales of the owned columns, loaded one K block ahead
+      float sap[NSC];
 #pragma unroll
-      for (int m = 0; m < NG; ++m) {
-        const int col = 32 * (half + 2 * m) + lane;
-        sap[m] = col < tl.rows ? a.sa[(int64_t(tl.row0) + col) * KB] : 0.0f;
+      for (int m = 0; m < NSC; ++m) {
+        const int col = c0 + 32 * m + lane;
+        sap[m] = (32 * m + lane < EPI_COLS && col < tl.rows) ? a.sa[(int64_t(tl.row0) + col) * KB] : 0.0f;
       }
       float swv = swp[0];
+      float acc[EPI_COLS];
+#pragma unroll
+      for (int j = 0; j < EPI_COLS; ++j) acc[j] = 0.0f;  // acc starts at +0
       for (int kb = 0; kb < KB; ++kb, ++gk) {
-        const int b = gk & 1;
+        const int b = gk % NCH;
         // column scales sa[col][kb] * sw[kb] (0 past the tile's rows)
 #pragma unroll
-        for (int m = 0; m < NG; ++m)
-          if (32 * (half + 2 * m) < TN) scal[32 * (half + 2 * m) + lane] = __fmul_rn(sap[m], swv);
+        for (int m = 0; m < NSC; ++m)
+          if (32 * m + lane < EPI_COLS) scal[32 * m + lane] = __fmul_rn(sap[m], swv);
         if (kb + 1 < KB) {
           swv = swp[kb + 1];
 #pragma unroll
-          for (int m = 0; m < NG; ++m) {
-            const int col = 32 * (half + 2 * m) + lane;
-            sap[m] = col < tl.rows ? a.sa[(int64_t(tl.row0) + col) * KB + kb + 1] : 0.0f;
+          for (int m = 0; m < NSC; ++m) {
+            const int col = c0 + 32 * m + lane;
+            sap[m] = (32 * m + lane < EPI_COLS && col < tl.rows)
+                         ? a.sa[(int64_t(tl.row0) + col) * KB + kb + 1] : 0.0f;
           }
         }
         __syncwarp();
-        if (!__all_sync(0xffffffffu, mbar_wait<1000>(bar(B_ACC_FULL + b), (gk >> 1) & 1, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait<1000>(bar(B_ACC_FULL + b), (gk / NCH) & 1, abort_flag))) {
           fail();
           ok = false;
           break;
         }
         tc_fence_after();
-        const bool last = kb == KB - 1;
-        const uint32_t tch = tq + uint32_t(b ? CH1 : CH0);
-        for (int p = half; p < ngrp; p += 2) {
-          uint32_t v[32], u[32];
-          tmem_ld32(tch + 32u * p, v);
-          if (kb > 0) {
-            tmem_ld32(tq + uint32_t(RUN) + 32u * p, u);
-          } else {
+        const uint32_t tch = tq + uint32_t(b * TN + c0);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) u[j] = 0u;  // acc starts at +0
-          }
+        for (int piece = 0; piece < EPI_COLS / 16; ++piece) {
+          uint32_t v[16];
+          tmem_ld16(tch + 16u * piece, v);
           tmem_wait_ld();
-          const float4 *s4 = reinterpret_cast<const float4 *>(scal + 32 * p);
+          const float4 *s4 = reinterpret_cast<const float4 *>(scal + 16 * piece);
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            const float4 s = s4[j / 4];
-            float r0, r1, r2, r3;
-            mul_add2(r0, r1, __uint_as_float(v[j]), __uint_as_float(v[j + 1]), s.x, s.y,
-                     __uint_as_float(u[j]), __uint_as_float(u[j + 1]));
-            mul_add2(r2, r3, __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]), s.z, s.w,
-                     __uint_as_float(u[j + 2]), __uint_as_float(u[j + 3]));
-            u[j] = __float_as_uint(r0);
-            u[j + 1] = __float_as_uint(r1);
-            u[j + 2] = __float_as_uint(r2);
-            u[j + 3] = __float_as_uint(r3);
-          }
-          if (!last) {
-            tmem_st32(tq + uint32_t(RUN) + 32u * p, u);
-          } else {
-            const int tok0 = p * 32;
-            const int lim = min(32, tl.rows - tok0);
-            uint16_t *o = static_cast<uint16_t *>(a.out) + (int64_t(tl.row0) + tok0) * a.N + n;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < lim) o[int64_t(j) * a.N] = f_to_bf16(__uint_as_float(u[j]));
+          for (int j = 0; j < 16; j += 4) {
+            const float4 sc = s4[j / 4];
+            float *r = acc + 16 * piece + j;
+            mul_add2(r[0], r[1], __uint_as_float(v[j]), __uint_as_float(v[j + 1]), sc.x, sc.y, r[0], r[1]);
+            mul_add2(r[2], r[3], __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]), sc.z, sc.w, r[2], r[3]);
           }
         }
-        if (!last) tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_ACC_EMPTY + b));
       }
+      if (!ok) break;
+      // after the last K block: bf16 out for the owned columns inside the tile
+      uint16_t *o = static_cast<uint16_t *>(a.out) + (int64_t(tl.row0) + c0) * a.N + n;
+#pragma unroll
+      for (int j = 0; j < EPI_COLS; ++j)
+        if (c0 + j < tl.rows) o[int64_t(j) * a.N] = f_to_bf16(acc[j]);
     }
   }
 
