@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (j < NJW || c < tchunks) {
             const int row = c >> 2;
             store_f16_row_piece(dst + (j < NJW ? 0 : W16) + row * 128, row, c & 3, v[j]);
-            nrm[j] = sq4(v[j].w, sq4(v[j].z, sq4(v[j].y, sq4(v[j].x, nrm[j]))));
+            nrm[j] += sq4(v[j].w, sq4(v[j].z, 0)) + sq4(v[j].y, sq4(v[j].x, 0));
           }
         }
         fence_async_smem();

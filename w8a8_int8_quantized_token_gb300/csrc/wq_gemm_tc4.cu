@@ -261,7 +261,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           const int c = j * GCONV + t;
           const int row = c >> 2;
           store_f16_row_piece(dst + row * 128, row, c & 3, v[j]);
-          nrm[j] = sq4(v[j].w, sq4(v[j].z, sq4(v[j].y, sq4(v[j].x, nrm[j]))));
+          nrm[j] += sq4(v[j].w, sq4(v[j].z, 0)) + sq4(v[j].y, sq4(v[j].x, 0));
         }
         fence_async_smem();
         // the stage's token slot has landed too: the MMA issuer then checks a

@@ -321,14 +321,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(P::B_W8_EMPTY + sw));
         uint32_t f[32];
+        int part[4];  // the stage's squared norm in four independent partial sums
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           s8x4_to_f16x4(v[m].x, f[8 * m + 0], f[8 * m + 1]);
           s8x4_to_f16x4(v[m].y, f[8 * m + 2], f[8 * m + 3]);
           s8x4_to_f16x4(v[m].z, f[8 * m + 4], f[8 * m + 5]);
           s8x4_to_f16x4(v[m].w, f[8 * m + 6], f[8 * m + 7]);
-          nrm = sq4(v[m].w, sq4(v[m].z, sq4(v[m].y, sq4(v[m].x, nrm))));
+          part[m] = sq4(v[m].w, sq4(v[m].z, 0)) + sq4(v[m].y, sq4(v[m].x, 0));
         }
+        // one add per stage joins the running norm (a serial chain of dot
+        // products through it was the converters' critical path)
+        nrm += (part[0] + part[1]) + (part[2] + part[3]);
         if (!__all_sync(0xffffffffu,
                         mbar_wait(bar(P::B_T_EMPTY + swt), ((g / P::NWT) & 1) ^ 1, abort_flag))) {
           fail();
