@@ -538,7 +538,10 @@ bool gemm_tc5_supported(const GemmArgs &a) {
 // 384-token items when the experts average more than 320 rows (fewer items,
 // each expert's weights streamed fewer times), else 320-token items with
 // the shared-memory output boxes
-static bool tc5_wide(const GemmArgs &a) { return int64_t(a.R) > 320 * int64_t(a.E); }
+static bool tc5_wide(const GemmArgs &a) {
+  // (the masked layout's row count includes its invalid rows: the box plan)
+  return a.masked_m == nullptr && int64_t(a.R) > 320 * int64_t(a.E);
+}
 
 int gemm_tc5_tile_rows(const GemmArgs &a) { return tc5_wide(a) ? 384 : 320; }
 
