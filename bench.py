@@ -255,7 +255,8 @@ class Layer:
         self.hq, self.sh = e(R, I, dt=cdt), e(R * self.g2, dt=torch.float32)
         self.y = e(R, H, dt=torch.bfloat16)
         self.out = e(T, H, dt=torch.bfloat16)
-        self.gws_n = self.lib.wq_grouped_gemm_workspace_size(R, E)
+        self.gws_n = max(self.lib.wq_grouped_gemm_workspace_size(R, E),
+                         self.lib.wq_grouped_gemm_silu_quant_workspace_size(R, E))
         self.gws = e(self.gws_n, dt=torch.uint8)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.W13, self.S13, self.W2, self.S2 = weights
@@ -316,6 +317,36 @@ class Layer:
         ok(L.wq_moe_combine(P(self.y), P(self.p2r), P(self.w), T, k, H, P(self.out), st), "combine")
         rec(8)
         return self.out
+
+
+    def time_fused(self, steps):
+        """Block scheme: the fused gate_up -> SiLU-and-mul -> re-quantization
+        entry on the last staged step's inputs, timed against the two staged
+        calls it replaces; its codes and scales must equal theirs bit for bit."""
+        c, L, P = self.cfg, self.lib, lambda t: ctypes.c_void_p(t.data_ptr())
+        R, I, H, E = c.T * c.k, c.I, c.H, c.E
+        st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        hq, sh = torch.empty_like(self.hq), torch.empty_like(self.sh)
+
+        def call():
+            rc = L.wq_grouped_gemm_w8a8_silu_quant_f16codes(
+                P(self.A), P(self.sa), P(self.W13), P(self.S13), P(self.offsets), E, R, I, H,
+                SCHEME[c.scheme], P(hq), P(sh), P(self.gws), self.gws_n, P(self.status), st)
+            if rc != 0:
+                raise RuntimeError(f"fused gemm1 failed: {rc}")
+        call()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        same = bool(torch.equal(hq.view(torch.int16), self.hq.view(torch.int16))
+                    and torch.equal(sh, self.sh))
+        if not same:
+            raise RuntimeError("fused gemm1 codes differ from the staged ones")
+        return {"ms": e0.elapsed_time(e1) / steps, "bit_exact_vs_staged": same,
+                "replaces": "stages gemm1 + silu_mul_quant"}
 
 
 def make_weights(wq, cfg, dev):
@@ -727,6 +758,7 @@ def run_layer(args, cfg):
         staged_ms = start.elapsed_time(end) / args.steps
     stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]))
                 for j, s in enumerate(Layer.STAGES)}
+    fused = layer.time_fused(args.steps) if cfg.scheme == "block" and layer.f16 else None
     for st in (layer.status, fst):
         if int(st.item()) != 0:
             raise RuntimeError(f"device status {int(st.item())}")
@@ -776,6 +808,7 @@ def run_layer(args, cfg):
                              "activations are streamed every step",
                        "parallelism": "single"},
             "tokens_per_s": tok_s, "stages_ms": stage_ms, "staged_ms_per_step": staged_ms,
+            "fused_gemm1_silu_quant": fused,
             "gpu_launches": launches,
             "roofline": roofline,
             "roofline_gemm2": roof2,

@@ -247,6 +247,35 @@ WQ_API int wq_grouped_gemm_w8a8_f16codes(const uint16_t *A16, const int32_t *a_n
                                          void *ws, size_t ws_bytes, int32_t *status,
                                          wq_stream_t stream);
 
+/* Fused gate_up GEMM -> SiLU-and-mul -> re-quantization, block-wise scheme
+ * ("[Feature] DeepSeek V3/R1 INT8 Quantization (channel-wise)", Performance:
+ * the accumulator and epilogue cost set the throughput; Meituan INT8 DeepSeek
+ * R1 article, 量化技术的探索: activations quantized per token per 128-group,
+ * weights per [128,128] block).  A16 fp16 codes [R][K] with sa [R][K/128],
+ * W13 int8 [E][2I][K] (gate rows [0, I), up rows [I, 2I)) with sw13
+ * [E][2I/128][K/128], segments from offsets [E+1].  The result is exactly
+ *   wq_silu_mul_quant_f16(gu, R, I, 128, ...) of
+ *   gu = wq_grouped_gemm_w8a8_f16codes(..., N = 2I, WQ_SCHEME_BLOCK, bf16 out)
+ * (gate and up rounded to bf16 before SiLU), written as hq16 fp16 codes
+ * [R][I] and sh float [R][I/128]; gu itself never reaches memory.  Each
+ * 128-column group of h depends on one gate and one up weight block only, so
+ * the two CTAs of a pair compute the matching blocks and finish the group.
+ * scheme must be WQ_SCHEME_BLOCK: the channel scheme re-quantizes h with one
+ * scale per whole row of I columns, which no single tile sees
+ * (WQ_ERR_UNSUPPORTED).
+ * Requirements: I % 128 == 0, K % 128 == 0, K <= 65536, 16-byte aligned
+ * A16, W13 and hq16.  Workspace: wq_grouped_gemm_silu_quant_workspace_size(R, E)
+ * bytes (the grouped GEMM's plus a silu table).
+ * hq16 and sh rows outside every segment are not written. */
+WQ_API size_t wq_grouped_gemm_silu_quant_workspace_size(int64_t R, int E);
+WQ_API int wq_grouped_gemm_w8a8_silu_quant_f16codes(const uint16_t *A16, const float *sa,
+                                                    const int8_t *W13, const float *sw13,
+                                                    const int32_t *offsets, int E, int64_t R,
+                                                    int64_t I, int64_t K, int scheme,
+                                                    uint16_t *hq16, float *sh, void *ws,
+                                                    size_t ws_bytes, int32_t *status,
+                                                    wq_stream_t stream);
+
 /* Per-token quantization into fp16 codes with row norms (the rule of
  * wq_quantize_per_token, Meituan INT8 DeepSeek R1 article, 量化技术的探索:
  * online per-token activation quantization): codes as fp16 bits q16 [T][K]

@@ -488,6 +488,53 @@ def test_grouped_gemm_f16codes_block(K):
                       "f16 codes block gemm")
 
 
+@pytest.mark.parametrize("K,I", [(384, 256), (2048, 384)])
+def test_grouped_gemm_silu_quant_block(K, I):
+    """GEMM1 with SiLU-and-mul and the per-128-group re-quantization in its
+    epilogue (block scheme; the gate and up blocks of one 128-column group on
+    the two CTAs of a pair, which trade halves of their token columns).  fp16
+    codes and group scales bit-exact against the oracle's block GEMM followed
+    by its SiLU-and-mul-quant; segments around the 160-token tile and its
+    80- and 40-column splits; rows past the last segment stay untouched."""
+    counts = [3, 0, 160, 1, 161, 330, 16, 17, 159, 41, 79]
+    E = len(counts)
+    rng = np.random.default_rng(31 + K + I)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    R = int(offs[-1])
+    Rt = R + 5
+    A = rng.integers(-127, 128, (Rt, K), dtype=np.int8)
+    W = rng.integers(-127, 128, (E, 2 * I, K), dtype=np.int8)
+    A[:3] = 127
+    W[2, :I] = -127  # saturated gate block: silu of large negatives
+    sa = (rng.random((Rt, K // 128)) * 0.05).astype(np.float32)
+    sw = (rng.random((E, 2 * I // 128, K // 128)) * 1e-3).astype(np.float32)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    st = wq.new_status()
+    hq16 = torch.full((Rt, I), 7.0, dtype=torch.float16, device=DEV)
+    sh = torch.full((Rt, I // 128), -1.0, dtype=torch.float32, device=DEV)
+    wq.grouped_gemm_w8a8_silu_quant_f16codes(t(A).to(torch.float16), t(sa), t(W), t(sw), t(offs),
+                                             hq16=hq16, sh=sh, status=st)
+    assert int(st.item()) == 0
+    gu = O.grouped_gemm_w8a8(A[:R], sa[:R], W, sw, offs, "block", "f32")
+    hqo, sho = O.silu_mul_quant(gu, I, 128)
+    got = np_(hq16)
+    assert np.array_equal(got[:R].astype(np.int32), hqo.astype(np.int32))
+    assert np.array_equal(np_(sh)[:R], sho.reshape(R, I // 128))
+    assert np.all(got[R:] == 7.0) and np.all(np_(sh)[R:] == -1.0)
+
+
+def test_grouped_gemm_silu_quant_channel_refused():
+    """The channel scheme needs each row's maximum over all I columns, which
+    no tile of the fused epilogue sees: the entry refuses it."""
+    K, I, E = 256, 256, 1
+    A16 = torch.zeros(4, K, dtype=torch.float16, device=DEV)
+    W = torch.zeros(E, 2 * I, K, dtype=torch.int8, device=DEV)
+    with pytest.raises(wq.WQError):
+        wq.grouped_gemm_w8a8_silu_quant_f16codes(
+            A16, torch.ones(4, device=DEV), W, torch.ones(E, 2 * I, device=DEV),
+            torch.tensor([0, 4], dtype=torch.int32, device=DEV), scheme="channel")
+
+
 @pytest.mark.parametrize("K,counts", [
     (512, [3, 0, 270, 1, 513]),    # K < 1024: shared-memory-weights pair engine
     (2048, [3, 0, 270, 1, 513]),   # tensor-memory weights, 320-token items with

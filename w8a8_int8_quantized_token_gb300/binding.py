@@ -51,6 +51,8 @@ _SIGS = {
     "wq_silu_mul_quant_f16": (_I, [_P, _L, _L, _I, _P, _P, _P, _P]),
     "wq_grouped_gemm_w8a8_f16codes": (_I, [_P, _P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
     "wq_quantize_per_token_f16": (_I, [_P, _L, _L, _L, _P, _P, _P, _P]),
+    "wq_grouped_gemm_silu_quant_workspace_size": (_S, [_L, _I]),
+    "wq_grouped_gemm_w8a8_silu_quant_f16codes": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _P, _P, _P, _S, _P, _P]),
     "wq_grouped_gemm_masked_workspace_size": (_S, [_I, _I]),
     "wq_grouped_gemm_w8a8_masked": (_I, [_P, _P, _P, _I, _I, _P, _P, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
     "wq_silu_mul_quant": (_I, [_P, _L, _L, _I, _P, _P, _P]),
@@ -286,6 +288,33 @@ def grouped_gemm_w8a8_f16codes(A16, a_norm2, sa, W, sw, offsets, acc="i32", out_
                                                _ptr(ws), nws, _ptr(st), _stream()),
            "wq_grouped_gemm_w8a8_f16codes")
     return out
+
+
+def grouped_gemm_w8a8_silu_quant_f16codes(A16, sa, W13, sw13, offsets, hq16=None, sh=None,
+                                           status=None, scheme="block", ws=None):
+    """Fused gate_up GEMM -> SiLU-and-mul -> per-128-group re-quantization
+    (block scheme): (hq16 fp16 codes [R, I], sh [R, I/128])."""
+    _dev(A16, torch.float16, "A16")
+    _dev(sa, torch.float32, "sa")
+    _dev(W13, torch.int8, "W13")
+    _dev(sw13, torch.float32, "sw13")
+    _dev(offsets, torch.int32, "offsets")
+    R, K = A16.shape
+    E, N2, _ = W13.shape
+    I = N2 // 2
+    if hq16 is None:
+        hq16 = torch.empty(R, I, dtype=torch.float16, device=A16.device)
+    if sh is None:
+        sh = torch.empty(R, max(I // 128, 1), dtype=torch.float32, device=A16.device)
+    nws = lib().wq_grouped_gemm_silu_quant_workspace_size(R, E)
+    if ws is None:
+        ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=A16.device)
+    st = status if status is not None else new_status(A16.device)
+    _check(lib().wq_grouped_gemm_w8a8_silu_quant_f16codes(
+        _ptr(A16), _ptr(sa), _ptr(W13), _ptr(sw13), _ptr(offsets), E, R, I, K, SCHEME[scheme],
+        _ptr(hq16), _ptr(sh), _ptr(ws), nws, _ptr(st), _stream()),
+        "wq_grouped_gemm_w8a8_silu_quant_f16codes")
+    return hq16, sh
 
 
 def quantize_per_token_f16(x):

@@ -104,10 +104,11 @@ struct GemmWs {
   Tile *t64, *t128, *t256, *tsm;
   int32_t *n64, *n128, *n256, *nsm, *redo;
   int64_t m64, m128, m256, msm;
+  float *silu;  // silu_tab entries for the fused GEMM1 epilogue, or nullptr
   size_t bytes;
 };
 
-GemmWs carve_gemm_ws(void *ws, int64_t R, int E, int Mmax, bool masked) {
+GemmWs carve_gemm_ws(void *ws, int64_t R, int E, int Mmax, bool masked, bool silu = false) {
   GemmWs w;
   Carver c(ws);
   w.m64 = gemm_max_tiles(R, E, Mmax, masked, 64);
@@ -123,17 +124,18 @@ GemmWs carve_gemm_ws(void *ws, int64_t R, int E, int Mmax, bool masked) {
   w.tsm = c.take<Tile>(size_t(w.msm));
   w.nsm = c.take<int32_t>(1);
   w.redo = c.take<int32_t>(1);
+  w.silu = silu ? c.take<float>(silu_tab::kSize) : nullptr;
   w.bytes = c.used;
   return w;
 }
 
-size_t gemm_ws_bytes(int64_t R, int E, int Mmax, bool masked) {
-  return carve_gemm_ws(nullptr, R, E, Mmax, masked).bytes;
+size_t gemm_ws_bytes(int64_t R, int E, int Mmax, bool masked, bool silu) {
+  return carve_gemm_ws(nullptr, R, E, Mmax, masked, silu).bytes;
 }
 
 int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
   const bool masked = a.masked_m != nullptr;
-  GemmWs w = carve_gemm_ws(a.ws, a.R, a.E, a.Mmax, masked);
+  GemmWs w = carve_gemm_ws(a.ws, a.R, a.E, a.Mmax, masked, a.fused_hq16 != nullptr);
   const int32_t *gate = nullptr;
   if (a.A16 != nullptr && a.scheme == WQ_SCHEME_BLOCK) {
     // block-wise on fp16 codes: every K block's sum is exact in float32, so
@@ -141,7 +143,12 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
     if (!gemm_tc6_supported(a)) return WQ_ERR_UNSUPPORTED;
     WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, gemm_tc6_tile_rows(), a.R,
                               w.t128, w.n128, nullptr, st));
-    return launch_gemm_tc6(a, w.t128, w.n128, int(w.m128), st);
+    if (a.fused_hq16 == nullptr) return launch_gemm_tc6(a, w.t128, w.n128, int(w.m128), st);
+    // the fused epilogue looks silu up in a table of the workspace
+    WQ_TRY(launch_silu_table(w.silu, st));
+    GemmArgs f = a;
+    f.fused_silu_tab = w.silu;
+    return launch_gemm_tc6(f, w.t128, w.n128, int(w.m128), st);
   }
   if (a.A16 != nullptr && a.A != nullptr) {
     // both forms given (the masked layer's widened rows): remainders of at
@@ -416,6 +423,32 @@ int wq_grouped_gemm_w8a8_f16codes(const uint16_t *A16, const int32_t *a_norm2, c
   return launch_grouped_gemm(a, stream);
 }
 
+size_t wq_grouped_gemm_silu_quant_workspace_size(int64_t R, int E) {
+  if (R < 0 || E < 1) return 0;
+  return gemm_ws_bytes(R, E, 0, false, true);
+}
+
+int wq_grouped_gemm_w8a8_silu_quant_f16codes(const uint16_t *A16, const float *sa, const int8_t *W13,
+                                             const float *sw13, const int32_t *offsets, int E,
+                                             int64_t R, int64_t I, int64_t K, int scheme,
+                                             uint16_t *hq16, float *sh, void *ws, size_t ws_bytes,
+                                             int32_t *status, wq_stream_t stream) {
+  if (R < 0 || E > 4096 || I <= 0) return WQ_ERR_INVALID_ARG;
+  if (scheme == WQ_SCHEME_CHANNEL) return WQ_ERR_UNSUPPORTED;  // needs the whole row's maximum
+  if (R == 0) return WQ_OK;
+  WQ_TRY(check_gemm_common(W13, sw13, E, 2 * I, K, scheme, WQ_ACC_F32, WQ_OUT_BF16, hq16));
+  if (!A16 || !sa || !offsets || !sh) return WQ_ERR_INVALID_ARG;
+  if (!al16(A16) || I % 128 || K > 65536) return WQ_ERR_UNSUPPORTED;
+  if (R >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;
+  if (ws_bytes < gemm_ws_bytes(R, E, 0, false, true) || !ws) return WQ_ERR_WORKSPACE;
+  WQ_TRY(check_device());
+  GemmArgs a{nullptr, A16, nullptr, sa, W13, sw13, offsets, nullptr, 0, E, R, 2 * I, K, scheme,
+             WQ_ACC_F32, WQ_OUT_BF16, nullptr, ws, status};
+  a.fused_hq16 = hq16;
+  a.fused_sh = sh;
+  return launch_grouped_gemm(a, stream);
+}
+
 int wq_quantize_per_token_f16(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, uint16_t *q16,
                               float *s, int32_t *norm2, wq_stream_t stream) {
   if (T < 0 || K < 0 || ldx < K) return WQ_ERR_INVALID_ARG;
@@ -560,6 +593,9 @@ int run_forward(const uint16_t *x, const float *logits, const int8_t *W13, const
                               b.anorm, st));
     GemmArgs f1{nullptr, A16, b.anorm, b.sa, W13, sw13, b.offsets, nullptr, 0, E, R,
                 int64_t(2) * I, H, scheme, acc, WQ_OUT_BF16, b.gu, b.gemm_ws, status};
+    // (the block scheme's fused gate_up -> SiLU-and-mul -> re-quantization
+    // entry computes the same codes; on the converter-bound block engine its
+    // epilogue costs more than this separate memory-bound pass)
     WQ_TRY(launch_grouped_gemm(f1, st));
     WQ_TRY(launch_silu_mul_quant_f16(b.gu, R, I, blk ? 128 : 0, nullptr, 0, hq16, b.sh, b.hnorm,
                                      st));

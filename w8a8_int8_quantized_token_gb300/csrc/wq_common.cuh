@@ -77,6 +77,38 @@ __device__ __forceinline__ float silu(float g) {
   return __fdiv_rn(g, __fadd_rn(1.0f, exp_cw(-g)));
 }
 
+// silu(g) of every bf16 g whose magnitude lies in [2^-24, 17) (g > 0) or
+// [2^-24, 89) (g < 0), each entry computed with silu() itself, so a lookup
+// returns exactly what the formula returns; any other g (smaller, larger,
+// non-finite) takes the formula directly.  Outside those ranges silu is
+// trivial anyway (g / 2, g, or -0), and a GEMM output rarely lands there.
+namespace silu_tab {
+constexpr uint32_t kLo = 0x3380u;        // bf16 bits of 2^-24
+constexpr uint32_t kPosHi = 0x4188u;     // bf16 bits of 17
+constexpr uint32_t kNegHi = 0x42B2u;     // bf16 bits of 89
+constexpr int kPos = int(kPosHi - kLo);  // entries for g > 0
+constexpr int kNeg = int(kNegHi - kLo);  // entries for g < 0
+constexpr int kSize = kPos + kNeg;
+constexpr int kBytes = kSize * 4;
+}  // namespace silu_tab
+
+// entries [i0, kSize) with stride `step` of the table
+__device__ __forceinline__ void silu_table_fill(float *tab, int i0, int step) {
+  using namespace silu_tab;
+  for (int i = i0; i < kSize; i += step) {
+    const uint32_t b = i < kPos ? kLo + uint32_t(i) : (0x8000u | (kLo + uint32_t(i - kPos)));
+    tab[i] = silu(bf16_to_f(uint16_t(b)));
+  }
+}
+
+// Table index of the bf16 pattern b, or -1 when b lies outside the table
+__device__ __forceinline__ int silu_index(uint32_t b) {
+  using namespace silu_tab;
+  const bool neg = (b & 0x8000u) != 0;
+  const uint32_t k = (b & 0x7fffu) - kLo;  // wraps (large) below 2^-24
+  return k < (neg ? uint32_t(kNeg) : uint32_t(kPos)) ? int(neg ? k + uint32_t(kPos) : k) : -1;
+}
+
 // Quantization scale from an absolute maximum: max(a, 1e-10) / 127.
 __device__ __forceinline__ float quant_scale(float amax) {
   return __fdiv_rn(fmaxf(amax, 1e-10f), 127.0f);
@@ -183,6 +215,8 @@ int launch_widen_masked(const int8_t *a, int64_t K, const int32_t *masked_m, int
 int launch_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, int group,
                               const int32_t *masked_m, int Mmax, uint16_t *hq16, float *sh,
                               int32_t *norm2, cudaStream_t st);
+// silu_tab's entries into tab (silu_tab::kSize floats, global memory)
+int launch_silu_table(float *tab, cudaStream_t st);
 int launch_combine(const uint16_t *y, const int32_t *pair_to_row, const float *w, int T, int k,
                    int64_t H, uint16_t *out, cudaStream_t st);
 
@@ -205,6 +239,11 @@ struct GemmArgs {
   void *out;
   void *ws;
   int32_t *status;
+  // block scheme, N = 2I gate_up weights: write SiLU-and-mul re-quantized
+  // fp16 codes [R][I] and group scales [R][I/128] instead of `out`
+  uint16_t *fused_hq16 = nullptr;
+  float *fused_sh = nullptr;
+  const float *fused_silu_tab = nullptr;  // silu_tab entries (set by the dispatcher)
 };
 // The single-pass float32 engines serve both channel-wise accumulator modes.
 // In the float32 mode the accumulator is the running sum, over 128-wide K
@@ -222,6 +261,6 @@ int launch_build_tiles(const int32_t *offsets, const int32_t *masked_m, int Mmax
                        int64_t R, Tile *tiles, int32_t *ntiles, int32_t *zero_word,
                        cudaStream_t st, int small_max = 0, Tile *small = nullptr,
                        int32_t *nsmall = nullptr);
-size_t gemm_ws_bytes(int64_t R, int E, int Mmax, bool masked);
+size_t gemm_ws_bytes(int64_t R, int E, int Mmax, bool masked, bool silu = false);
 int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st);
 }  // namespace wq

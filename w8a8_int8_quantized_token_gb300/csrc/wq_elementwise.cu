@@ -683,44 +683,23 @@ __global__ void __launch_bounds__(1024) silu_mul_quant_f16_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// The silu table in global memory (the fused GEMM1 epilogue reads it).
+__global__ void __launch_bounds__(256) silu_table_kernel(float *__restrict__ tab) {
+  silu_table_fill(tab, int(blockIdx.x * blockDim.x + threadIdx.x), int(gridDim.x * blockDim.x));
+}
+
+int launch_silu_table(float *tab, cudaStream_t st) {
+  silu_table_kernel<<<unsigned((silu_tab::kSize + 255) / 256), 256, 0, st>>>(tab);
+  return launched(1);
+}
+
 // SiLU-and-mul + re-quantization, table form (rows of at most 2048 outputs).
-// The gate value g is a bf16 number, so silu(g) takes one of finitely many
-// values.  Each CTA first tabulates silu(g) in shared memory for every bf16
-// g whose magnitude lies in [2^-24, 17) (g > 0) or [2^-24, 89) (g < 0),
-// computing each entry with silu() itself, so a lookup returns exactly what
-// the formula returns; any other g (smaller, larger, non-finite) takes the
-// formula directly.  Outside those ranges silu is trivial anyway (g / 2, g,
-// or -0), and a GEMM output rarely lands there, so the branch is almost
-// never taken.  Then one warp per row (persistent CTAs loop over rows):
+// Each CTA first tabulates silu(g) in shared memory (silu_tab: exact by
+// construction).  Then one warp per row (persistent CTAs loop over rows):
 // 8-element vectors v = i*32 + lane (each warp access is 512 contiguous
 // bytes), h = silu(g) * u, the row's or each group's absolute maximum by
 // xor shuffles, the codes (int8, or the same integers as fp16 with the
 // row's squared norm), the scale.
-namespace silu_tab {
-constexpr uint32_t kLo = 0x3380u;        // bf16 bits of 2^-24
-constexpr uint32_t kPosHi = 0x4188u;     // bf16 bits of 17
-constexpr uint32_t kNegHi = 0x42B2u;     // bf16 bits of 89
-constexpr int kPos = int(kPosHi - kLo);  // entries for g > 0
-constexpr int kNeg = int(kNegHi - kLo);  // entries for g < 0
-constexpr int kSize = kPos + kNeg;
-constexpr int kBytes = kSize * 4;
-}  // namespace silu_tab
-
-__device__ __forceinline__ void silu_table_fill(float *tab) {
-  using namespace silu_tab;
-  for (int i = threadIdx.x; i < kSize; i += blockDim.x) {
-    const uint32_t b = i < kPos ? kLo + uint32_t(i) : (0x8000u | (kLo + uint32_t(i - kPos)));
-    tab[i] = silu(bf16_to_f(uint16_t(b)));
-  }
-}
-
-// Table index of the bf16 pattern b, or -1 when b lies outside the table
-__device__ __forceinline__ int silu_index(uint32_t b) {
-  using namespace silu_tab;
-  const bool neg = (b & 0x8000u) != 0;
-  const uint32_t k = (b & 0x7fffu) - kLo;  // wraps (large) below 2^-24
-  return k < (neg ? uint32_t(kNeg) : uint32_t(kPos)) ? int(neg ? k + uint32_t(kPos) : k) : -1;
-}
 
 // silu of the eight bf16 gate values in w[0..3] (low half first): table
 // lookups (an out-of-table value reads entry 0 and is marked), then, only if
@@ -749,7 +728,7 @@ __global__ void __launch_bounds__(512, 1) silu_mul_quant_tab_kernel(
     const uint16_t *__restrict__ gu, int64_t R, int64_t I, const int32_t *__restrict__ masked_m,
     int Mmax, void *__restrict__ hq_out, float *__restrict__ sh, int32_t *__restrict__ norm2) {
   extern __shared__ float tab[];
-  silu_table_fill(tab);
+  silu_table_fill(tab, threadIdx.x, blockDim.x);
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int nvec = int(I >> 3);

@@ -43,30 +43,49 @@ namespace {
 using namespace tc;
 
 constexpr int WM = 128, TN = 160, BK = 64;
-constexpr int SW8 = 8, SW16 = 4, ST = 4;        // ring depths: int8 W, fp16 W, fp16 tokens
+constexpr int SW16 = 4, ST = 4;                 // ring depths: fp16 W, fp16 tokens
 static_assert(SW16 == ST, "a widened-weight slot is released with its token slot");
 constexpr int W8B = WM * BK, W16B = 2 * W8B;    // weight stage bytes
 constexpr int TB = TN * BK * 2;                 // token stage bytes (fp16)
 constexpr int NCH = 3;                          // chunk accumulators (tensor-memory columns [0, 3*TN))
 constexpr int EPI_COLS = TN / 2;                // token columns each epilogue warp owns
-constexpr int OFF_T = 0;
-constexpr int OFF_W16 = OFF_T + ST * TB;
-constexpr int OFF_W8 = OFF_W16 + SW16 * W16B;
 constexpr int NEPI = 8;                         // epilogue warps
-constexpr int OFF_SC = OFF_W8 + SW8 * W8B;      // float [NEPI][EPI_COLS] column scales
-constexpr int OFF_BAR = OFF_SC + NEPI * EPI_COLS * 4;
-constexpr int B_W8_FULL = 0, B_W8_EMPTY = SW8, B_W16_FULL = 2 * SW8,
-              B_T_FULL = 2 * SW8 + SW16, B_T_EMPTY = B_T_FULL + ST,
-              B_ACC_FULL = B_T_EMPTY + ST,  // [NCH]
-    B_ACC_EMPTY = B_ACC_FULL + NCH,         // [NCH]
-    B_MMA_DONE = B_ACC_FULL + 2 * NCH, NBAR = B_ACC_FULL + 2 * NCH + 1;
-constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
-constexpr int OFF_ABORT = OFF_TMEM + 4;
-constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
-static_assert(TB % 1024 == 0 && OFF_W16 % 1024 == 0 && OFF_W8 % 1024 == 0, "swizzle alignment");
+constexpr int KEEP = EPI_COLS / 2;              // fused: columns a thread finishes itself
+constexpr int XW = KEEP / 2;                    // fused: bf16 pairs a thread sends to the peer
+
+// Shared-memory plan.  The fused variant (SiLU-and-mul and re-quantization in
+// the epilogue) adds an exchange area that the peer CTA writes, the group
+// maxima of the four lane-quarter warps and their barriers, and gives up one
+// int8 weight stage to make room.
+template <bool FUSE>
+struct Plan {
+  static constexpr int SW8 = FUSE ? 7 : 8;      // int8 weight ring depth
+  static constexpr int OFF_T = 0;
+  static constexpr int OFF_W16 = OFF_T + ST * TB;
+  static constexpr int OFF_W8 = OFF_W16 + SW16 * W16B;
+  static constexpr int OFF_SC = OFF_W8 + SW8 * W8B;         // float [NEPI][EPI_COLS] column scales
+  static constexpr int OFF_XCH = OFF_SC + NEPI * EPI_COLS * 4;  // uint32 [NEPI][32][XW]
+  static constexpr int OFF_RED = OFF_XCH + (FUSE ? NEPI * 32 * XW * 4 : 0);  // float [2][2][4][KEEP]
+  static constexpr int OFF_BAR = OFF_RED + (FUSE ? 2 * 2 * 4 * KEEP * 4 : 0);
+  static constexpr int B_W8_FULL = 0, B_W8_EMPTY = SW8, B_W16_FULL = 2 * SW8,
+                       B_T_FULL = 2 * SW8 + SW16, B_T_EMPTY = B_T_FULL + ST,
+                       B_ACC_FULL = B_T_EMPTY + ST,  // [NCH]
+      B_ACC_EMPTY = B_ACC_FULL + NCH,                // [NCH]
+      B_MMA_DONE = B_ACC_FULL + 2 * NCH,
+                       B_XF = B_MMA_DONE + 1,        // fused: [NEPI] peer's half arrived
+      B_XE = B_XF + NEPI,                            // fused: [NEPI] peer has read our half
+      B_RED = B_XE + NEPI,                           // fused: [2 item parities][2 halves]
+      NBAR = FUSE ? B_RED + 4 : B_MMA_DONE + 1;
+  static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_ABORT = OFF_TMEM + 4;
+  static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
+  static_assert(TB % 1024 == 0 && OFF_W16 % 1024 == 0 && OFF_W8 % 1024 == 0, "swizzle alignment");
+  static_assert(OFF_XCH % 16 == 0 && OFF_BAR % 8 == 0, "exchange and barrier alignment");
+  static_assert(SMEM_BYTES <= 232448, "shared memory plan too large");
+};
 static_assert(NCH * TN <= 512, "tensor memory plan");
 static_assert(EPI_COLS % 16 == 0 && NEPI == 8, "each epilogue warp owns 16-column pieces");
-static_assert(SMEM_BYTES <= 232448, "shared memory plan too large");
+static_assert(XW % 4 == 0, "the exchange goes in 16-byte pieces");
 constexpr int NTHREADS = 480;
 constexpr int WARP_TOK = 14;            // token producer
 constexpr int GCONV = 128;              // threads of one converter group
@@ -86,11 +105,19 @@ __device__ __forceinline__ void mul_add2(float &r0, float &r1, float a0, float a
       : "f"(c0), "f"(c1), "f"(t0), "f"(t1));
 }
 
+template <bool FUSE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     gemm_tc6_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT8,
                     const __grid_constant__ CUtensorMap tmT32,
                     const __grid_constant__ CUtensorMap tmT80, const GemmArgs a,
                     const Tile *__restrict__ tiles, const int32_t *__restrict__ ntiles) {
+  using P = Plan<FUSE>;
+  constexpr int SW8 = P::SW8, OFF_T = P::OFF_T, OFF_W16 = P::OFF_W16, OFF_W8 = P::OFF_W8,
+                OFF_SC = P::OFF_SC, OFF_BAR = P::OFF_BAR, OFF_TMEM = P::OFF_TMEM,
+                OFF_ABORT = P::OFF_ABORT;
+  constexpr int B_W8_FULL = P::B_W8_FULL, B_W8_EMPTY = P::B_W8_EMPTY, B_W16_FULL = P::B_W16_FULL,
+                B_T_FULL = P::B_T_FULL, B_T_EMPTY = P::B_T_EMPTY, B_ACC_FULL = P::B_ACC_FULL,
+                B_ACC_EMPTY = P::B_ACC_EMPTY, B_MMA_DONE = P::B_MMA_DONE;
   extern __shared__ uint8_t smem_raw[];
   const int NBP = int(a.N / (2 * WM));  // pairs of 128-row weight blocks
   const int items = ntiles[0] * NBP;
@@ -126,6 +153,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(B_ACC_EMPTY + b), NEPI);
     }
     mbar_init(bar(B_MMA_DONE), 1);
+    if constexpr (FUSE) {
+      for (int w = 0; w < NEPI; ++w) {
+        mbar_init(bar(P::B_XF + w), 1);  // one elected lane of the peer's warp
+        mbar_init(bar(P::B_XE + w), 1);
+      }
+      for (int i = 0; i < 4; ++i) mbar_init(bar(P::B_RED + i), 4);  // the four lane quarters
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
@@ -140,6 +174,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     set_status(a.status, WQ_ERR_TIMEOUT);
   };
   auto nmma_of = [](int rows) { return (rows + 15) & ~15; };
+  // this CTA's 128-row weight block of item ip: adjacent blocks per pair, or
+  // (fused) gate block p on rank 0 and the matching up block NBP + p on rank 1
+  auto wblock = [&](int ip) {
+    return FUSE ? ip % NBP + int(rank) * NBP : (ip % NBP) * 2 + int(rank);
+  };
   // token rows each CTA of the pair loads for an MMA of width nmma
   auto box_of = [](int nmma) { return nmma <= 16 ? 8 : (nmma <= 64 ? 32 : 80); };
 
@@ -150,7 +189,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       bool ok = true;
       for (int ip = pair; ip < items && ok; ip += npairs) {
         const Tile tl = tiles[ip / NBP];
-        const int wb = (ip % NBP) * 2 + int(rank);
+        const int wb = wblock(ip);
         const int wrow = int(int64_t(tl.expert) * a.N + int64_t(wb) * WM);
         for (int i = 0; i < KT; ++i, ++g) {
           const int sw = g % SW8;
@@ -291,11 +330,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     float *scal = reinterpret_cast<float *>(sm + OFF_SC) + (warp - 6) * EPI_COLS;
     const uint32_t tq = tmem + (uint32_t(q * 32) << 16);
     constexpr int NSC = (EPI_COLS + 31) / 32;  // owned columns per lane when staging scales
-    int gk = 0;
+    int gk = 0, it = 0;  // K blocks and items so far
     bool ok = true;
-    for (int ip = pair; ip < items && ok; ip += npairs) {
+    for (int ip = pair; ip < items && ok; ip += npairs, ++it) {
       const Tile tl = tiles[ip / NBP];
-      const int wb = (ip % NBP) * 2 + int(rank);  // this CTA's weight block = scale block row
+      const int wb = wblock(ip);  // this CTA's weight block = scale block row
       const int64_t n = int64_t(wb) * WM + q * 32 + lane;  // this thread's output channel
       const float *swp = a.sw + (int64_t(tl.expert) * (a.N / 128) + wb) * KB;
       // token scales of the owned columns, loaded one K block ahead
@@ -351,11 +390,155 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         if (lane == 0) mbar_arrive(bar(B_ACC_EMPTY + b));
       }
       if (!ok) break;
-      // after the last K block: bf16 out for the owned columns inside the tile
-      uint16_t *o = static_cast<uint16_t *>(a.out) + (int64_t(tl.row0) + c0) * a.N + n;
+      if constexpr (!FUSE) {
+        // after the last K block: bf16 out for the owned columns inside the tile
+        uint16_t *o = static_cast<uint16_t *>(a.out) + (int64_t(tl.row0) + c0) * a.N + n;
 #pragma unroll
-      for (int j = 0; j < EPI_COLS; ++j)
-        if (c0 + j < tl.rows) o[int64_t(j) * a.N] = f_to_bf16(acc[j]);
+        for (int j = 0; j < EPI_COLS; ++j)
+          if (c0 + j < tl.rows) o[int64_t(j) * a.N] = f_to_bf16(acc[j]);
+      } else {
+        // SiLU-and-mul and re-quantization of h column p*128 + q*32 + lane.
+        // This thread holds the gate (rank 0) or up (rank 1) value of that
+        // column for the owned tokens, rounded to bf16 exactly as the GEMM's
+        // output; the peer thread at the same position holds the partner.
+        // This CTA finishes tokens [rank*KEEP, rank*KEEP + KEEP) of the owned
+        // columns and sends the other half to the peer.
+        const int ew = warp - 6;
+        const uint32_t peer = rank ^ 1u;
+        const uint32_t xoff = uint32_t(P::OFF_XCH + (ew * 32 + lane) * XW * 4);
+        const int col0 = c0 + int(rank) * KEEP;  // first kept token column of the tile
+        // the peer has read what this warp sent for the previous item
+        ok = mbar_wait_cluster(bar(P::B_XE + ew), (it & 1) ^ 1, abort_flag);
+        if (ok) {
+          const uint32_t dst = mapa(base + xoff, peer);
+#pragma unroll
+          for (int j = 0; j < XW; j += 4) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int c = 2 * (j + i);
+              w4[i] = rank ? pack_bf16x2(acc[c], acc[c + 1]) : pack_bf16x2(acc[KEEP + c], acc[KEEP + c + 1]);
+            }
+            st_cluster_v4(dst + 4u * j, w4[0], w4[1], w4[2], w4[3]);
+          }
+          __syncwarp();  // every lane's copy before the one release below
+          if (lane == 0) mbar_arrive_cluster(mapa(bar(P::B_XF + ew), peer));
+        }
+        uint32_t own[XW];
+#pragma unroll
+        for (int j = 0; j < XW; ++j)
+          own[j] = rank ? pack_bf16x2(acc[KEEP + 2 * j], acc[KEEP + 2 * j + 1])
+                        : pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
+        uint32_t oth[XW];
+        ok = ok && mbar_wait_cluster(bar(P::B_XF + ew), it & 1, abort_flag);
+        if (ok) {
+          const uint4 *src = reinterpret_cast<const uint4 *>(sm + xoff);
+#pragma unroll
+          for (int j = 0; j < XW / 4; ++j) {
+            const uint4 v4 = src[j];
+            oth[4 * j] = v4.x, oth[4 * j + 1] = v4.y, oth[4 * j + 2] = v4.z, oth[4 * j + 3] = v4.w;
+          }
+          __syncwarp();  // every lane's read before the release
+          if (lane == 0) mbar_arrive_cluster(mapa(bar(P::B_XE + ew), peer));  // the peer may send again
+        } else {
+#pragma unroll
+          for (int j = 0; j < XW; ++j) oth[j] = 0u;
+        }
+        // silu(g) of the kept tokens from the table (exact by construction);
+        // misses (out-of-table gates of tokens inside the tile; the columns
+        // past the tile's rows hold zeros) take the formula afterwards
+        float hv[KEEP];
+        uint64_t miss = 0;
+#pragma unroll
+        for (int jj = 0; jj < KEEP; ++jj) {
+          const uint32_t g2 = rank ? oth[jj >> 1] : own[jj >> 1];
+          const int idx = silu_index((jj & 1) ? g2 >> 16 : g2 & 0xffffu);
+          miss |= uint64_t(idx < 0 && col0 + jj < tl.rows) << jj;
+          hv[jj] = __ldg(a.fused_silu_tab + (idx < 0 ? 0 : idx));
+        }
+        if (__any_sync(0xffffffffu, miss != 0)) {
+#pragma unroll
+          for (int jj = 0; jj < KEEP; ++jj) {
+            const uint32_t g2 = rank ? oth[jj >> 1] : own[jj >> 1];
+            if (miss >> jj & 1u) hv[jj] = silu((jj & 1) ? bf16_hi(g2) : bf16_lo(g2));
+          }
+        }
+        // h = silu(g) * u, each product rounded once
+#pragma unroll
+        for (int jj = 0; jj < KEEP; ++jj) {
+          const uint32_t u2 = rank ? own[jj >> 1] : oth[jj >> 1];
+          hv[jj] = __fmul_rn(hv[jj], (jj & 1) ? bf16_hi(u2) : bf16_lo(u2));
+        }
+        // each token's maximum |h| over the 128 columns of group p: this
+        // warp's 32 lanes (tokens 0..31 by a reduce-scatter that leaves token
+        // jj's maximum in lane jj, tokens 32.. by full reductions), then the
+        // four lane quarters through shared memory
+        const int par = it & 1;
+        float *red = reinterpret_cast<float *>(sm + P::OFF_RED) + (par * 2 + h) * 4 * KEEP;
+        if (ok) {
+          float m[32];
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) m[jj] = fabsf(hv[jj]);
+#pragma unroll
+          for (int w = 16; w >= 1; w >>= 1) {
+            const bool up = (lane & w) != 0;  // this lane keeps the upper half
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+              const float send = up ? m[i] : m[i + w];
+              const float keep = up ? m[i + w] : m[i];
+              m[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, w));
+            }
+          }
+          red[q * KEEP + lane] = m[0];
+#pragma unroll
+          for (int jj = 32; jj < KEEP; ++jj) {
+            const float mx = warp_max(fabsf(hv[jj]));
+            if (lane == jj - 32) red[q * KEEP + jj] = mx;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(P::B_RED + par * 2 + h));
+        }
+        ok = ok && mbar_wait(bar(P::B_RED + par * 2 + h), (it >> 1) & 1, abort_flag);
+        if (!ok) {
+          fail();
+          break;
+        }
+        float scl[2], rsl[2];  // scales of kept tokens lane and lane + 32
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const int jj = lane + 32 * m;
+          scl[m] = 1.0f, rsl[m] = 1.0f;
+          if (jj < KEEP) {
+            const float am = fmaxf(fmaxf(red[jj], red[KEEP + jj]),
+                                   fmaxf(red[2 * KEEP + jj], red[3 * KEEP + jj]));
+            scl[m] = quant_scale(am);
+            rsl[m] = __frcp_rn(scl[m]);
+          }
+        }
+        const int64_t I = a.N / 2;
+        const int p = ip % NBP;
+        uint16_t *o16 = a.fused_hq16 + (int64_t(tl.row0) + col0) * I + int64_t(p) * WM + q * 32 + lane;
+#pragma unroll
+        for (int jj = 0; jj < KEEP; jj += 2) {
+          const float sc0 = __shfl_sync(0xffffffffu, scl[jj >> 5], jj & 31);
+          const float rs0 = __shfl_sync(0xffffffffu, rsl[jj >> 5], jj & 31);
+          const float sc1 = __shfl_sync(0xffffffffu, scl[(jj + 1) >> 5], (jj + 1) & 31);
+          const float rs1 = __shfl_sync(0xffffffffu, rsl[(jj + 1) >> 5], (jj + 1) & 31);
+          const uint32_t b = __byte_perm(quant_bits(hv[jj], sc0, rs0), quant_bits(hv[jj + 1], sc1, rs1), 0x0040);
+          uint32_t f01, f23;  // the two codes as fp16 values (exact)
+          s8x4_to_f16x4(b, f01, f23);
+          if (col0 + jj < tl.rows) o16[int64_t(jj) * I] = uint16_t(f01);
+          if (col0 + jj + 1 < tl.rows) o16[int64_t(jj + 1) * I] = uint16_t(f01 >> 16);
+        }
+        if (q == 0) {
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            const int jj = lane + 32 * m;
+            if (jj < KEEP && col0 + jj < tl.rows)
+              a.fused_sh[(int64_t(tl.row0) + col0 + jj) * (I / WM) + p] = scl[m];
+          }
+        }
+      }
     }
   }
 
@@ -379,10 +562,11 @@ bool gemm_tc6_supported(const GemmArgs &a) {
 
 int gemm_tc6_tile_rows() { return TN; }
 
-// `tiles` holds token tiles of at most TN rows.
-int launch_gemm_tc6(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
-                    cudaStream_t st) {
-  if (max_tiles <= 0) return WQ_OK;
+namespace {
+template <bool FUSE>
+int launch_tc6(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
+               cudaStream_t st) {
+  constexpr int SMEM_BYTES = Plan<FUSE>::SMEM_BYTES;
   CUtensorMap mW, m8, m32, m80;
   if (!make_tma_2d_u8(&mW, a.W, int64_t(a.E) * a.N, a.K, BK, WM) ||
       !make_tma_2d_b16_sw128(&m8, a.A16, a.R, a.K, 8) ||
@@ -392,7 +576,7 @@ int launch_gemm_tc6(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles,
   static bool attr = false;
   static int pairs_resident = 0;
   if (!attr) {
-    if (cudaFuncSetAttribute(gemm_tc6_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gemm_tc6_kernel<FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES) != cudaSuccess)
       return WQ_ERR_LAUNCH;
     // a persistent grid must be fully co-resident: ask how many 2-CTA
@@ -402,7 +586,7 @@ int launch_gemm_tc6(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles,
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc6_kernel, &cfg) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc6_kernel<FUSE>, &cfg) != cudaSuccess || n < 1) {
       cudaGetLastError();
       n = num_sms() / 2;
     }
@@ -411,8 +595,23 @@ int launch_gemm_tc6(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles,
   }
   const int64_t max_items = int64_t(max_tiles) * (a.N / (2 * WM));
   const int pairs = int(max_items < pairs_resident ? max_items : pairs_resident);
-  gemm_tc6_kernel<<<2 * pairs, NTHREADS, SMEM_BYTES, st>>>(mW, m8, m32, m80, a, tiles, ntiles);
+  gemm_tc6_kernel<FUSE><<<2 * pairs, NTHREADS, SMEM_BYTES, st>>>(mW, m8, m32, m80, a, tiles,
+                                                                 ntiles);
   return launched(1);
+}
+}  // namespace
+
+// `tiles` holds token tiles of at most TN rows.  With a.fused_hq16 set the
+// kernel writes SiLU-and-mul re-quantized fp16 codes and group scales
+// instead of a.out.
+int launch_gemm_tc6(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
+                    cudaStream_t st) {
+  if (max_tiles <= 0) return WQ_OK;
+  if (a.fused_hq16 != nullptr) {
+    if (a.fused_sh == nullptr || a.N % (2 * WM) != 0) return WQ_ERR_INVALID_ARG;
+    return launch_tc6<true>(a, tiles, ntiles, max_tiles, st);
+  }
+  return launch_tc6<false>(a, tiles, ntiles, max_tiles, st);
 }
 
 }  // namespace wq
