@@ -55,8 +55,8 @@ def layer_ops(T, H, I, k):
 # holds only for the kernel source it was measured on: it is reported while
 # that file's SHA-256 matches, else the traffic is null.
 _TC5 = {"kernel": "gemm_tc5_kernel", "file": "wq_gemm_tc5.cu",
-        "sha256": "0371ec48d23b80f7e62d1618579bb7c963acd55212b87399377995b7a4a796b1",
-        "bytes": 8 * (1.077663e9 + 62.478848e6),
+        "sha256": "db9e099160b6b7e5446c806d9ae2b61a365f1a677f44434f7a38d0609c271633",
+        "bytes": 8 * (1.078574e9 + 63.97824e6),
         "how": "ncu capture of GEMM1 at 1024 tokens / 32 experts (same 256 rows per expert), "
                "dram read+write scaled by the expert count (x 8)"}
 TRAFFIC = {
@@ -497,7 +497,10 @@ def run_masked(args, cfg):
     peaks, src = load_peaks()
     touched = int((mm > 0).sum())
     roofline = gemm_roofline(peaks, src, clocks, g1_ms, rows, touched, 2 * I, H, cfg.scheme, 1,
-                             measured_traffic(cfg.name), "grouped_gemm_w8a8_masked gate_up (GEMM1)")
+                             measured_traffic(cfg.name),
+                             "grouped_gemm_w8a8_masked gate_up (GEMM1) through the public masked "
+                             "entry (int8-code engines); the layer itself widens the valid rows "
+                             "and runs the fp16-code pair engine")
     # minimal bytes: touched experts' weights and scales, valid rows' codes and
     # scales in, bf16 outputs of the valid rows
     nbytes = touched * (3 * H * I + (2 * I + H) * 4) + rows * (H + 4) + rows * H * 2
