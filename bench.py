@@ -470,10 +470,12 @@ def run_masked(args, cfg):
     with ClockSampler(0) as clk:
         torch.cuda.synchronize()
         n0 = wq.lib().wq_kernel_launches()
+        torch.cuda.nvtx.range_push("timed")
         e0.record()
         for _ in range(args.steps):
             step()
         e1.record()
+        torch.cuda.nvtx.range_pop()
         launches = wq.lib().wq_kernel_launches() - n0
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / args.steps

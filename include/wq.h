@@ -89,6 +89,20 @@ WQ_API const char *wq_status_string(int code);
  * counterpart. */
 WQ_API uint64_t wq_kernel_launches(void);
 
+/* Failure-path self-test of the bounded pipeline waits.  Takes the arguments
+ * of wq_grouped_gemm_w8a8_f16codes for the block scheme (bf16 out, workspace
+ * wq_grouped_gemm_workspace_size(R, E)) and launches the block-wise CTA-pair
+ * engine with a wait on a barrier that nothing completes, placed before any
+ * copy or MMA is issued.  The wait gives up after its 1 s limit; the kernel
+ * writes WQ_ERR_TIMEOUT into *status (device, required) and releases tensor
+ * memory.  out is not written.  The call itself returns WQ_OK once the launch
+ * is enqueued, and the device context stays usable for the next call.  The
+ * pages have no counterpart. */
+WQ_API int wq_selftest_wait_timeout(const uint16_t *A16, const float *sa, const int8_t *W,
+                                    const float *sw, const int32_t *offsets, int E, int64_t R,
+                                    int64_t N, int64_t K, void *out, void *ws, size_t ws_bytes,
+                                    int32_t *status, wq_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Online activation quantization [MT] (and offline weight quantization).
  *

@@ -52,6 +52,7 @@ _SIGS = {
     "wq_grouped_gemm_w8a8_f16codes": (_I, [_P, _P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
     "wq_quantize_per_token_f16": (_I, [_P, _L, _L, _L, _P, _P, _P, _P]),
     "wq_grouped_gemm_silu_quant_workspace_size": (_S, [_L, _I]),
+    "wq_selftest_wait_timeout": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _P, _P, _S, _P, _P]),
     "wq_grouped_gemm_w8a8_silu_quant_f16codes": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _P, _P, _P, _S, _P, _P]),
     "wq_grouped_gemm_masked_workspace_size": (_S, [_I, _I]),
     "wq_grouped_gemm_w8a8_masked": (_I, [_P, _P, _P, _I, _I, _P, _P, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
@@ -315,6 +316,19 @@ def grouped_gemm_w8a8_silu_quant_f16codes(A16, sa, W13, sw13, offsets, hq16=None
         _ptr(hq16), _ptr(sh), _ptr(ws), nws, _ptr(st), _stream()),
         "wq_grouped_gemm_w8a8_silu_quant_f16codes")
     return hq16, sh
+
+
+def selftest_wait_timeout(A16, sa, W, sw, offsets, out, status):
+    """Launch the block engine with a wait that nothing completes (failure-path
+    test); the device writes WQ_ERR_TIMEOUT into `status` after 1 s."""
+    R, K = A16.shape
+    E, N, _ = W.shape
+    nws = lib().wq_grouped_gemm_workspace_size(R, E)
+    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=A16.device)
+    _check(lib().wq_selftest_wait_timeout(_ptr(A16), _ptr(sa), _ptr(W), _ptr(sw), _ptr(offsets), E,
+                                          R, N, K, _ptr(out), _ptr(ws), nws, _ptr(status),
+                                          _stream()),
+           "wq_selftest_wait_timeout")
 
 
 def quantize_per_token_f16(x):

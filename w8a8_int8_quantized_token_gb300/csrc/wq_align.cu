@@ -176,8 +176,11 @@ int launch_align(const int32_t *ids, int T, int k, int E, int pad_m, int32_t *co
 // and, for a remainder of rem rows, one more tile: in the small list when
 // 0 < rem <= small_max (a small list is given), else in the main list.
 // The main list is ordered longest first, so that persistent engines that
-// hand items out in order finish with their shortest ones: the full tiles
-// (BM rows) in expert order, then the partial tiles by row count,
+// hand items out in order finish with their shortest ones: first the
+// experts with full tiles (BM rows), in expert order, each followed at once
+// by its own partial tile (the tiles of one expert stay adjacent, so the
+// engines read that expert's weights from DRAM once and from L2 for the
+// other tiles), then the partial tiles of the other experts by row count,
 // descending (equal counts in arbitrary order: the tiles write disjoint
 // rows, so the order changes no result).  ntiles[0] / nsmall[0] = numbers
 // written.
@@ -227,8 +230,9 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
     bool ts;
     seg(e, r0, len);
     plan(len, nfull, rem, ts);
-    local += nfull;
-    if (rem > 0 && !ts) atomicAdd(&hist[rem], 1);
+    const bool part_main = rem > 0 && !ts;
+    local += nfull + (nfull > 0 && part_main ? 1 : 0);  // beside its full tiles
+    if (nfull == 0 && part_main) atomicAdd(&hist[rem], 1);
     local_s += ts ? 1 : 0;
   }
   part[threadIdx.x] = local;
@@ -242,7 +246,7 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
     part_s[threadIdx.x] += vs;
     __syncthreads();
   }
-  const int nfull_total = part[blockDim.x - 1];
+  const int nfull_total = part[blockDim.x - 1];  // tiles of the experts with full tiles
   if (threadIdx.x == 0) {
     // first position of the partial tiles of each row count, longest first
     int pos = nfull_total;
@@ -276,6 +280,7 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
       tl.rows = rem;
       tl.pad = 0;
       if (ts) small[ts_i++] = tl;
+      else if (nfull > 0) tiles[t++] = tl;
       else tiles[atomicAdd(&hist[rem], 1)] = tl;
     }
   }

@@ -423,6 +423,22 @@ int wq_grouped_gemm_w8a8_f16codes(const uint16_t *A16, const int32_t *a_norm2, c
   return launch_grouped_gemm(a, stream);
 }
 
+int wq_selftest_wait_timeout(const uint16_t *A16, const float *sa, const int8_t *W, const float *sw,
+                             const int32_t *offsets, int E, int64_t R, int64_t N, int64_t K,
+                             void *out, void *ws, size_t ws_bytes, int32_t *status,
+                             wq_stream_t stream) {
+  if (R <= 0 || E < 1 || E > 4096 || !status) return WQ_ERR_INVALID_ARG;
+  WQ_TRY(check_gemm_common(W, sw, E, N, K, WQ_SCHEME_BLOCK, WQ_ACC_F32, WQ_OUT_BF16, out));
+  if (!A16 || !sa || !offsets) return WQ_ERR_INVALID_ARG;
+  if (!al16(A16) || N % 256 || K > 65536 || R >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;
+  if (ws_bytes < gemm_ws_bytes(R, E, 0, false) || !ws) return WQ_ERR_WORKSPACE;
+  WQ_TRY(check_device());
+  GemmArgs a{nullptr, A16, nullptr, sa, W, sw, offsets, nullptr, 0, E, R, N, K, WQ_SCHEME_BLOCK,
+             WQ_ACC_F32, WQ_OUT_BF16, out, ws, status};
+  a.wait_test = 1;
+  return launch_grouped_gemm(a, stream);
+}
+
 size_t wq_grouped_gemm_silu_quant_workspace_size(int64_t R, int E) {
   if (R < 0 || E < 1) return 0;
   return gemm_ws_bytes(R, E, 0, false, true);

@@ -244,6 +244,7 @@ struct GemmArgs {
   uint16_t *fused_hq16 = nullptr;
   float *fused_sh = nullptr;
   const float *fused_silu_tab = nullptr;  // silu_tab entries (set by the dispatcher)
+  int wait_test = 0;  // failure-path test: a wait that nothing completes (block engine)
 };
 // The single-pass float32 engines serve both channel-wise accumulator modes.
 // In the float32 mode the accumulator is the running sum, over 128-wide K

@@ -75,7 +75,8 @@ struct Plan {
                        B_XF = B_MMA_DONE + 1,        // fused: [NEPI] peer's half arrived
       B_XE = B_XF + NEPI,                            // fused: [NEPI] peer has read our half
       B_RED = B_XE + NEPI,                           // fused: [2 item parities][2 halves]
-      NBAR = FUSE ? B_RED + 4 : B_MMA_DONE + 1;
+      B_TEST = FUSE ? B_RED + 4 : B_MMA_DONE + 1,    // never completed (failure-path test)
+      NBAR = B_TEST + 1;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
@@ -153,6 +154,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(B_ACC_EMPTY + b), NEPI);
     }
     mbar_init(bar(B_MMA_DONE), 1);
+    mbar_init(bar(P::B_TEST), 1);
     if constexpr (FUSE) {
       for (int w = 0; w < NEPI; ++w) {
         mbar_init(bar(P::B_XF + w), 1);  // one elected lane of the peer's warp
@@ -182,7 +184,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   // token rows each CTA of the pair loads for an MMA of width nmma
   auto box_of = [](int nmma) { return nmma <= 16 ? 8 : (nmma <= 64 ? 32 : 80); };
 
-  if (warp == 0) {
+  if (a.wait_test) {
+    // failure-path test: thread 0 waits on a barrier that nothing completes;
+    // the bounded wait gives up, the kernel records WQ_ERR_TIMEOUT and every
+    // role skips to the teardown before any copy or MMA is issued
+    if (threadIdx.x == 0 && !mbar_wait(bar(P::B_TEST), 0, abort_flag)) fail();
+  } else if (warp == 0) {
     // ------------------------------------------------------------ weight producer
     if (lane == 0) {
       int g = 0, gw = 0;  // stage counter; weight stages issued
