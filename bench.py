@@ -499,10 +499,7 @@ def run_masked(args, cfg):
     peaks, src = load_peaks()
     touched = int((mm > 0).sum())
     roofline = gemm_roofline(peaks, src, clocks, g1_ms, rows, touched, 2 * I, H, cfg.scheme, 1,
-                             measured_traffic(cfg.name),
-                             "grouped_gemm_w8a8_masked gate_up (GEMM1) through the public masked "
-                             "entry (int8-code engines); the layer itself widens the valid rows "
-                             "and runs the fp16-code pair engine")
+                             measured_traffic(cfg.name), "grouped_gemm_w8a8_masked gate_up (GEMM1)")
     # minimal bytes: touched experts' weights and scales, valid rows' codes and
     # scales in, bf16 outputs of the valid rows
     nbytes = touched * (3 * H * I + (2 * I + H) * 4) + rows * (H + 4) + rows * H * 2

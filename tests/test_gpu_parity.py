@@ -406,32 +406,6 @@ def test_silu_mul_quant_shapes(R, I, group):
         assert np.array_equal(np_(sh16).reshape(sho.shape), sho)
 
 
-@pytest.mark.parametrize("mm", [[150, 0, 1, 77, 16, 17, 400], [3, 330, 0, 9]])
-def test_layer_forward_masked_pair_engine(mm):
-    """The masked layer at widths where both contractions are at least 1024
-    deep: valid rows are widened to fp16 codes, experts above 16 rows run on
-    the tensor-memory-weights pair engine (a 400-row expert splits at 320) and
-    the remainders of at most 16 rows on the CUDA-core engine; invalid rows
-    stay untouched."""
-    mm = np.array(mm, np.int32)
-    E, Mmax = len(mm), 400
-    cfg = synth.small_config("masked_pair", T=0, H=1024, I=1024, E=E, k=1)
-    x = synth.activations(E * Mmax, cfg.H, True, 5)
-    a, sa = wq.quantize_per_token(x.to(DEV))
-    qo, so = O.quantize_per_token(bits(x))
-    (W13, S13, W2, S2), orc = quantized_weights(cfg, DEV)
-    y = torch.full((E, Mmax, cfg.H), 5.0, dtype=torch.bfloat16, device=DEV)
-    st = wq.new_status()
-    wq.moe_forward_masked(a.view(E, Mmax, cfg.H), sa.view(E, Mmax), torch.from_numpy(mm).to(DEV),
-                          W13, S13, W2, S2, y=y, status=st)
-    assert int(st.item()) == 0
-    ref, valid = O.moe_forward_masked(qo.reshape(E, Mmax, cfg.H), so.reshape(E, Mmax), mm,
-                                      *stack_oracle(orc, E))
-    yb = bits(y)
-    assert_bf16_equal(yb[valid], ref[valid], "masked layer, pair engine")
-    assert np.all(O.bf16_to_f32(yb[~valid]) == 5.0)
-
-
 # ---------------------------------------------------------------- fp16-stored codes
 @pytest.mark.parametrize("groups", [1, 56])
 def test_moe_permute_f16(groups):

@@ -150,22 +150,6 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
     f.fused_silu_tab = w.silu;
     return launch_gemm_tc6(f, w.t128, w.n128, int(w.m128), st);
   }
-  if (a.A16 != nullptr && a.A != nullptr) {
-    // both forms given (the masked layer's widened rows): remainders of at
-    // most 16 rows on the small-token engine (int8 codes), every other tile
-    // on the tensor-memory-weights pair engine (fp16 codes), then the gated
-    // exact recompute over all rows (fp16 codes)
-    if (!(a.K >= 1024 && gemm_tc5_supported(a) && gemm_small_supported(a))) return WQ_ERR_UNSUPPORTED;
-    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, gemm_tc5_tile_rows(a), a.R,
-                              w.t256, w.n256, w.redo, st, gemm_small_max_rows(), w.tsm, w.nsm));
-    WQ_TRY(launch_gemm_small(a, w.tsm, w.nsm, int(w.msm), st));
-    WQ_TRY(launch_gemm_tc5(a, w.t256, w.n256, int(w.m256), w.redo, st));
-    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 64, a.R, w.t64, w.n64, nullptr,
-                              st));
-    GemmArgs r = a;
-    r.A = nullptr;  // the recompute reads the fp16 codes
-    return launch_gemm_simt(r, w.t64, w.n64, int(w.m64), w.redo, st);
-  }
   if (a.A16 != nullptr) {
     // fp16-stored codes: the CTA-pair engine, then the CUDA-core engine reading
     // fp16 codes as its exact recompute (it exits at once when *redo == 0)
@@ -778,31 +762,17 @@ int wq_linear_w8a8(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, const i
 
 namespace {
 
-struct MaskedBufs {
-  uint16_t *gu;
-  int8_t *hq;
-  float *sh;
-  uint16_t *a16, *hq16;  // widened valid rows (fp16 codes) for the pair engine
-  int32_t *anorm, *hnorm;
-  void *gws;
-  size_t gws_bytes;
-};
-
-size_t carve_masked(void *ws, int E, int Mmax, int H, int I, int scheme, MaskedBufs *out) {
+size_t carve_masked(void *ws, int E, int Mmax, int H, int I, int scheme, uint16_t **gu,
+                    int8_t **hq, float **sh, void **gws, size_t *gws_bytes) {
   Carver c(ws);
   const int64_t R = int64_t(E) * Mmax;
   const int64_t g2 = scheme == WQ_SCHEME_BLOCK ? I / 128 : 1;
-  MaskedBufs b;
-  b.gu = c.take<uint16_t>(size_t(R) * 2 * I);
-  b.hq = c.take<int8_t>(size_t(R) * I);
-  b.sh = c.take<float>(size_t(R) * g2);
-  b.a16 = c.take<uint16_t>(size_t(R) * H);
-  b.hq16 = c.take<uint16_t>(size_t(R) * I);
-  b.anorm = c.take<int32_t>(size_t(R));
-  b.hnorm = c.take<int32_t>(size_t(R));
-  b.gws_bytes = gemm_ws_bytes(R, E, Mmax, true);
-  b.gws = c.take<char>(b.gws_bytes);
-  if (out) *out = b;
+  uint16_t *a = c.take<uint16_t>(size_t(R) * 2 * I);
+  int8_t *b = c.take<int8_t>(size_t(R) * I);
+  float *d = c.take<float>(size_t(R) * g2);
+  const size_t gb = gemm_ws_bytes(R, E, Mmax, true);
+  void *g = c.take<char>(gb);
+  if (gu) { *gu = a; *hq = b; *sh = d; *gws = g; *gws_bytes = gb; }
   return c.used;
 }
 
@@ -810,7 +780,7 @@ size_t carve_masked(void *ws, int E, int Mmax, int H, int I, int scheme, MaskedB
 
 size_t wq_moe_forward_masked_workspace_size(int E, int Mmax, int H, int I, int scheme) {
   if (E < 1 || Mmax < 0 || H <= 0 || I <= 0) return 0;
-  return carve_masked(nullptr, E, Mmax, H, I, scheme, nullptr);
+  return carve_masked(nullptr, E, Mmax, H, I, scheme, nullptr, nullptr, nullptr, nullptr, nullptr);
 }
 
 int wq_moe_forward_masked(const int8_t *a, const float *sa, const int32_t *masked_m, int E,
@@ -825,37 +795,22 @@ int wq_moe_forward_masked(const int8_t *a, const float *sa, const int32_t *maske
   if (!a || !sa || !masked_m || !W13 || !sw13 || !W2 || !sw2 || !y) return WQ_ERR_INVALID_ARG;
   if (!al16(a) || !al16(y) || !al16(W13) || !al16(W2)) return WQ_ERR_UNSUPPORTED;
   if (int64_t(E) * Mmax >= (int64_t(1) << 31) / 2) return WQ_ERR_UNSUPPORTED;
-  MaskedBufs b;
-  const size_t need = carve_masked(ws, E, Mmax, H, I, scheme, &b);
+  uint16_t *gu;
+  int8_t *hq;
+  float *sh;
+  void *gws;
+  size_t gwsb;
+  const size_t need = carve_masked(ws, E, Mmax, H, I, scheme, &gu, &hq, &sh, &gws, &gwsb);
   if (!ws || !al16(ws) || ws_bytes < need) return WQ_ERR_WORKSPACE;
   WQ_TRY(check_device());
   const int64_t R = int64_t(E) * Mmax;
   GemmArgs g1{a, nullptr, nullptr, sa, W13, sw13, nullptr, masked_m, Mmax, E, R, int64_t(2) * I, H, scheme, acc,
-              WQ_OUT_BF16, b.gu, b.gws, status};
-  GemmArgs g2{b.hq, nullptr, nullptr, b.sh, W2, sw2, nullptr, masked_m, Mmax, E, R, H, I, scheme, acc,
-              WQ_OUT_BF16, y, b.gws, status};
-  // channel scheme with both contractions at least 1024 deep and widths that
-  // are multiples of 256: the valid rows are also widened to fp16 codes, so
-  // experts above 16 rows run on the tensor-memory-weights pair engine and
-  // the small remainders on the CUDA-core engine
-  GemmArgs p1 = g1, p2 = g2;
-  p1.A16 = b.a16;
-  p1.a_norm2 = b.anorm;
-  p2.A16 = b.hq16;
-  p2.a_norm2 = b.hnorm;
-  const bool pair = scheme == WQ_SCHEME_CHANNEL && H >= 1024 && I >= 1024 &&
-                    gemm_tc5_supported(p1) && gemm_tc5_supported(p2) &&
-                    gemm_small_supported(p1) && gemm_small_supported(p2);
-  if (pair) {
-    WQ_TRY(launch_widen_masked(a, H, masked_m, E, Mmax, b.a16, b.anorm, stream));
-    WQ_TRY(launch_grouped_gemm(p1, stream));
-    WQ_TRY(launch_silu_mul_quant(b.gu, R, I, 0, masked_m, Mmax, b.hq, b.sh, stream));
-    WQ_TRY(launch_widen_masked(b.hq, I, masked_m, E, Mmax, b.hq16, b.hnorm, stream));
-    return launch_grouped_gemm(p2, stream);
-  }
+              WQ_OUT_BF16, gu, gws, status};
   WQ_TRY(launch_grouped_gemm(g1, stream));
-  WQ_TRY(launch_silu_mul_quant(b.gu, R, I, scheme == WQ_SCHEME_BLOCK ? 128 : 0, masked_m, Mmax,
-                               b.hq, b.sh, stream));
+  WQ_TRY(launch_silu_mul_quant(gu, R, I, scheme == WQ_SCHEME_BLOCK ? 128 : 0, masked_m, Mmax, hq,
+                               sh, stream));
+  GemmArgs g2{hq, nullptr, nullptr, sh, W2, sw2, nullptr, masked_m, Mmax, E, R, H, I, scheme, acc, WQ_OUT_BF16, y,
+              gws, status};
   return launch_grouped_gemm(g2, stream);
 }
 

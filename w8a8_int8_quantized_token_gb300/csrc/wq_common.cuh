@@ -209,9 +209,6 @@ int launch_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group,
 int launch_permute_f16(const int8_t *q, const float *s, int groups, int k, int64_t K,
                        const int32_t *sorted_pair, int64_t R, uint16_t *A16, float *sa,
                        int32_t *norm2, cudaStream_t st);
-// the masked layout's valid int8 rows as fp16 codes with squared norms
-int launch_widen_masked(const int8_t *a, int64_t K, const int32_t *masked_m, int E, int Mmax,
-                        uint16_t *a16, int32_t *norm2, cudaStream_t st);
 int launch_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, int group,
                               const int32_t *masked_m, int Mmax, uint16_t *hq16, float *sh,
                               int32_t *norm2, cudaStream_t st);

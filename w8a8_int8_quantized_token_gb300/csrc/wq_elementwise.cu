@@ -470,47 +470,6 @@ __global__ void __launch_bounds__(128) permute_f16_kernel(const int8_t *__restri
   if (threadIdx.x == 0) norm2[r] = red[0] + red[1] + red[2] + red[3];
 }
 
-// Widening of the masked layout's valid rows: a16[r] = the int8 codes of row
-// r as fp16 values, norm2[r] = their squared L2 norm, for r = e * Mmax + m
-// with m < masked_m[e]; other rows are not written.  One warp per row.
-__global__ void __launch_bounds__(256) widen_masked_kernel(const int8_t *__restrict__ a, int64_t K,
-                                                           const int32_t *__restrict__ masked_m,
-                                                           int Mmax, int64_t R,
-                                                           uint16_t *__restrict__ a16,
-                                                           int32_t *__restrict__ norm2) {
-  const int lane = threadIdx.x & 31;
-  const int64_t r = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (r >= R || int(r % Mmax) >= masked_m[r / Mmax]) return;  // warp-uniform
-  const uint4 *src = reinterpret_cast<const uint4 *>(a + r * K);
-  uint4 *dst = reinterpret_cast<uint4 *>(a16 + r * K);
-  const int64_t nvec = K >> 4;
-  int acc = 0;
-  for (int64_t i = lane; i < nvec; i += 32) {
-    const uint4 v = __ldg(src + i);
-    uint4 o0, o1;
-    tc::s8x4_to_f16x4(v.x, o0.x, o0.y);
-    tc::s8x4_to_f16x4(v.y, o0.z, o0.w);
-    tc::s8x4_to_f16x4(v.z, o1.x, o1.y);
-    tc::s8x4_to_f16x4(v.w, o1.z, o1.w);
-    dst[2 * i] = o0;
-    dst[2 * i + 1] = o1;
-    acc += __dp4a(int(v.x), int(v.x), __dp4a(int(v.y), int(v.y), 0)) +
-           __dp4a(int(v.z), int(v.z), __dp4a(int(v.w), int(v.w), 0));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) norm2[r] = acc;
-}
-
-int launch_widen_masked(const int8_t *a, int64_t K, const int32_t *masked_m, int E, int Mmax,
-                        uint16_t *a16, int32_t *norm2, cudaStream_t st) {
-  const int64_t R = int64_t(E) * Mmax;
-  if (R == 0 || K == 0) return WQ_OK;
-  if ((R + 7) / 8 > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
-  widen_masked_kernel<<<unsigned((R + 7) / 8), 256, 0, st>>>(a, K, masked_m, Mmax, R, a16, norm2);
-  return launched(1);
-}
-
 int launch_permute_f16(const int8_t *q, const float *s, int groups, int k, int64_t K,
                        const int32_t *sorted_pair, int64_t R, uint16_t *A16, float *sa,
                        int32_t *norm2, cudaStream_t st) {
