@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
                                                            int32_t *__restrict__ nsmall) {
   __shared__ int32_t part[1024], part_s[1024];
   __shared__ int32_t hist[kMaxTileRows + 1];  // partial main tiles by row count, then cursors
-  if (zero_word != nullptr && threadIdx.x == 0) *zero_word = 0;
+  if (zero_word != nullptr && threadIdx.x < 2) zero_word[threadIdx.x] = 0;  // flag, item counter
   for (int i = threadIdx.x; i <= kMaxTileRows; i += blockDim.x) hist[i] = 0;
   const int per = (E + blockDim.x - 1) / blockDim.x;
   const int e0 = threadIdx.x * per;

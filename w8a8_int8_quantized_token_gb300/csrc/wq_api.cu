@@ -123,7 +123,7 @@ GemmWs carve_gemm_ws(void *ws, int64_t R, int E, int Mmax, bool masked, bool sil
   w.msm = E;
   w.tsm = c.take<Tile>(size_t(w.msm));
   w.nsm = c.take<int32_t>(1);
-  w.redo = c.take<int32_t>(1);
+  w.redo = c.take<int32_t>(2);  // recompute flag, then an engine's item counter
   w.silu = silu ? c.take<float>(silu_tab::kSize) : nullptr;
   w.bytes = c.used;
   return w;

@@ -255,6 +255,8 @@ struct GemmArgs {
 inline bool acc_modes_agree(const GemmArgs &a) {
   return a.scheme == WQ_SCHEME_CHANNEL && (a.acc == WQ_ACC_I32 || a.acc == WQ_ACC_F32);
 }
+// zero_word: two int32 words the builder sets to 0 before the engine runs
+// (the exact-recompute flag and an engine's item counter), or nullptr
 int launch_build_tiles(const int32_t *offsets, const int32_t *masked_m, int Mmax, int E, int BM,
                        int64_t R, Tile *tiles, int32_t *ntiles, int32_t *zero_word,
                        cudaStream_t st, int small_max = 0, Tile *small = nullptr,

@@ -18,9 +18,14 @@
 // M = 128 rows are output channels (weights, A operand) and its N = 16..256
 // columns are tokens (B operand), so a ragged expert wastes at most 15 token
 // columns.  Persistent CTAs; work item = (token tile <= 256 rows of one expert)
-// x (128 output channels).  Two tensor-memory accumulators (columns [0,256)
-// and [256,512)) let the epilogue of one item overlap the MMAs of the next.
-//   warp 0      TMA producer (weights 128 x 64, tokens box x 64 int8)
+// x (128 output channels), handed out dynamically: a CTA starts with item
+// blockIdx.x and claims each further item from a global counter
+// (gridDim.x + atomicAdd), so CTAs that drew short items take more of them;
+// the producer posts the claimed indices into a small ring in shared memory,
+// from which every role reads the same sequence.  Two tensor-memory
+// accumulators (columns [0,256) and [256,512)) let the epilogue of one item
+// overlap the MMAs of the next.
+//   warp 0      item claims and TMA producer (weights 128 x 64, tokens box x 64 int8)
 //   warp 1      TMEM allocator and MMA issuer (one thread)
 //   warps 2-9   converters (two groups taking alternate K stages): int8 ->
 //               fp16 (128-byte swizzled K-major) + squared row norms
@@ -38,6 +43,10 @@ constexpr int WM = 128, BK = 64;
 constexpr int NTHREADS = 448;
 constexpr int NCONV = 256;  // converter threads: two groups of 128
 constexpr int GCONV = 128;  // threads of one converter group (its stages alternate with the other's)
+constexpr int NR = 8;       // item ring depth
+// readers of each posted item: the MMA thread, the eight converter warps and
+// the four epilogue warps (one arrival each)
+constexpr int ITEM_READERS = 1 + NCONV / 32 + 4;
 
 // Shared-memory plan of one instantiation: TN = most tokens per item (MMA N),
 // S8 / S16 = depths of the int8 staging ring and of the fp16 ring.  Large
@@ -58,10 +67,14 @@ struct Plan {
       B_NORM_READY = B_ACC_FULL + 4,                                               // [2]
       B_NORM_FREE = B_ACC_FULL + 6,                                                // [2]
       B_NORM_READ = B_ACC_FULL + 8,                                                // [2]
-      B_MMA_DONE = B_ACC_FULL + 10, NBAR = B_ACC_FULL + 11;
+      B_MMA_DONE = B_ACC_FULL + 10,
+                       B_ITEM_FULL = B_ACC_FULL + 11,   // [NR] a claimed item index posted
+      B_ITEM_EMPTY = B_ITEM_FULL + NR,                 // [NR] every role has read it
+      NBAR = B_ITEM_EMPTY + NR;
   // int32 [2 buffers][2 converter groups][weights, tokens]
   static constexpr int OFF_NORM = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_TMEM = OFF_NORM + 32;
+  static constexpr int OFF_ITEMS = OFF_NORM + 32;  // int32 [NR] item ring
+  static constexpr int OFF_TMEM = OFF_ITEMS + NR * 4;
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
   static constexpr int NJW = WM * 4 / GCONV;  // weight 16-byte pieces per converter thread
@@ -78,7 +91,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const __grid_constant__ CUtensorMap tmT64,
                     const __grid_constant__ CUtensorMap tmT256, const GemmArgs a,
                     const Tile *__restrict__ tiles, const int32_t *__restrict__ ntiles,
-                    int32_t *__restrict__ redo) {
+                    int32_t *__restrict__ redo, int32_t *__restrict__ claim) {
   using P = Plan<TN, S8, S16>;
   constexpr int W8 = P::W8, W16 = P::W16, ST8 = P::ST8, ST16 = P::ST16;
   constexpr int OFF_F16 = P::OFF_F16, OFF_I8 = P::OFF_I8, OFF_BAR = P::OFF_BAR;
@@ -86,7 +99,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 B_F16_EMPTY = P::B_F16_EMPTY, B_ACC_FULL = P::B_ACC_FULL,
                 B_ACC_EMPTY = P::B_ACC_EMPTY, B_NORM_READY = P::B_NORM_READY,
                 B_NORM_FREE = P::B_NORM_FREE, B_NORM_READ = P::B_NORM_READ,
-                B_MMA_DONE = P::B_MMA_DONE;
+                B_MMA_DONE = P::B_MMA_DONE, B_ITEM_FULL = P::B_ITEM_FULL,
+                B_ITEM_EMPTY = P::B_ITEM_EMPTY;
   constexpr int OFF_NORM = P::OFF_NORM, OFF_TMEM = P::OFF_TMEM, OFF_ABORT = P::OFF_ABORT;
   constexpr int NJW = P::NJW, NJT = P::NJT;
   extern __shared__ uint8_t smem_raw[];
@@ -98,6 +112,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t *sm = smem_raw + (base - raw);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_ABORT);
   volatile int *norm = reinterpret_cast<volatile int *>(sm + OFF_NORM);
+  volatile int *item_ring = reinterpret_cast<volatile int *>(sm + P::OFF_ITEMS);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_TMEM);
   auto bar = [&](int i) { return base + OFF_BAR + 8u * uint32_t(i); };
 
@@ -123,6 +138,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar(B_NORM_READ + b), 4);
     }
     mbar_init(bar(B_MMA_DONE), 1);
+    for (int r = 0; r < NR; ++r) {
+      mbar_init(bar(B_ITEM_FULL + r), 1);
+      mbar_init(bar(B_ITEM_EMPTY + r), ITEM_READERS);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
@@ -138,13 +157,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // token box height for a tile of `rows` tokens, and the MMA's N
   auto nmma_of = [](int rows) { return (rows + 15) & ~15; };
   auto box_of = [](int nmma) { return nmma <= 16 ? 16 : (nmma <= 64 || TN <= 64 ? 64 : 256); };
+  // the r-th item of this CTA (-1: none left), read from the ring by every
+  // thread of a role; the caller then arrives once per warp on ITEM_EMPTY
+  auto read_item = [&](int r, int &it) {
+    if (!mbar_wait(bar(B_ITEM_FULL + r % NR), (r / NR) & 1, abort_flag)) return false;
+    it = item_ring[r % NR];
+    return true;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int g = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+      int it = blockIdx.x;  // the first item is the CTA's own; later ones are claimed
+      for (int r = 0; ok; ++r) {
+        const int s = r % NR;
+        if (!mbar_wait<200>(bar(B_ITEM_EMPTY + s), ((r / NR) & 1) ^ 1, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        item_ring[s] = it < items ? it : -1;
+        mbar_arrive(bar(B_ITEM_FULL + s));
+        if (it >= items) break;
+        const int next = int(gridDim.x) + atomicAdd(claim, 1);  // claimed while this item streams
         const Tile tl = tiles[it / NB];
         const int wb = it % NB;
         const int box = box_of(nmma_of(tl.rows));
@@ -152,17 +189,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t tx = W8 + box * BK;
         const int wrow = int(int64_t(tl.expert) * a.N + int64_t(wb) * WM);
         for (int i = 0; i < KT; ++i, ++g) {
-          const int s = g % S8;
-          if (!mbar_wait<200>(bar(B_S8_EMPTY + s), ((g / S8) & 1) ^ 1, abort_flag)) {
+          const int s8 = g % S8;
+          if (!mbar_wait<200>(bar(B_S8_EMPTY + s8), ((g / S8) & 1) ^ 1, abort_flag)) {
             fail();
             ok = false;
             break;
           }
-          const uint32_t dst = base + OFF_I8 + uint32_t(s) * ST8;
-          mbar_expect_tx(bar(B_S8_FULL + s), tx);
-          tma_load_2d(dst, &tmW, i * BK, wrow, bar(B_S8_FULL + s));
-          tma_load_2d(dst + W8, tmT, i * BK, tl.row0, bar(B_S8_FULL + s));
+          const uint32_t dst = base + OFF_I8 + uint32_t(s8) * ST8;
+          mbar_expect_tx(bar(B_S8_FULL + s8), tx);
+          tma_load_2d(dst, &tmW, i * BK, wrow, bar(B_S8_FULL + s8));
+          tma_load_2d(dst + W8, tmT, i * BK, tl.row0, bar(B_S8_FULL + s8));
         }
+        it = next;
       }
       if (!ok) {
         for (int j = g > S8 ? g - S8 : 0; j < g; ++j)
@@ -172,9 +210,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int g = 0, ii = 0;
+      int g = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++ii) {
+      for (int ii = 0; ok; ++ii) {
+        int it;
+        if (!read_item(ii, it)) {
+          fail();
+          break;
+        }
+        mbar_arrive(bar(B_ITEM_EMPTY + ii % NR));
+        if (it < 0) break;
         const Tile tl = tiles[it / NB];
         const uint32_t idesc = idesc_f16(WM, nmma_of(tl.rows));
         const int b = ii & 1;
@@ -209,9 +254,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // (K / 64 is even), so two stages are in flight through the converters.
     const int grp = (warp - 2) >> 2;
     const int t = threadIdx.x - 64 - grp * GCONV;  // 0..127 within the group
-    int gbase = 0, ii = 0;
+    int gbase = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++ii, gbase += KT) {
+    for (int ii = 0; ok; ++ii, gbase += KT) {
+      int it;
+      if (!__all_sync(0xffffffffu, read_item(ii, it))) {
+        fail();
+        break;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_ITEM_EMPTY + ii % NR));
+      if (it < 0) break;
       const Tile tl = tiles[it / NB];
       const int box = box_of(nmma_of(tl.rows));
       const int tchunks = box * 4;  // 16-byte pieces of the token tile
@@ -296,8 +349,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // tensor-memory lane quarter of this warp
-    int ii = 0;
-    for (int it = blockIdx.x; it < items; it += gridDim.x, ++ii) {
+    for (int ii = 0;; ++ii) {
+      int it;
+      if (!__all_sync(0xffffffffu, read_item(ii, it))) {
+        fail();
+        break;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_ITEM_EMPTY + ii % NR));
+      if (it < 0) break;
       const Tile tl = tiles[it / NB];
       const int wb = it % NB;
       const int b = ii & 1, par = (ii >> 1) & 1;
@@ -406,8 +466,9 @@ int launch_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int 
   }
   const int64_t max_items = int64_t(max_tiles) * (a.N / WM);
   const int grid = int(max_items < num_sms() ? max_items : num_sms());
+  // redo[1] is the item counter (zeroed with the flag by the tile builder)
   gemm_tc2_kernel<TN, S8, S16><<<grid, NTHREADS, P::SMEM_BYTES, st>>>(mW, m16, m64, m256, a, tiles,
-                                                                      ntiles, redo);
+                                                                      ntiles, redo, redo + 1);
   return launched(1);
 }
 

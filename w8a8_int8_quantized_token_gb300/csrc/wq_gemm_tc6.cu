@@ -43,8 +43,6 @@ namespace {
 using namespace tc;
 
 constexpr int WM = 128, TN = 160, BK = 64;
-constexpr int SW16 = 4, ST = 4;                 // ring depths: fp16 W, fp16 tokens
-static_assert(SW16 == ST, "a widened-weight slot is released with its token slot");
 constexpr int W8B = WM * BK, W16B = 2 * W8B;    // weight stage bytes
 constexpr int TB = TN * BK * 2;                 // token stage bytes (fp16)
 constexpr int NCH = 3;                          // chunk accumulators (tensor-memory columns [0, 3*TN))
@@ -59,6 +57,8 @@ constexpr int XW = KEEP / 2;                    // fused: bf16 pairs a thread se
 // int8 weight stage to make room.
 template <bool FUSE>
 struct Plan {
+  static constexpr int ST = 4;                  // token ring depth (fp16 tokens)
+  static constexpr int SW16 = ST;               // widened-weight ring depth
   static constexpr int SW8 = FUSE ? 7 : 8;      // int8 weight ring depth
   static constexpr int OFF_T = 0;
   static constexpr int OFF_W16 = OFF_T + ST * TB;
@@ -80,6 +80,7 @@ struct Plan {
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
+  static_assert(SW16 == ST, "a widened-weight slot is released with its token slot");
   static_assert(TB % 1024 == 0 && OFF_W16 % 1024 == 0 && OFF_W8 % 1024 == 0, "swizzle alignment");
   static_assert(OFF_XCH % 16 == 0 && OFF_BAR % 8 == 0, "exchange and barrier alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory plan too large");
@@ -113,6 +114,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
                     const __grid_constant__ CUtensorMap tmT80, const GemmArgs a,
                     const Tile *__restrict__ tiles, const int32_t *__restrict__ ntiles) {
   using P = Plan<FUSE>;
+  constexpr int ST = P::ST, SW16 = P::SW16;
   constexpr int SW8 = P::SW8, OFF_T = P::OFF_T, OFF_W16 = P::OFF_W16, OFF_W8 = P::OFF_W8,
                 OFF_SC = P::OFF_SC, OFF_BAR = P::OFF_BAR, OFF_TMEM = P::OFF_TMEM,
                 OFF_ABORT = P::OFF_ABORT;
