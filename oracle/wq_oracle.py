@@ -22,7 +22,9 @@ computes, one function per step, in the order of the pages:
   per-expert counts with a leading zero; tokens are scattered by expert
   before the grouped GEMMs and gathered after them;
 * "Support DeepSeek-R1 w4a8 low latency deepep" (sglang pull request 8311),
-  Highlights: the masked low-latency layout with per-expert problem sizes.
+  Highlights: the masked low-latency layout with per-expert problem sizes,
+  and its w4a8 weight path (int4 weights; the format is a reading, stated
+  with the functions at the end of this module).
 
 Precision.  The pages fix the data types of the method: int8 codes, float
 scales, an int32 or fp32 accumulator, bf16 activations in and out.  Where a
@@ -498,3 +500,85 @@ def convert_fp8_weights(w8: np.ndarray, s8: np.ndarray, scheme: str):
     block).  Returns (int8 codes [N, K], scales)."""
     bf = dequant_fp8_block(w8, s8)
     return quantize_weight_channel(bf) if scheme == "channel" else quantize_weight_block(bf)
+
+
+# ---------------------------------------------------------------------------
+# W4A8: int4 weights with int8 activations on the masked layout
+# ("Support DeepSeek-R1 w4a8 low latency deepep" (sglang pull request 8311),
+# Highlights and the forward_cutlass_w4a8_masked hunk: a w4a8 weight path for
+# the masked low-latency layout with per-expert problem sizes)
+# ---------------------------------------------------------------------------
+# Readings.  The page names the path but states no format: neither the int4
+# code range, group or scale layout, nor the activation type, nor how two
+# codes share a byte.  This oracle takes the plainest reading that the rest
+# of the method supports: the channel-wise rule of the INT8 weights with 7 in
+# place of 127 (symmetric codes in [-7, 7], one float32 scale per output
+# channel), activations quantized per token to int8 exactly as in the W8A8
+# layer, and two codes per byte with code 2j in the low nibble and code 2j+1
+# in the high nibble (two's complement nibbles).
+Q4MAX = F32(7.0)
+
+
+def quantize_weight_int4(w_bf16: np.ndarray):
+    """Channel-wise symmetric int4 weight quantization, one scale per output
+    channel (row of the [N, K] storage):
+        a = max_k |w_k|;  s = max(a, 1e-10) / 7  (float32 divide);
+        q_k = clamp(rint(w_k / s), -7, 7)  (float32 divide, ties to even).
+    Returns (q int8 [N, K] with values in [-7, 7], s float32 [N])."""
+    w = bf16_to_f32(w_bf16)
+    a = np.max(np.abs(w), axis=-1) if w.shape[-1] > 0 else np.zeros(w.shape[:-1], np.float32)
+    s = (np.maximum(a, SCALE_EPS) / Q4MAX).astype(np.float32)
+    q = np.clip(np.rint(w / s[..., None]), -7, 7).astype(np.int8)
+    return q, s
+
+
+def pack_int4(q: np.ndarray) -> np.ndarray:
+    """int4 codes [..., K] (K even, values in [-8, 7]) -> bytes [..., K/2]:
+    code 2j in bits 0-3 and code 2j+1 in bits 4-7 of byte j."""
+    q = np.asarray(q)
+    assert q.shape[-1] % 2 == 0
+    u = (q.astype(np.int16) & 0xF).astype(np.uint8)
+    return (u[..., 0::2] | (u[..., 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_int4(b: np.ndarray) -> np.ndarray:
+    """Bytes [..., K/2] -> int4 codes [..., K] as int8 (the inverse of
+    pack_int4; a nibble n >= 8 is the code n - 16)."""
+    b = np.asarray(b, dtype=np.uint8)
+    lo = (b & 0xF).astype(np.int16)
+    hi = (b >> 4).astype(np.int16)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), np.int8)
+    out[..., 0::2] = np.where(lo >= 8, lo - 16, lo)
+    out[..., 1::2] = np.where(hi >= 8, hi - 16, hi)
+    return out
+
+
+def grouped_gemm_w4a8_masked(a_q, a_s, masked_m, W4, S4):
+    """The masked grouped GEMM with int4 weights: for expert e and rows
+    r < masked_m[e],  C = sum_k a[e,r,k] * w[e,n,k]  (exact integers, |C| <=
+    127 * 7 * K), then  v = (float(C) * sa[e,r]) * s4[e,n]  (the channel
+    int32 epilogue), rounded to bf16.  a_q int8 [E, Mmax, K], a_s [E, Mmax],
+    W4 packed uint8 [E, N, K/2], S4 [E, N].  Returns (out bf16 [E, Mmax, N],
+    valid [E, Mmax]); rows at or past masked_m[e] are not defined."""
+    E, Mmax, K = a_q.shape
+    N = W4.shape[1]
+    out = np.zeros((E, Mmax, N), np.uint16)
+    valid = np.zeros((E, Mmax), bool)
+    for e in range(E):
+        m = min(int(masked_m[e]), Mmax)
+        if m <= 0:
+            continue
+        valid[e, :m] = True
+        out[e, :m] = f32_to_bf16(gemm_dequant(a_q[e, :m], a_s[e, :m], unpack_int4(W4[e]), S4[e],
+                                              "channel", "i32"))
+    return out, valid
+
+
+def moe_forward_masked_w4a8(a_q, a_s, masked_m, W13_4, S13_4, W2_4, S2_4):
+    """The masked layer with int4 weights: GEMM1 (gate_up) -> SiLU-mul +
+    per-token int8 re-quantization -> GEMM2 (down), on the valid rows.  It is
+    the W8A8 masked layer (channel scheme, int32 accumulator) applied to the
+    unpacked int4 codes and their scales.  Returns (y bf16 [E, Mmax, H],
+    valid [E, Mmax])."""
+    return moe_forward_masked(a_q, a_s, masked_m, unpack_int4(W13_4), S13_4, unpack_int4(W2_4),
+                              S2_4, "channel", "i32")

@@ -569,3 +569,85 @@ def test_fp8_dequant_and_conversion():
     qb, sb = O.convert_fp8_weights(w8b, np.array([[0.25]], np.float32), "block")
     assert sb[0, 0] == np.float32(np.float32(0.25) / np.float32(127.0))
     assert np.all(np.abs(qb) == 127)
+
+
+# ---------------------------------------------------------------------------
+# W4A8 (int4 weights, int8 activations, masked layout)
+# ---------------------------------------------------------------------------
+def test_w4a8_golden():
+    G = golden("w4a8_worked.json")
+    u = G["unpack"]
+    codes = O.unpack_int4(np.array(u["bytes"], np.uint8))
+    assert codes.tolist() == u["codes"]
+    assert O.pack_int4(codes).tolist() == u["bytes"]
+    qg = G["quant"]
+    w = np.array(qg["w"], np.float32)
+    q, s = O.quantize_weight_int4(O.f32_to_bf16(w)[None, :])
+    assert q[0].tolist() == qg["codes"] and float(s[0]) == qg["scale"]
+    g = G["gemm"]
+    a = np.array(g["a"], np.int8)[None]
+    sa = np.array(g["sa"], np.float32)[None]
+    W4 = np.array(g["w_bytes"], np.uint8)[None]
+    assert O.pack_int4(np.array(g["w_codes"], np.int8)).tolist() == g["w_bytes"]
+    out, valid = O.grouped_gemm_w4a8_masked(a, sa, np.array(g["masked_m"]), W4,
+                                            np.array(g["s4"], np.float32)[None])
+    m = g["masked_m"][0]
+    assert valid[0].tolist() == [True] * m + [False] * (a.shape[1] - m)
+    assert O.bf16_to_f32(out[0, :m, 0]).tolist() == g["out"]
+    assert (O.int_matmul(a[0, :m], O.unpack_int4(W4[0])).reshape(-1)).tolist() == g["C"]
+
+
+def test_int4_pack_round_trips():
+    every = np.arange(256, dtype=np.uint8)
+    codes = O.unpack_int4(every)
+    assert codes.min() == -8 and codes.max() == 7
+    assert np.array_equal(O.pack_int4(codes), every)
+    pairs = np.array([(lo, hi) for lo in range(-8, 8) for hi in range(-8, 8)], np.int8)
+    assert np.array_equal(O.unpack_int4(O.pack_int4(pairs)), pairs)
+
+
+def test_quantize_weight_int4_invariants():
+    rng = np.random.default_rng(5)
+    w = (rng.standard_normal((64, 256)) * 0.02).astype(np.float32)
+    w[3] = 0.0                      # a zero row
+    w[4, :] = 0.01                  # an all-equal row
+    wb = O.f32_to_bf16(w)
+    wf = O.bf16_to_f32(wb)
+    q, s = O.quantize_weight_int4(wb)
+    assert q.dtype == np.int8 and np.abs(q).max() <= 7
+    assert np.all(q[3] == 0) and s[3] == np.float32(1e-10) / np.float32(7.0)
+    assert np.all(q[4] == 7)
+    nz = np.abs(wf).max(1) > 0
+    assert np.all(np.abs(q[nz]).max(1) == 7)  # the absmax element takes the end code
+    # dequantization stays within half a scale step (plus float32 rounding)
+    err = np.abs(s[:, None].astype(np.float64) * q - wf)
+    assert np.all(err <= s[:, None] * (0.5 + 2.0 ** -20))
+    # codes are the round-half-even of the exact quotient away from ties
+    from fractions import Fraction
+    for r in (0, 7, 63):
+        for k in range(0, 256, 17):
+            exact = Fraction(float(wf[r, k])) / Fraction(float(s[r]))
+            if abs(abs(exact - int(exact)) - Fraction(1, 2)) > Fraction(1, 1 << 16):
+                assert int(q[r, k]) == max(-7, min(7, round(exact)))
+
+
+def test_w4a8_gemm_is_the_exact_integer_product():
+    """The int4 GEMM's integer sums against an int64 einsum of the unpacked
+    codes, and its outputs against the W8A8 masked GEMM on those codes
+    (pinned in its own tests): a wrong nibble, sign or scale index fails."""
+    rng = np.random.default_rng(6)
+    E, Mmax, K, N = 3, 5, 64, 8
+    a = rng.integers(-127, 128, (E, Mmax, K), dtype=np.int8)
+    sa = (rng.random((E, Mmax)) * 0.05).astype(np.float32)
+    codes = rng.integers(-7, 8, (E, N, K), dtype=np.int8)
+    W4 = O.pack_int4(codes)
+    S4 = (rng.random((E, N)) * 1e-2).astype(np.float32)
+    mm = np.array([5, 0, 3])
+    out, valid = O.grouped_gemm_w4a8_masked(a, sa, mm, W4, S4)
+    for e in range(E):
+        m = mm[e]
+        C = np.einsum("rk,nk->rn", a[e, :m].astype(np.int64), codes[e].astype(np.int64))
+        assert np.array_equal(O.int_matmul(a[e, :m], O.unpack_int4(W4[e])), C)
+        want = O.f32_to_bf16(O.gemm_dequant(a[e, :m], sa[e, :m], codes[e], S4[e], "channel", "i32"))
+        assert np.array_equal(out[e, :m], want)
+    assert valid.sum() == mm.sum()
