@@ -371,6 +371,46 @@ WQ_API int wq_moe_forward_masked(const int8_t *a, const float *sa, const int32_t
                           void *ws, size_t ws_bytes, int32_t *status, wq_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * W4A8 on the masked layout [LL] ("Support DeepSeek-R1 w4a8 low latency
+ * deepep", Highlights: a w4a8 weight path for the masked low-latency layer).
+ * The page fixes no int4 format; this library reads it as the channel-wise
+ * rule of the INT8 weights with 7 in place of 127:
+ *   per output channel n: s4[n] = max(max_k |w[n][k]|, 1e-10) / 7,
+ *   q[n][k] = clamp(rint(w[n][k] / s4[n]), -7, 7)   (ties to even),
+ * stored two codes a byte, code 2j in bits 0-3 and code 2j+1 in bits 4-7 of
+ * byte j (two's complement nibbles): W4 uint8 [N][K/2] per expert.
+ * Activations are the int8 per-token codes of wq_quantize_per_token.
+ *
+ * wq_quantize_weight_int4: w bf16 [N][K] -> q4 uint8 [N][K/2], s4 float [N].
+ *   Requirements: K % 8 == 0, 16-byte aligned w, 4-byte aligned q4.
+ * wq_grouped_gemm_w4a8_masked: as wq_grouped_gemm_w8a8_masked (channel
+ *   scheme, int32 accumulator) with W4 uint8 [E][N][K/2] and s4 [E][N]:
+ *   C = sum_k a[e][r][k] * q[e][n][k] exactly (|C| <= 127 * 7 * K), then
+ *   out = bf16((float(C) * sa[e][r]) * s4[e][n]), or C itself for
+ *   WQ_OUT_I32.  Rows at or past masked_m[e] are not written.
+ *   Requirements: N % 128 == 0, K % 128 == 0, K <= 16384 (every float32
+ *   partial sum of the tensor-core pass is then an exact integer), 16-byte
+ *   aligned A, W4 and out.  Workspace:
+ *   wq_grouped_gemm_masked_workspace_size(E, Mmax).
+ * wq_moe_forward_masked_w4a8: the masked layer of wq_moe_forward_masked
+ *   (channel scheme, int32 accumulator) with int4 W13 [E][2I][H/2] (s13
+ *   [E][2I]) and W2 [E][H][I/2] (s2 [E][H]).  Requirements: H, I multiples
+ *   of 128 and at most 16384.  Workspace:
+ *   wq_moe_forward_masked_w4a8_workspace_size(). */
+WQ_API int wq_quantize_weight_int4(const uint16_t *w, int64_t N, int64_t K, uint8_t *q4,
+                                   float *s4, wq_stream_t stream);
+WQ_API int wq_grouped_gemm_w4a8_masked(const int8_t *A, const float *sa, const int32_t *masked_m,
+                                       int E, int Mmax, const uint8_t *W4, const float *s4,
+                                       int64_t N, int64_t K, int out_type, void *out, void *ws,
+                                       size_t ws_bytes, int32_t *status, wq_stream_t stream);
+WQ_API size_t wq_moe_forward_masked_w4a8_workspace_size(int E, int Mmax, int H, int I);
+WQ_API int wq_moe_forward_masked_w4a8(const int8_t *a, const float *sa, const int32_t *masked_m,
+                                      int E, int Mmax, const uint8_t *W13, const float *s13,
+                                      const uint8_t *W2, const float *s2, int H, int I,
+                                      uint16_t *y, void *ws, size_t ws_bytes, int32_t *status,
+                                      wq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Dense W8A8 INT8 linear [CW] (Modifications, "Norm Linear": the model's
  * non-MoE linear layers run as a w8a8 INT8 GEMM).  out = dequant(quant(x)
  * W^T): the activation quantization of the scheme (per token, or per token

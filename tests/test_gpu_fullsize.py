@@ -264,3 +264,52 @@ def test_linear_full_size(T):
     max_abs, rel = tolerance_report(got, ref)
     assert max_abs <= 2e-2 and rel <= 1e-2
     assert_bf16_equal(got, ref, f"linear T{T} sampled rows {rows}")
+
+
+def test_masked_w4a8_full_size():
+    """The masked layer with int4 weights at its full size (32 experts x 512
+    rows, H 7168, I 2048, Zipf(1.2) counts): the library's int4 codes and
+    scales of eight experts against the oracle's quantization, and sampled
+    valid rows of those experts against the oracle's layer."""
+    cfg = synth.CONFIGS["masked"]
+    xm, mm = synth.masked_inputs(cfg, device=DEV)
+    E, Mmax, H, I = cfg.E, cfg.Mmax, cfg.H, cfg.I
+    a, sa = wq.quantize_per_token(xm.reshape(E * Mmax, H))
+    W13 = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=DEV)
+    W2 = torch.empty(E, H, I // 2, dtype=torch.uint8, device=DEV)
+    S13 = torch.empty(E, 2 * I, device=DEV)
+    S2 = torch.empty(E, H, device=DEV)
+    bf = {}
+    experts = sorted({int(np.argmax(mm)), *[e for e in range(E) if mm[e] > 0][:7]})
+    for e in range(E):
+        w13, w2 = synth.expert_weights(cfg, e, device=DEV)
+        W13[e], S13[e] = wq.quantize_weight_int4(w13)
+        W2[e], S2[e] = wq.quantize_weight_int4(w2)
+        if e in experts:
+            bf[e] = (bits(w13), bits(w2))
+    y = torch.full((E, Mmax, H), 3.0, dtype=torch.bfloat16, device=DEV)
+    st = wq.new_status()
+    wq.moe_forward_masked_w4a8(a.view(E, Mmax, H), sa.view(E, Mmax), torch.from_numpy(mm).to(DEV),
+                               W13, S13, W2, S2, y=y, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    yb = bits(y)
+    rng = np.random.default_rng(8)
+    got, want = [], []
+    for e in experts:
+        q13, s13 = O.quantize_weight_int4(bf[e][0])
+        q2, s2 = O.quantize_weight_int4(bf[e][1])
+        assert np.array_equal(np_(W13[e]), O.pack_int4(q13)) and np.array_equal(np_(S13[e]), s13)
+        assert np.array_equal(np_(W2[e]), O.pack_int4(q2)) and np.array_equal(np_(S2[e]), s2)
+        m = int(mm[e])
+        assert np.all(O.bf16_to_f32(yb[e, m:]) == 3.0)
+        rows = list(range(m)) if m <= 16 else sorted({0, m - 1, *rng.choice(m, 14, replace=False).tolist()})
+        q, s = O.quantize_per_token(bits(xm[e, rows]))
+        gu = O.f32_to_bf16(O.gemm_dequant(q, s, q13, s13, "channel", "i32"))
+        hq, sh = O.silu_mul_quant(gu, I)
+        want.append(O.f32_to_bf16(O.gemm_dequant(hq, sh, q2, s2, "channel", "i32")))
+        got.append(yb[e, rows])
+    got, want = np.concatenate(got), np.concatenate(want)
+    max_abs, rel = tolerance_report(got, want)
+    assert max_abs <= 2e-2 and rel <= 1e-2, (max_abs, rel)
+    assert_bf16_equal(got, want, "w4a8 masked sampled rows")

@@ -664,3 +664,113 @@ def test_convert_fp8_weights(scheme, N, K):
     assert np.array_equal(np_(q), qo)
     assert np.array_equal(np_(s), so)
 
+
+
+# ---------------------------------------------------------------------------
+# W4A8: int4 weights (two codes a byte), int8 activations, masked layout
+# ---------------------------------------------------------------------------
+def test_quantize_weight_int4():
+    g = torch.Generator().manual_seed(41)
+    w = (torch.randn(300, 640, generator=g) * 0.02)
+    w[3] = 0.0
+    w[5, 7] = 0.5   # an outlier channel
+    w = w.to(torch.bfloat16)
+    q4, s = wq.quantize_weight_int4(w.to(DEV))
+    qo, so = O.quantize_weight_int4(bits(w))
+    assert np.array_equal(np_(q4), O.pack_int4(qo))
+    assert np.array_equal(np_(s), so)
+
+
+def _w4_problem(rng, counts, Mmax, N, K, extreme=False):
+    E = len(counts)
+    if extreme:
+        a = np.where(rng.random((E, Mmax, K)) < 0.5, -127, 127).astype(np.int8)
+        codes = np.where(rng.random((E, N, K)) < 0.5, -7, 7).astype(np.int8)
+    else:
+        a = rng.integers(-127, 128, (E, Mmax, K), dtype=np.int8)
+        codes = rng.integers(-7, 8, (E, N, K), dtype=np.int8)
+    sa = (rng.random((E, Mmax)) * 0.05).astype(np.float32)
+    s4 = (rng.random((E, N)) * 1e-2).astype(np.float32)
+    return a, sa, codes, O.pack_int4(codes), s4, np.array(counts, np.int32)
+
+
+@pytest.mark.parametrize("K,N,counts,Mmax", [
+    (512, 256, [0, 1, 17, 300, 257, 16], 300),   # 256-token tiles, short ones, an empty expert
+    (2048, 384, [64, 3, 129], 160),
+    (7168, 256, [5, 40], 48),                    # 64-token tiles (few rows per expert)
+])
+def test_grouped_gemm_w4a8_masked(K, N, counts, Mmax):
+    rng = np.random.default_rng(K + N)
+    a, sa, codes, W4, s4, mm = _w4_problem(rng, counts, Mmax, N, K)
+    t = lambda x: torch.from_numpy(x).to(DEV)
+    E = len(counts)
+    for out_type in ("i32", "bf16"):
+        fill = torch.full((E, Mmax, N), 7, dtype=torch.int32 if out_type == "i32" else torch.bfloat16,
+                          device=DEV)
+        st = wq.new_status()
+        out = wq.grouped_gemm_w4a8_masked(t(a), t(sa), t(mm), t(W4), t(s4), out_type=out_type,
+                                          out=fill, status=st)
+        assert int(st.item()) == 0
+        got = np_(out) if out_type == "i32" else O.bf16_to_f32(bits(out))
+        for e in range(E):
+            m = int(mm[e])
+            if out_type == "i32":
+                want = np.einsum("rk,nk->rn", a[e, :m].astype(np.int64), codes[e].astype(np.int64))
+                assert np.array_equal(got[e, :m].astype(np.int64), want)
+            assert np.all(got[e, m:].astype(np.float32) == 7)  # rows past the count untouched
+        if out_type == "bf16":
+            want, valid = O.grouped_gemm_w4a8_masked(a, sa, mm, W4, s4)
+            assert_bf16_equal(bits(out)[valid], want[valid], "w4a8 masked gemm")
+
+
+def test_grouped_gemm_w4a8_extreme_sums():
+    """All codes +-7 against activations +-127 at K = 16384: sums reach
+    127 * 7 * 16384 = 14.6 M, exact in the single float32 pass."""
+    rng = np.random.default_rng(9)
+    a, sa, codes, W4, s4, mm = _w4_problem(rng, [64, 20], 64, 128, 16384, extreme=True)
+    a[0, 0] = 127
+    codes[0, 0] = 7
+    W4 = O.pack_int4(codes)
+    t = lambda x: torch.from_numpy(x).to(DEV)
+    st = wq.new_status()
+    out = wq.grouped_gemm_w4a8_masked(t(a), t(sa), t(mm), t(W4), t(s4), out_type="i32", status=st)
+    assert int(st.item()) == 0
+    got = np_(out)
+    assert got[0, 0, 0] == 127 * 7 * 16384
+    for e in range(2):
+        m = int(mm[e])
+        want = np.einsum("rk,nk->rn", a[e, :m].astype(np.int64), codes[e].astype(np.int64))
+        assert np.array_equal(got[e, :m].astype(np.int64), want)
+
+
+def test_layer_forward_masked_w4a8():
+    E, Mmax, H, I = 4, 80, 256, 256
+    rng = np.random.default_rng(12)
+    g = torch.Generator().manual_seed(12)
+    w13 = (torch.randn(E, 2 * I, H, generator=g) * 0.02).to(torch.bfloat16)
+    w2 = (torch.randn(E, H, I, generator=g) * 0.02).to(torch.bfloat16)
+    x = torch.randn(E * Mmax, H, generator=g).to(torch.bfloat16)
+    mm = np.array([80, 0, 33, 1], np.int32)
+    W13 = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=DEV)
+    W2 = torch.empty(E, H, I // 2, dtype=torch.uint8, device=DEV)
+    S13 = torch.empty(E, 2 * I, device=DEV)
+    S2 = torch.empty(E, H, device=DEV)
+    for e in range(E):
+        W13[e], S13[e] = wq.quantize_weight_int4(w13[e].to(DEV))
+        W2[e], S2[e] = wq.quantize_weight_int4(w2[e].to(DEV))
+    a, sa = wq.quantize_per_token(x.to(DEV))
+    y = torch.full((E, Mmax, H), 3.0, dtype=torch.bfloat16, device=DEV)
+    st = wq.new_status()
+    wq.moe_forward_masked_w4a8(a.view(E, Mmax, H), sa.view(E, Mmax), torch.from_numpy(mm).to(DEV),
+                               W13, S13, W2, S2, y=y, status=st)
+    assert int(st.item()) == 0
+    q13 = [O.quantize_weight_int4(bits(w13[e])) for e in range(E)]
+    q2 = [O.quantize_weight_int4(bits(w2[e])) for e in range(E)]
+    aq, as_ = O.quantize_per_token(bits(x))
+    want, valid = O.moe_forward_masked_w4a8(
+        aq.reshape(E, Mmax, H), as_.reshape(E, Mmax), mm,
+        np.stack([O.pack_int4(q[0]) for q in q13]), np.stack([q[1] for q in q13]),
+        np.stack([O.pack_int4(q[0]) for q in q2]), np.stack([q[1] for q in q2]))
+    got = bits(y)
+    assert_bf16_equal(got[valid], want[valid], "w4a8 masked layer")
+    assert np.all(O.bf16_to_f32(got[~valid]) == 3.0)

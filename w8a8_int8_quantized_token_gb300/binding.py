@@ -52,6 +52,10 @@ _SIGS = {
     "wq_grouped_gemm_w8a8_f16codes": (_I, [_P, _P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
     "wq_quantize_per_token_f16": (_I, [_P, _L, _L, _L, _P, _P, _P, _P]),
     "wq_grouped_gemm_silu_quant_workspace_size": (_S, [_L, _I]),
+    "wq_quantize_weight_int4": (_I, [_P, _L, _L, _P, _P, _P]),
+    "wq_grouped_gemm_w4a8_masked": (_I, [_P, _P, _P, _I, _I, _P, _P, _L, _L, _I, _P, _P, _S, _P, _P]),
+    "wq_moe_forward_masked_w4a8_workspace_size": (_S, [_I, _I, _I, _I]),
+    "wq_moe_forward_masked_w4a8": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _S, _P, _P]),
     "wq_selftest_wait_timeout": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _P, _P, _S, _P, _P]),
     "wq_grouped_gemm_w8a8_silu_quant_f16codes": (_I, [_P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _P, _P, _P, _S, _P, _P]),
     "wq_grouped_gemm_masked_workspace_size": (_S, [_I, _I]),
@@ -482,6 +486,60 @@ def moe_forward_masked(a, sa, masked_m, W13, sw13, W2, sw2, scheme="channel", ac
                                        _ptr(sw13), _ptr(W2), _ptr(sw2), H, I, SCHEME[scheme],
                                        ACC[acc], _ptr(y), _ptr(ws), ws.numel(), _ptr(st),
                                        _stream()), "wq_moe_forward_masked")
+    return y
+
+
+# ---------------------------------------------------------------- W4A8 (int4 weights)
+def quantize_weight_int4(w):
+    """bf16 [N, K] -> (int4 codes two per byte uint8 [N, K/2], scales [N])."""
+    _dev(w, torch.bfloat16, "w")
+    N, K = w.shape
+    q4 = torch.empty(N, K // 2, dtype=torch.uint8, device=w.device)
+    s = torch.empty(N, dtype=torch.float32, device=w.device)
+    _check(lib().wq_quantize_weight_int4(_ptr(w), N, K, _ptr(q4), _ptr(s), _stream()),
+           "wq_quantize_weight_int4")
+    return q4, s
+
+
+def grouped_gemm_w4a8_masked(A, sa, masked_m, W4, s4, out_type="bf16", out=None, status=None):
+    _dev(A, torch.int8, "A")
+    _dev(sa, torch.float32, "sa")
+    _dev(masked_m, torch.int32, "masked_m")
+    _dev(W4, torch.uint8, "W4")
+    _dev(s4, torch.float32, "s4")
+    E, Mmax, K = A.shape
+    N = W4.shape[1]
+    if out is None:
+        out = torch.empty(E, Mmax, N, dtype=torch.bfloat16 if out_type == "bf16" else torch.int32,
+                          device=A.device)
+    nws = lib().wq_grouped_gemm_masked_workspace_size(E, Mmax)
+    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=A.device)
+    st = status if status is not None else new_status(A.device)
+    _check(lib().wq_grouped_gemm_w4a8_masked(_ptr(A), _ptr(sa), _ptr(masked_m), E, Mmax, _ptr(W4),
+                                             _ptr(s4), N, K, OUT[out_type], _ptr(out), _ptr(ws),
+                                             nws, _ptr(st), _stream()),
+           "wq_grouped_gemm_w4a8_masked")
+    return out
+
+
+def moe_forward_masked_w4a8(a, sa, masked_m, W13, s13, W2, s2, y=None, ws=None, status=None):
+    _dev(a, torch.int8, "a")
+    _dev(sa, torch.float32, "sa")
+    _dev(masked_m, torch.int32, "masked_m")
+    _dev(W13, torch.uint8, "W13")
+    _dev(W2, torch.uint8, "W2")
+    E, Mmax, H = a.shape
+    I = W13.shape[1] // 2
+    if y is None:
+        y = torch.empty(E, Mmax, H, dtype=torch.bfloat16, device=a.device)
+    if ws is None:
+        n = lib().wq_moe_forward_masked_w4a8_workspace_size(E, Mmax, H, I)
+        ws = torch.empty(max(n, 1), dtype=torch.uint8, device=a.device)
+    st = status if status is not None else new_status(a.device)
+    _check(lib().wq_moe_forward_masked_w4a8(_ptr(a), _ptr(sa), _ptr(masked_m), E, Mmax, _ptr(W13),
+                                            _ptr(s13), _ptr(W2), _ptr(s2), H, I, _ptr(y), _ptr(ws),
+                                            ws.numel(), _ptr(st), _stream()),
+           "wq_moe_forward_masked_w4a8")
     return y
 
 

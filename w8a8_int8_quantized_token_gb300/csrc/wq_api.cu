@@ -137,6 +137,20 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
   const bool masked = a.masked_m != nullptr;
   GemmWs w = carve_gemm_ws(a.ws, a.R, a.E, a.Mmax, masked, a.fused_hq16 != nullptr);
   const int32_t *gate = nullptr;
+  if (a.w4) {
+    // int4 weights (two codes a byte): the int8-code engine unpacks and widens
+    // them on chip.  With |w| <= 7 and |a| <= 127, ||a||^2 ||w||^2 <=
+    // 127^2 * 7^2 * K^2 < 2^48 for K <= 16384, so every float32 partial sum
+    // is an exact integer, the engine's check always passes and no recompute
+    // follows.  Every tile, however short, runs on this engine.
+    if (a.A == nullptr || a.K > 16384 || !gemm_tc2_supported(a)) return WQ_ERR_UNSUPPORTED;
+    const int rows = gemm_tc2_tile_rows(a);
+    Tile *t = rows == 64 ? w.t64 : w.t256;
+    int32_t *n = rows == 64 ? w.n64 : w.n256;
+    const int64_t m = rows == 64 ? w.m64 : w.m256;
+    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, rows, a.R, t, n, w.redo, st));
+    return launch_gemm_tc2(a, t, n, int(m), w.redo, st);
+  }
   if (a.A16 != nullptr && a.scheme == WQ_SCHEME_BLOCK) {
     // block-wise on fp16 codes: every K block's sum is exact in float32, so
     // the CTA-pair block engine needs no check and no recompute
@@ -778,15 +792,13 @@ size_t carve_masked(void *ws, int E, int Mmax, int H, int I, int scheme, uint16_
 
 }  // namespace
 
-size_t wq_moe_forward_masked_workspace_size(int E, int Mmax, int H, int I, int scheme) {
-  if (E < 1 || Mmax < 0 || H <= 0 || I <= 0) return 0;
-  return carve_masked(nullptr, E, Mmax, H, I, scheme, nullptr, nullptr, nullptr, nullptr, nullptr);
-}
-
-int wq_moe_forward_masked(const int8_t *a, const float *sa, const int32_t *masked_m, int E,
-                          int Mmax, const int8_t *W13, const float *sw13, const int8_t *W2,
-                          const float *sw2, int H, int I, int scheme, int acc, uint16_t *y,
-                          void *ws, size_t ws_bytes, int32_t *status, wq_stream_t stream) {
+namespace wq {
+// The masked layer on W8A8 weights, or (w4) on int4 weights packed two per
+// byte: GEMM1 -> SiLU-mul + re-quantization -> GEMM2 on the valid rows.
+int forward_masked(const int8_t *a, const float *sa, const int32_t *masked_m, int E, int Mmax,
+                   const int8_t *W13, const float *sw13, const int8_t *W2, const float *sw2, int H,
+                   int I, int scheme, int acc, bool w4, uint16_t *y, void *ws, size_t ws_bytes,
+                   int32_t *status, cudaStream_t stream) {
   if (E < 1 || E > 4096 || Mmax < 0 || H <= 0 || I <= 0) return WQ_ERR_INVALID_ARG;
   if (scheme != WQ_SCHEME_CHANNEL && scheme != WQ_SCHEME_BLOCK) return WQ_ERR_INVALID_ARG;
   if (acc != WQ_ACC_I32 && acc != WQ_ACC_F32) return WQ_ERR_INVALID_ARG;
@@ -806,12 +818,73 @@ int wq_moe_forward_masked(const int8_t *a, const float *sa, const int32_t *maske
   const int64_t R = int64_t(E) * Mmax;
   GemmArgs g1{a, nullptr, nullptr, sa, W13, sw13, nullptr, masked_m, Mmax, E, R, int64_t(2) * I, H, scheme, acc,
               WQ_OUT_BF16, gu, gws, status};
+  g1.w4 = w4 ? 1 : 0;
   WQ_TRY(launch_grouped_gemm(g1, stream));
   WQ_TRY(launch_silu_mul_quant(gu, R, I, scheme == WQ_SCHEME_BLOCK ? 128 : 0, masked_m, Mmax, hq,
                                sh, stream));
   GemmArgs g2{hq, nullptr, nullptr, sh, W2, sw2, nullptr, masked_m, Mmax, E, R, H, I, scheme, acc, WQ_OUT_BF16, y,
               gws, status};
+  g2.w4 = w4 ? 1 : 0;
   return launch_grouped_gemm(g2, stream);
+}
+}  // namespace wq
+
+
+size_t wq_moe_forward_masked_workspace_size(int E, int Mmax, int H, int I, int scheme) {
+  if (E < 1 || Mmax < 0 || H <= 0 || I <= 0) return 0;
+  return carve_masked(nullptr, E, Mmax, H, I, scheme, nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+int wq_moe_forward_masked(const int8_t *a, const float *sa, const int32_t *masked_m, int E,
+                          int Mmax, const int8_t *W13, const float *sw13, const int8_t *W2,
+                          const float *sw2, int H, int I, int scheme, int acc, uint16_t *y,
+                          void *ws, size_t ws_bytes, int32_t *status, wq_stream_t stream) {
+  return wq::forward_masked(a, sa, masked_m, E, Mmax, W13, sw13, W2, sw2, H, I, scheme, acc, false,
+                            y, ws, ws_bytes, status, stream);
+}
+
+int wq_quantize_weight_int4(const uint16_t *w, int64_t N, int64_t K, uint8_t *q4, float *s,
+                            wq_stream_t stream) {
+  if (N < 0 || K < 0) return WQ_ERR_INVALID_ARG;
+  if (N == 0 || K == 0) return WQ_OK;
+  if (!w || !q4 || !s) return WQ_ERR_INVALID_ARG;
+  if (K % 8 || !al16(w) || (reinterpret_cast<uintptr_t>(q4) & 3u)) return WQ_ERR_UNSUPPORTED;
+  if (N >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;
+  WQ_TRY(check_device());
+  return launch_quant_weight_int4(w, N, K, q4, s, stream);
+}
+
+int wq_grouped_gemm_w4a8_masked(const int8_t *A, const float *sa, const int32_t *masked_m, int E,
+                                int Mmax, const uint8_t *W4, const float *s4, int64_t N,
+                                int64_t K, int out_type, void *out, void *ws, size_t ws_bytes,
+                                int32_t *status, wq_stream_t stream) {
+  if (Mmax < 0 || E > 4096) return WQ_ERR_INVALID_ARG;
+  if (Mmax == 0) return WQ_OK;
+  WQ_TRY(check_gemm_common(reinterpret_cast<const int8_t *>(W4), s4, E, N, K, WQ_SCHEME_CHANNEL,
+                           WQ_ACC_I32, out_type, out));
+  if (!A || !sa || !masked_m) return WQ_ERR_INVALID_ARG;
+  if (!al16(A) || K > 16384 || int64_t(E) * Mmax >= (int64_t(1) << 31)) return WQ_ERR_UNSUPPORTED;
+  const int64_t R = int64_t(E) * Mmax;
+  if (ws_bytes < gemm_ws_bytes(R, E, Mmax, true) || !ws) return WQ_ERR_WORKSPACE;
+  WQ_TRY(check_device());
+  GemmArgs g{A, nullptr, nullptr, sa, reinterpret_cast<const int8_t *>(W4), s4, nullptr, masked_m,
+             Mmax, E, R, N, K, WQ_SCHEME_CHANNEL, WQ_ACC_I32, out_type, out, ws, status};
+  g.w4 = 1;
+  return launch_grouped_gemm(g, stream);
+}
+
+size_t wq_moe_forward_masked_w4a8_workspace_size(int E, int Mmax, int H, int I) {
+  return wq_moe_forward_masked_workspace_size(E, Mmax, H, I, WQ_SCHEME_CHANNEL);
+}
+
+int wq_moe_forward_masked_w4a8(const int8_t *a, const float *sa, const int32_t *masked_m, int E,
+                               int Mmax, const uint8_t *W13, const float *s13, const uint8_t *W2,
+                               const float *s2, int H, int I, uint16_t *y, void *ws,
+                               size_t ws_bytes, int32_t *status, wq_stream_t stream) {
+  if (H > 16384 || I > 16384) return WQ_ERR_UNSUPPORTED;
+  return wq::forward_masked(a, sa, masked_m, E, Mmax, reinterpret_cast<const int8_t *>(W13), s13,
+                            reinterpret_cast<const int8_t *>(W2), s2, H, I, WQ_SCHEME_CHANNEL,
+                            WQ_ACC_I32, true, y, ws, ws_bytes, status, stream);
 }
 
 }  // extern "C"

@@ -196,6 +196,9 @@ int launch_convert_fp8(const uint8_t *w8, const float *s8, int64_t N, int64_t K,
                        int8_t *q, float *s, cudaStream_t st);
 int launch_quant_weight_block(const uint16_t *w, int64_t N, int64_t K, int8_t *q, float *s,
                               cudaStream_t st);
+// int4 weights, one scale per row, two codes per byte (low nibble first)
+int launch_quant_weight_int4(const uint16_t *w, int64_t N, int64_t K, uint8_t *q4, float *s,
+                             cudaStream_t st);
 int launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w, cudaStream_t st);
 size_t align_ws_bytes(int T, int k, int E);
 int launch_align(const int32_t *ids, int T, int k, int E, int pad_m, int32_t *counts,
@@ -242,6 +245,7 @@ struct GemmArgs {
   float *fused_sh = nullptr;
   const float *fused_silu_tab = nullptr;  // silu_tab entries (set by the dispatcher)
   int wait_test = 0;  // failure-path test: a wait that nothing completes (block engine)
+  int w4 = 0;         // W holds int4 codes, two per byte (low nibble first): [E][N][K/2]
 };
 // The single-pass float32 engines serve both channel-wise accumulator modes.
 // In the float32 mode the accumulator is the running sum, over 128-wide K

@@ -161,6 +161,51 @@ int launch_quant_rows_f16(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, 
 }
 
 // ---------------------------------------------------------------------------
+// int4 weights for the w4a8 path ("Support DeepSeek-R1 w4a8 low latency
+// deepep", Highlights; the page fixes no format, read as symmetric codes per
+// output channel): per row a = max|w|, s = max(a, 1e-10) / 7,
+// q = clamp(rint(w / s), -7, 7) with the exact quotient's rounding (as
+// quant_bits; the clamp never binds, |w / s| <= 7 (1 + 2^-23)), two codes
+// per byte with code 2j in the low nibble.  One CTA per row, 8 values a step.
+__global__ void __launch_bounds__(256) quant_w4_row_kernel(const uint16_t *__restrict__ w, int64_t K,
+                                                           uint8_t *__restrict__ q4,
+                                                           float *__restrict__ s) {
+  __shared__ float red[32];
+  const int64_t row = blockIdx.x;
+  const uint4 *src = reinterpret_cast<const uint4 *>(w + row * K);
+  const int nvec = int(K >> 3);
+  float amax = 0.0f;
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    float f[8];
+    unpack8(src[v], f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+  }
+  amax = block_max(amax, red);
+  const float sc = __fdiv_rn(fmaxf(amax, 1e-10f), 7.0f);
+  const float rs = __frcp_rn(sc);
+  uint32_t *dst = reinterpret_cast<uint32_t *>(q4 + row * (K / 2));
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    float f[8];
+    unpack8(src[v], f);
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) word |= (quant_bits(f[j], sc, rs) & 0xFu) << (4 * j);
+    dst[v] = word;
+  }
+  if (threadIdx.x == 0) s[row] = sc;
+}
+
+int launch_quant_weight_int4(const uint16_t *w, int64_t N, int64_t K, uint8_t *q4, float *s,
+                             cudaStream_t st) {
+  if (N <= 0) return WQ_OK;
+  const int64_t nvec = K / 8;
+  const int th = nvec >= 256 ? 256 : int((nvec + 31) / 32 * 32);
+  quant_w4_row_kernel<<<unsigned(N), th, 0, st>>>(w, K, q4, s);
+  return launched(1);
+}
+
+// ---------------------------------------------------------------------------
 // FP8 (e4m3, one float32 scale per [128,128] block) -> BF16 -> INT8 weight
 // conversion (Meituan INT8 article, 量化技术的探索: DeepSeek releases FP8
 // weights only, so they are dequantized to BF16 and then quantized to INT8,

@@ -53,10 +53,12 @@ constexpr int ITEM_READERS = 1 + NCONV / 32 + 4;
 // TN suits many rows per expert (prefill); a small TN with a deep int8 ring
 // keeps enough weight bytes in flight when experts hold a few tokens each
 // (decode), where the GEMM streams weights from HBM.
-template <int TN, int S8, int S16>
+template <int TN, int S8, int S16, bool W4>
 struct Plan {
-  static constexpr int W8 = WM * BK, T8 = TN * BK;  // int8 bytes per stage
-  static constexpr int W16 = 2 * W8, T16 = 2 * T8;  // fp16 bytes per stage
+  // bytes per stage: W8 the staged weight codes (int8, or int4 two per byte),
+  // T8 the int8 token codes; W16 / T16 the widened fp16 tiles
+  static constexpr int W8 = WM * BK / (W4 ? 2 : 1), T8 = TN * BK;
+  static constexpr int W16 = 2 * WM * BK, T16 = 2 * T8;
   static constexpr int ST8 = W8 + T8, ST16 = W16 + T16;
   static constexpr int OFF_F16 = 0;
   static constexpr int OFF_I8 = OFF_F16 + S16 * ST16;
@@ -85,14 +87,25 @@ struct Plan {
 
 __device__ __forceinline__ int sq4(uint32_t w, int acc) { return __dp4a(int(w), int(w), acc); }
 
-template <int TN, int S8, int S16>
+// Eight int4 codes (code j in bits 4j..4j+3, two's complement) -> eight int8
+// codes: codes 0-3 in lo, 4-7 in hi (byte i = code i).  The even and odd
+// nibbles are masked out per byte, sign-extended as (n ^ 8) - 8 per byte, and
+// interleaved back into code order.
+__device__ __forceinline__ void s4x8_to_s8x8(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t e = __vsub4((w & 0x0F0F0F0Fu) ^ 0x08080808u, 0x08080808u);         // codes 0,2,4,6
+  const uint32_t o = __vsub4(((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u, 0x08080808u);  // codes 1,3,5,7
+  lo = __byte_perm(e, o, 0x5140);
+  hi = __byte_perm(e, o, 0x7362);
+}
+
+template <int TN, int S8, int S16, bool W4>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT16,
                     const __grid_constant__ CUtensorMap tmT64,
                     const __grid_constant__ CUtensorMap tmT256, const GemmArgs a,
                     const Tile *__restrict__ tiles, const int32_t *__restrict__ ntiles,
                     int32_t *__restrict__ redo, int32_t *__restrict__ claim) {
-  using P = Plan<TN, S8, S16>;
+  using P = Plan<TN, S8, S16, W4>;
   constexpr int W8 = P::W8, W16 = P::W16, ST8 = P::ST8, ST16 = P::ST16;
   constexpr int OFF_F16 = P::OFF_F16, OFF_I8 = P::OFF_I8, OFF_BAR = P::OFF_BAR;
   constexpr int B_S8_FULL = P::B_S8_FULL, B_S8_EMPTY = P::B_S8_EMPTY, B_F16_FULL = P::B_F16_FULL,
@@ -197,7 +210,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           const uint32_t dst = base + OFF_I8 + uint32_t(s8) * ST8;
           mbar_expect_tx(bar(B_S8_FULL + s8), tx);
-          tma_load_2d(dst, &tmW, i * BK, wrow, bar(B_S8_FULL + s8));
+          tma_load_2d(dst, &tmW, i * (W4 ? BK / 2 : BK), wrow, bar(B_S8_FULL + s8));  // bytes
           tma_load_2d(dst + W8, tmT, i * BK, tl.row0, bar(B_S8_FULL + s8));
         }
         it = next;
@@ -281,12 +294,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const uint8_t *src = sm + OFF_I8 + s8 * ST8;
         uint4 v[NJW + NJT];
+        if constexpr (W4) {
+          // packed piece c4 = 32 codes: row c4 >> 1, codes 32 * (c4 & 1) onwards
 #pragma unroll
-        for (int j = 0; j < NJW + NJT; ++j) {
-          const int c = (j < NJW ? j : j - NJW) * GCONV + t;
-          v[j] = (j < NJW || c < tchunks)
-                     ? *reinterpret_cast<const uint4 *>(src + (j < NJW ? 0 : W8) + c * 16)
-                     : make_uint4(0, 0, 0, 0);
+          for (int j = 0; j < NJW / 2; ++j) {
+            const uint4 p = *reinterpret_cast<const uint4 *>(src + (j * GCONV + t) * 16);
+            s4x8_to_s8x8(p.x, v[2 * j].x, v[2 * j].y);
+            s4x8_to_s8x8(p.y, v[2 * j].z, v[2 * j].w);
+            s4x8_to_s8x8(p.z, v[2 * j + 1].x, v[2 * j + 1].y);
+            s4x8_to_s8x8(p.w, v[2 * j + 1].z, v[2 * j + 1].w);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < NJW; ++j)
+            v[j] = *reinterpret_cast<const uint4 *>(src + (j * GCONV + t) * 16);
+        }
+#pragma unroll
+        for (int j = NJW; j < NJW + NJT; ++j) {
+          const int c = (j - NJW) * GCONV + t;
+          v[j] = c < tchunks ? *reinterpret_cast<const uint4 *>(src + W8 + c * 16)
+                             : make_uint4(0, 0, 0, 0);
         }
         fence_async_smem();  // these reads before the next copy into the slot
         __syncwarp();
@@ -302,8 +329,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int j = 0; j < NJW + NJT; ++j) {
           const int c = (j < NJW ? j : j - NJW) * GCONV + t;
           if (j < NJW || c < tchunks) {
-            const int row = c >> 2;
-            store_f16_row_piece(dst + (j < NJW ? 0 : W16) + row * 128, row, c & 3, v[j]);
+            // 16 int8 codes: row and 16-code part within the 64-code stage row
+            int row = c >> 2, part = c & 3;
+            if (W4 && j < NJW) {
+              const int c4 = (j >> 1) * GCONV + t;
+              row = c4 >> 1;
+              part = 2 * (c4 & 1) + (j & 1);
+            }
+            store_f16_row_piece(dst + (j < NJW ? 0 : W16) + row * 128, row, part, v[j]);
             nrm[j] += sq4(v[j].w, sq4(v[j].z, 0)) + sq4(v[j].y, sq4(v[j].x, 0));
           }
         }
@@ -318,6 +351,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       int wmax = 0, tmax = 0;
 #pragma unroll
       for (int j = 0; j < NJW + NJT; ++j) {
+        if (W4 && j < NJW) {
+          // int4: a row's 64 codes of a stage are the two pieces of one
+          // thread and its neighbour t ^ 1
+          if (j & 1) continue;
+          int n2 = nrm[j] + nrm[j + 1];
+          n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
+          wmax = max(wmax, n2);
+          continue;
+        }
         int n2 = nrm[j];
         n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
         n2 += __shfl_xor_sync(0xffffffffu, n2, 2);
@@ -448,18 +490,19 @@ int gemm_tc2_tile_rows(const GemmArgs &a) {
   return rows <= int64_t(64) * a.E ? 64 : 256;
 }
 
-template <int TN, int S8, int S16>
+template <int TN, int S8, int S16, bool W4>
 int launch_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
                int32_t *redo, cudaStream_t st) {
-  using P = Plan<TN, S8, S16>;
+  using P = Plan<TN, S8, S16, W4>;
   CUtensorMap mW, m16, m64, m256;
-  if (!make_tma_2d_u8(&mW, a.W, int64_t(a.E) * a.N, a.K, BK, WM) ||
+  // int4 weights: K / 2 bytes a row, a 32-byte box per 64-code stage
+  if (!make_tma_2d_u8(&mW, a.W, int64_t(a.E) * a.N, W4 ? a.K / 2 : a.K, W4 ? BK / 2 : BK, WM) ||
       !make_tma_2d_u8(&m16, a.A, a.R, a.K, BK, 16) || !make_tma_2d_u8(&m64, a.A, a.R, a.K, BK, 64) ||
       !make_tma_2d_u8(&m256, a.A, a.R, a.K, BK, TN > 64 ? 256 : 64))
     return WQ_ERR_LAUNCH;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(gemm_tc2_kernel<TN, S8, S16>,
+    if (cudaFuncSetAttribute(gemm_tc2_kernel<TN, S8, S16, W4>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES) != cudaSuccess)
       return WQ_ERR_LAUNCH;
     attr = true;
@@ -467,8 +510,9 @@ int launch_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int 
   const int64_t max_items = int64_t(max_tiles) * (a.N / WM);
   const int grid = int(max_items < num_sms() ? max_items : num_sms());
   // redo[1] is the item counter (zeroed with the flag by the tile builder)
-  gemm_tc2_kernel<TN, S8, S16><<<grid, NTHREADS, P::SMEM_BYTES, st>>>(mW, m16, m64, m256, a, tiles,
-                                                                      ntiles, redo, redo + 1);
+  gemm_tc2_kernel<TN, S8, S16, W4><<<grid, NTHREADS, P::SMEM_BYTES, st>>>(mW, m16, m64, m256, a,
+                                                                          tiles, ntiles, redo,
+                                                                          redo + 1);
   return launched(1);
 }
 
@@ -476,8 +520,13 @@ int launch_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int 
 int launch_gemm_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
                     int32_t *redo, cudaStream_t st) {
   if (max_tiles <= 0) return WQ_OK;
-  if (gemm_tc2_tile_rows(a) == 64) return launch_tc2<64, 8, 4>(a, tiles, ntiles, max_tiles, redo, st);
-  return launch_tc2<256, 3, 3>(a, tiles, ntiles, max_tiles, redo, st);
+  const bool small = gemm_tc2_tile_rows(a) == 64;
+  if (a.w4) {
+    return small ? launch_tc2<64, 8, 4, true>(a, tiles, ntiles, max_tiles, redo, st)
+                 : launch_tc2<256, 3, 3, true>(a, tiles, ntiles, max_tiles, redo, st);
+  }
+  return small ? launch_tc2<64, 8, 4, false>(a, tiles, ntiles, max_tiles, redo, st)
+               : launch_tc2<256, 3, 3, false>(a, tiles, ntiles, max_tiles, redo, st);
 }
 
 }  // namespace wq
