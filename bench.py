@@ -102,15 +102,16 @@ def tensor_peak(peaks, clocks):
 
 
 def gemm_roofline(peaks, src, clocks, ms, rows, touched, N, K, scheme, code_bytes, traffic,
-                  kernel):
+                  kernel, weight_bytes=1.0):
     """Roofline of one grouped GEMM launch: algorithmic flops 2*rows*N*K and
     bytes (touched experts' int8 weights and scales, the activation codes and
     scales, the bf16 output), bound by whichever of the measured bf16 dense
     rate (tcgen05 kind::f16 runs at it) and the measured HBM copy bandwidth
-    the arithmetic intensity reaches first."""
+    the arithmetic intensity reaches first.  weight_bytes: bytes per weight
+    code (1 for int8, 0.5 for int4)."""
     blk = scheme == "block"
     flops = 2.0 * rows * N * K
-    nbytes = (touched * N * K + touched * ((N // 128) * (K // 128) if blk else N) * 4
+    nbytes = (touched * N * K * weight_bytes + touched * ((N // 128) * (K // 128) if blk else N) * 4
               + rows * K * code_bytes + rows * (K // 128 if blk else 1) * 4 + rows * N * 2)
     tf, which = tensor_peak(peaks, clocks)
     bw = peaks["hbm_gbs"]
@@ -441,12 +442,28 @@ def run_reference(args, cfg):
     print(json.dumps(line), flush=True)
 
 
-def run_masked(args, cfg):
+def make_weights_int4(wq, cfg, dev):
+    """Each expert's bf16 weights drawn on the device and quantized to int4
+    codes (two per byte) with per-channel scales by the library."""
+    E, I, H = cfg.E, cfg.I, cfg.H
+    W13 = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=dev)
+    W2 = torch.empty(E, H, I // 2, dtype=torch.uint8, device=dev)
+    S13 = torch.empty(E, 2 * I, dtype=torch.float32, device=dev)
+    S2 = torch.empty(E, H, dtype=torch.float32, device=dev)
+    for e in range(E):
+        w13, w2 = synth.expert_weights(cfg, e, device=dev)
+        W13[e], S13[e] = wq.quantize_weight_int4(w13)
+        W2[e], S2[e] = wq.quantize_weight_int4(w2)
+    return W13, S13, W2, S2
+
+
+def run_masked(args, cfg, w4=False):
     """The masked (expert-parallel-shaped) layout: per-expert buffers
     [E, Mmax, H] of int8 codes with per-row scales and Zipf(1.2) valid counts;
     one step = wq_moe_forward_masked (GEMM1 -> SiLU-mul + re-quantize -> GEMM2
-    on the valid rows).  GEMM1 alone is timed in a second pass for the
-    roofline figure."""
+    on the valid rows), or with w4 its int4-weight form
+    wq_moe_forward_masked_w4a8.  GEMM1 alone is timed in a second pass for
+    the roofline figure."""
     from w8a8_int8_quantized_token_gb300 import binding as wq
     from w8a8_int8_quantized_token_gb300 import build_lib
     dev = torch.device("cuda", 0)
@@ -454,7 +471,7 @@ def run_masked(args, cfg):
     build_lib.build()
     wq.init(0)
     E, Mmax, H, I = cfg.E, cfg.Mmax, cfg.H, cfg.I
-    weights = make_weights(wq, cfg, dev)
+    weights = make_weights_int4(wq, cfg, dev) if w4 else make_weights(wq, cfg, dev)
     xm, mm = synth.masked_inputs(cfg, device=dev)
     a, sa = wq.quantize_per_token(xm.reshape(E * Mmax, H))
     a, sa = a.view(E, Mmax, H), sa.view(E, Mmax)
@@ -463,7 +480,11 @@ def run_masked(args, cfg):
     n = wq.lib().wq_moe_forward_masked_workspace_size(E, Mmax, H, I, SCHEME[cfg.scheme])
     ws = torch.empty(n, dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    step = lambda: wq.moe_forward_masked(a, sa, mmd, *weights, cfg.scheme, cfg.acc, y=y, ws=ws, status=st)
+    if w4:
+        step = lambda: wq.moe_forward_masked_w4a8(a, sa, mmd, *weights, y=y, ws=ws, status=st)
+    else:
+        step = lambda: wq.moe_forward_masked(a, sa, mmd, *weights, cfg.scheme, cfg.acc, y=y, ws=ws,
+                                             status=st)
     for _ in range(args.warmup):
         step()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -480,8 +501,12 @@ def run_masked(args, cfg):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / args.steps
         gu = torch.empty(E, Mmax, 2 * I, dtype=torch.bfloat16, device=dev)
-        g1 = lambda: wq.grouped_gemm_w8a8_masked(a, sa, mmd, weights[0], weights[1], cfg.scheme,
-                                                 cfg.acc, out=gu, status=st)
+        if w4:
+            g1 = lambda: wq.grouped_gemm_w4a8_masked(a, sa, mmd, weights[0], weights[1], out=gu,
+                                                     status=st)
+        else:
+            g1 = lambda: wq.grouped_gemm_w8a8_masked(a, sa, mmd, weights[0], weights[1], cfg.scheme,
+                                                     cfg.acc, out=gu, status=st)
         for _ in range(args.warmup):
             g1()
         torch.cuda.synchronize()
@@ -498,15 +523,20 @@ def run_masked(args, cfg):
     ops = 2.0 * rows * 3 * H * I
     peaks, src = load_peaks()
     touched = int((mm > 0).sum())
+    wb = 0.5 if w4 else 1.0  # bytes per weight code
     roofline = gemm_roofline(peaks, src, clocks, g1_ms, rows, touched, 2 * I, H, cfg.scheme, 1,
-                             measured_traffic(cfg.name), "grouped_gemm_w8a8_masked gate_up (GEMM1)")
+                             None if w4 else measured_traffic(cfg.name),
+                             ("grouped_gemm_w4a8_masked" if w4 else "grouped_gemm_w8a8_masked")
+                             + " gate_up (GEMM1)", weight_bytes=wb)
     # minimal bytes: touched experts' weights and scales, valid rows' codes and
     # scales in, bf16 outputs of the valid rows
-    nbytes = touched * (3 * H * I + (2 * I + H) * 4) + rows * (H + 4) + rows * H * 2
+    nbytes = int(touched * (3 * H * I * wb + (2 * I + H) * 4) + rows * (H + 4) + rows * H * 2)
     line = {"metric": METRIC, "value": ops / (ms / 1e3) / 1e12, "unit": "TOPS", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-            "config": {"workload": f"masked-layout W8A8 grouped FFN: {E} local experts x {Mmax} rows, "
+            "scaling": "weak", "vs_baseline": None, "dtype": "int4 x int8" if w4 else "int8",
+            "data": "synthetic",
+            "config": {"workload": f"masked-layout {'W4A8 (int4 weights)' if w4 else 'W8A8'} grouped "
+                                   f"FFN: {E} local experts x {Mmax} rows, "
                                    f"hidden {H}, intermediate {I}, valid rows Zipf(1.2) = {rows}",
                        "parallelism": "single"},
             "tokens_per_s": rows / (ms / 1e3), "gemm1_ms": g1_ms, "gpu_launches": launches,
@@ -673,7 +703,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", default="prefill",
-                    choices=list(synth.CONFIGS) + list(LINEAR) + ["convert"])
+                    choices=list(synth.CONFIGS) + list(LINEAR) + ["convert", "masked_w4a8"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -698,6 +728,9 @@ def main():
         return
     if args.config == "convert":
         run_convert(args)
+        return
+    if args.config == "masked_w4a8":
+        run_masked(args, synth.CONFIGS["masked"], w4=True)
         return
     if cfg.masked:
         run_masked(args, cfg)

@@ -142,13 +142,17 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
     // them on chip.  With |w| <= 7 and |a| <= 127, ||a||^2 ||w||^2 <=
     // 127^2 * 7^2 * K^2 < 2^48 for K <= 16384, so every float32 partial sum
     // is an exact integer, the engine's check always passes and no recompute
-    // follows.  Every tile, however short, runs on this engine.
+    // follows.  Remainders of at most 16 rows go to the small-token engine,
+    // which reads the packed codes (half the bytes of int8 weights).
     if (a.A == nullptr || a.K > 16384 || !gemm_tc2_supported(a)) return WQ_ERR_UNSUPPORTED;
+    const bool small = gemm_small_supported(a);
     const int rows = gemm_tc2_tile_rows(a);
     Tile *t = rows == 64 ? w.t64 : w.t256;
     int32_t *n = rows == 64 ? w.n64 : w.n256;
     const int64_t m = rows == 64 ? w.m64 : w.m256;
-    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, rows, a.R, t, n, w.redo, st));
+    WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, rows, a.R, t, n, w.redo, st,
+                              small ? gemm_small_max_rows() : 0, w.tsm, w.nsm));
+    if (small) WQ_TRY(launch_gemm_small(a, w.tsm, w.nsm, int(w.msm), st));
     return launch_gemm_tc2(a, t, n, int(m), w.redo, st);
   }
   if (a.A16 != nullptr && a.scheme == WQ_SCHEME_BLOCK) {

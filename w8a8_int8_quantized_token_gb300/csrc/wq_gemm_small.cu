@@ -56,7 +56,7 @@ __device__ __forceinline__ int token_box(int rows) {
 // One item for a consumer thread: NT token rows are resident per stage (the
 // tile's valid rows first); row r of the 256-channel weight tile is this
 // thread's channel.  Returns false if a wait gave up.
-template <int NT>
+template <int NT, bool W4>
 __device__ __forceinline__ bool consume_item(const GemmArgs &a, const Tile &tl, int nb, int KT,
                                              const uint8_t *sm, uint32_t base, int &g, int r,
                                              volatile int *abort_flag) {
@@ -78,18 +78,48 @@ __device__ __forceinline__ bool consume_item(const GemmArgs &a, const Tile &tl, 
     const int s = g % STAGES;
     if (!mbar_wait(base + OFF_BAR + 8u * uint32_t(s), uint32_t(g / STAGES) & 1u, abort_flag))
       return false;
-    const uint8_t *wrow = sm + s * ST_BYTES + r * BK;
     const uint8_t *tk = sm + s * ST_BYTES + W_BYTES;
+    if constexpr (W4) {
+      // int4 weights: 64 bytes (128 codes) of this channel's row, unswizzled;
+      // chunk (c + r/2) % 4 at step c, so the 8 rows of a quarter warp hit
+      // all 32 banks once; each chunk is 32 codes against 32 token bytes
+      const uint8_t *wrow = sm + s * ST_BYTES + r * (BK / 2);
 #pragma unroll
-    for (int c = 0; c < BK / 16; ++c) {
-      const uint4 w = *reinterpret_cast<const uint4 *>(wrow + ((c ^ sw8) << 4));
+      for (int c = 0; c < 4; ++c) {
+        const int cc = (c + (r >> 1)) & 3;
+        const uint4 p = *reinterpret_cast<const uint4 *>(wrow + cc * 16);
+        uint32_t w8[8];
+        s4x8_to_s8x8(p.x, w8[0], w8[1]);
+        s4x8_to_s8x8(p.y, w8[2], w8[3]);
+        s4x8_to_s8x8(p.z, w8[4], w8[5]);
+        s4x8_to_s8x8(p.w, w8[6], w8[7]);
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const uint4 x = *reinterpret_cast<const uint4 *>(tk + t * BK + c * 16);
-        acc[t] = __dp4a(int(w.x), int(x.x), acc[t]);
-        acc[t] = __dp4a(int(w.y), int(x.y), acc[t]);
-        acc[t] = __dp4a(int(w.z), int(x.z), acc[t]);
-        acc[t] = __dp4a(int(w.w), int(x.w), acc[t]);
+        for (int t = 0; t < NT; ++t) {
+          const uint4 x0 = *reinterpret_cast<const uint4 *>(tk + t * BK + cc * 32);
+          const uint4 x1 = *reinterpret_cast<const uint4 *>(tk + t * BK + cc * 32 + 16);
+          acc[t] = __dp4a(int(w8[0]), int(x0.x), acc[t]);
+          acc[t] = __dp4a(int(w8[1]), int(x0.y), acc[t]);
+          acc[t] = __dp4a(int(w8[2]), int(x0.z), acc[t]);
+          acc[t] = __dp4a(int(w8[3]), int(x0.w), acc[t]);
+          acc[t] = __dp4a(int(w8[4]), int(x1.x), acc[t]);
+          acc[t] = __dp4a(int(w8[5]), int(x1.y), acc[t]);
+          acc[t] = __dp4a(int(w8[6]), int(x1.z), acc[t]);
+          acc[t] = __dp4a(int(w8[7]), int(x1.w), acc[t]);
+        }
+      }
+    } else {
+      const uint8_t *wrow = sm + s * ST_BYTES + r * BK;
+#pragma unroll
+      for (int c = 0; c < BK / 16; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(wrow + ((c ^ sw8) << 4));
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const uint4 x = *reinterpret_cast<const uint4 *>(tk + t * BK + c * 16);
+          acc[t] = __dp4a(int(w.x), int(x.x), acc[t]);
+          acc[t] = __dp4a(int(w.y), int(x.y), acc[t]);
+          acc[t] = __dp4a(int(w.z), int(x.z), acc[t]);
+          acc[t] = __dp4a(int(w.w), int(x.w), acc[t]);
+        }
       }
     }
     fence_async_smem();  // these reads before the next copy into the slot
@@ -139,6 +169,7 @@ __device__ __forceinline__ bool consume_item(const GemmArgs &a, const Tile &tl, 
   return true;
 }
 
+template <bool W4>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_small_kernel(const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmT4,
@@ -178,7 +209,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int nb = it % NB;
         const int box = token_box(tl.rows);
         const CUtensorMap *tmT = box == 4 ? &tmT4 : (box == 8 ? &tmT8 : &tmT16);
-        const uint32_t tx = uint32_t(W_BYTES + box * BK);
+        const uint32_t tx = uint32_t((W4 ? W_BYTES / 2 : W_BYTES) + box * BK);
         const int wrow = int(int64_t(tl.expert) * a.N + int64_t(nb) * WN);
         for (int i = 0; i < KT; ++i, ++g) {
           const int s = g % STAGES;
@@ -190,7 +221,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           const uint32_t dst = base + uint32_t(s) * ST_BYTES;
           mbar_expect_tx(full(s), tx);
-          tma_load_2d(dst, &tmW, i * BK, wrow, full(s));
+          tma_load_2d(dst, &tmW, i * (W4 ? BK / 2 : BK), wrow, full(s));  // bytes
           tma_load_2d(dst + W_BYTES, tmT, i * BK, tl.row0, full(s));
         }
       }
@@ -208,11 +239,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int box = token_box(tl.rows);
       bool ok;
       if (box == 4)
-        ok = consume_item<4>(a, tl, nb, KT, sm, base, g, r, abort_flag);
+        ok = consume_item<4, W4>(a, tl, nb, KT, sm, base, g, r, abort_flag);
       else if (box == 8)
-        ok = consume_item<8>(a, tl, nb, KT, sm, base, g, r, abort_flag);
+        ok = consume_item<8, W4>(a, tl, nb, KT, sm, base, g, r, abort_flag);
       else
-        ok = consume_item<16>(a, tl, nb, KT, sm, base, g, r, abort_flag);
+        ok = consume_item<16, W4>(a, tl, nb, KT, sm, base, g, r, abort_flag);
       if (!ok) {
         *abort_flag = 1;
         set_status(a.status, WQ_ERR_TIMEOUT);
@@ -225,6 +256,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }  // namespace
 
 bool gemm_small_supported(const GemmArgs &a) {
+  if (a.w4 && (a.scheme != WQ_SCHEME_CHANNEL || a.acc != WQ_ACC_I32)) return false;
   return a.A != nullptr && a.K % BK == 0 && a.K <= 65536 && a.N % 32 == 0 &&
          (a.scheme == WQ_SCHEME_CHANNEL || a.scheme == WQ_SCHEME_BLOCK) &&
          int64_t(a.E) * a.N < (int64_t(1) << 31) && a.R < (int64_t(1) << 31) && tma_available();
@@ -237,20 +269,24 @@ int launch_gemm_small(const GemmArgs &a, const Tile *tiles, const int32_t *ntile
                       cudaStream_t st) {
   if (max_tiles <= 0) return WQ_OK;
   CUtensorMap mW, m4, m8, m16;
-  if (!make_tma_2d_u8_sw128(&mW, a.W, int64_t(a.E) * a.N, a.K, WN) ||
-      !make_tma_2d_u8(&m4, a.A, a.R, a.K, BK, 4) || !make_tma_2d_u8(&m8, a.A, a.R, a.K, BK, 8) ||
-      !make_tma_2d_u8(&m16, a.A, a.R, a.K, BK, 16))
+  // int8 weights: 128-byte rows per stage, 128-byte swizzled; int4 weights
+  // (two codes a byte): 64-byte rows per stage, unswizzled
+  const bool wok = a.w4 ? make_tma_2d_u8(&mW, a.W, int64_t(a.E) * a.N, a.K / 2, BK / 2, WN)
+                        : make_tma_2d_u8_sw128(&mW, a.W, int64_t(a.E) * a.N, a.K, WN);
+  if (!wok || !make_tma_2d_u8(&m4, a.A, a.R, a.K, BK, 4) ||
+      !make_tma_2d_u8(&m8, a.A, a.R, a.K, BK, 8) || !make_tma_2d_u8(&m16, a.A, a.R, a.K, BK, 16))
     return WQ_ERR_LAUNCH;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(gemm_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES) != cudaSuccess)
+  static bool attr[2] = {false, false};
+  auto kern = a.w4 ? gemm_small_kernel<true> : gemm_small_kernel<false>;
+  if (!attr[a.w4 ? 1 : 0]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+        cudaSuccess)
       return WQ_ERR_LAUNCH;
-    attr = true;
+    attr[a.w4 ? 1 : 0] = true;
   }
   const int64_t max_items = int64_t(max_tiles) * ((a.N + WN - 1) / WN);
   const int grid = int(max_items < num_sms() ? max_items : num_sms());
-  gemm_small_kernel<<<grid, NTHREADS, SMEM_BYTES, st>>>(mW, m4, m8, m16, a, tiles, ntiles);
+  kern<<<grid, NTHREADS, SMEM_BYTES, st>>>(mW, m4, m8, m16, a, tiles, ntiles);
   return launched(1);
 }
 

@@ -274,6 +274,17 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 // named barrier `id` over `n` threads
+// Eight int4 codes (code j in bits 4j..4j+3, two's complement) -> eight int8
+// codes: codes 0-3 in lo, 4-7 in hi (byte i = code i).  The even and odd
+// nibbles are masked out per byte, sign-extended as (n ^ 8) - 8 per byte, and
+// interleaved back into code order.
+__device__ __forceinline__ void s4x8_to_s8x8(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t e = __vsub4((w & 0x0F0F0F0Fu) ^ 0x08080808u, 0x08080808u);         // codes 0,2,4,6
+  const uint32_t o = __vsub4(((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u, 0x08080808u);  // codes 1,3,5,7
+  lo = __byte_perm(e, o, 0x5140);
+  hi = __byte_perm(e, o, 0x7362);
+}
+
 // --- distributed shared memory between the two CTAs of a cluster ---------
 // address of the same shared-memory location in CTA `rank` of the cluster
 __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
