@@ -4,6 +4,7 @@
 #include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "wq_common.cuh"
 
@@ -133,6 +134,54 @@ size_t gemm_ws_bytes(int64_t R, int E, int Mmax, bool masked, bool silu) {
   return carve_gemm_ws(nullptr, R, E, Mmax, masked, silu).bytes;
 }
 
+// A second stream per device, on which the small-token engine runs beside
+// the tensor-core engine of the same GEMM launch.  Both engines are
+// persistent, write disjoint rows and never wait on each other; the second
+// one to start takes the SMs the first leaves idle (the tensor-core engine
+// claims its items from a counter, so CTAs that start late take fewer).
+// Fork and join go through events, so the pair records into a CUDA graph
+// like any other stream work; the stream and events are created on first
+// use, outside any capture, else both engines run one after the other.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[kMaxDevices];
+
+template <class Side, class Main>
+int fork_join(cudaStream_t st, Side &&side, Main &&main) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return WQ_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_side_mu);  // one fork/join pair at a time
+  SideStream &sd = g_side[dev];
+  if (sd.s == nullptr) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    SideStream n;
+    const bool made = cudaStreamIsCapturing(st, &cs) == cudaSuccess &&
+                      cs == cudaStreamCaptureStatusNone &&
+                      cudaStreamCreateWithFlags(&n.s, cudaStreamNonBlocking) == cudaSuccess &&
+                      cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) == cudaSuccess &&
+                      cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) == cudaSuccess;
+    if (!made) {
+      cudaGetLastError();
+      if (n.join) cudaEventDestroy(n.join);
+      if (n.fork) cudaEventDestroy(n.fork);
+      if (n.s) cudaStreamDestroy(n.s);
+      WQ_TRY(side(st));
+      return main(st);
+    }
+    sd = n;
+  }
+  if (cudaEventRecord(sd.fork, st) != cudaSuccess || cudaStreamWaitEvent(sd.s, sd.fork, 0) != cudaSuccess)
+    return WQ_ERR_LAUNCH;
+  const int rs = side(sd.s);
+  if (cudaEventRecord(sd.join, sd.s) != cudaSuccess) return WQ_ERR_LAUNCH;
+  const int rm = rs == WQ_OK ? main(st) : rs;
+  if (cudaStreamWaitEvent(st, sd.join, 0) != cudaSuccess) return WQ_ERR_LAUNCH;
+  return rm;
+}
+
 int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
   const bool masked = a.masked_m != nullptr;
   GemmWs w = carve_gemm_ws(a.ws, a.R, a.E, a.Mmax, masked, a.fused_hq16 != nullptr);
@@ -152,8 +201,14 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
     const int64_t m = rows == 64 ? w.m64 : w.m256;
     WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, rows, a.R, t, n, w.redo, st,
                               small ? gemm_small_max_rows() : 0, w.tsm, w.nsm));
-    if (small) WQ_TRY(launch_gemm_small(a, w.tsm, w.nsm, int(w.msm), st));
-    return launch_gemm_tc2(a, t, n, int(m), w.redo, st);
+    auto tc2 = [&](cudaStream_t s) { return launch_gemm_tc2(a, t, n, int(m), w.redo, s); };
+    if (!small) return tc2(st);
+    if (rows == 64) {  // few rows per expert: the small-token engine does nearly all
+      WQ_TRY(launch_gemm_small(a, w.tsm, w.nsm, int(w.msm), st));
+      return tc2(st);
+    }
+    return fork_join(
+        st, [&](cudaStream_t s) { return launch_gemm_small(a, w.tsm, w.nsm, int(w.msm), s); }, tc2);
   }
   if (a.A16 != nullptr && a.scheme == WQ_SCHEME_BLOCK) {
     // block-wise on fp16 codes: every K block's sum is exact in float32, so
@@ -206,8 +261,16 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
     const int64_t m = rows == 64 ? w.m64 : w.m256;
     WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, rows, a.R, t, n, w.redo, st,
                               small_max, w.tsm, w.nsm));
-    if (small) WQ_TRY(launch_gemm_small(a, w.tsm, w.nsm, int(w.msm), st));
-    WQ_TRY(launch_gemm_tc2(a, t, n, int(m), w.redo, st));
+    auto tc2 = [&](cudaStream_t s) { return launch_gemm_tc2(a, t, n, int(m), w.redo, s); };
+    if (small && rows == 64) {  // few rows per expert: the small-token engine does nearly all
+      WQ_TRY(launch_gemm_small(a, w.tsm, w.nsm, int(w.msm), st));
+      WQ_TRY(tc2(st));
+    } else if (small)
+      WQ_TRY(fork_join(
+          st, [&](cudaStream_t s) { return launch_gemm_small(a, w.tsm, w.nsm, int(w.msm), s); },
+          tc2));
+    else
+      WQ_TRY(tc2(st));
     gate = w.redo;
   }
   if (gemm_tc_supported(a)) {
