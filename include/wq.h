@@ -348,11 +348,16 @@ WQ_API int wq_moe_forward(const uint16_t *x, const float *logits, const int8_t *
                    int scheme, int acc, uint16_t *out, void *ws, size_t ws_bytes,
                    int32_t *status, wq_stream_t stream);
 
-/* Same layer with HOST activations: x_host bf16 [T][H] and logits_host
- * float [T][E] are copied to the workspace on `stream`, the layer runs, and
- * the result is copied to out_host bf16 [T][H].  Pinned host memory makes
- * the copies asynchronous; the caller synchronises the stream before reading
- * out_host.  Workspace: wq_moe_forward_host_workspace_size(). */
+/* Same layer with HOST activations x_host bf16 [T][H] and logits_host
+ * float [T][E], result in out_host bf16 [T][H].  When all three buffers are
+ * pinned host memory mapped into the device's address space (16-byte
+ * aligned x_host and out_host), the quantization kernel reads x_host, the
+ * router reads logits_host and the combine writes out_host across the
+ * CPU-GPU link, with no staging copies.  Otherwise the inputs are copied to
+ * the workspace on `stream` and the result copied back (asynchronous for
+ * pinned memory).  Either way the caller synchronises the stream before
+ * reading out_host and leaves x_host and logits_host unchanged until then.
+ * Workspace: wq_moe_forward_host_workspace_size() (it covers both cases). */
 WQ_API size_t wq_moe_forward_host_workspace_size(int T, int H, int I, int E, int k, int scheme);
 WQ_API int wq_moe_forward_host(const uint16_t *x_host, const float *logits_host, const int8_t *W13,
                         const float *sw13, const int8_t *W2, const float *sw2, int T, int H,

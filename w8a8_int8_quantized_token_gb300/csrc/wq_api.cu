@@ -719,6 +719,19 @@ int wq_moe_forward(const uint16_t *x, const float *logits, const int8_t *W13, co
                      stream);
 }
 
+namespace {
+// The device address of a host buffer that is mapped into the device's
+// address space (pinned host memory), else nullptr.
+const void *host_mapping(const void *p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+}  // namespace
+
 size_t wq_moe_forward_host_workspace_size(int T, int H, int I, int E, int k, int scheme) {
   const size_t inner = wq_moe_forward_workspace_size(T, H, I, E, k, scheme);
   if (inner == 0) return 0;
@@ -743,6 +756,16 @@ int wq_moe_forward_host(const uint16_t *x_host, const float *logits_host, const 
   uint16_t *out = c.take<uint16_t>(size_t(T) * H);
   FwdBufs b;
   carve_forward(c.base + c.used, T, H, I, E, k, scheme, &b);
+  // Pinned host buffers are mapped into the device's address space: then the
+  // quantization kernel reads x, the router reads the logits and the combine
+  // writes the output across the CPU-GPU link themselves (each is the only
+  // kernel touching that buffer), with no staging copies.
+  const void *xm = host_mapping(x_host), *lm = host_mapping(logits_host),
+             *om = host_mapping(out_host);
+  if (xm && lm && om && al16(xm) && al16(om))
+    return run_forward(static_cast<const uint16_t *>(xm), static_cast<const float *>(lm), W13, sw13,
+                       W2, sw2, T, H, I, E, k, scheme, acc,
+                       static_cast<uint16_t *>(const_cast<void *>(om)), b, status, stream);
   if (cudaMemcpyAsync(x, x_host, size_t(T) * H * 2, cudaMemcpyHostToDevice, stream) != cudaSuccess)
     return WQ_ERR_LAUNCH;
   if (cudaMemcpyAsync(logits, logits_host, size_t(T) * E * 4, cudaMemcpyHostToDevice, stream) !=
