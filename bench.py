@@ -63,8 +63,8 @@ TRAFFIC = {
     "prefill": _TC5,
     "prefill_f32": _TC5,
     "decode": {"kernel": "gemm_small_kernel", "file": "wq_gemm_small.cu",
-               "sha256": "e53537d8fa0b3b99d98faf1a3cf1183a0faa56d97eb8a556f491ad0c06afdbdc",
-               "bytes": 8 * (941.189888e6 + 4.634624e6),
+               "sha256": "631ff97a218b338aa2afea514f46c03c798e2cd5a0ca728857fe4b05d6b34390",
+               "bytes": 8 * (941.271296e6 + 4.564736e6),
                "how": "ncu capture of GEMM1 at 16 tokens / 32 experts (same 4 rows per expert), "
                       "dram read+write scaled by the expert count (x 8)"},
 }
