@@ -30,7 +30,14 @@
  *     given.
  *   - Every call is asynchronous on the given CUDA stream (cudaStream_t, may
  *     be NULL for the legacy default stream), performs no host
- *     synchronisation and reads no device data on the host.
+ *     synchronisation and reads no device data on the host, so it can be
+ *     recorded into a CUDA graph.  Grouped GEMMs over many small segments
+ *     (the masked layout) run two engines concurrently: the second on a
+ *     stream of the library's own, forked from and joined back into the
+ *     caller's stream through events (recorded into a graph like any other
+ *     stream work).  That stream and its two events are created once per
+ *     device, on first use outside a graph capture, and kept for the
+ *     process; without them both engines run on the caller's stream.
  *   - Return value: WQ_OK (0) when the work was enqueued, otherwise a
  *     negative WQ_ERR_* code and nothing was enqueued.  Argument errors are
  *     detected on the host before any launch.
