@@ -40,14 +40,20 @@ constexpr int TMAX = 16;
 constexpr int NCW = WN / 32;             // consumer warps
 constexpr int NTHREADS = 32 * (NCW + 1);  // + the producer warp
 constexpr int STAGES = 6;
-constexpr int W_BYTES = WN * BK;           // 32 KB of weight codes per stage
-constexpr int ST_BYTES = W_BYTES + 2048;       // + 2 KB of token codes (1024-byte steps)
-constexpr int OFF_BAR = STAGES * ST_BYTES;     // full[STAGES], empty[STAGES]
-constexpr int OFF_ABORT = OFF_BAR + 2 * STAGES * 8;
-constexpr int SMEM_BYTES = OFF_ABORT + 16 + 1024;  // + alignment slack
-static_assert(TMAX * BK <= ST_BYTES - W_BYTES, "token tile must fit its stage");
-static_assert(ST_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
-static_assert(SMEM_BYTES <= 232448, "shared memory plan too large");
+constexpr int W_BYTES = WN * BK;           // 32 KB of weight bytes per stage (256 rows x 128 B)
+// Stage plan: int8 weights take BK = 128 codes of K a stage; int4 weights
+// (two codes a byte) take 256, so a stage still carries 32 KB of weights and
+// six stages keep the same bytes in flight.  Token rows are one byte a code.
+template <bool W4>
+struct SPlan {
+  static constexpr int BKC = W4 ? 2 * BK : BK;         // K codes per stage
+  static constexpr int ST_BYTES = W_BYTES + TMAX * BKC;  // + the token tile
+  static constexpr int OFF_BAR = STAGES * ST_BYTES;      // full[STAGES], empty[STAGES]
+  static constexpr int OFF_ABORT = OFF_BAR + 2 * STAGES * 8;
+  static constexpr int SMEM_BYTES = OFF_ABORT + 16 + 1024;  // + alignment slack
+  static_assert(ST_BYTES % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+  static_assert(SMEM_BYTES <= 232448, "shared memory plan too large");
+};
 
 __device__ __forceinline__ int token_box(int rows) {
   return rows <= 4 ? 4 : (rows <= 8 ? 8 : 16);
@@ -73,6 +79,7 @@ __device__ __forceinline__ bool consume_item(const GemmArgs &a, const Tile &tl, 
     acc[t] = 0;
     accf[t] = 0.0f;
   }
+  constexpr int BKC = SPlan<W4>::BKC, ST_BYTES = SPlan<W4>::ST_BYTES, OFF_BAR = SPlan<W4>::OFF_BAR;
   const int sw8 = r & 7;
   for (int i = 0; i < KT; ++i, ++g) {
     const int s = g % STAGES;
@@ -80,14 +87,13 @@ __device__ __forceinline__ bool consume_item(const GemmArgs &a, const Tile &tl, 
       return false;
     const uint8_t *tk = sm + s * ST_BYTES + W_BYTES;
     if constexpr (W4) {
-      // int4 weights: 64 bytes (128 codes) of this channel's row, unswizzled;
-      // chunk (c + r/2) % 4 at step c, so the 8 rows of a quarter warp hit
-      // all 32 banks once; each chunk is 32 codes against 32 token bytes
-      const uint8_t *wrow = sm + s * ST_BYTES + r * (BK / 2);
+      // int4 weights: this channel's 128-byte row of the stage (256 codes),
+      // 128-byte swizzled like the int8 rows; each 16-byte chunk is 32 codes
+      // against 32 token bytes (read as broadcasts)
+      const uint8_t *wrow = sm + s * ST_BYTES + r * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int cc = (c + (r >> 1)) & 3;
-        const uint4 p = *reinterpret_cast<const uint4 *>(wrow + cc * 16);
+      for (int c = 0; c < 8; ++c) {
+        const uint4 p = *reinterpret_cast<const uint4 *>(wrow + ((c ^ sw8) << 4));
         uint32_t w8[8];
         s4x8_to_s8x8(p.x, w8[0], w8[1]);
         s4x8_to_s8x8(p.y, w8[2], w8[3]);
@@ -95,8 +101,8 @@ __device__ __forceinline__ bool consume_item(const GemmArgs &a, const Tile &tl, 
         s4x8_to_s8x8(p.w, w8[6], w8[7]);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          const uint4 x0 = *reinterpret_cast<const uint4 *>(tk + t * BK + cc * 32);
-          const uint4 x1 = *reinterpret_cast<const uint4 *>(tk + t * BK + cc * 32 + 16);
+          const uint4 x0 = *reinterpret_cast<const uint4 *>(tk + t * BKC + c * 32);
+          const uint4 x1 = *reinterpret_cast<const uint4 *>(tk + t * BKC + c * 32 + 16);
           acc[t] = __dp4a(int(w8[0]), int(x0.x), acc[t]);
           acc[t] = __dp4a(int(w8[1]), int(x0.y), acc[t]);
           acc[t] = __dp4a(int(w8[2]), int(x0.z), acc[t]);
@@ -183,11 +189,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *sm = smem_raw + (base - raw);
+  constexpr int BKC = SPlan<W4>::BKC, ST_BYTES = SPlan<W4>::ST_BYTES, OFF_BAR = SPlan<W4>::OFF_BAR,
+                OFF_ABORT = SPlan<W4>::OFF_ABORT;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_ABORT);
   auto full = [&](int s) { return base + OFF_BAR + 8u * uint32_t(s); };
   auto empty = [&](int s) { return base + OFF_BAR + 8u * uint32_t(STAGES + s); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int KT = int(a.K / BK);
+  const int KT = int(a.K / BKC);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -209,7 +217,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int nb = it % NB;
         const int box = token_box(tl.rows);
         const CUtensorMap *tmT = box == 4 ? &tmT4 : (box == 8 ? &tmT8 : &tmT16);
-        const uint32_t tx = uint32_t((W4 ? W_BYTES / 2 : W_BYTES) + box * BK);
+        const uint32_t tx = uint32_t(W_BYTES + box * BKC);
         const int wrow = int(int64_t(tl.expert) * a.N + int64_t(nb) * WN);
         for (int i = 0; i < KT; ++i, ++g) {
           const int s = g % STAGES;
@@ -221,8 +229,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           const uint32_t dst = base + uint32_t(s) * ST_BYTES;
           mbar_expect_tx(full(s), tx);
-          tma_load_2d(dst, &tmW, i * (W4 ? BK / 2 : BK), wrow, full(s));  // bytes
-          tma_load_2d(dst + W_BYTES, tmT, i * BK, tl.row0, full(s));
+          tma_load_2d(dst, &tmW, i * 128, wrow, full(s));  // 128 weight bytes a row per stage
+          tma_load_2d(dst + W_BYTES, tmT, i * BKC, tl.row0, full(s));
         }
       }
       // the last copies issued into each slot must land before the CTA exits
@@ -256,7 +264,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }  // namespace
 
 bool gemm_small_supported(const GemmArgs &a) {
-  if (a.w4 && (a.scheme != WQ_SCHEME_CHANNEL || a.acc != WQ_ACC_I32)) return false;
+  if (a.w4 && (a.scheme != WQ_SCHEME_CHANNEL || a.acc != WQ_ACC_I32 || a.K % (2 * BK))) return false;
   return a.A != nullptr && a.K % BK == 0 && a.K <= 65536 && a.N % 32 == 0 &&
          (a.scheme == WQ_SCHEME_CHANNEL || a.scheme == WQ_SCHEME_BLOCK) &&
          int64_t(a.E) * a.N < (int64_t(1) << 31) && a.R < (int64_t(1) << 31) && tma_available();
@@ -269,24 +277,25 @@ int launch_gemm_small(const GemmArgs &a, const Tile *tiles, const int32_t *ntile
                       cudaStream_t st) {
   if (max_tiles <= 0) return WQ_OK;
   CUtensorMap mW, m4, m8, m16;
-  // int8 weights: 128-byte rows per stage, 128-byte swizzled; int4 weights
-  // (two codes a byte): 64-byte rows per stage, unswizzled
-  const bool wok = a.w4 ? make_tma_2d_u8(&mW, a.W, int64_t(a.E) * a.N, a.K / 2, BK / 2, WN)
-                        : make_tma_2d_u8_sw128(&mW, a.W, int64_t(a.E) * a.N, a.K, WN);
-  if (!wok || !make_tma_2d_u8(&m4, a.A, a.R, a.K, BK, 4) ||
-      !make_tma_2d_u8(&m8, a.A, a.R, a.K, BK, 8) || !make_tma_2d_u8(&m16, a.A, a.R, a.K, BK, 16))
+  // weights: a 128-byte row per stage (128 int8 codes, or 256 int4 codes),
+  // 128-byte swizzled; tokens: one byte a code, BKC codes a stage
+  const int bkc = a.w4 ? SPlan<true>::BKC : SPlan<false>::BKC;
+  const int smem = a.w4 ? SPlan<true>::SMEM_BYTES : SPlan<false>::SMEM_BYTES;
+  if (!make_tma_2d_u8_sw128(&mW, a.W, int64_t(a.E) * a.N, a.w4 ? a.K / 2 : a.K, WN) ||
+      !make_tma_2d_u8(&m4, a.A, a.R, a.K, bkc, 4) || !make_tma_2d_u8(&m8, a.A, a.R, a.K, bkc, 8) ||
+      !make_tma_2d_u8(&m16, a.A, a.R, a.K, bkc, 16))
     return WQ_ERR_LAUNCH;
   static bool attr[2] = {false, false};
   auto kern = a.w4 ? gemm_small_kernel<true> : gemm_small_kernel<false>;
   if (!attr[a.w4 ? 1 : 0]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return WQ_ERR_LAUNCH;
     attr[a.w4 ? 1 : 0] = true;
   }
   const int64_t max_items = int64_t(max_tiles) * ((a.N + WN - 1) / WN);
   const int grid = int(max_items < num_sms() ? max_items : num_sms());
-  kern<<<grid, NTHREADS, SMEM_BYTES, st>>>(mW, m4, m8, m16, a, tiles, ntiles);
+  kern<<<grid, NTHREADS, smem, st>>>(mW, m4, m8, m16, a, tiles, ntiles);
   return launched(1);
 }
 
