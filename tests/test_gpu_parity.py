@@ -359,8 +359,8 @@ def test_layer_forward_masked():
 def test_silu_mul_quant_every_bf16_gate(group, f16):
     """Every finite bf16 gate value g (65280 patterns: both signs, subnormals,
     zeros, the largest) through SiLU-mul + re-quantization: the kernel looks
-    silu(g) up in a table for g in [2^-24, 17) and (-89, -2^-24] and takes
-    the formula elsewhere; codes and scales must equal the oracle's.  The
+    silu(g) up in a table for |g| in [2^-24, 89), either sign, and takes the
+    formula elsewhere; codes and scales must equal the oracle's.  The
     patterns are sorted by magnitude so the values sharing a row (or a
     128-group) are alike and their codes carry information; |u| < 1 keeps
     every product finite."""
@@ -389,10 +389,14 @@ def test_silu_mul_quant_every_bf16_gate(group, f16):
 
 
 @pytest.mark.parametrize("R,I,group", [(1, 8, 0), (3, 24, 0), (2, 256, 32), (40, 1024, 64),
-                                       (17, 2048, 256), (5, 4096, 0), (4, 4096, 128)])
+                                       (17, 2048, 256), (6, 1544, 0), (5, 1280, 128),
+                                       (6000, 2048, 0), (5, 4096, 0), (4, 4096, 128)])
 def test_silu_mul_quant_shapes(R, I, group):
-    """Row widths around the table kernel's per-lane vector counts (1 to 8
-    vectors of 8 per lane, partly filled last vectors), every group size, and
+    """Row widths around the table kernel's per-lane vector counts (1 to 4
+    vectors of 8 per lane, partly filled last vectors), rows split between
+    two warps (I > 1024, the second warp's part partly filled at I = 1544 and
+    1280), more rows than the launch has row slots (R = 6000: each warp pair
+    takes several rows, reusing its exchange slots), every group size, and
     rows too wide for it (I = 4096: the block-per-row kernels)."""
     g = torch.Generator().manual_seed(R * 7 + I)
     gu = (torch.randn(R, 2 * I, generator=g) * 3).to(torch.bfloat16)

@@ -77,18 +77,17 @@ __device__ __forceinline__ float silu(float g) {
   return __fdiv_rn(g, __fadd_rn(1.0f, exp_cw(-g)));
 }
 
-// silu(g) of every bf16 g whose magnitude lies in [2^-24, 17) (g > 0) or
-// [2^-24, 89) (g < 0), each entry computed with silu() itself, so a lookup
-// returns exactly what the formula returns; any other g (smaller, larger,
-// non-finite) takes the formula directly.  Outside those ranges silu is
-// trivial anyway (g / 2, g, or -0), and a GEMM output rarely lands there.
+// silu(g) of every bf16 g whose magnitude lies in [2^-24, 89), of either
+// sign, each entry computed with silu() itself, so a lookup returns exactly
+// what the formula returns; any other g (smaller, larger, non-finite) takes
+// the formula directly.  Outside that range silu is trivial anyway (g / 2,
+// g, or -0), and a GEMM output rarely lands there.  Entry k holds the
+// positive value with bf16 bits kLo + k, entry kHalf + k its negative.
 namespace silu_tab {
 constexpr uint32_t kLo = 0x3380u;        // bf16 bits of 2^-24
-constexpr uint32_t kPosHi = 0x4188u;     // bf16 bits of 17
-constexpr uint32_t kNegHi = 0x42B2u;     // bf16 bits of 89
-constexpr int kPos = int(kPosHi - kLo);  // entries for g > 0
-constexpr int kNeg = int(kNegHi - kLo);  // entries for g < 0
-constexpr int kSize = kPos + kNeg;
+constexpr uint32_t kHi = 0x42B2u;        // bf16 bits of 89
+constexpr int kHalf = int(kHi - kLo);    // entries of each sign
+constexpr int kSize = 2 * kHalf;
 constexpr int kBytes = kSize * 4;
 }  // namespace silu_tab
 
@@ -96,17 +95,17 @@ constexpr int kBytes = kSize * 4;
 __device__ __forceinline__ void silu_table_fill(float *tab, int i0, int step) {
   using namespace silu_tab;
   for (int i = i0; i < kSize; i += step) {
-    const uint32_t b = i < kPos ? kLo + uint32_t(i) : (0x8000u | (kLo + uint32_t(i - kPos)));
+    const uint32_t b = i < kHalf ? kLo + uint32_t(i) : (0x8000u | (kLo + uint32_t(i - kHalf)));
     tab[i] = silu(bf16_to_f(uint16_t(b)));
   }
 }
 
-// Table index of the bf16 pattern b, or -1 when b lies outside the table
+// Table index of the bf16 pattern b (bits 0-15), or -1 when b lies outside
+// the table
 __device__ __forceinline__ int silu_index(uint32_t b) {
   using namespace silu_tab;
-  const bool neg = (b & 0x8000u) != 0;
   const uint32_t k = (b & 0x7fffu) - kLo;  // wraps (large) below 2^-24
-  return k < (neg ? uint32_t(kNeg) : uint32_t(kPos)) ? int(neg ? k + uint32_t(kPos) : k) : -1;
+  return k < uint32_t(kHalf) ? int(k + (b >> 15) * uint32_t(kHalf)) : -1;
 }
 
 // Quantization scale from an absolute maximum: max(a, 1e-10) / 127.

@@ -699,84 +699,158 @@ int launch_silu_table(float *tab, cudaStream_t st) {
 
 // SiLU-and-mul + re-quantization, table form (rows of at most 2048 outputs).
 // Each CTA first tabulates silu(g) in shared memory (silu_tab: exact by
-// construction).  Then one warp per row (persistent CTAs loop over rows):
-// 8-element vectors v = i*32 + lane (each warp access is 512 contiguous
-// bytes), h = silu(g) * u, the row's or each group's absolute maximum by
-// xor shuffles, the codes (int8, or the same integers as fp16 with the
-// row's squared norm), the scale.
+// construction).  Then WPR warps per row (persistent CTAs loop over rows),
+// each warp a contiguous part of VPL 8-element vectors v = i*32 + lane (each
+// warp access is 512 contiguous bytes): h = silu(g) * u, the row's or each
+// group's absolute maximum (xor shuffles; two warps of a row exchange theirs
+// through shared memory behind a named barrier), the codes (int8, or the
+// same integers as fp16 with the row's squared norm), the scale.
+//
+// Arithmetic in pairs: packed float32 instructions (mul/add/sub .rn.f32x2)
+// round each lane to nearest even exactly as the scalar ones do, so the
+// codes are those of quant_bits(): y = x * rs, t = y + 1.5 * 2^23, r = t -
+// 1.5 * 2^23 = rint(y), and the exact quotient wherever |y - r| comes within
+// 2^-15 of one half.  fp16 codes are r converted (exact: |r| <= 127, an
+// integer); squared norms are sums of r * r (exact: a lane's sum stays below
+// 2^24).
 
-// silu of the eight bf16 gate values in w[0..3] (low half first): table
-// lookups (an out-of-table value reads entry 0 and is marked), then, only if
-// some lane of the warp has a marked value, the formula for those values
-__device__ __forceinline__ void silu8(const uint32_t (&w)[4], const float *tab, float (&sv)[8]) {
-  uint32_t miss = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t b = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
-    const int idx = silu_index(b);
-    miss |= idx < 0 ? 1u << j : 0u;
-    sv[j] = tab[idx < 0 ? 0 : idx];
-  }
-  if (__any_sync(0xffffffffu, miss != 0)) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (miss >> j & 1u) sv[j] = silu((j & 1) ? bf16_hi(w[j >> 1]) : bf16_lo(w[j >> 1]));
-  }
+namespace silu2 {
+__device__ __forceinline__ void add2(float &a0, float &a1, float b0, float b1) {
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%0, %1};\n mov.b64 b, {%2, %3};\n"
+      " add.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
 }
+// d = a - b, each lane rounded to nearest even
+__device__ __forceinline__ void sub2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " sub.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// acc += x * x for exact integers x (every sum an integer below 2^24)
+__device__ __forceinline__ void sq_acc2(float &a0, float &a1, float x0, float x1) {
+  asm("{\n .reg .b64 a, x, d;\n mov.b64 a, {%0, %1};\n mov.b64 x, {%2, %3};\n"
+      " fma.rn.f32x2 d, x, x, a;\n mov.b64 {%0, %1}, d;\n}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1));
+}
+__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ void pair_bar(int id) {
+  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+// silu of the two bf16 gate values of word w from the table; `miss` is set
+// when either lies outside it (the entry read is then a stand-in)
+__device__ __forceinline__ void silu_pair(uint32_t w, const float *tab, float &s0, float &s1,
+                                          bool &miss) {
+  using namespace silu_tab;
+  const uint32_t k0 = (w & 0x7fffu) - kLo;
+  const uint32_t k1 = ((w >> 16) & 0x7fffu) - kLo;
+  miss |= (k0 >= uint32_t(kHalf)) | (k1 >= uint32_t(kHalf));
+  const uint32_t i0 = k0 + ((w >> 15) & 1u) * uint32_t(kHalf);
+  const uint32_t i1 = k1 + (w >> 31) * uint32_t(kHalf);
+  s0 = tab[min(i0, uint32_t(kSize - 1))];
+  s1 = tab[min(i1, uint32_t(kSize - 1))];
+}
+// silu of one bf16 value: the table where it holds the value, else the formula
+__device__ __forceinline__ float silu_one(uint32_t b, const float *tab) {
+  const int idx = silu_index(b);
+  return idx >= 0 ? tab[idx] : silu(bf16_to_f(uint16_t(b)));
+}
+}  // namespace silu2
 
-// VPL vectors of 8 per lane (rows up to 256 * VPL outputs); GV lanes per
-// quantization group (0: one scale per row); F16: fp16 codes (with the row's
-// squared norm when GV == 0).
-template <int VPL, int GV, bool F16>
-__global__ void __launch_bounds__(512, 1) silu_mul_quant_tab_kernel(
+template <int VPL, int GV, bool F16, int WPR>
+__global__ void __launch_bounds__(512, 2) silu_mul_quant_tab_kernel(
     const uint16_t *__restrict__ gu, int64_t R, int64_t I, const int32_t *__restrict__ masked_m,
     int Mmax, void *__restrict__ hq_out, float *__restrict__ sh, int32_t *__restrict__ norm2) {
+  using namespace silu2;
+  static_assert(WPR == 1 || WPR == 2, "one or two warps per row");
   extern __shared__ float tab[];
+  __shared__ float xmax[2][16];  // a warp's row maximum for the row's other warp
+  __shared__ int xnorm[2][16];   // a warp's squared-norm part, likewise
   silu_table_fill(tab, threadIdx.x, blockDim.x);
   __syncthreads();
-  const int lane = threadIdx.x & 31;
+  constexpr float kRound = 12582912.0f;             // 1.5 * 2^23
+  constexpr float kNear = 0.499969482421875f;       // 0.5 - 2^-15
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int part = WPR == 2 ? (warp & 1) : 0;
   const int nvec = int(I >> 3);
-  const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t row = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); row < R;
-       row += nwarps) {
-    if (masked_m != nullptr && int(row % Mmax) >= masked_m[row / Mmax]) continue;  // warp-uniform
+  const int v0 = part * VPL * 32 + lane;
+  const int64_t rstep = int64_t(gridDim.x) * (blockDim.x >> 5) / WPR;
+  int par = 0;
+  for (int64_t row = (int64_t(blockIdx.x) * (blockDim.x >> 5) + warp) / WPR; row < R;
+       row += rstep) {
+    if (masked_m != nullptr && int(row % Mmax) >= masked_m[row / Mmax]) continue;  // row-uniform
     const uint4 *g4 = reinterpret_cast<const uint4 *>(gu + row * 2 * I);
     const uint4 *u4 = reinterpret_cast<const uint4 *>(gu + row * 2 * I + I);
     uint4 gv[VPL], uv[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
-      const int v = i * 32 + lane;
-      gv[i] = v < nvec ? __ldcs(g4 + v) : make_uint4(0, 0, 0, 0);
+      const int v = v0 + i * 32;
+      // past the row: gate 1.0 (in the table), up 0, so h = 0
+      gv[i] = v < nvec ? __ldcs(g4 + v) : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
       uv[i] = v < nvec ? __ldcs(u4 + v) : make_uint4(0, 0, 0, 0);
     }
-    float h[VPL][8], am[VPL];
+    float h[VPL][8];
+    bool miss = false;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       const uint32_t gw[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
       const uint32_t uw[4] = {uv[i].x, uv[i].y, uv[i].z, uv[i].w};
-      float sv[8];
-      silu8(gw, tab, sv);
-      am[i] = 0.0f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        h[i][2 * j] = __fmul_rn(sv[2 * j], bf16_lo(uw[j]));
-        h[i][2 * j + 1] = __fmul_rn(sv[2 * j + 1], bf16_hi(uw[j]));
-        am[i] = fmaxf(am[i], fabsf(h[i][2 * j]));
-        am[i] = fmaxf(am[i], fabsf(h[i][2 * j + 1]));
+        float s0, s1;
+        silu_pair(gw[j], tab, s0, s1, miss);
+        tc::fmul2(s0, s1, bf16_lo(uw[j]), bf16_hi(uw[j]));
+        h[i][2 * j] = s0;
+        h[i][2 * j + 1] = s1;
       }
+    }
+    if (miss) {  // rare: a gate value of this lane outside the table; redo the lane's values
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int v = v0 + i * 32;
+        if (v < nvec) {
+          const uint4 g = g4[v], u = u4[v];
+          const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+          const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            h[i][2 * j] = __fmul_rn(silu_one(gw[j] & 0xffffu, tab), bf16_lo(uw[j]));
+            h[i][2 * j + 1] = __fmul_rn(silu_one(gw[j] >> 16, tab), bf16_hi(uw[j]));
+          }
+        }
+      }
+    }
+    float am[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      am[i] = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) am[i] = fmaxf(am[i], fmaxf(fabsf(h[i][e]), fabsf(h[i][e + 1])));
     }
     float sc = 0.0f, rs = 0.0f;
     if constexpr (GV == 0) {
       float a = am[0];
 #pragma unroll
       for (int i = 1; i < VPL; ++i) a = fmaxf(a, am[i]);
-      sc = quant_scale(warp_max(a));
+      a = warp_max(a);
+      if constexpr (WPR == 2) {
+        if (lane == 0) xmax[par][warp] = a;
+        pair_bar(1 + (warp >> 1));
+        a = fmaxf(a, xmax[par][warp ^ 1]);
+      }
+      sc = quant_scale(a);
       rs = __frcp_rn(sc);
     }
-    int n2 = 0;
+    float n0 = 0.0f, n1 = 0.0f;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
-      const int v = i * 32 + lane;
+      const int v = v0 + i * 32;
       if constexpr (GV != 0) {
         float a = am[i];
 #pragma unroll
@@ -784,18 +858,44 @@ __global__ void __launch_bounds__(512, 1) silu_mul_quant_tab_kernel(
         sc = quant_scale(a);
         rs = __frcp_rn(sc);
       }
+      float t[8], r[8];
+      float dm = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        float y0 = h[i][e], y1 = h[i][e + 1];
+        tc::fmul2(y0, y1, rs, rs);
+        t[e] = y0;
+        t[e + 1] = y1;
+        add2(t[e], t[e + 1], kRound, kRound);
+        sub2(r[e], r[e + 1], t[e], t[e + 1], kRound, kRound);
+        float d0, d1;
+        sub2(d0, d1, y0, y1, r[e], r[e + 1]);
+        dm = fmaxf(dm, fmaxf(fabsf(d0), fabsf(d1)));
+      }
+      if (dm >= kNear) {  // rare: a quotient near a half-integer; exact quotients
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          t[e] = __uint_as_float(quant_bits(h[i][e], sc, rs));
+          r[e] = __fsub_rn(t[e], kRound);
+        }
+      }
       if (v < nvec) {
-        const uint32_t lo = pack_s8x4(quant_bits(h[i][0], sc, rs), quant_bits(h[i][1], sc, rs),
-                                      quant_bits(h[i][2], sc, rs), quant_bits(h[i][3], sc, rs));
-        const uint32_t hi = pack_s8x4(quant_bits(h[i][4], sc, rs), quant_bits(h[i][5], sc, rs),
-                                      quant_bits(h[i][6], sc, rs), quant_bits(h[i][7], sc, rs));
         if constexpr (F16) {
-          uint4 w;  // the same integers as fp16 values (exact)
-          tc::s8x4_to_f16x4(lo, w.x, w.y);
-          tc::s8x4_to_f16x4(hi, w.z, w.w);
+          uint4 w;
+          w.x = f16x2_rn(r[0], r[1]);
+          w.y = f16x2_rn(r[2], r[3]);
+          w.z = f16x2_rn(r[4], r[5]);
+          w.w = f16x2_rn(r[6], r[7]);
           reinterpret_cast<uint4 *>(static_cast<uint16_t *>(hq_out) + row * I)[v] = w;
-          n2 = __dp4a(int(hi), int(hi), __dp4a(int(lo), int(lo), n2));
+          if constexpr (GV == 0) {
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) sq_acc2(n0, n1, r[e], r[e + 1]);
+          }
         } else {
+          const uint32_t lo = pack_s8x4(__float_as_uint(t[0]), __float_as_uint(t[1]),
+                                        __float_as_uint(t[2]), __float_as_uint(t[3]));
+          const uint32_t hi = pack_s8x4(__float_as_uint(t[4]), __float_as_uint(t[5]),
+                                        __float_as_uint(t[6]), __float_as_uint(t[7]));
           reinterpret_cast<uint2 *>(static_cast<int8_t *>(hq_out) + row * I)[v] = make_uint2(lo, hi);
         }
         if constexpr (GV != 0) {
@@ -805,12 +905,19 @@ __global__ void __launch_bounds__(512, 1) silu_mul_quant_tab_kernel(
     }
     if constexpr (GV == 0) {
       if constexpr (F16) {
+        int n2 = __float2int_rn(__fadd_rn(n0, n1));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
-        if (lane == 0) norm2[row] = n2;
+        if constexpr (WPR == 2) {
+          if (lane == 0) xnorm[par][warp] = n2;
+          pair_bar(1 + (warp >> 1));
+          n2 += xnorm[par][warp ^ 1];
+        }
+        if (lane == 0 && part == 0) norm2[row] = n2;
       }
-      if (lane == 0) sh[row] = sc;
+      if (lane == 0 && part == 0) sh[row] = sc;
     }
+    par ^= 1;
   }
 }
 
@@ -821,32 +928,35 @@ int launch_silu_tab(const uint16_t *gu, int64_t R, int64_t I, int group, const i
                     int Mmax, void *hq, float *sh, int32_t *norm2, cudaStream_t st) {
   const int64_t nvec = I / 8;
   if (nvec > 256) return WQ_ERR_UNSUPPORTED;
-  // one CTA of 16 warps per SM (the table fits the default 48 KB of shared
-  // memory), fewer for short launches
-  const int64_t rows_per_cta = 16;
+  // two CTAs of 16 warps per SM (the table fits the default 48 KB of shared
+  // memory), fewer for short launches; rows of more than 1024 outputs take
+  // two warps each
+  const int wpr = nvec > 128 ? 2 : 1;
+  const int64_t rows_per_cta = 16 / wpr;
   int64_t grid = (R + rows_per_cta - 1) / rows_per_cta;
-  const int64_t cap = int64_t(num_sms());
+  const int64_t cap = 2 * int64_t(num_sms());
   if (grid > cap) grid = cap;
   const size_t smem = silu_tab::kBytes;
-#define WQ_SILU_TAB(VPL, GV) \
-  silu_mul_quant_tab_kernel<VPL, GV, F16><<<unsigned(grid), 512, smem, st>>>(gu, R, I, masked_m, Mmax, hq, sh, norm2)
-#define WQ_SILU_TAB_G(VPL)                         \
+#define WQ_SILU_TAB(VPL, GV, WPR)                                                               \
+  silu_mul_quant_tab_kernel<VPL, GV, F16, WPR><<<unsigned(grid), 512, smem, st>>>(gu, R, I, masked_m, \
+                                                                                  Mmax, hq, sh, norm2)
+#define WQ_SILU_TAB_G(VPL, WPR)                    \
   switch (group) {                                 \
-    case 0: WQ_SILU_TAB(VPL, 0); break;            \
-    case 32: WQ_SILU_TAB(VPL, 4); break;           \
-    case 64: WQ_SILU_TAB(VPL, 8); break;           \
-    case 128: WQ_SILU_TAB(VPL, 16); break;         \
-    case 256: WQ_SILU_TAB(VPL, 32); break;         \
+    case 0: WQ_SILU_TAB(VPL, 0, WPR); break;       \
+    case 32: WQ_SILU_TAB(VPL, 4, WPR); break;      \
+    case 64: WQ_SILU_TAB(VPL, 8, WPR); break;      \
+    case 128: WQ_SILU_TAB(VPL, 16, WPR); break;    \
+    case 256: WQ_SILU_TAB(VPL, 32, WPR); break;    \
     default: return WQ_ERR_UNSUPPORTED;            \
   }
   if (nvec <= 32) {
-    WQ_SILU_TAB_G(1)
+    WQ_SILU_TAB_G(1, 1)
   } else if (nvec <= 64) {
-    WQ_SILU_TAB_G(2)
+    WQ_SILU_TAB_G(2, 1)
   } else if (nvec <= 128) {
-    WQ_SILU_TAB_G(4)
+    WQ_SILU_TAB_G(4, 1)
   } else {
-    WQ_SILU_TAB_G(8)
+    WQ_SILU_TAB_G(4, 2)
   }
 #undef WQ_SILU_TAB_G
 #undef WQ_SILU_TAB
