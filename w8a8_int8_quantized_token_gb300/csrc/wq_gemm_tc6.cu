@@ -380,19 +380,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         }
         tc_fence_after();
         const uint32_t tch = tq + uint32_t(b * TN + c0);
+        // 8-column pieces, the next one's load in flight while this one is
+        // scaled and added (two register sets, alternating)
+        auto add_piece = [&](int piece, const uint32_t (&v)[8]) {
+          const float4 *s4 = reinterpret_cast<const float4 *>(scal + 8 * piece);
 #pragma unroll
-        for (int piece = 0; piece < EPI_COLS / 16; ++piece) {
-          uint32_t v[16];
-          tmem_ld16(tch + 16u * piece, v);
-          tmem_wait_ld();
-          const float4 *s4 = reinterpret_cast<const float4 *>(scal + 16 * piece);
-#pragma unroll
-          for (int j = 0; j < 16; j += 4) {
+          for (int j = 0; j < 8; j += 4) {
             const float4 sc = s4[j / 4];
-            float *r = acc + 16 * piece + j;
+            float *r = acc + 8 * piece + j;
             mul_add2(r[0], r[1], __uint_as_float(v[j]), __uint_as_float(v[j + 1]), sc.x, sc.y, r[0], r[1]);
             mul_add2(r[2], r[3], __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]), sc.z, sc.w, r[2], r[3]);
           }
+        };
+        constexpr int NPC = EPI_COLS / 8;
+        static_assert(NPC % 2 == 0, "pieces go in pairs");
+        uint32_t va[8], vb[8];
+        tmem_ld8(tch, va);
+        tmem_wait_ld(va);
+#pragma unroll
+        for (int piece = 0; piece < NPC; piece += 2) {
+          tmem_ld8(tch + 8u * uint32_t(piece + 1), vb);
+          add_piece(piece, va);
+          tmem_wait_ld(vb);
+          if (piece + 2 < NPC) tmem_ld8(tch + 8u * uint32_t(piece + 2), va);
+          add_piece(piece + 1, vb);
+          if (piece + 2 < NPC) tmem_wait_ld(va);
         }
         tc_fence_before();
         __syncwarp();
