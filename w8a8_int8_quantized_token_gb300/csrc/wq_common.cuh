@@ -148,6 +148,83 @@ __device__ __forceinline__ uint32_t pack_s8x4(uint32_t a, uint32_t b, uint32_t c
   return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
 }
 
+// Packed float32 pairs (.rn.f32x2): each lane rounds to nearest even exactly
+// as the scalar instruction does, and nothing is fused unless written as fma.
+__device__ __forceinline__ void mul2(float &a0, float &a1, float b0, float b1) {
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%0, %1};\n mov.b64 b, {%2, %3};\n"
+      " mul.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void add2(float &a0, float &a1, float b0, float b1) {
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%0, %1};\n mov.b64 b, {%2, %3};\n"
+      " add.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+// d = a - b
+__device__ __forceinline__ void sub2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " sub.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// acc += x * x for integers x whose every partial sum stays below 2^24 (exact)
+__device__ __forceinline__ void sq_acc2(float &a0, float &a1, float x0, float x1) {
+  asm("{\n .reg .b64 a, x, d;\n mov.b64 a, {%0, %1};\n mov.b64 x, {%2, %3};\n"
+      " fma.rn.f32x2 d, x, x, a;\n mov.b64 {%0, %1}, d;\n}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1));
+}
+// two floats -> an fp16 pair, lo in bits 0-15 (exact for the integer codes)
+__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Eight codes as quant_bits() gives them, the arithmetic in pairs: y = x *
+// rs, t = y + 1.5 * 2^23 (its bits: the code in the low byte), r = t - 1.5 *
+// 2^23 = rint(y) as a float, and |y - r| checked; when any of the eight lies
+// within 2^-15 of one half, all eight take quant_bits() itself.
+__device__ __forceinline__ void quant8(const float (&x)[8], float s, float rs, float (&t)[8],
+                                       float (&r)[8]) {
+  constexpr float kRound = 12582912.0f;        // 1.5 * 2^23
+  constexpr float kNear = 0.499969482421875f;  // 0.5 - 2^-15
+  float dm = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    float y0 = x[e], y1 = x[e + 1];
+    mul2(y0, y1, rs, rs);
+    t[e] = y0;
+    t[e + 1] = y1;
+    add2(t[e], t[e + 1], kRound, kRound);
+    sub2(r[e], r[e + 1], t[e], t[e + 1], kRound, kRound);
+    float d0, d1;
+    sub2(d0, d1, y0, y1, r[e], r[e + 1]);
+    dm = fmaxf(dm, fmaxf(fabsf(d0), fabsf(d1)));
+  }
+  if (dm >= kNear) {  // rare
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      t[e] = __uint_as_float(quant_bits(x[e], s, rs));
+      r[e] = __fsub_rn(t[e], kRound);
+    }
+  }
+}
+// The int8 codes of quant8's t as two words (element 0 in the low byte)
+__device__ __forceinline__ uint2 pack_codes8(const float (&t)[8]) {
+  return make_uint2(pack_s8x4(__float_as_uint(t[0]), __float_as_uint(t[1]), __float_as_uint(t[2]),
+                              __float_as_uint(t[3])),
+                    pack_s8x4(__float_as_uint(t[4]), __float_as_uint(t[5]), __float_as_uint(t[6]),
+                              __float_as_uint(t[7])));
+}
+// The fp16 codes of quant8's r as four words
+__device__ __forceinline__ uint4 f16_codes8(const float (&r)[8]) {
+  return make_uint4(f16x2_rn(r[0], r[1]), f16x2_rn(r[2], r[3]), f16x2_rn(r[4], r[5]),
+                    f16x2_rn(r[6], r[7]));
+}
+
 __device__ __forceinline__ void set_status(int32_t *status, int code) {
   if (status) atomicCAS(status, 0, code);
 }

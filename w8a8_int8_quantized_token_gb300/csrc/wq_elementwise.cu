@@ -706,40 +706,12 @@ int launch_silu_table(float *tab, cudaStream_t st) {
 // through shared memory behind a named barrier), the codes (int8, or the
 // same integers as fp16 with the row's squared norm), the scale.
 //
-// Arithmetic in pairs: packed float32 instructions (mul/add/sub .rn.f32x2)
-// round each lane to nearest even exactly as the scalar ones do, so the
-// codes are those of quant_bits(): y = x * rs, t = y + 1.5 * 2^23, r = t -
-// 1.5 * 2^23 = rint(y), and the exact quotient wherever |y - r| comes within
-// 2^-15 of one half.  fp16 codes are r converted (exact: |r| <= 127, an
-// integer); squared norms are sums of r * r (exact: a lane's sum stays below
-// 2^24).
+// Arithmetic in pairs (quant8: packed float32 instructions that round each
+// lane as the scalar ones do, so the codes are quant_bits()'s).  fp16 codes
+// are the rounded values r converted (exact: |r| <= 127, an integer);
+// squared norms are sums of r * r (exact: a lane's sum stays below 2^24).
 
 namespace silu2 {
-__device__ __forceinline__ void add2(float &a0, float &a1, float b0, float b1) {
-  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%0, %1};\n mov.b64 b, {%2, %3};\n"
-      " add.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
-      : "+f"(a0), "+f"(a1)
-      : "f"(b0), "f"(b1));
-}
-// d = a - b, each lane rounded to nearest even
-__device__ __forceinline__ void sub2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
-  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
-      " sub.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-// acc += x * x for exact integers x (every sum an integer below 2^24)
-__device__ __forceinline__ void sq_acc2(float &a0, float &a1, float x0, float x1) {
-  asm("{\n .reg .b64 a, x, d;\n mov.b64 a, {%0, %1};\n mov.b64 x, {%2, %3};\n"
-      " fma.rn.f32x2 d, x, x, a;\n mov.b64 {%0, %1}, d;\n}"
-      : "+f"(a0), "+f"(a1)
-      : "f"(x0), "f"(x1));
-}
-__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 __device__ __forceinline__ void pair_bar(int id) {
   asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
 }
@@ -774,8 +746,6 @@ __global__ void __launch_bounds__(512, 2) silu_mul_quant_tab_kernel(
   __shared__ int xnorm[2][16];   // a warp's squared-norm part, likewise
   silu_table_fill(tab, threadIdx.x, blockDim.x);
   __syncthreads();
-  constexpr float kRound = 12582912.0f;             // 1.5 * 2^23
-  constexpr float kNear = 0.499969482421875f;       // 0.5 - 2^-15
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int part = WPR == 2 ? (warp & 1) : 0;
   const int nvec = int(I >> 3);
@@ -805,7 +775,7 @@ __global__ void __launch_bounds__(512, 2) silu_mul_quant_tab_kernel(
       for (int j = 0; j < 4; ++j) {
         float s0, s1;
         silu_pair(gw[j], tab, s0, s1, miss);
-        tc::fmul2(s0, s1, bf16_lo(uw[j]), bf16_hi(uw[j]));
+        mul2(s0, s1, bf16_lo(uw[j]), bf16_hi(uw[j]));
         h[i][2 * j] = s0;
         h[i][2 * j + 1] = s1;
       }
@@ -859,44 +829,16 @@ __global__ void __launch_bounds__(512, 2) silu_mul_quant_tab_kernel(
         rs = __frcp_rn(sc);
       }
       float t[8], r[8];
-      float dm = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 8; e += 2) {
-        float y0 = h[i][e], y1 = h[i][e + 1];
-        tc::fmul2(y0, y1, rs, rs);
-        t[e] = y0;
-        t[e + 1] = y1;
-        add2(t[e], t[e + 1], kRound, kRound);
-        sub2(r[e], r[e + 1], t[e], t[e + 1], kRound, kRound);
-        float d0, d1;
-        sub2(d0, d1, y0, y1, r[e], r[e + 1]);
-        dm = fmaxf(dm, fmaxf(fabsf(d0), fabsf(d1)));
-      }
-      if (dm >= kNear) {  // rare: a quotient near a half-integer; exact quotients
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          t[e] = __uint_as_float(quant_bits(h[i][e], sc, rs));
-          r[e] = __fsub_rn(t[e], kRound);
-        }
-      }
+      quant8(h[i], sc, rs, t, r);
       if (v < nvec) {
         if constexpr (F16) {
-          uint4 w;
-          w.x = f16x2_rn(r[0], r[1]);
-          w.y = f16x2_rn(r[2], r[3]);
-          w.z = f16x2_rn(r[4], r[5]);
-          w.w = f16x2_rn(r[6], r[7]);
-          reinterpret_cast<uint4 *>(static_cast<uint16_t *>(hq_out) + row * I)[v] = w;
+          reinterpret_cast<uint4 *>(static_cast<uint16_t *>(hq_out) + row * I)[v] = f16_codes8(r);
           if constexpr (GV == 0) {
 #pragma unroll
             for (int e = 0; e < 8; e += 2) sq_acc2(n0, n1, r[e], r[e + 1]);
           }
         } else {
-          const uint32_t lo = pack_s8x4(__float_as_uint(t[0]), __float_as_uint(t[1]),
-                                        __float_as_uint(t[2]), __float_as_uint(t[3]));
-          const uint32_t hi = pack_s8x4(__float_as_uint(t[4]), __float_as_uint(t[5]),
-                                        __float_as_uint(t[6]), __float_as_uint(t[7]));
-          reinterpret_cast<uint2 *>(static_cast<int8_t *>(hq_out) + row * I)[v] = make_uint2(lo, hi);
+          reinterpret_cast<uint2 *>(static_cast<int8_t *>(hq_out) + row * I)[v] = pack_codes8(t);
         }
         if constexpr (GV != 0) {
           if (lane % GV == 0) sh[row * (nvec / GV) + v / GV] = sc;
