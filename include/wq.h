@@ -308,6 +308,25 @@ WQ_API int wq_grouped_gemm_w8a8_silu_quant_f16codes(const uint16_t *A16, const f
 WQ_API int wq_quantize_per_token_f16(const uint16_t *x, int64_t T, int64_t K, int64_t ldx,
                                      uint16_t *q16, float *s, int32_t *norm2, wq_stream_t stream);
 
+/* Quantization and permute in one pass, scatter form (the quantization rule
+ * of wq_quantize_per_token / wq_quantize_per_token_group, Meituan INT8
+ * DeepSeek R1 article, 量化技术的探索; the ep_scatter placement of
+ * "[WIP] feat: support cutlass_moe_fp8 for deepepmoe", review).  Each token
+ * of x bf16 [T][K] is quantized once (group 0: one scale per token; 32, 64,
+ * 128 or 256: one per group) and its codes, as fp16 bits, go to every row
+ * r = pair_to_row[t * k + j] (j < k, the map wq_moe_align returns):
+ * A16 [R][K] (row pitch K), sa [R] or [R][K/group], and with group 0 also
+ * norm2 int32 [R] = the row's sum of code^2 (with a group norm2 is not
+ * written and may be NULL).  The result equals wq_quantize_per_token(_group)
+ * followed by wq_moe_permute_f16 on every row some pair maps to; rows no pair
+ * maps to (alignment padding) are not written, and map entries outside
+ * [0, R) are skipped.
+ * Requirements: 1 <= k <= 32, K % 8 == 0, K % group == 0, K <= 65536,
+ * 16-byte aligned x and A16. */
+WQ_API int wq_quantize_permute_f16(const uint16_t *x, int64_t T, int64_t K, int group,
+                                   const int32_t *pair_to_row, int k, int64_t R, uint16_t *A16,
+                                   float *sa, int32_t *norm2, wq_stream_t stream);
+
 /* Masked layout [LL]: A int8 [E][Mmax][K] with per-row scales sa
  * ([E][Mmax] or [E][Mmax][K/128]) and valid counts masked_m int32 [E]
  * (device).  Expert e computes rows [0, min(masked_m[e], Mmax)) with the

@@ -427,6 +427,61 @@ def test_moe_permute_f16(groups):
     assert np.array_equal(np_(n2), (Ao.astype(np.int64) ** 2).sum(1))
 
 
+@pytest.mark.parametrize("T,K,k,E,group,pad", [(200, 7168, 8, 64, 0, 1), (200, 7168, 8, 64, 128, 1),
+                                                (33, 256, 1, 4, 0, 1), (40, 512, 32, 64, 32, 1),
+                                                (70, 2048, 4, 16, 0, 4), (5, 65536, 2, 4, 256, 1)])
+def test_quantize_permute_f16(T, K, k, E, group, pad):
+    """Quantization and permute in one pass (scatter form) against the
+    oracle's quantization followed by its permute: every routed row's fp16
+    codes, scale(s) and squared norm.  With padded alignment (pad 4) the
+    padding rows, which no pair maps to, keep their previous contents."""
+    rng = np.random.default_rng(T * 31 + K + k)
+    x = (torch.randn(T, K, generator=torch.Generator().manual_seed(K + T)) * 2).to(torch.bfloat16)
+    x[0, :3] = torch.tensor([0.0, 1e-30, -5e4])  # a zero, a tiny and a large value in one row
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    _, _, spo, p2r = O.moe_align(ids, E, pad)
+    R = spo.size
+    if group == 0:
+        qo, so = O.quantize_per_token(bits(x))
+    else:
+        qo, so = O.quantize_per_token_group(bits(x), group)
+    Ao, sao = O.moe_permute(qo, so, spo, k)
+    A16 = torch.full((R, K), 7.0, dtype=torch.float16, device=DEV)
+    sa = torch.full((R,) if group == 0 else (R, K // group), -3.0, device=DEV)
+    n2 = torch.full((R,), -5, dtype=torch.int32, device=DEV) if group == 0 else None
+    wq.quantize_permute_f16(x.to(DEV), torch.from_numpy(p2r).to(DEV), k, R, group, out=(A16, sa, n2))
+    valid = spo >= 0
+    assert np.array_equal(np_(A16)[valid].astype(np.int32), Ao[valid].astype(np.int32))
+    assert np.array_equal(np_(sa)[valid], sao[valid])
+    if group == 0:
+        assert np.array_equal(np_(n2)[valid], (Ao[valid].astype(np.int64) ** 2).sum(1))
+    # padding rows untouched
+    assert bool((np_(A16)[~valid] == 7.0).all()) and bool((np_(sa)[~valid] == -3.0).all())
+    if group == 0:
+        assert bool((np_(n2)[~valid] == -5).all())
+
+
+def test_quantize_permute_f16_skips_rows_outside():
+    """Map entries outside [0, R) are skipped (no write anywhere)."""
+    T, K, k, R = 4, 256, 2, 6
+    x = (torch.randn(T, K, generator=torch.Generator().manual_seed(2))).to(torch.bfloat16)
+    p2r = torch.tensor([0, 1, -1, 2, 6, 3, 1000, 5], dtype=torch.int32)
+    A16 = torch.full((R, K), 7.0, dtype=torch.float16, device=DEV)
+    sa = torch.full((R,), -3.0, device=DEV)
+    n2 = torch.full((R,), -5, dtype=torch.int32, device=DEV)
+    wq.quantize_permute_f16(x.to(DEV), p2r.to(DEV), k, R, 0, out=(A16, sa, n2))
+    torch.cuda.synchronize()
+    qo, so = O.quantize_per_token(bits(x))
+    written = {0: 0, 1: 0, 2: 1, 3: 2, 5: 3}  # row -> token
+    for r in range(R):
+        if r in written:
+            t = written[r]
+            assert np.array_equal(np_(A16[r]).astype(np.int32), qo[t].astype(np.int32))
+            assert float(sa[r]) == float(so[t])
+        else:
+            assert bool((A16[r] == 7.0).all()) and float(sa[r]) == -3.0 and int(n2[r]) == -5
+
+
 @pytest.mark.parametrize("group", [0, 32, 128])
 def test_silu_mul_quant_f16(group):
     R, I = 70, 2048
