@@ -229,7 +229,6 @@ class ClockSampler:
 class Layer:
     """Preallocated buffers and the staged C-ABI calls of one layer step."""
 
-    STAGES = ["route", "quant", "align", "permute", "gemm1", "silu_mul_quant", "gemm2", "combine"]
 
     def __init__(self, wq, cfg, dev, weights):
         self.wq, self.lib, self.cfg, self.dev = wq, wq.lib(), cfg, dev
@@ -250,6 +249,12 @@ class Layer:
         self.f16 = ((2 * I) % 256 == 0
                     and H % 256 == 0 and R > 64 * E)
         cdt = torch.float16 if self.f16 else torch.int8
+        # the one-call layer's kernels, in its order (fp16 codes: each token
+        # quantized once and written to its k rows; int8 codes: quantize,
+        # then permute)
+        self.stages = (["route", "align", "quant_permute"] if self.f16 else
+                       ["route", "align", "quant", "permute"]) + [
+                           "gemm1", "silu_mul_quant", "gemm2", "combine"]
         self.A, self.sa = e(R, H, dt=cdt), e(R * self.g1, dt=torch.float32)
         self.anorm, self.hnorm = e(R, dt=torch.int32), e(R, dt=torch.int32)
         self.gu = e(R, 2 * I, dt=torch.bfloat16)
@@ -268,55 +273,63 @@ class Layer:
         R = T * k
         st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
         sc, ac = SCHEME[c.scheme], ACC[c.acc]
-        rec = (lambda i: ev[i].record()) if ev is not None else (lambda i: None)
+        n = [0]
+
+        def rec():
+            if ev is not None:
+                ev[n[0]].record()
+            n[0] += 1
 
         def ok(rc, what):
             if rc != 0:
                 raise RuntimeError(f"{what} failed: {rc}")
-        rec(0)
+        rec()
         ok(L.wq_route_topk(P(logits), T, E, k, P(self.ids), P(self.w), st), "route")
-        rec(1)
-        if c.scheme == "channel":
-            ok(L.wq_quantize_per_token(P(x), T, H, H, P(self.q), P(self.s), st), "quant")
-        else:
-            ok(L.wq_quantize_per_token_group(P(x), T, H, H, 128, P(self.q), P(self.s), st), "quant")
-        rec(2)
+        rec()
         ok(L.wq_moe_align(P(self.ids), T, k, E, 1, P(self.counts), P(self.offsets), P(self.sp),
                           P(self.p2r), P(self.aws), self.aws_n, P(self.status), st), "align")
-        rec(3)
+        rec()
+        group = 128 if c.scheme == "block" else 0
         if self.f16:
-            ok(L.wq_moe_permute_f16(P(self.q), P(self.s), self.g1, T, k, H, P(self.sp), R, P(self.A),
-                                    P(self.sa), P(self.anorm), st), "permute")
-            rec(4)
+            ok(L.wq_quantize_permute_f16(P(x), T, H, group, P(self.p2r), k, R, P(self.A), P(self.sa),
+                                         P(self.anorm), st), "quant_permute")
+            rec()
             ok(L.wq_grouped_gemm_w8a8_f16codes(P(self.A), P(self.anorm), P(self.sa), P(self.W13),
                                                P(self.S13), P(self.offsets), E, R, 2 * I, H, sc, ac,
                                                0, P(self.gu), P(self.gws), self.gws_n,
                                                P(self.status), st), "gemm1")
-            rec(5)
+            rec()
             ok(L.wq_silu_mul_quant_f16(P(self.gu), R, I, 128 if c.scheme == "block" else 0,
                                        P(self.hq), P(self.sh), P(self.hnorm), st), "silu_mul_quant")
-            rec(6)
+            rec()
             ok(L.wq_grouped_gemm_w8a8_f16codes(P(self.hq), P(self.hnorm), P(self.sh), P(self.W2),
                                                P(self.S2), P(self.offsets), E, R, H, I, sc, ac, 0,
                                                P(self.y), P(self.gws), self.gws_n, P(self.status),
                                                st), "gemm2")
         else:
+            if group == 0:
+                ok(L.wq_quantize_per_token(P(x), T, H, H, P(self.q), P(self.s), st), "quant")
+            else:
+                ok(L.wq_quantize_per_token_group(P(x), T, H, H, group, P(self.q), P(self.s), st),
+                   "quant")
+            rec()
             ok(L.wq_moe_permute(P(self.q), P(self.s), self.g1, T, k, H, P(self.sp), R, P(self.A),
                                 P(self.sa), st), "permute")
-            rec(4)
+            rec()
             ok(L.wq_grouped_gemm_w8a8(P(self.A), P(self.sa), P(self.W13), P(self.S13),
                                       P(self.offsets), E, R, 2 * I, H, sc, ac, 0, P(self.gu),
                                       P(self.gws), self.gws_n, P(self.status), st), "gemm1")
-            rec(5)
+            rec()
             ok(L.wq_silu_mul_quant(P(self.gu), R, I, 128 if c.scheme == "block" else 0, P(self.hq),
                                    P(self.sh), st), "silu_mul_quant")
-            rec(6)
+            rec()
             ok(L.wq_grouped_gemm_w8a8(P(self.hq), P(self.sh), P(self.W2), P(self.S2),
                                       P(self.offsets), E, R, H, I, sc, ac, 0, P(self.y),
                                       P(self.gws), self.gws_n, P(self.status), st), "gemm2")
-        rec(7)
+        rec()
         ok(L.wq_moe_combine(P(self.y), P(self.p2r), P(self.w), T, k, H, P(self.out), st), "combine")
-        rec(8)
+        rec()
+        assert n[0] == len(self.stages) + 1
         return self.out
 
 
@@ -765,7 +778,7 @@ def run_layer(args, cfg):
     for _ in range(args.warmup):
         fwd()
         layer.step(x, logits)
-    nst = len(Layer.STAGES)
+    nst = len(layer.stages)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -792,7 +805,7 @@ def run_layer(args, cfg):
         torch.cuda.synchronize()
         staged_ms = start.elapsed_time(end) / args.steps
     stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]))
-                for j, s in enumerate(Layer.STAGES)}
+                for j, s in enumerate(layer.stages)}
     fused = layer.time_fused(args.steps) if cfg.scheme == "block" and layer.f16 else None
     for st in (layer.status, fst):
         if int(st.item()) != 0:
