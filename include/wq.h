@@ -355,8 +355,8 @@ WQ_API int wq_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group
  * per-expert host loop [LL]):
  *   out[t] = bf16( acc ),  acc = 0; for j ascending: acc = acc + w[t][j] * y[pair_to_row[t*k+j]]
  * y bf16 [*][H], pair_to_row int32 [T*k] (a -1 entry contributes nothing),
- * w float [T][k], out bf16 [T][H].  Requirements: H % 8 == 0, 16-byte
- * aligned y and out. */
+ * w float [T][k], out bf16 [T][H].  Requirements: 1 <= k <= 32, H % 8 == 0,
+ * 16-byte aligned y and out (k > 32: WQ_ERR_UNSUPPORTED). */
 WQ_API int wq_moe_combine(const uint16_t *y, const int32_t *pair_to_row, const float *w, int T, int k,
                    int64_t H, uint16_t *out, wq_stream_t stream);
 

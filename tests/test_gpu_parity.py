@@ -145,12 +145,15 @@ def test_silu_mul_quant(R, I, group):
     assert np.array_equal(np_(hq), hqo) and np.array_equal(np_(sh), sho)
 
 
-def test_moe_combine():
-    T, k, H = 129, 8, 7168
-    rng = np.random.default_rng(3)
+@pytest.mark.parametrize("T,k,H", [(129, 8, 7168), (3, 8, 7168), (1, 1, 8), (64, 16, 512),
+                                   (5, 32, 256), (200, 2, 1032)])
+def test_moe_combine(T, k, H):
+    """Every k up to 32 (register sets of 8, 16 and 32 rows), few tokens (rows
+    split over several CTAs), odd widths; a -1 row contributes nothing."""
+    rng = np.random.default_rng(3 + T + k)
     y = (torch.randn(T * k + 5, H, generator=torch.Generator().manual_seed(1)) * 3).to(torch.bfloat16)
     p2r = rng.permutation(T * k).astype(np.int32)
-    p2r[5] = -1
+    p2r[min(5, T * k - 1)] = -1
     w = rng.random((T, k)).astype(np.float32)
     out = wq.moe_combine(y.to(DEV), torch.from_numpy(p2r).to(DEV), torch.from_numpy(w).to(DEV), k)
     yb = bits(y)
@@ -158,6 +161,14 @@ def test_moe_combine():
     yz = np.concatenate([yb, np.zeros((1, H), np.uint16)])
     p2r_o = np.where(p2r < 0, yb.shape[0], p2r)
     assert_bf16_equal(bits(out), O.moe_combine(yz, p2r_o, w, k), "combine")
+
+
+def test_moe_combine_refuses_k_above_32():
+    y = torch.zeros(33, 8, dtype=torch.bfloat16, device=DEV)
+    p2r = torch.arange(33, dtype=torch.int32, device=DEV)
+    w = torch.ones(1, 33, device=DEV)
+    with pytest.raises(wq.WQError):
+        wq.moe_combine(y, p2r, w, 33)
 
 
 # ---------------------------------------------------------------- grouped GEMM

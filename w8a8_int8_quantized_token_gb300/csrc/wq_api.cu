@@ -594,7 +594,7 @@ int wq_moe_combine(const uint16_t *y, const int32_t *pair_to_row, const float *w
   if (T < 0 || k < 1 || H < 0) return WQ_ERR_INVALID_ARG;
   if (T == 0 || H == 0) return WQ_OK;
   if (!y || !pair_to_row || !w || !out) return WQ_ERR_INVALID_ARG;
-  if (H % 8 || !al16(y) || !al16(out)) return WQ_ERR_UNSUPPORTED;
+  if (k > 32 || H % 8 || !al16(y) || !al16(out)) return WQ_ERR_UNSUPPORTED;
   WQ_TRY(check_device());
   return launch_combine(y, pair_to_row, w, T, k, H, out, stream);
 }

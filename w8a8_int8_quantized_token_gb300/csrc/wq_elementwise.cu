@@ -1113,25 +1113,40 @@ int launch_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group,
 }
 
 // ---------------------------------------------------------------------------
-// Weighted combine (the gather after the down GEMM): one CTA per token.
+// Weighted combine (the gather after the down GEMM): blockIdx.x = token,
+// blockIdx.y = slice of its row.  A thread loads its 16-byte piece of all k
+// routed rows first (KMAX >= k, so the loads are independent and in flight
+// together), then sums w_j * y_j in j order, as the method writes it.
+template <int KMAX>
 __global__ void __launch_bounds__(128) combine_kernel(const uint16_t *__restrict__ y,
                                                       const int32_t *__restrict__ p2r,
                                                       const float *__restrict__ w, int k,
                                                       int64_t H, uint16_t *__restrict__ out) {
   const int64_t t = blockIdx.x;
   const int64_t nvec = H >> 3;
-  for (int64_t i = threadIdx.x; i < nvec; i += blockDim.x) {
+  int rows[KMAX];
+  float wt[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    rows[j] = j < k ? p2r[t * k + j] : -1;
+    wt[j] = j < k ? w[t * k + j] : 0.0f;
+  }
+  for (int64_t i = int64_t(blockIdx.y) * blockDim.x + threadIdx.x; i < nvec;
+       i += int64_t(gridDim.y) * blockDim.x) {
+    uint4 v[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (rows[j] >= 0) v[j] = __ldcs(reinterpret_cast<const uint4 *>(y + int64_t(rows[j]) * H) + i);
     float acc[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      const int row = p2r[t * k + j];
-      if (row < 0) continue;
-      const float wj = w[t * k + j];
-      float f[8];
-      unpack8(__ldcs(reinterpret_cast<const uint4 *>(y + int64_t(row) * H) + i), f);
+    for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) acc[c] = __fadd_rn(acc[c], __fmul_rn(wj, f[c]));
+    for (int j = 0; j < KMAX; ++j) {
+      if (rows[j] < 0) continue;
+      float f[8];
+      unpack8(v[j], f);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[c] = __fadd_rn(acc[c], __fmul_rn(wt[j], f[c]));
     }
     uint4 o;
     o.x = pack_bf16x2(acc[0], acc[1]);
@@ -1145,7 +1160,21 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint16_t *__restrict
 int launch_combine(const uint16_t *y, const int32_t *pair_to_row, const float *w, int T, int k,
                    int64_t H, uint16_t *out, cudaStream_t st) {
   if (T == 0 || H == 0) return WQ_OK;
-  combine_kernel<<<unsigned(T), 128, 0, st>>>(y, pair_to_row, w, k, H, out);
+  if (k > 32) return WQ_ERR_UNSUPPORTED;
+  // few tokens: split each row over several CTAs so that about four CTAs per
+  // SM are in flight
+  const int64_t nvec = H >> 3;
+  int64_t splits = (int64_t(4) * num_sms() + T - 1) / T;
+  const int64_t max_splits = (nvec + 127) / 128;
+  if (splits > max_splits) splits = max_splits;
+  if (splits < 1) splits = 1;
+  const dim3 grid{unsigned(T), unsigned(splits), 1u};
+  if (k <= 8)
+    combine_kernel<8><<<grid, 128, 0, st>>>(y, pair_to_row, w, k, H, out);
+  else if (k <= 16)
+    combine_kernel<16><<<grid, 128, 0, st>>>(y, pair_to_row, w, k, H, out);
+  else
+    combine_kernel<32><<<grid, 128, 0, st>>>(y, pair_to_row, w, k, H, out);
   return launched(1);
 }
 
