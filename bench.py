@@ -63,8 +63,8 @@ TRAFFIC = {
     "prefill": _TC5,
     "prefill_f32": _TC5,
     "decode": {"kernel": "gemm_small_kernel", "file": "wq_gemm_small.cu",
-               "sha256": "631ff97a218b338aa2afea514f46c03c798e2cd5a0ca728857fe4b05d6b34390",
-               "bytes": 8 * (941.271296e6 + 4.564736e6),
+               "sha256": "97e5d6ef521a4ed0bec73de5804f6968d9db907316f3dcdca4395170e2a3132a",
+               "bytes": 8 * (941.216512e6 + 4.608e6),
                "how": "ncu capture of GEMM1 at 16 tokens / 32 experts (same 4 rows per expert), "
                       "dram read+write scaled by the expert count (x 8)"},
 }
