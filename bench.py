@@ -67,6 +67,11 @@ TRAFFIC = {
                "bytes": 8 * (941.216512e6 + 4.608e6),
                "how": "ncu capture of GEMM1 at 16 tokens / 32 experts (same 4 rows per expert), "
                       "dram read+write scaled by the expert count (x 8)"},
+    "block": {"kernel": "gemm_tc6_kernel", "file": "wq_gemm_tc6.cu",
+              "sha256": "05be324188f32a9e8f688e68d5af108bc705afdcf669ac468d45b2ef63f5f898",
+              "bytes": 8 * (1.021679e9 + 33.830144e6),
+              "how": "ncu capture of GEMM1 at 512 tokens / 32 experts (same 128 rows per expert), "
+                     "dram read+write scaled by the expert count (x 8)"},
 }
 
 
