@@ -254,12 +254,10 @@ class Layer:
         self.f16 = ((2 * I) % 256 == 0
                     and H % 256 == 0 and R > 64 * E)
         cdt = torch.float16 if self.f16 else torch.int8
-        # the one-call layer's kernels, in its order (fp16 codes: each token
-        # quantized once and written to its k rows; int8 codes: quantize,
-        # then permute)
-        self.stages = (["route", "align", "quant_permute"] if self.f16 else
-                       ["route", "align", "quant", "permute"]) + [
-                           "gemm1", "silu_mul_quant", "gemm2", "combine"]
+        # the one-call layer's kernels, in its order (each token quantized
+        # once and written to its k rows, as int8 or fp16 codes)
+        self.stages = ["route", "align", "quant_permute", "gemm1", "silu_mul_quant", "gemm2",
+                       "combine"]
         self.A, self.sa = e(R, H, dt=cdt), e(R * self.g1, dt=torch.float32)
         self.anorm, self.hnorm = e(R, dt=torch.int32), e(R, dt=torch.int32)
         self.gu = e(R, 2 * I, dt=torch.bfloat16)
@@ -312,14 +310,8 @@ class Layer:
                                                P(self.y), P(self.gws), self.gws_n, P(self.status),
                                                st), "gemm2")
         else:
-            if group == 0:
-                ok(L.wq_quantize_per_token(P(x), T, H, H, P(self.q), P(self.s), st), "quant")
-            else:
-                ok(L.wq_quantize_per_token_group(P(x), T, H, H, group, P(self.q), P(self.s), st),
-                   "quant")
-            rec()
-            ok(L.wq_moe_permute(P(self.q), P(self.s), self.g1, T, k, H, P(self.sp), R, P(self.A),
-                                P(self.sa), st), "permute")
+            ok(L.wq_quantize_permute(P(x), T, H, group, P(self.p2r), k, R, P(self.A), P(self.sa), st),
+               "quant_permute")
             rec()
             ok(L.wq_grouped_gemm_w8a8(P(self.A), P(self.sa), P(self.W13), P(self.S13),
                                       P(self.offsets), E, R, 2 * I, H, sc, ac, 0, P(self.gu),

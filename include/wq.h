@@ -322,10 +322,14 @@ WQ_API int wq_quantize_per_token_f16(const uint16_t *x, int64_t T, int64_t K, in
  * maps to (alignment padding) are not written, and map entries outside
  * [0, R) are skipped.
  * Requirements: 1 <= k <= 32, K % 8 == 0, K % group == 0, K <= 65536,
- * 16-byte aligned x and A16. */
+ * 16-byte aligned x and A16. * wq_quantize_permute: the same with int8 codes A int8 [R][K] (row pitch K)
+ * and no norms; 16-byte aligned x and A. */
 WQ_API int wq_quantize_permute_f16(const uint16_t *x, int64_t T, int64_t K, int group,
                                    const int32_t *pair_to_row, int k, int64_t R, uint16_t *A16,
                                    float *sa, int32_t *norm2, wq_stream_t stream);
+WQ_API int wq_quantize_permute(const uint16_t *x, int64_t T, int64_t K, int group,
+                               const int32_t *pair_to_row, int k, int64_t R, int8_t *A, float *sa,
+                               wq_stream_t stream);
 
 /* Masked layout [LL]: A int8 [E][Mmax][K] with per-row scales sa
  * ([E][Mmax] or [E][Mmax][K/128]) and valid counts masked_m int32 [E]

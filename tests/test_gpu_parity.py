@@ -438,14 +438,16 @@ def test_moe_permute_f16(groups):
     assert np.array_equal(np_(n2), (Ao.astype(np.int64) ** 2).sum(1))
 
 
+@pytest.mark.parametrize("f16", [True, False], ids=["f16", "i8"])
 @pytest.mark.parametrize("T,K,k,E,group,pad", [(200, 7168, 8, 64, 0, 1), (200, 7168, 8, 64, 128, 1),
                                                 (33, 256, 1, 4, 0, 1), (40, 512, 32, 64, 32, 1),
                                                 (70, 2048, 4, 16, 0, 4), (5, 65536, 2, 4, 256, 1)])
-def test_quantize_permute_f16(T, K, k, E, group, pad):
+def test_quantize_permute(T, K, k, E, group, pad, f16):
     """Quantization and permute in one pass (scatter form) against the
-    oracle's quantization followed by its permute: every routed row's fp16
-    codes, scale(s) and squared norm.  With padded alignment (pad 4) the
-    padding rows, which no pair maps to, keep their previous contents."""
+    oracle's quantization followed by its permute: every routed row's codes
+    (fp16 or int8), scale(s) and, for fp16 codes, squared norm.  With padded
+    alignment (pad 4) the padding rows, which no pair maps to, keep their
+    previous contents."""
     rng = np.random.default_rng(T * 31 + K + k)
     x = (torch.randn(T, K, generator=torch.Generator().manual_seed(K + T)) * 2).to(torch.bfloat16)
     x[0, :3] = torch.tensor([0.0, 1e-30, -5e4])  # a zero, a tiny and a large value in one row
@@ -457,19 +459,22 @@ def test_quantize_permute_f16(T, K, k, E, group, pad):
     else:
         qo, so = O.quantize_per_token_group(bits(x), group)
     Ao, sao = O.moe_permute(qo, so, spo, k)
-    A16 = torch.full((R, K), 7.0, dtype=torch.float16, device=DEV)
     sa = torch.full((R,) if group == 0 else (R, K // group), -3.0, device=DEV)
-    n2 = torch.full((R,), -5, dtype=torch.int32, device=DEV) if group == 0 else None
-    wq.quantize_permute_f16(x.to(DEV), torch.from_numpy(p2r).to(DEV), k, R, group, out=(A16, sa, n2))
     valid = spo >= 0
-    assert np.array_equal(np_(A16)[valid].astype(np.int32), Ao[valid].astype(np.int32))
+    if f16:
+        A = torch.full((R, K), 7.0, dtype=torch.float16, device=DEV)
+        n2 = torch.full((R,), -5, dtype=torch.int32, device=DEV) if group == 0 else None
+        wq.quantize_permute_f16(x.to(DEV), torch.from_numpy(p2r).to(DEV), k, R, group, out=(A, sa, n2))
+        if group == 0:
+            assert np.array_equal(np_(n2)[valid], (Ao[valid].astype(np.int64) ** 2).sum(1))
+            assert bool((np_(n2)[~valid] == -5).all())
+    else:
+        A = torch.full((R, K), 7, dtype=torch.int8, device=DEV)
+        wq.quantize_permute(x.to(DEV), torch.from_numpy(p2r).to(DEV), k, R, group, out=(A, sa))
+    assert np.array_equal(np_(A)[valid].astype(np.int32), Ao[valid].astype(np.int32))
     assert np.array_equal(np_(sa)[valid], sao[valid])
-    if group == 0:
-        assert np.array_equal(np_(n2)[valid], (Ao[valid].astype(np.int64) ** 2).sum(1))
     # padding rows untouched
-    assert bool((np_(A16)[~valid] == 7.0).all()) and bool((np_(sa)[~valid] == -3.0).all())
-    if group == 0:
-        assert bool((np_(n2)[~valid] == -5).all())
+    assert bool((np_(A)[~valid] == 7).all()) and bool((np_(sa)[~valid] == -3.0).all())
 
 
 def test_quantize_permute_f16_skips_rows_outside():

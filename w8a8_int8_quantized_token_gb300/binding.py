@@ -52,6 +52,7 @@ _SIGS = {
     "wq_grouped_gemm_w8a8_f16codes": (_I, [_P, _P, _P, _P, _P, _P, _I, _L, _L, _L, _I, _I, _I, _P, _P, _S, _P, _P]),
     "wq_quantize_per_token_f16": (_I, [_P, _L, _L, _L, _P, _P, _P, _P]),
     "wq_quantize_permute_f16": (_I, [_P, _L, _L, _I, _P, _I, _L, _P, _P, _P, _P]),
+    "wq_quantize_permute": (_I, [_P, _L, _L, _I, _P, _I, _L, _P, _P, _P]),
     "wq_grouped_gemm_silu_quant_workspace_size": (_S, [_L, _I]),
     "wq_quantize_weight_int4": (_I, [_P, _L, _L, _P, _P, _P]),
     "wq_grouped_gemm_w4a8_masked": (_I, [_P, _P, _P, _I, _I, _P, _P, _L, _L, _I, _P, _P, _S, _P, _P]),
@@ -365,6 +366,23 @@ def quantize_permute_f16(x, pair_to_row, k, R, group=0, out=None):
                                          _ptr(sa), _ptr(n2) if n2 is not None else None, _stream()),
            "wq_quantize_permute_f16")
     return A16, sa, n2
+
+
+def quantize_permute(x, pair_to_row, k, R, group=0, out=None):
+    """Quantization and permute in one pass, int8 codes: (A int8 [R, K], sa
+    [R] or [R, K/group]).  Rows no pair maps to keep the contents of `out`
+    (a tuple of the two tensors) or are left uninitialised."""
+    _dev(x, torch.bfloat16, "x")
+    _dev(pair_to_row, torch.int32, "pair_to_row")
+    T, K = x.shape
+    if out is None:
+        A = torch.empty(R, K, dtype=torch.int8, device=x.device)
+        sa = torch.empty((R,) if group == 0 else (R, K // group), dtype=torch.float32, device=x.device)
+    else:
+        A, sa = out
+    _check(lib().wq_quantize_permute(_ptr(x), T, K, group, _ptr(pair_to_row), k, R, _ptr(A), _ptr(sa),
+                                     _stream()), "wq_quantize_permute")
+    return A, sa
 
 
 # ---------------------------------------------------------------- GEMMs

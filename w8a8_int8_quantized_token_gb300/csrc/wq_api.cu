@@ -541,6 +541,20 @@ int wq_quantize_per_token_f16(const uint16_t *x, int64_t T, int64_t K, int64_t l
   return launch_quant_rows_f16(x, T, K, ldx, 0, q16, s, norm2, stream);
 }
 
+int wq_quantize_permute(const uint16_t *x, int64_t T, int64_t K, int group,
+                        const int32_t *pair_to_row, int k, int64_t R, int8_t *A, float *sa,
+                        wq_stream_t stream) {
+  if (T < 0 || K < 0 || k < 1 || k > 32 || R < 0) return WQ_ERR_INVALID_ARG;
+  if (group != 0 && group != 32 && group != 64 && group != 128 && group != 256)
+    return WQ_ERR_INVALID_ARG;
+  if (T == 0 || K == 0 || R == 0) return WQ_OK;
+  if (!x || !pair_to_row || !A || !sa) return WQ_ERR_INVALID_ARG;
+  if (K % 8 || (group != 0 && K % group) || !al16(x) || !al16(A)) return WQ_ERR_UNSUPPORTED;
+  if (K > 65536) return WQ_ERR_UNSUPPORTED;
+  WQ_TRY(check_device());
+  return launch_quant_scatter_i8(x, T, K, K, group, pair_to_row, k, R, A, sa, stream);
+}
+
 int wq_quantize_permute_f16(const uint16_t *x, int64_t T, int64_t K, int group,
                             const int32_t *pair_to_row, int k, int64_t R, uint16_t *A16,
                             float *sa, int32_t *norm2, wq_stream_t stream) {
@@ -699,8 +713,7 @@ int run_forward(const uint16_t *x, const float *logits, const int8_t *W13, const
     WQ_TRY(launch_grouped_gemm(f2, st));
     return launch_combine(b.y, b.pair_to_row, b.w, T, k, H, out, st);
   }
-  WQ_TRY(launch_quant_rows(x, T, H, H, blk ? 128 : 0, b.q, b.s, st));
-  WQ_TRY(launch_permute(b.q, b.s, blk ? H / 128 : 1, k, H, b.sorted_pair, R, b.A, b.sa, st));
+  WQ_TRY(launch_quant_scatter_i8(x, T, H, H, blk ? 128 : 0, b.pair_to_row, k, R, b.A, b.sa, st));
   GemmArgs g1{b.A, nullptr, nullptr, b.sa, W13, sw13, b.offsets, nullptr, 0, E, R, int64_t(2) * I, H, scheme, acc,
               WQ_OUT_BF16, b.gu, b.gemm_ws, status};
   WQ_TRY(launch_grouped_gemm(g1, st));

@@ -288,6 +288,9 @@ int launch_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group,
 int launch_quant_scatter_f16(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group,
                              const int32_t *pair_to_row, int k, int64_t R, uint16_t *A16,
                              float *sa, int32_t *norm2, cudaStream_t st);
+int launch_quant_scatter_i8(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group,
+                            const int32_t *pair_to_row, int k, int64_t R, int8_t *A, float *sa,
+                            cudaStream_t st);
 int launch_permute_f16(const int8_t *q, const float *s, int groups, int k, int64_t K,
                        const int32_t *sorted_pair, int64_t R, uint16_t *A16, float *sa,
                        int32_t *norm2, cudaStream_t st);

@@ -136,15 +136,15 @@ int launch_quant_v(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int gro
 
 // Quantization fused with the permute, scatter form: one CTA per token
 // quantizes its row once (the rule of quant_row_kernel) and writes the codes
-// as fp16 values, the scale(s) and, with one scale per row, the squared norm
-// to each of the token's k routed rows pair_to_row[t * k + j] (a row outside
-// [0, R) is skipped).  Each token is read once and the int8 codes never reach memory
+// (int8, or with F16 as fp16 values), the scale(s) and, with F16 and one
+// scale per row, the squared norm to each of the token's k routed rows
+// pair_to_row[t * k + j] (a row outside [0, R) is skipped).  Each token is read once and the int8 codes never reach memory
 // ("[WIP] feat: support cutlass_moe_fp8 for deepepmoe", review: ep_scatter
 // places each token's activations at its experts' rows).
-template <int V, int GV>
-__global__ void __launch_bounds__(1024) quant_scatter_f16_kernel(
+template <int V, int GV, bool F16>
+__global__ void __launch_bounds__(1024) quant_scatter_kernel(
     const uint16_t *__restrict__ x, int64_t K, int64_t ldx, const int32_t *__restrict__ pair_to_row,
-    int k, int64_t R, uint16_t *__restrict__ A16, float *__restrict__ sa,
+    int k, int64_t R, void *__restrict__ A_out, float *__restrict__ sa,
     int32_t *__restrict__ norm2) {
   __shared__ float red[32];
   __shared__ int redi[32];
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(1024) quant_scatter_f16_kernel(
     }
     __syncthreads();  // dst
   }
-  uint4 w[V];
+  uint4 w[V];  // F16: eight fp16 codes; else two words of int8 codes in .x, .y
   int n2 = 0;
 #pragma unroll
   for (int i = 0; i < V; ++i) {
@@ -208,20 +208,27 @@ __global__ void __launch_bounds__(1024) quant_scatter_f16_kernel(
                                     quant_bits(f[2], sc[i], rs[i]), quant_bits(f[3], sc[i], rs[i]));
       const uint32_t hi = pack_s8x4(quant_bits(f[4], sc[i], rs[i]), quant_bits(f[5], sc[i], rs[i]),
                                     quant_bits(f[6], sc[i], rs[i]), quant_bits(f[7], sc[i], rs[i]));
-      tc::s8x4_to_f16x4(lo, w[i].x, w[i].y);
-      tc::s8x4_to_f16x4(hi, w[i].z, w[i].w);
-      if constexpr (GV == 0) n2 = __dp4a(int(hi), int(hi), __dp4a(int(lo), int(lo), n2));
+      if constexpr (F16) {
+        tc::s8x4_to_f16x4(lo, w[i].x, w[i].y);
+        tc::s8x4_to_f16x4(hi, w[i].z, w[i].w);
+        if constexpr (GV == 0) n2 = __dp4a(int(hi), int(hi), __dp4a(int(lo), int(lo), n2));
+      } else {
+        w[i] = make_uint4(lo, hi, 0u, 0u);
+      }
     }
   }
   for (int j = 0; j < k; ++j) {
     const int64_t r = dst[j];
     if (r < 0) continue;  // CTA-uniform
-    uint4 *o = reinterpret_cast<uint4 *>(A16 + r * K);
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int idx = threadIdx.x + i * blockDim.x;
       if (idx < nvec) {
-        __stcs(o + idx, w[i]);
+        if constexpr (F16)
+          __stcs(reinterpret_cast<uint4 *>(static_cast<uint16_t *>(A_out) + r * K) + idx, w[i]);
+        else
+          __stcs(reinterpret_cast<uint2 *>(static_cast<int8_t *>(A_out) + r * K) + idx,
+                 make_uint2(w[i].x, w[i].y));
         if constexpr (GV != 0) {
           if (idx % GV == 0) sa[r * (nvec / GV) + idx / GV] = sc[i];
         }
@@ -229,33 +236,37 @@ __global__ void __launch_bounds__(1024) quant_scatter_f16_kernel(
     }
   }
   if constexpr (GV == 0) {
+    if constexpr (F16) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
-    const int wi = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
-    if (l == 0) redi[wi] = n2;
-    __syncthreads();
+      for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+      const int wi = threadIdx.x >> 5, l = threadIdx.x & 31;
+      if (l == 0) redi[wi] = n2;
+      __syncthreads();
+    }
     if (threadIdx.x < k) {
       const int64_t r = dst[threadIdx.x];
       if (r >= 0) {
-        int tot = 0;
-        for (int q = 0; q < nw; ++q) tot += redi[q];
-        norm2[r] = tot;
+        if constexpr (F16) {
+          int tot = 0;
+          for (int q = 0; q < int(blockDim.x >> 5); ++q) tot += redi[q];
+          norm2[r] = tot;
+        }
         sa[r] = sc[0];
       }
     }
   }
 }
 
-template <int V>
+template <int V, bool F16>
 int launch_quant_scatter_v(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group,
-                           const int32_t *pair_to_row, int k, int64_t R, uint16_t *A16, float *sa,
+                           const int32_t *pair_to_row, int k, int64_t R, void *A, float *sa,
                            int32_t *norm2, cudaStream_t st) {
   const int64_t nvec = K / 8;
   int threads = int((nvec + V - 1) / V);
   threads = ((threads + 31) / 32) * 32;
   if (threads < k) threads = ((k + 31) / 32) * 32;
 #define WQ_QSC(GV) \
-  quant_scatter_f16_kernel<V, GV><<<unsigned(T), threads, 0, st>>>(x, K, ldx, pair_to_row, k, R, A16, sa, norm2)
+  quant_scatter_kernel<V, GV, F16><<<unsigned(T), threads, 0, st>>>(x, K, ldx, pair_to_row, k, R, A, sa, norm2)
   switch (group) {
     case 0: WQ_QSC(0); break;
     case 32: WQ_QSC(4); break;
@@ -269,16 +280,29 @@ int launch_quant_scatter_v(const uint16_t *x, int64_t T, int64_t K, int64_t ldx,
 }
 
 // k <= 32 destinations per token; rows up to 8192 vectors (K <= 65536)
-int launch_quant_scatter_f16(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group,
-                             const int32_t *pair_to_row, int k, int64_t R, uint16_t *A16,
-                             float *sa, int32_t *norm2, cudaStream_t st) {
+template <bool F16>
+static int launch_quant_scatter_t(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group,
+                                  const int32_t *pair_to_row, int k, int64_t R, void *A,
+                                  float *sa, int32_t *norm2, cudaStream_t st) {
   if (T == 0 || K == 0) return WQ_OK;
   const int64_t nvec = K / 8;
   if (k < 1 || k > 32 || nvec > 8 * 1024 || T > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
   if (group != 0 && K % group) return WQ_ERR_UNSUPPORTED;
-  if (nvec <= 2 * 1024) return launch_quant_scatter_v<2>(x, T, K, ldx, group, pair_to_row, k, R, A16, sa, norm2, st);
-  if (nvec <= 4 * 1024) return launch_quant_scatter_v<4>(x, T, K, ldx, group, pair_to_row, k, R, A16, sa, norm2, st);
-  return launch_quant_scatter_v<8>(x, T, K, ldx, group, pair_to_row, k, R, A16, sa, norm2, st);
+  if (nvec <= 2 * 1024) return launch_quant_scatter_v<2, F16>(x, T, K, ldx, group, pair_to_row, k, R, A, sa, norm2, st);
+  if (nvec <= 4 * 1024) return launch_quant_scatter_v<4, F16>(x, T, K, ldx, group, pair_to_row, k, R, A, sa, norm2, st);
+  return launch_quant_scatter_v<8, F16>(x, T, K, ldx, group, pair_to_row, k, R, A, sa, norm2, st);
+}
+
+int launch_quant_scatter_f16(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group,
+                             const int32_t *pair_to_row, int k, int64_t R, uint16_t *A16,
+                             float *sa, int32_t *norm2, cudaStream_t st) {
+  return launch_quant_scatter_t<true>(x, T, K, ldx, group, pair_to_row, k, R, A16, sa, norm2, st);
+}
+
+int launch_quant_scatter_i8(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group,
+                            const int32_t *pair_to_row, int k, int64_t R, int8_t *A, float *sa,
+                            cudaStream_t st) {
+  return launch_quant_scatter_t<false>(x, T, K, ldx, group, pair_to_row, k, R, A, sa, nullptr, st);
 }
 
 template <bool F16>
