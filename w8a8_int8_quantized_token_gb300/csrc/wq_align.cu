@@ -194,7 +194,10 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
                                                            int32_t *__restrict__ zero_word,
                                                            int small_max,
                                                            Tile *__restrict__ small,
-                                                           int32_t *__restrict__ nsmall) {
+                                                           int32_t *__restrict__ nsmall,
+                                                           const int32_t *__restrict__ gate) {
+  // the list of a gated exact recompute: not needed unless its flag is set
+  if (gate != nullptr && *gate == 0) return;
   __shared__ int32_t part[1024], part_s[1024];
   __shared__ int32_t hist[kMaxTileRows + 1];  // partial main tiles by row count, then cursors
   if (zero_word != nullptr && threadIdx.x < 2) zero_word[threadIdx.x] = 0;  // flag, item counter
@@ -288,10 +291,11 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
 
 int launch_build_tiles(const int32_t *offsets, const int32_t *masked_m, int Mmax, int E, int BM,
                        int64_t R, Tile *tiles, int32_t *ntiles, int32_t *zero_word,
-                       cudaStream_t st, int small_max, Tile *small, int32_t *nsmall) {
+                       cudaStream_t st, int small_max, Tile *small, int32_t *nsmall,
+                       const int32_t *gate) {
   if (BM < 1 || BM > kMaxTileRows) return WQ_ERR_UNSUPPORTED;
   build_tiles_kernel<<<1, 1024, 0, st>>>(offsets, masked_m, Mmax, E, BM, R, tiles, ntiles,
-                                         zero_word, small_max, small, nsmall);
+                                         zero_word, small_max, small, nsmall, gate);
   return launched(1);
 }
 

@@ -243,7 +243,7 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
       WQ_TRY(launch_gemm_tc4(a, w.t256, w.n256, int(w.m256), w.redo, st));
     }
     WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 64, a.R, w.t64, w.n64, nullptr,
-                              st));
+                              st, 0, nullptr, nullptr, w.redo));
     return launch_gemm_simt(a, w.t64, w.n64, int(w.m64), w.redo, st);
   }
   // Segment remainders of at most 16 rows (all of a decode batch's experts,
@@ -278,12 +278,12 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
     // small remainders to the small-token engine
     const bool split = small && gate == nullptr;
     WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 128, a.R, w.t128, w.n128,
-                              nullptr, st, split ? small_max : 0, w.tsm, w.nsm));
+                              nullptr, st, split ? small_max : 0, w.tsm, w.nsm, gate));
     if (split) WQ_TRY(launch_gemm_small(a, w.tsm, w.nsm, int(w.msm), st));
     return launch_gemm_tc(a, w.t128, w.n128, int(w.m128), gate, st);
   }
   WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, 64, a.R, w.t64, w.n64, nullptr,
-                            st));
+                            st, 0, nullptr, nullptr, gate));
   return launch_gemm_simt(a, w.t64, w.n64, int(w.m64), gate, st);
 }
 

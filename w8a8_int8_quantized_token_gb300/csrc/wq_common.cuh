@@ -346,7 +346,7 @@ inline bool acc_modes_agree(const GemmArgs &a) {
 int launch_build_tiles(const int32_t *offsets, const int32_t *masked_m, int Mmax, int E, int BM,
                        int64_t R, Tile *tiles, int32_t *ntiles, int32_t *zero_word,
                        cudaStream_t st, int small_max = 0, Tile *small = nullptr,
-                       int32_t *nsmall = nullptr);
+                       int32_t *nsmall = nullptr, const int32_t *gate = nullptr);
 size_t gemm_ws_bytes(int64_t R, int E, int Mmax, bool masked, bool silu = false);
 int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st);
 }  // namespace wq
