@@ -849,3 +849,49 @@ def test_layer_forward_masked_w4a8():
     got = bits(y)
     assert_bf16_equal(got[valid], want[valid], "w4a8 masked layer")
     assert np.all(O.bf16_to_f32(got[~valid]) == 3.0)
+
+
+# ---------------------------------------------------------------- empty inputs
+def test_empty_inputs_write_nothing():
+    """Zero tokens, zero routed rows and all-zero masked counts: every entry
+    returns success and leaves its outputs untouched."""
+    H, I, E, k = 256, 128, 4, 2
+    x0 = torch.empty(0, H, dtype=torch.bfloat16, device=DEV)
+    q, s = wq.quantize_per_token(x0)
+    assert q.shape == (0, H) and s.shape == (0,)
+    q, s = wq.quantize_per_token_group(x0, 128)
+    assert q.shape == (0, H)
+    p2r0 = torch.empty(0, dtype=torch.int32, device=DEV)
+    A16 = torch.full((4, H), 7.0, dtype=torch.float16, device=DEV)
+    sa = torch.full((4,), -3.0, device=DEV)
+    n2 = torch.full((4,), -5, dtype=torch.int32, device=DEV)
+    wq.quantize_permute_f16(x0, p2r0, k, 4, 0, out=(A16, sa, n2))
+    A8 = torch.full((4, H), 7, dtype=torch.int8, device=DEV)
+    wq.quantize_permute(x0, p2r0, k, 4, 0, out=(A8, sa))
+    gu0 = torch.empty(0, 2 * I, dtype=torch.bfloat16, device=DEV)
+    hq, sh = wq.silu_mul_quant(gu0, 0)
+    assert hq.shape == (0, I)
+    hq16, sh16, hn = wq.silu_mul_quant_f16(gu0, 0)
+    assert hq16.shape == (0, I)
+    out = wq.moe_combine(torch.empty(0, H, dtype=torch.bfloat16, device=DEV), p2r0,
+                         torch.empty(0, k, device=DEV), k)
+    assert out.shape == (0, H)
+    cfg = synth.small_config("empty", T=0, H=H, I=I, E=E, k=k)
+    (W13, S13, W2, S2), _ = quantized_weights(cfg, DEV, experts=[])
+    lg0 = torch.empty(0, E, dtype=torch.float32, device=DEV)
+    assert wq.moe_forward(x0, lg0, W13, S13, W2, S2, k).shape == (0, H)
+    # grouped GEMM with every expert empty
+    offs = torch.zeros(E + 1, dtype=torch.int32, device=DEV)
+    g = wq.grouped_gemm_w8a8(torch.empty(0, H, dtype=torch.int8, device=DEV),
+                             torch.empty(0, device=DEV), W13, S13, offs)
+    assert g.shape == (0, 2 * I)
+    # masked layer with every count zero: y untouched
+    Mmax = 16
+    a = torch.ones(E, Mmax, H, dtype=torch.int8, device=DEV)
+    sam = torch.ones(E, Mmax, device=DEV)
+    y = torch.full((E, Mmax, H), 5.0, dtype=torch.bfloat16, device=DEV)
+    wq.moe_forward_masked(a, sam, torch.zeros(E, dtype=torch.int32, device=DEV), W13, S13, W2, S2, y=y)
+    torch.cuda.synchronize()
+    assert bool((y == 5.0).all())
+    assert bool((A16 == 7.0).all()) and bool((A8 == 7).all()) and bool((sa == -3.0).all())
+    assert bool((n2 == -5).all())
