@@ -289,8 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   } else if (warp < WARP_EPI) {
     // ------------------------------------------------------------ converters
     // thread = weight row (its tensor-memory lane); group `grp` takes the K
-    // stages of parity grp; the 16-byte pieces of a row are read in a
-    // lane-rotated order so a warp's reads hit distinct banks
+    // stages of parity grp
     const int grp = (warp - 2) >> 2;
     const int q = warp & 3;
     const int row = q * 32 + lane;
@@ -307,16 +306,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
           ok = false;
           break;
         }
+        // the slot is 64-byte swizzled: piece m of a row sits at piece
+        // m ^ ((row / 2) % 4), so the eight rows a quarter-warp reads at once
+        // hit eight different 16-byte bank groups
         const uint8_t *src = sm + P::OFF_W8 + sw * P::W8B + row * 64;
+        const int swz = (row >> 1) & 3;
         uint4 v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int c = (j + (lane >> 1)) & 3;
-          const uint4 x = *reinterpret_cast<const uint4 *>(src + c * 16);
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-            if (c == m) v[m] = x;
-        }
+        for (int m = 0; m < 4; ++m) v[m] = *reinterpret_cast<const uint4 *>(src + ((m ^ swz) << 4));
         fence_async_smem();  // these reads before the next copy into the slot
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(P::B_W8_EMPTY + sw));
@@ -553,7 +550,8 @@ static int launch_tc5(const GemmArgs &a, const Tile *tiles, const int32_t *ntile
   TokenMaps<TN> mT;
   // the output box map: bf16 [R][N]; the direct-store plan and int32 output
   // never use it (the same rows read as 16-bit values stay inside the buffer)
-  if (!make_tma_2d_u8(&mW, a.W, int64_t(a.E) * a.N, a.K, BK, WM) ||
+  static_assert(BK == 64, "one 64-byte-swizzled row of weight codes per K stage");
+  if (!make_tma_2d_u8_sw64(&mW, a.W, int64_t(a.E) * a.N, a.K, WM) ||
       !make_tma_2d_b16(&mO, a.out, a.R, a.N, WM, 32))
     return WQ_ERR_LAUNCH;
   for (int i = 0; i < TokenMaps<TN>::N; ++i)

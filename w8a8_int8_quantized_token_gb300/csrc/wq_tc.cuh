@@ -372,6 +372,7 @@ bool make_tma_2d_u8(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, in
                     int box_rows);
 // 2-D 8-bit tensor [rows][K], box 128 x box_rows landing 128-byte swizzled
 bool make_tma_2d_u8_sw128(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows);
+bool make_tma_2d_u8_sw64(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows);
 // 2-D 16-bit tensor [rows][K], box 64 x box_rows landing 128-byte swizzled
 bool make_tma_2d_b16_sw128(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K,
                            int box_rows);

@@ -42,6 +42,21 @@ bool make_tma_2d_u8(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, in
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D 8-bit tensor [rows][K] (K contiguous), box 64 x box_rows written to
+// shared memory 64-byte swizzled (16-byte piece c of row r lands at piece
+// c ^ ((r / 2) % 4) of that row), zero fill outside the tensor.
+bool make_tma_2d_u8_sw64(CUtensorMap *m, const void *ptr, int64_t rows, int64_t K, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(K)};
+  cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D 8-bit tensor [rows][K] (K contiguous), box 128 x box_rows written to
 // shared memory 128-byte swizzled (16-byte piece c of row r lands at piece
 // c ^ (r % 8) of that row), zero fill outside the tensor.
