@@ -4,7 +4,10 @@ One step = the whole hot path on one batch: route -> quantize -> align ->
 permute -> GEMM1 (gate_up) -> SiLU-mul + re-quantize -> GEMM2 (down) ->
 combine.  Weights (11.3 GB of int8) and the step's activations are resident
 in HBM before the timed region.  `value` times the one-call layer
-(wq_moe_forward) over K steps; a second timed pass runs the same steps as
+(wq_moe_forward), recorded once into a CUDA graph before the timed region
+and replayed K times (every kernel of every step runs; the same steps
+launched call by call are reported as eager_ms_per_step); a second timed
+pass runs the same steps as
 separate C-ABI calls with CUDA events between them for the per-stage times
 and the rooflines; `e2e` runs the layer through wq_moe_forward_host with
 pinned host activations, copies included.
@@ -229,6 +232,25 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def capture_graph(wq, step, dev):
+    """Record one call of `step` into a CUDA graph (first use and any
+    side-stream setup happen in a plain call on the capture stream first);
+    returns the graph and the library kernels one replay launches."""
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        step()
+    torch.cuda.current_stream().wait_stream(cs)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    n0 = wq.lib().wq_kernel_launches()
+    with torch.cuda.graph(graph):
+        step()
+    per_step = wq.lib().wq_kernel_launches() - n0
+    torch.cuda.synchronize()
+    return graph, per_step
 
 
 class Layer:
@@ -497,19 +519,29 @@ def run_masked(args, cfg, w4=False):
                                              status=st)
     for _ in range(args.warmup):
         step()
+    # one layer call recorded into a CUDA graph (the small-segment engine's
+    # second stream included), outside the timed region
+    graph, per_step = capture_graph(wq, step, dev)
+    for _ in range(args.warmup):
+        graph.replay()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(0) as clk:
         torch.cuda.synchronize()
-        n0 = wq.lib().wq_kernel_launches()
         torch.cuda.nvtx.range_push("timed")
+        e0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record()
+        torch.cuda.nvtx.range_pop()
+        launches = per_step * args.steps
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
         e0.record()
         for _ in range(args.steps):
             step()
         e1.record()
-        torch.cuda.nvtx.range_pop()
-        launches = wq.lib().wq_kernel_launches() - n0
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / args.steps
+        eager_ms = e0.elapsed_time(e1) / args.steps
         gu = torch.empty(E, Mmax, 2 * I, dtype=torch.bfloat16, device=dev)
         if w4:
             g1 = lambda: wq.grouped_gemm_w4a8_masked(a, sa, mmd, weights[0], weights[1], out=gu,
@@ -549,7 +581,8 @@ def run_masked(args, cfg, w4=False):
                                    f"FFN: {E} local experts x {Mmax} rows, "
                                    f"hidden {H}, intermediate {I}, valid rows Zipf(1.2) = {rows}",
                        "parallelism": "single"},
-            "tokens_per_s": rows / (ms / 1e3), "gemm1_ms": g1_ms, "gpu_launches": launches,
+            "tokens_per_s": rows / (ms / 1e3), "launch": "cuda_graph", "eager_ms_per_step": eager_ms,
+            "gemm1_ms": g1_ms, "gpu_launches": launches,
             "roofline": roofline,
             "layer_roofline": layer_roofline(peaks, clocks, ms, ops, nbytes),
             "clocks": clocks}
@@ -775,6 +808,11 @@ def run_layer(args, cfg):
     for _ in range(args.warmup):
         fwd()
         layer.step(x, logits)
+    # the one-call layer recorded once into a CUDA graph, outside the timed
+    # region; each timed step replays every one of its kernels
+    graph, per_step = capture_graph(wq, fwd, dev)
+    for _ in range(args.warmup):
+        graph.replay()
     nst = len(layer.stages)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -783,15 +821,21 @@ def run_layer(args, cfg):
         # timed region 1: the one-call layer, K steps (the headline value)
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_push("timed")
-        n0 = wq.lib().wq_kernel_launches()
+        start.record()
+        for _ in range(args.steps):
+            graph.replay()
+        end.record()
+        launches = per_step * args.steps
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        total_ms = start.elapsed_time(end)
+        # the same steps launched one call at a time (reported beside it)
         start.record()
         for _ in range(args.steps):
             fwd()
         end.record()
-        launches = wq.lib().wq_kernel_launches() - n0
-        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
-        total_ms = start.elapsed_time(end)
+        eager_ms = start.elapsed_time(end) / args.steps
         # timed region 2: the same steps as separate calls, events between stages
         torch.cuda.nvtx.range_push("staged")
         start.record()
@@ -852,7 +896,8 @@ def run_layer(args, cfg):
                        "l2": "inputs larger than L2: 11.3 GB of int8 weights and ~2 GB of "
                              "activations are streamed every step",
                        "parallelism": "single"},
-            "tokens_per_s": tok_s, "stages_ms": stage_ms, "staged_ms_per_step": staged_ms,
+            "tokens_per_s": tok_s, "launch": "cuda_graph", "eager_ms_per_step": eager_ms,
+            "stages_ms": stage_ms, "staged_ms_per_step": staged_ms,
             "fused_gemm1_silu_quant": fused,
             "gpu_launches": launches,
             "roofline": roofline,
