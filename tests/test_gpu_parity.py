@@ -303,6 +303,40 @@ def test_grouped_gemm_masked(scheme, acc):
         assert np.all(O.bf16_to_f32(ob[e, m:]) == -3.0)
 
 
+def test_grouped_gemm_masked_norm_bound_fails():
+    """Masked layout, channel scheme, 256-token tiles: the launch sums its
+    valid rows' squared norms once for the int8-code engine's exactness
+    check.  A row of 127s against a weight row of 127s with one 126 (an odd
+    sum above 2^24) fails the bound, so the exact recompute must run: every
+    int32 accumulator equals the oracle's."""
+    E, Mmax, N, K = 3, 300, 256, 7168
+    mm = np.array([300, 40, 5], np.int32)
+    rng = np.random.default_rng(12)
+    A = rng.integers(-127, 128, (E, Mmax, K), dtype=np.int8)
+    W = rng.integers(-127, 128, (E, N, K), dtype=np.int8)
+    A[0, 7, :] = 127
+    W[0, 0, :] = 127
+    W[0, 0, 5] = 126
+    A[1, 3, :] = -127
+    W[1, 1, :] = 127
+    sa = (rng.random((E, Mmax)) * 0.05).astype(np.float32)
+    sw = (rng.random((E, N)) * 1e-3).astype(np.float32)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    st = wq.new_status()
+    out = torch.full((E, Mmax, N), -3, dtype=torch.int32, device=DEV)
+    wq.grouped_gemm_w8a8_masked(t(A), t(sa), t(mm), t(W), t(sw), "channel", "i32", out_type="i32",
+                                out=out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    o = np_(out)
+    for e in range(E):
+        m = int(mm[e])
+        Co = O.grouped_gemm_i32(A[e, :m], W[e:e + 1], np.array([0, m]))
+        assert np.array_equal(o[e, :m], Co), f"masked expert {e}"
+        assert np.all(o[e, m:] == -3)
+    assert o[0, 7, 0] == 127 * (127 * (K - 1) + 126) and o[1, 3, 1] == -127 * 127 * K
+
+
 # ---------------------------------------------------------------- the layer
 def _layer_case(cfg):
     x, lg = synth.layer_inputs(cfg)
@@ -362,6 +396,32 @@ def test_layer_forward_masked():
                                       *stack_oracle(orc, cfg.E))
     yb = bits(y)
     assert_bf16_equal(yb[valid], ref[valid], "masked layer")
+    assert np.all(O.bf16_to_f32(yb[~valid]) == 5.0)
+
+
+def test_layer_forward_masked_norm_bound_fails():
+    """The masked layer hands the int8-code engine its rows' squared norms
+    (computed once per launch) instead of having it sum them stage by stage.
+    With every activation code at 127 and K = 7168 the exactness bound
+    ||a||^2 ||w||^2 < 2^48 fails, so the gated exact recompute must run; the
+    output still equals the oracle's, and so do the rows of the experts the
+    small-token engine takes."""
+    cfg = synth.small_config("masked_extreme", T=0, H=7168, I=256, E=3, k=1)
+    Mmax = 300
+    qo = np.full((cfg.E, Mmax, cfg.H), 127, np.int8)
+    qo[1, :, ::7] = -127
+    so = np.random.default_rng(5).random((cfg.E, Mmax)).astype(np.float32) * 1e-3 + 1e-4
+    mm = np.array([300, 40, 5], np.int32)
+    (W13, S13, W2, S2), orc = quantized_weights(cfg, DEV)
+    y = torch.full((cfg.E, Mmax, cfg.H), 5.0, dtype=torch.bfloat16, device=DEV)
+    st = wq.new_status()
+    wq.moe_forward_masked(torch.from_numpy(qo).to(DEV), torch.from_numpy(so).to(DEV),
+                          torch.from_numpy(mm).to(DEV), W13, S13, W2, S2, y=y, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref, valid = O.moe_forward_masked(qo, so, mm, *stack_oracle(orc, cfg.E))
+    yb = bits(y)
+    assert_bf16_equal(yb[valid], ref[valid], "masked layer, bound failing")
     assert np.all(O.bf16_to_f32(yb[~valid]) == 5.0)
 
 

@@ -105,7 +105,8 @@ struct GemmWs {
   Tile *t64, *t128, *t256, *tsm;
   int32_t *n64, *n128, *n256, *nsm, *redo;
   int64_t m64, m128, m256, msm;
-  float *silu;  // silu_tab entries for the fused GEMM1 epilogue, or nullptr
+  float *silu;     // silu_tab entries for the fused GEMM1 epilogue, or nullptr
+  int32_t *anorm;  // masked layout: the rows' squared norms, or nullptr
   size_t bytes;
 };
 
@@ -126,6 +127,7 @@ GemmWs carve_gemm_ws(void *ws, int64_t R, int E, int Mmax, bool masked, bool sil
   w.nsm = c.take<int32_t>(1);
   w.redo = c.take<int32_t>(2);  // recompute flag, then an engine's item counter
   w.silu = silu ? c.take<float>(silu_tab::kSize) : nullptr;
+  w.anorm = masked ? c.take<int32_t>(size_t(R)) : nullptr;
   w.bytes = c.used;
   return w;
 }
@@ -261,7 +263,19 @@ int launch_grouped_gemm(const GemmArgs &a, cudaStream_t st) {
     const int64_t m = rows == 64 ? w.m64 : w.m256;
     WQ_TRY(launch_build_tiles(a.offsets, a.masked_m, a.Mmax, a.E, rows, a.R, t, n, w.redo, st,
                               small_max, w.tsm, w.nsm));
-    auto tc2 = [&](cudaStream_t s) { return launch_gemm_tc2(a, t, n, int(m), w.redo, s); };
+    // masked layout, channel scheme, 256-token tiles: the valid rows' squared
+    // norms once per launch (unless given), so that the engine's converters,
+    // which widen each token stage again for every weight block, need not
+    // sum them for the exactness check.  This pass runs before the fork: on
+    // the engine's own stream, beside the small-token engine, the masked
+    // layer took 0.703 ms instead of 0.684.
+    GemmArgs an = a;
+    if (rows == 256 && w.anorm != nullptr && an.a_norm2 == nullptr &&
+        a.scheme == WQ_SCHEME_CHANNEL) {
+      WQ_TRY(launch_row_norm_i8(a.A, a.R, a.K, a.masked_m, a.Mmax, w.anorm, st));
+      an.a_norm2 = w.anorm;
+    }
+    auto tc2 = [&](cudaStream_t s) { return launch_gemm_tc2(an, t, n, int(m), w.redo, s); };
     if (small && rows == 64) {  // few rows per expert: the small-token engine does nearly all
       WQ_TRY(launch_gemm_small(a, w.tsm, w.nsm, int(w.msm), st));
       WQ_TRY(tc2(st));
@@ -895,7 +909,8 @@ int wq_linear_w8a8(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, const i
 namespace {
 
 size_t carve_masked(void *ws, int E, int Mmax, int H, int I, int scheme, uint16_t **gu,
-                    int8_t **hq, float **sh, void **gws, size_t *gws_bytes) {
+                    int8_t **hq, float **sh, void **gws, size_t *gws_bytes,
+                    int32_t **hnorm = nullptr) {
   Carver c(ws);
   const int64_t R = int64_t(E) * Mmax;
   const int64_t g2 = scheme == WQ_SCHEME_BLOCK ? I / 128 : 1;
@@ -904,7 +919,9 @@ size_t carve_masked(void *ws, int E, int Mmax, int H, int I, int scheme, uint16_
   float *d = c.take<float>(size_t(R) * g2);
   const size_t gb = gemm_ws_bytes(R, E, Mmax, true);
   void *g = c.take<char>(gb);
+  int32_t *n2 = c.take<int32_t>(size_t(R));  // squared norms of the rows of hq
   if (gu) { *gu = a; *hq = b; *sh = d; *gws = g; *gws_bytes = gb; }
+  if (hnorm) *hnorm = n2;
   return c.used;
 }
 
@@ -930,18 +947,31 @@ int forward_masked(const int8_t *a, const float *sa, const int32_t *masked_m, in
   float *sh;
   void *gws;
   size_t gwsb;
-  const size_t need = carve_masked(ws, E, Mmax, H, I, scheme, &gu, &hq, &sh, &gws, &gwsb);
+  int32_t *hnorm;
+  const size_t need = carve_masked(ws, E, Mmax, H, I, scheme, &gu, &hq, &sh, &gws, &gwsb, &hnorm);
   if (!ws || !al16(ws) || ws_bytes < need) return WQ_ERR_WORKSPACE;
   WQ_TRY(check_device());
   const int64_t R = int64_t(E) * Mmax;
-  GemmArgs g1{a, nullptr, nullptr, sa, W13, sw13, nullptr, masked_m, Mmax, E, R, int64_t(2) * I, H, scheme, acc,
-              WQ_OUT_BF16, gu, gws, status};
+  // Channel scheme, int8 weights: GEMM1 sums its rows' squared norms once
+  // (the masked GEMM does), and the SiLU pass writes those of GEMM2's rows,
+  // so that the int8-code engine's converters need not sum them for its
+  // exactness check; with int4 weights no check is needed
+  const bool norms = !w4 && scheme == WQ_SCHEME_CHANNEL;
+  GemmArgs g1{a, nullptr, nullptr, sa, W13, sw13, nullptr, masked_m, Mmax, E, R, int64_t(2) * I,
+              H, scheme, acc, WQ_OUT_BF16, gu, gws, status};
   g1.w4 = w4 ? 1 : 0;
   WQ_TRY(launch_grouped_gemm(g1, stream));
-  WQ_TRY(launch_silu_mul_quant(gu, R, I, scheme == WQ_SCHEME_BLOCK ? 128 : 0, masked_m, Mmax, hq,
-                               sh, stream));
-  GemmArgs g2{hq, nullptr, nullptr, sh, W2, sw2, nullptr, masked_m, Mmax, E, R, H, I, scheme, acc, WQ_OUT_BF16, y,
-              gws, status};
+  bool hnorms = false;
+  if (norms) {
+    const int rc = launch_silu_mul_quant_norm(gu, R, I, masked_m, Mmax, hq, sh, hnorm, stream);
+    if (rc != WQ_OK && rc != WQ_ERR_UNSUPPORTED) return rc;
+    hnorms = rc == WQ_OK;
+  }
+  if (!hnorms)
+    WQ_TRY(launch_silu_mul_quant(gu, R, I, scheme == WQ_SCHEME_BLOCK ? 128 : 0, masked_m, Mmax,
+                                 hq, sh, stream));
+  GemmArgs g2{hq, nullptr, hnorms ? hnorm : nullptr, sh, W2, sw2, nullptr, masked_m, Mmax, E, R,
+              H, I, scheme, acc, WQ_OUT_BF16, y, gws, status};
   g2.w4 = w4 ? 1 : 0;
   return launch_grouped_gemm(g2, stream);
 }

@@ -291,6 +291,10 @@ int launch_quant_scatter_f16(const uint16_t *x, int64_t T, int64_t K, int64_t ld
 int launch_quant_scatter_i8(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group,
                             const int32_t *pair_to_row, int k, int64_t R, int8_t *A, float *sa,
                             cudaStream_t st);
+int launch_silu_mul_quant_norm(const uint16_t *gu, int64_t R, int64_t I, const int32_t *masked_m,
+                               int Mmax, int8_t *hq, float *sh, int32_t *norm2, cudaStream_t st);
+int launch_row_norm_i8(const int8_t *A, int64_t R, int64_t K, const int32_t *masked_m, int Mmax,
+                       int32_t *norm2, cudaStream_t st);
 int launch_permute_f16(const int8_t *q, const float *s, int groups, int k, int64_t K,
                        const int32_t *sorted_pair, int64_t R, uint16_t *A16, float *sa,
                        int32_t *norm2, cudaStream_t st);
@@ -306,7 +310,7 @@ int launch_combine(const uint16_t *y, const int32_t *pair_to_row, const float *w
 struct GemmArgs {
   const int8_t *A;           // int8 codes [R][K], or nullptr when A16 is given
   const uint16_t *A16;       // the same codes as fp16 values [R][K] (fast int32 engine)
-  const int32_t *a_norm2;    // squared L2 norm of each row of A16 (with A16)
+  const int32_t *a_norm2;    // squared L2 norm of each row of A16 (with A16); with int8 A optional (tc2 reads it instead of summing)
   const float *sa;
   const int8_t *W;
   const float *sw;

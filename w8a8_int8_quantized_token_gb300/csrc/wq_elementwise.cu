@@ -875,7 +875,8 @@ int launch_silu_table(float *tab, cudaStream_t st) {
 // warp access is 512 contiguous bytes): h = silu(g) * u, the row's or each
 // group's absolute maximum (xor shuffles; two warps of a row exchange theirs
 // through shared memory behind a named barrier), the codes (int8, or the
-// same integers as fp16 with the row's squared norm), the scale.
+// same integers as fp16), the scale, and with one scale per row and norm2
+// given the row's squared norm.
 //
 // Arithmetic in pairs (quant8: packed float32 instructions that round each
 // lane as the scalar ones do, so the codes are quant_bits()'s).  fp16 codes
@@ -1002,14 +1003,15 @@ __global__ void __launch_bounds__(512, 2) silu_mul_quant_tab_kernel(
       float t[8], r[8];
       quant8(h[i], sc, rs, t, r);
       if (v < nvec) {
-        if constexpr (F16) {
+        if constexpr (F16)
           reinterpret_cast<uint4 *>(static_cast<uint16_t *>(hq_out) + row * I)[v] = f16_codes8(r);
-          if constexpr (GV == 0) {
+        else
+          reinterpret_cast<uint2 *>(static_cast<int8_t *>(hq_out) + row * I)[v] = pack_codes8(t);
+        if constexpr (GV == 0) {
+          if (norm2 != nullptr) {
 #pragma unroll
             for (int e = 0; e < 8; e += 2) sq_acc2(n0, n1, r[e], r[e + 1]);
           }
-        } else {
-          reinterpret_cast<uint2 *>(static_cast<int8_t *>(hq_out) + row * I)[v] = pack_codes8(t);
         }
         if constexpr (GV != 0) {
           if (lane % GV == 0) sh[row * (nvec / GV) + v / GV] = sc;
@@ -1017,7 +1019,7 @@ __global__ void __launch_bounds__(512, 2) silu_mul_quant_tab_kernel(
       }
     }
     if constexpr (GV == 0) {
-      if constexpr (F16) {
+      if (norm2 != nullptr) {  // (uniform over the launch: both warps of a row take it)
         int n2 = __float2int_rn(__fadd_rn(n0, n1));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
@@ -1106,6 +1108,15 @@ int launch_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, int grou
   return launched(1);
 }
 
+// int8 codes with the rows' squared norms: one scale per row, rows of at most
+// 2048 outputs (the table kernel); WQ_ERR_UNSUPPORTED otherwise
+int launch_silu_mul_quant_norm(const uint16_t *gu, int64_t R, int64_t I, const int32_t *masked_m,
+                               int Mmax, int8_t *hq, float *sh, int32_t *norm2, cudaStream_t st) {
+  if (R == 0 || I == 0) return WQ_OK;
+  if (R > 0x7fffffff || I / 8 > 256) return WQ_ERR_UNSUPPORTED;
+  return launch_silu_tab<false>(gu, R, I, 0, masked_m, Mmax, hq, sh, norm2, st);
+}
+
 int launch_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group,
                           const int32_t *masked_m, int Mmax, int8_t *hq, float *sh,
                           cudaStream_t st) {
@@ -1133,6 +1144,38 @@ int launch_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group,
       default: return WQ_ERR_UNSUPPORTED;
     }
   }
+  return launched(1);
+}
+
+// ---------------------------------------------------------------------------
+// Squared L2 norm of each int8 row (sum of code^2), one warp per row; with
+// masked_m, rows past their expert's valid count are skipped.
+__global__ void __launch_bounds__(256) row_norm_i8_kernel(const int8_t *__restrict__ A, int64_t R,
+                                                          int64_t K, const int32_t *__restrict__ masked_m,
+                                                          int Mmax, int32_t *__restrict__ norm2) {
+  const int64_t row = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= R) return;
+  if (masked_m != nullptr && int(row % Mmax) >= masked_m[row / Mmax]) return;  // warp-uniform
+  const uint4 *a = reinterpret_cast<const uint4 *>(A + row * K);
+  int n = 0;
+  for (int64_t i = lane; i < (K >> 4); i += 32) {
+    const uint4 v = __ldg(a + i);
+    n = __dp4a(int(v.x), int(v.x), n);
+    n = __dp4a(int(v.y), int(v.y), n);
+    n = __dp4a(int(v.z), int(v.z), n);
+    n = __dp4a(int(v.w), int(v.w), n);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+  if (lane == 0) norm2[row] = n;
+}
+
+int launch_row_norm_i8(const int8_t *A, int64_t R, int64_t K, const int32_t *masked_m, int Mmax,
+                       int32_t *norm2, cudaStream_t st) {
+  if (R == 0) return WQ_OK;
+  if (K % 16 || K > 65536 || (R + 7) / 8 > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
+  row_norm_i8_kernel<<<unsigned((R + 7) / 8), 256, 0, st>>>(A, R, K, masked_m, Mmax, norm2);
   return launched(1);
 }
 

@@ -87,7 +87,9 @@ struct Plan {
 
 __device__ __forceinline__ int sq4(uint32_t w, int acc) { return __dp4a(int(w), int(w), acc); }
 
-template <int TN, int S8, int S16, bool W4>
+// TG: the token rows' squared norms come in a.a_norm2 (int8 weights only),
+// so the converters sum only the weight rows'
+template <int TN, int S8, int S16, bool W4, bool TG>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT16,
                     const __grid_constant__ CUtensorMap tmT64,
@@ -326,7 +328,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               part = 2 * (c4 & 1) + (j & 1);
             }
             store_f16_row_piece(dst + (j < NJW ? 0 : W16) + row * 128, row, part, v[j]);
-            nrm[j] += sq4(v[j].w, sq4(v[j].z, 0)) + sq4(v[j].y, sq4(v[j].x, 0));
+            // squared norms of the weight rows, and of the token rows unless
+            // the caller gave them (then the epilogue reads those).  The int4
+            // form needs none: with |w| <= 7 and K <= 16384 every partial
+            // sum stays below 127 * 7 * 16384 < 2^24, exact in float32.
+            if (!W4 && (j < NJW || !TG))
+              nrm[j] += sq4(v[j].w, sq4(v[j].z, 0)) + sq4(v[j].y, sq4(v[j].x, 0));
           }
         }
         fence_async_smem();
@@ -401,6 +408,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
       for (int p = 0; p < NGRP; ++p)
         sal[p] = p * 32 + lane < tl.rows ? a.sa[int64_t(tl.row0) + p * 32 + lane] : 0.0f;
+      // given token-row norms: the item's largest, also read while the MMAs run
+      int tgiven = 0;
+      if constexpr (TG) {
+        for (int r = lane; r < tl.rows; r += 32) tgiven = max(tgiven, a.a_norm2[int64_t(tl.row0) + r]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tgiven = max(tgiven, __shfl_xor_sync(0xffffffffu, tgiven, o));
+      }
       if (!__all_sync(0xffffffffu, mbar_wait<500>(bar(B_ACC_FULL + b), par, abort_flag)) ||
           !__all_sync(0xffffffffu, mbar_wait(bar(B_NORM_READY + b), par, abort_flag))) {
         fail();
@@ -408,7 +422,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       tc_fence_after();
       const long long nw = (long long)norm[4 * b] + norm[4 * b + 2];
-      const long long nt = (long long)norm[4 * b + 1] + norm[4 * b + 3];
+      const long long nt =
+          TG ? (long long)tgiven : (long long)norm[4 * b + 1] + norm[4 * b + 3];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_NORM_READ + b));
       if (warp == 10 && lane == 0) {
@@ -421,7 +436,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           fail();
         }
       }
-      if (nw * nt >= (1ll << 48) && q == 0 && lane == 0) atomicExch(redo, 1);
+      if (!W4 && nw * nt >= (1ll << 48) && q == 0 && lane == 0) atomicExch(redo, 1);
       const int nmma = nmma_of(tl.rows);
       const uint32_t taddr = tmem + (uint32_t(q * 32) << 16) + uint32_t(b) * 256u;
 #pragma unroll 1
@@ -479,7 +494,7 @@ int gemm_tc2_tile_rows(const GemmArgs &a) {
   return rows <= int64_t(64) * a.E ? 64 : 256;
 }
 
-template <int TN, int S8, int S16, bool W4>
+template <int TN, int S8, int S16, bool W4, bool TG = false>
 int launch_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
                int32_t *redo, cudaStream_t st) {
   using P = Plan<TN, S8, S16, W4>;
@@ -491,7 +506,7 @@ int launch_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int 
     return WQ_ERR_LAUNCH;
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(gemm_tc2_kernel<TN, S8, S16, W4>,
+    if (cudaFuncSetAttribute(gemm_tc2_kernel<TN, S8, S16, W4, TG>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES) != cudaSuccess)
       return WQ_ERR_LAUNCH;
     attr = true;
@@ -499,7 +514,7 @@ int launch_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int 
   const int64_t max_items = int64_t(max_tiles) * (a.N / WM);
   const int grid = int(max_items < num_sms() ? max_items : num_sms());
   // redo[1] is the item counter (zeroed with the flag by the tile builder)
-  gemm_tc2_kernel<TN, S8, S16, W4><<<grid, NTHREADS, P::SMEM_BYTES, st>>>(mW, m16, m64, m256, a,
+  gemm_tc2_kernel<TN, S8, S16, W4, TG><<<grid, NTHREADS, P::SMEM_BYTES, st>>>(mW, m16, m64, m256, a,
                                                                           tiles, ntiles, redo,
                                                                           redo + 1);
   return launched(1);
@@ -514,8 +529,11 @@ int launch_gemm_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles,
     return small ? launch_tc2<64, 8, 4, true>(a, tiles, ntiles, max_tiles, redo, st)
                  : launch_tc2<256, 3, 3, true>(a, tiles, ntiles, max_tiles, redo, st);
   }
-  return small ? launch_tc2<64, 8, 4, false>(a, tiles, ntiles, max_tiles, redo, st)
-               : launch_tc2<256, 3, 3, false>(a, tiles, ntiles, max_tiles, redo, st);
+  if (small) return launch_tc2<64, 8, 4, false>(a, tiles, ntiles, max_tiles, redo, st);
+  // given token-row norms are used by the 256-token form only (the 64-token
+  // form sums its own: correct either way, one instantiation fewer)
+  return a.a_norm2 != nullptr ? launch_tc2<256, 3, 3, false, true>(a, tiles, ntiles, max_tiles, redo, st)
+                              : launch_tc2<256, 3, 3, false>(a, tiles, ntiles, max_tiles, redo, st);
 }
 
 }  // namespace wq
