@@ -900,10 +900,11 @@ __device__ __forceinline__ void silu_pair(uint32_t w, const float *tab, float &s
   s0 = tab[min(i0, uint32_t(kSize - 1))];
   s1 = tab[min(i1, uint32_t(kSize - 1))];
 }
-// silu of one bf16 value: the table where it holds the value, else the formula
-__device__ __forceinline__ float silu_one(uint32_t b, const float *tab) {
-  const int idx = silu_index(b);
-  return idx >= 0 ? tab[idx] : silu(bf16_to_f(uint16_t(b)));
+// silu of a bf16 value outside the table: the formula, except for +-0,
+// whose silu is +-0 / 2 = +-0 (an integer GEMM lands on exact zeros often
+// enough, more so with int4 weights, to make the formula's cost show)
+__device__ __forceinline__ float silu_outside(uint32_t b) {
+  return (b & 0x7fffu) == 0 ? __uint_as_float((b & 0x8000u) << 16) : silu(bf16_to_f(uint16_t(b)));
 }
 }  // namespace silu2
 
@@ -952,7 +953,7 @@ __global__ void __launch_bounds__(512, 2) silu_mul_quant_tab_kernel(
         h[i][2 * j + 1] = s1;
       }
     }
-    if (miss) {  // rare: a gate value of this lane outside the table; redo the lane's values
+    if (miss) {  // rare: some gate value of this lane lies outside the table; redo those
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         const int v = v0 + i * 32;
@@ -962,8 +963,10 @@ __global__ void __launch_bounds__(512, 2) silu_mul_quant_tab_kernel(
           const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            h[i][2 * j] = __fmul_rn(silu_one(gw[j] & 0xffffu, tab), bf16_lo(uw[j]));
-            h[i][2 * j + 1] = __fmul_rn(silu_one(gw[j] >> 16, tab), bf16_hi(uw[j]));
+            if (silu_index(gw[j] & 0xffffu) < 0)
+              h[i][2 * j] = __fmul_rn(silu_outside(gw[j] & 0xffffu), bf16_lo(uw[j]));
+            if (silu_index(gw[j] >> 16) < 0)
+              h[i][2 * j + 1] = __fmul_rn(silu_outside(gw[j] >> 16), bf16_hi(uw[j]));
           }
         }
       }
