@@ -908,9 +908,16 @@ int wq_linear_w8a8(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, const i
 
 namespace {
 
+// The fp16 token form of the int8-code engine serves the masked layer when
+// the engine takes 256-token tiles (more than 64 rows per expert buffer; the
+// same rule as gemm_tc2_tile_rows) on the channel scheme, K within its range.
+bool masked_tok16(int scheme, int Mmax, int H, int I) {
+  return scheme == WQ_SCHEME_CHANNEL && Mmax > 64 && H <= 65536 && I <= 65536;
+}
+
 size_t carve_masked(void *ws, int E, int Mmax, int H, int I, int scheme, uint16_t **gu,
                     int8_t **hq, float **sh, void **gws, size_t *gws_bytes,
-                    int32_t **hnorm = nullptr) {
+                    int32_t **norm = nullptr, uint16_t **t16 = nullptr) {
   Carver c(ws);
   const int64_t R = int64_t(E) * Mmax;
   const int64_t g2 = scheme == WQ_SCHEME_BLOCK ? I / 128 : 1;
@@ -919,9 +926,14 @@ size_t carve_masked(void *ws, int E, int Mmax, int H, int I, int scheme, uint16_
   float *d = c.take<float>(size_t(R) * g2);
   const size_t gb = gemm_ws_bytes(R, E, Mmax, true);
   void *g = c.take<char>(gb);
-  int32_t *n2 = c.take<int32_t>(size_t(R));  // squared norms of the rows of hq
+  // fp16 token form: a GEMM input's valid rows as fp16 codes (x for GEMM1,
+  // then h for GEMM2, in the same buffer) and their squared norms
+  const bool f16t = masked_tok16(scheme, Mmax, H, I);
+  int32_t *n2 = f16t ? c.take<int32_t>(size_t(R)) : nullptr;
+  uint16_t *t = f16t ? c.take<uint16_t>(size_t(R) * size_t(H > I ? H : I)) : nullptr;
   if (gu) { *gu = a; *hq = b; *sh = d; *gws = g; *gws_bytes = gb; }
-  if (hnorm) *hnorm = n2;
+  if (norm) *norm = n2;
+  if (t16) *t16 = t;
   return c.used;
 }
 
@@ -947,32 +959,39 @@ int forward_masked(const int8_t *a, const float *sa, const int32_t *masked_m, in
   float *sh;
   void *gws;
   size_t gwsb;
-  int32_t *hnorm;
-  const size_t need = carve_masked(ws, E, Mmax, H, I, scheme, &gu, &hq, &sh, &gws, &gwsb, &hnorm);
+  int32_t *norm;
+  uint16_t *t16;
+  const size_t need =
+      carve_masked(ws, E, Mmax, H, I, scheme, &gu, &hq, &sh, &gws, &gwsb, &norm, &t16);
   if (!ws || !al16(ws) || ws_bytes < need) return WQ_ERR_WORKSPACE;
   WQ_TRY(check_device());
   const int64_t R = int64_t(E) * Mmax;
-  // Channel scheme, int8 weights: GEMM1 sums its rows' squared norms once
-  // (the masked GEMM does), and the SiLU pass writes those of GEMM2's rows,
-  // so that the int8-code engine's converters need not sum them for its
-  // exactness check; with int4 weights no check is needed
-  const bool norms = !w4 && scheme == WQ_SCHEME_CHANNEL;
+  // Channel scheme, 256-token tiles: before each GEMM one pass writes the
+  // valid rows' codes as fp16 values and their squared norms, so that the
+  // int8-code engine loads fp16 token tiles instead of widening each again for
+  // every weight block, and (int8 weights) need not sum their norms for its
+  // exactness check.  The small-token engine beside it reads the int8 codes.
+  const bool f16t = masked_tok16(scheme, Mmax, H, I);
+  if (f16t) WQ_TRY(launch_row_norm_i8(a, R, H, masked_m, Mmax, norm, stream, t16));
   GemmArgs g1{a, nullptr, nullptr, sa, W13, sw13, nullptr, masked_m, Mmax, E, R, int64_t(2) * I,
               H, scheme, acc, WQ_OUT_BF16, gu, gws, status};
   g1.w4 = w4 ? 1 : 0;
-  WQ_TRY(launch_grouped_gemm(g1, stream));
-  bool hnorms = false;
-  if (norms) {
-    const int rc = launch_silu_mul_quant_norm(gu, R, I, masked_m, Mmax, hq, sh, hnorm, stream);
-    if (rc != WQ_OK && rc != WQ_ERR_UNSUPPORTED) return rc;
-    hnorms = rc == WQ_OK;
+  if (f16t) {
+    g1.tok16 = t16;
+    g1.a_norm2 = w4 ? nullptr : norm;
   }
-  if (!hnorms)
-    WQ_TRY(launch_silu_mul_quant(gu, R, I, scheme == WQ_SCHEME_BLOCK ? 128 : 0, masked_m, Mmax,
-                                 hq, sh, stream));
-  GemmArgs g2{hq, nullptr, hnorms ? hnorm : nullptr, sh, W2, sw2, nullptr, masked_m, Mmax, E, R,
+  WQ_TRY(launch_grouped_gemm(g1, stream));
+  WQ_TRY(launch_silu_mul_quant(gu, R, I, scheme == WQ_SCHEME_BLOCK ? 128 : 0, masked_m, Mmax, hq,
+                               sh, stream));
+  // GEMM1 has finished with the fp16 rows and norms (same stream): h's replace them
+  if (f16t) WQ_TRY(launch_row_norm_i8(hq, R, I, masked_m, Mmax, norm, stream, t16));
+  GemmArgs g2{hq, nullptr, nullptr, sh, W2, sw2, nullptr, masked_m, Mmax, E, R,
               H, I, scheme, acc, WQ_OUT_BF16, y, gws, status};
   g2.w4 = w4 ? 1 : 0;
+  if (f16t) {
+    g2.tok16 = t16;
+    g2.a_norm2 = w4 ? nullptr : norm;
+  }
   return launch_grouped_gemm(g2, stream);
 }
 }  // namespace wq

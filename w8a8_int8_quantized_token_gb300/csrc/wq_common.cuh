@@ -291,10 +291,10 @@ int launch_quant_scatter_f16(const uint16_t *x, int64_t T, int64_t K, int64_t ld
 int launch_quant_scatter_i8(const uint16_t *x, int64_t T, int64_t K, int64_t ldx, int group,
                             const int32_t *pair_to_row, int k, int64_t R, int8_t *A, float *sa,
                             cudaStream_t st);
-int launch_silu_mul_quant_norm(const uint16_t *gu, int64_t R, int64_t I, const int32_t *masked_m,
-                               int Mmax, int8_t *hq, float *sh, int32_t *norm2, cudaStream_t st);
+// squared norms of the valid rows of int8 codes A [R][K], and with out16 the
+// same codes as fp16 values [R][K] (rows past a masked count untouched)
 int launch_row_norm_i8(const int8_t *A, int64_t R, int64_t K, const int32_t *masked_m, int Mmax,
-                       int32_t *norm2, cudaStream_t st);
+                       int32_t *norm2, cudaStream_t st, uint16_t *out16 = nullptr);
 int launch_permute_f16(const int8_t *q, const float *s, int groups, int k, int64_t K,
                        const int32_t *sorted_pair, int64_t R, uint16_t *A16, float *sa,
                        int32_t *norm2, cudaStream_t st);
@@ -332,6 +332,10 @@ struct GemmArgs {
   const float *fused_silu_tab = nullptr;  // silu_tab entries (set by the dispatcher)
   int wait_test = 0;  // failure-path test: a wait that nothing completes (block engine)
   int w4 = 0;         // W holds int4 codes, two per byte (low nibble first): [E][N][K/2]
+  // the codes of A as fp16 values [R][K] beside the int8 ones (masked layer):
+  // the int8-code tensor-core engine then loads its token tiles from here
+  // instead of widening them again for every weight block; optional
+  const uint16_t *tok16 = nullptr;
 };
 // The single-pass float32 engines serve both channel-wise accumulator modes.
 // In the float32 mode the accumulator is the running sum, over 128-wide K

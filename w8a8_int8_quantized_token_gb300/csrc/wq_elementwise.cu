@@ -1111,14 +1111,6 @@ int launch_silu_mul_quant_f16(const uint16_t *gu, int64_t R, int64_t I, int grou
   return launched(1);
 }
 
-// int8 codes with the rows' squared norms: one scale per row, rows of at most
-// 2048 outputs (the table kernel); WQ_ERR_UNSUPPORTED otherwise
-int launch_silu_mul_quant_norm(const uint16_t *gu, int64_t R, int64_t I, const int32_t *masked_m,
-                               int Mmax, int8_t *hq, float *sh, int32_t *norm2, cudaStream_t st) {
-  if (R == 0 || I == 0) return WQ_OK;
-  if (R > 0x7fffffff || I / 8 > 256) return WQ_ERR_UNSUPPORTED;
-  return launch_silu_tab<false>(gu, R, I, 0, masked_m, Mmax, hq, sh, norm2, st);
-}
 
 int launch_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group,
                           const int32_t *masked_m, int Mmax, int8_t *hq, float *sh,
@@ -1151,34 +1143,62 @@ int launch_silu_mul_quant(const uint16_t *gu, int64_t R, int64_t I, int group,
 }
 
 // ---------------------------------------------------------------------------
-// Squared L2 norm of each int8 row (sum of code^2), one warp per row; with
-// masked_m, rows past their expert's valid count are skipped.
+// Squared L2 norm of each int8 row (sum of code^2, exact: at most
+// 127^2 * 65536 < 2^31), one warp per row; with masked_m, rows past their
+// expert's valid count are skipped.  With W16 the warp also writes the row's
+// codes as fp16 values (exact), for the int8-code tensor-core engine to load
+// as token tiles.
+template <bool W16>
 __global__ void __launch_bounds__(256) row_norm_i8_kernel(const int8_t *__restrict__ A, int64_t R,
                                                           int64_t K, const int32_t *__restrict__ masked_m,
-                                                          int Mmax, int32_t *__restrict__ norm2) {
+                                                          int Mmax, int32_t *__restrict__ norm2,
+                                                          uint16_t *__restrict__ out16) {
   const int64_t row = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= R) return;
   if (masked_m != nullptr && int(row % Mmax) >= masked_m[row / Mmax]) return;  // warp-uniform
-  const uint4 *a = reinterpret_cast<const uint4 *>(A + row * K);
+  // 8-code units: lane l takes units l, l + 32, ... (8-byte loads, 256
+  // contiguous bytes a warp; 16-byte fp16 stores, 512 contiguous bytes)
+  const uint2 *a = reinterpret_cast<const uint2 *>(A + row * K);
+  uint4 *o = W16 ? reinterpret_cast<uint4 *>(out16 + row * K) : nullptr;
+  const int n8 = int(K >> 3);
+  constexpr int U = 8;  // loads a lane keeps in flight
   int n = 0;
-  for (int64_t i = lane; i < (K >> 4); i += 32) {
-    const uint4 v = __ldg(a + i);
-    n = __dp4a(int(v.x), int(v.x), n);
-    n = __dp4a(int(v.y), int(v.y), n);
-    n = __dp4a(int(v.z), int(v.z), n);
-    n = __dp4a(int(v.w), int(v.w), n);
+  for (int i0 = lane; i0 < n8; i0 += 32 * U) {
+    uint2 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      v[u] = i0 + 32 * u < n8 ? __ldg(a + i0 + 32 * u) : make_uint2(0, 0);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      n = __dp4a(int(v[u].x), int(v[u].x), n);
+      n = __dp4a(int(v[u].y), int(v[u].y), n);
+      if constexpr (W16) {
+        const int i = i0 + 32 * u;
+        if (i < n8) {
+          uint4 f;
+          tc::s8x4_to_f16x4(v[u].x, f.x, f.y);
+          tc::s8x4_to_f16x4(v[u].y, f.z, f.w);
+          o[i] = f;
+        }
+      }
+    }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+  for (int o2 = 16; o2 > 0; o2 >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o2);
   if (lane == 0) norm2[row] = n;
 }
 
 int launch_row_norm_i8(const int8_t *A, int64_t R, int64_t K, const int32_t *masked_m, int Mmax,
-                       int32_t *norm2, cudaStream_t st) {
+                       int32_t *norm2, cudaStream_t st, uint16_t *out16) {
   if (R == 0) return WQ_OK;
   if (K % 16 || K > 65536 || (R + 7) / 8 > 0x7fffffff) return WQ_ERR_UNSUPPORTED;
-  row_norm_i8_kernel<<<unsigned((R + 7) / 8), 256, 0, st>>>(A, R, K, masked_m, Mmax, norm2);
+  if (out16 != nullptr)
+    row_norm_i8_kernel<true><<<unsigned((R + 7) / 8), 256, 0, st>>>(A, R, K, masked_m, Mmax, norm2,
+                                                                   out16);
+  else
+    row_norm_i8_kernel<false><<<unsigned((R + 7) / 8), 256, 0, st>>>(A, R, K, masked_m, Mmax,
+                                                                    norm2, nullptr);
   return launched(1);
 }
 

@@ -30,6 +30,12 @@
 //   warps 2-9   converters (two groups taking alternate K stages): int8 ->
 //               fp16 (128-byte swizzled K-major) + squared row norms
 //   warps 10-13 epilogue: dequant, bf16, coalesced stores (32 channels/warp)
+//   warp 14     (fp16 token form only) token TMA producer
+// In the fp16 token form (GemmArgs::tok16, 256-token plan) the token tiles
+// arrive as fp16 codes by TMA, 128-byte swizzled, in a ring of their own, and
+// the converters widen only the weights: a token tile is no longer widened
+// again for each of the N / 128 weight blocks.  The token rows' squared
+// norms then come with them (a_norm2), or are not needed (int4 weights).
 // Every wait is bounded (1 s); on expiry the kernel records WQ_ERR_TIMEOUT,
 // waits (bounded) for its own copies and MMAs, frees tensor memory and exits.
 #include "wq_tc.cuh"
@@ -40,7 +46,8 @@ namespace {
 using namespace tc;
 
 constexpr int WM = 128, BK = 64;
-constexpr int NTHREADS = 448;
+constexpr int NTHREADS = 448;   // 480 in the fp16 token form (the token producer warp)
+constexpr int WARP_TOKP = 14;   // token producer warp of the fp16 token form
 constexpr int NCONV = 256;  // converter threads: two groups of 128
 constexpr int GCONV = 128;  // threads of one converter group (its stages alternate with the other's)
 constexpr int NR = 8;       // item ring depth
@@ -53,15 +60,19 @@ constexpr int ITEM_READERS = 1 + NCONV / 32 + 4;
 // TN suits many rows per expert (prefill); a small TN with a deep int8 ring
 // keeps enough weight bytes in flight when experts hold a few tokens each
 // (decode), where the GEMM streams weights from HBM.
-template <int TN, int S8, int S16, bool W4>
+template <int TN, int S8, int S16, bool W4, bool FT = false, int STK = 0>
 struct Plan {
   // bytes per stage: W8 the staged weight codes (int8, or int4 two per byte),
-  // T8 the int8 token codes; W16 / T16 the widened fp16 tiles
-  static constexpr int W8 = WM * BK / (W4 ? 2 : 1), T8 = TN * BK;
-  static constexpr int W16 = 2 * WM * BK, T16 = 2 * T8;
+  // T8 the int8 token codes; W16 / T16 the widened fp16 tiles.  FT: the fp16
+  // token form, whose STK-deep token ring holds TK16-byte fp16 tiles loaded
+  // by TMA (no int8 token staging, no widened token tile in the fp16 ring)
+  static_assert(FT == (STK > 0), "a token ring exactly in the fp16 token form");
+  static constexpr int W8 = WM * BK / (W4 ? 2 : 1), T8 = FT ? 0 : TN * BK;
+  static constexpr int W16 = 2 * WM * BK, T16 = 2 * T8, TK16 = FT ? 2 * TN * BK : 0;
   static constexpr int ST8 = W8 + T8, ST16 = W16 + T16;
   static constexpr int OFF_F16 = 0;
-  static constexpr int OFF_I8 = OFF_F16 + S16 * ST16;
+  static constexpr int OFF_TOK = OFF_F16 + S16 * ST16;  // 1024-aligned: every stage size is
+  static constexpr int OFF_I8 = OFF_TOK + STK * TK16;
   static constexpr int OFF_BAR = OFF_I8 + S8 * ST8;
   static constexpr int B_S8_FULL = 0, B_S8_EMPTY = S8, B_F16_FULL = 2 * S8,
                        B_F16_EMPTY = 2 * S8 + S16, B_ACC_FULL = 2 * S8 + 2 * S16,  // [2]
@@ -72,7 +83,9 @@ struct Plan {
       B_MMA_DONE = B_ACC_FULL + 10,
                        B_ITEM_FULL = B_ACC_FULL + 11,   // [NR] a claimed item index posted
       B_ITEM_EMPTY = B_ITEM_FULL + NR,                 // [NR] every role has read it
-      NBAR = B_ITEM_EMPTY + NR;
+      B_TOK_FULL = B_ITEM_EMPTY + NR,                  // [STK] fp16 token tile landed
+      B_TOK_EMPTY = B_TOK_FULL + STK,                  // [STK] its MMAs are done
+      NBAR = B_TOK_EMPTY + STK;
   // int32 [2 buffers][2 converter groups][weights, tokens]
   static constexpr int OFF_NORM = OFF_BAR + NBAR * 8;
   static constexpr int OFF_ITEMS = OFF_NORM + 32;  // int32 [NR] item ring
@@ -80,24 +93,29 @@ struct Plan {
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
   static constexpr int NJW = WM * 4 / GCONV;  // weight 16-byte pieces per converter thread
-  static constexpr int NJT = TN * 4 / GCONV;  // token 16-byte pieces per converter thread
-  static_assert(NJT >= 1 && TN * 4 == NJT * GCONV, "token tile must fill a converter group");
+  // token 16-byte pieces per converter thread (none in the fp16 token form)
+  static constexpr int NJT = FT ? 0 : TN * 4 / GCONV;
+  static_assert(FT || (NJT >= 1 && TN * 4 == NJT * GCONV), "token tile must fill a converter group");
   static_assert(SMEM_BYTES <= 232448, "shared memory plan too large");
 };
 
 __device__ __forceinline__ int sq4(uint32_t w, int acc) { return __dp4a(int(w), int(w), acc); }
 
 // TG: the token rows' squared norms come in a.a_norm2 (int8 weights only),
-// so the converters sum only the weight rows'
-template <int TN, int S8, int S16, bool W4, bool TG>
-__global__ void __launch_bounds__(NTHREADS, 1)
+// so the converters sum only the weight rows'.  FT: the fp16 token form, its
+// token maps (tmT16/64/256) describing a.tok16; STK its token ring depth.
+template <int TN, int S8, int S16, bool W4, bool TG, bool FT = false, int STK = 0>
+__global__ void __launch_bounds__(FT ? NTHREADS + 32 : NTHREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmT16,
                     const __grid_constant__ CUtensorMap tmT64,
                     const __grid_constant__ CUtensorMap tmT256, const GemmArgs a,
                     const Tile *__restrict__ tiles, const int32_t *__restrict__ ntiles,
                     int32_t *__restrict__ redo, int32_t *__restrict__ claim) {
-  using P = Plan<TN, S8, S16, W4>;
-  constexpr int W8 = P::W8, W16 = P::W16, ST8 = P::ST8, ST16 = P::ST16;
+  static_assert(!FT || TG || W4, "the fp16 token form sums no token norms");
+  using P = Plan<TN, S8, S16, W4, FT, STK>;
+  constexpr int W8 = P::W8, W16 = P::W16, ST8 = P::ST8, ST16 = P::ST16, TK16 = P::TK16;
+  constexpr int OFF_TOK = P::OFF_TOK, B_TOK_FULL = P::B_TOK_FULL, B_TOK_EMPTY = P::B_TOK_EMPTY;
+  constexpr int READERS = ITEM_READERS + (FT ? 1 : 0);
   constexpr int OFF_F16 = P::OFF_F16, OFF_I8 = P::OFF_I8, OFF_BAR = P::OFF_BAR;
   constexpr int B_S8_FULL = P::B_S8_FULL, B_S8_EMPTY = P::B_S8_EMPTY, B_F16_FULL = P::B_F16_FULL,
                 B_F16_EMPTY = P::B_F16_EMPTY, B_ACC_FULL = P::B_ACC_FULL,
@@ -144,7 +162,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(bar(B_MMA_DONE), 1);
     for (int r = 0; r < NR; ++r) {
       mbar_init(bar(B_ITEM_FULL + r), 1);
-      mbar_init(bar(B_ITEM_EMPTY + r), ITEM_READERS);
+      mbar_init(bar(B_ITEM_EMPTY + r), READERS);
+    }
+    for (int s = 0; s < STK; ++s) {
+      mbar_init(bar(B_TOK_FULL + s), 1);
+      mbar_init(bar(B_TOK_EMPTY + s), 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -190,7 +212,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int wb = it % NB;
         const int box = box_of(nmma_of(tl.rows));
         const CUtensorMap *tmT = box == 16 ? &tmT16 : (box == 64 ? &tmT64 : &tmT256);
-        const uint32_t tx = W8 + box * BK;
+        const uint32_t tx = W8 + (FT ? 0 : box * BK);
         const int wrow = int(int64_t(tl.expert) * a.N + int64_t(wb) * WM);
         for (int i = 0; i < KT; ++i, ++g) {
           const int s8 = g % S8;
@@ -202,7 +224,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint32_t dst = base + OFF_I8 + uint32_t(s8) * ST8;
           mbar_expect_tx(bar(B_S8_FULL + s8), tx);
           tma_load_2d(dst, &tmW, i * (W4 ? BK / 2 : BK), wrow, bar(B_S8_FULL + s8));  // bytes
-          tma_load_2d(dst + W8, tmT, i * BK, tl.row0, bar(B_S8_FULL + s8));
+          if constexpr (!FT) tma_load_2d(dst + W8, tmT, i * BK, tl.row0, bar(B_S8_FULL + s8));
         }
         it = next;
       }
@@ -234,18 +256,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t d = tmem + uint32_t(b) * 256u;
         for (int i = 0; i < KT; ++i, ++g) {
           const int s = g % S16;
-          if (!mbar_wait(bar(B_F16_FULL + s), (g / S16) & 1, abort_flag)) {
+          constexpr int SKD = FT ? STK : 1;  // token ring depth (no ring: unused)
+          const int sk = g % SKD;
+          if (!mbar_wait(bar(B_F16_FULL + s), (g / S16) & 1, abort_flag) ||
+              (FT && !mbar_wait(bar(B_TOK_FULL + sk), (g / SKD) & 1, abort_flag))) {
             fail();
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t w0 = base + OFF_F16 + uint32_t(s) * ST16;
-          const uint32_t t0 = w0 + W16;
+          const uint32_t t0 = FT ? base + OFF_TOK + uint32_t(sk) * TK16 : w0 + W16;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             mma_f16(d, sdesc(w0 + 32u * kk), sdesc(t0 + 32u * kk), idesc, (i | kk) ? 1u : 0u);
           mma_commit(bar(B_F16_EMPTY + s));
+          if constexpr (FT) mma_commit(bar(B_TOK_EMPTY + sk));
         }
         if (ok) mma_commit(bar(B_ACC_FULL + b));
       }
@@ -384,6 +410,44 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_NORM_READY + b));
     }
+  } else if (warp == WARP_TOKP) {
+    // ------------------------------------------------------------ token producer
+    // (fp16 token form): each item's K stages of fp16 token tiles, as deep
+    // ahead as the token ring allows, independent of the weight ring
+    if constexpr (FT) {
+      if (lane == 0) {
+        int gt = 0;
+        bool ok = true;
+        for (int ii = 0; ok; ++ii) {
+          int it;
+          if (!read_item(ii, it)) {
+            fail();
+            break;
+          }
+          mbar_arrive(bar(B_ITEM_EMPTY + ii % NR));
+          if (it < 0) break;
+          const Tile tl = tiles[it / NB];
+          const int box = box_of(nmma_of(tl.rows));
+          const CUtensorMap *tmT = box == 16 ? &tmT16 : (box == 64 ? &tmT64 : &tmT256);
+          const uint32_t tx = uint32_t(box) * BK * 2;
+          for (int i = 0; i < KT; ++i, ++gt) {
+            const int sk = gt % STK;
+            if (!mbar_wait<200>(bar(B_TOK_EMPTY + sk), ((gt / STK) & 1) ^ 1, abort_flag)) {
+              fail();
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(bar(B_TOK_FULL + sk), tx);
+            tma_load_2d(base + OFF_TOK + uint32_t(sk) * TK16, tmT, i * BK, tl.row0,
+                        bar(B_TOK_FULL + sk));
+          }
+        }
+        if (!ok) {
+          for (int j = gt > STK ? gt - STK : 0; j < gt; ++j)
+            mbar_wait_bounded(bar(B_TOK_FULL + j % STK), (j / STK) & 1);
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // tensor-memory lane quarter of this warp
@@ -494,19 +558,28 @@ int gemm_tc2_tile_rows(const GemmArgs &a) {
   return rows <= int64_t(64) * a.E ? 64 : 256;
 }
 
-template <int TN, int S8, int S16, bool W4, bool TG = false>
+template <int TN, int S8, int S16, bool W4, bool TG = false, bool FT = false, int STK = 0>
 int launch_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int max_tiles,
                int32_t *redo, cudaStream_t st) {
-  using P = Plan<TN, S8, S16, W4>;
+  using P = Plan<TN, S8, S16, W4, FT, STK>;
+  constexpr int NT = FT ? NTHREADS + 32 : NTHREADS;
   CUtensorMap mW, m16, m64, m256;
   // int4 weights: K / 2 bytes a row, a 32-byte box per 64-code stage
-  if (!make_tma_2d_u8(&mW, a.W, int64_t(a.E) * a.N, W4 ? a.K / 2 : a.K, W4 ? BK / 2 : BK, WM) ||
-      !make_tma_2d_u8(&m16, a.A, a.R, a.K, BK, 16) || !make_tma_2d_u8(&m64, a.A, a.R, a.K, BK, 64) ||
-      !make_tma_2d_u8(&m256, a.A, a.R, a.K, BK, TN > 64 ? 256 : 64))
+  if (!make_tma_2d_u8(&mW, a.W, int64_t(a.E) * a.N, W4 ? a.K / 2 : a.K, W4 ? BK / 2 : BK, WM))
     return WQ_ERR_LAUNCH;
+  if (FT) {  // fp16 token tiles, 128-byte swizzled as the MMA reads them
+    if (!make_tma_2d_b16_sw128(&m16, a.tok16, a.R, a.K, 16) ||
+        !make_tma_2d_b16_sw128(&m64, a.tok16, a.R, a.K, 64) ||
+        !make_tma_2d_b16_sw128(&m256, a.tok16, a.R, a.K, TN > 64 ? 256 : 64))
+      return WQ_ERR_LAUNCH;
+  } else if (!make_tma_2d_u8(&m16, a.A, a.R, a.K, BK, 16) ||
+             !make_tma_2d_u8(&m64, a.A, a.R, a.K, BK, 64) ||
+             !make_tma_2d_u8(&m256, a.A, a.R, a.K, BK, TN > 64 ? 256 : 64)) {
+    return WQ_ERR_LAUNCH;
+  }
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(gemm_tc2_kernel<TN, S8, S16, W4, TG>,
+    if (cudaFuncSetAttribute(gemm_tc2_kernel<TN, S8, S16, W4, TG, FT, STK>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES) != cudaSuccess)
       return WQ_ERR_LAUNCH;
     attr = true;
@@ -514,7 +587,7 @@ int launch_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles, int 
   const int64_t max_items = int64_t(max_tiles) * (a.N / WM);
   const int grid = int(max_items < num_sms() ? max_items : num_sms());
   // redo[1] is the item counter (zeroed with the flag by the tile builder)
-  gemm_tc2_kernel<TN, S8, S16, W4, TG><<<grid, NTHREADS, P::SMEM_BYTES, st>>>(mW, m16, m64, m256, a,
+  gemm_tc2_kernel<TN, S8, S16, W4, TG, FT, STK><<<grid, NT, P::SMEM_BYTES, st>>>(mW, m16, m64, m256, a,
                                                                           tiles, ntiles, redo,
                                                                           redo + 1);
   return launched(1);
@@ -525,6 +598,13 @@ int launch_gemm_tc2(const GemmArgs &a, const Tile *tiles, const int32_t *ntiles,
                     int32_t *redo, cudaStream_t st) {
   if (max_tiles <= 0) return WQ_OK;
   const bool small = gemm_tc2_tile_rows(a) == 64;
+  // fp16 token form: 256-token plan, token norms given (int8 weights) or not
+  // needed (int4)
+  if (a.tok16 != nullptr && !small) {
+    if (a.w4) return launch_tc2<256, 4, 4, true, false, true, 4>(a, tiles, ntiles, max_tiles, redo, st);
+    if (a.a_norm2 != nullptr)
+      return launch_tc2<256, 4, 4, false, true, true, 4>(a, tiles, ntiles, max_tiles, redo, st);
+  }
   if (a.w4) {
     return small ? launch_tc2<64, 8, 4, true>(a, tiles, ntiles, max_tiles, redo, st)
                  : launch_tc2<256, 3, 3, true>(a, tiles, ntiles, max_tiles, redo, st);
