@@ -186,6 +186,47 @@ int launch_align(const int32_t *ids, int T, int k, int E, int pad_m, int32_t *co
 // written.
 constexpr int kMaxTileRows = 384;
 
+// Inclusive prefix sums of a and b over the 1024 threads of the block (warp
+// shuffles, then one warp over the 32 warp totals); ta / tb: the totals.
+__device__ __forceinline__ void block_scan2(int &a, int &b, int &ta, int &tb) {
+  __shared__ int wa[32], wb[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
+    if (lane >= o) {
+      a += ya;
+      b += yb;
+    }
+  }
+  if (lane == 31) {
+    wa[warp] = a;
+    wb[warp] = b;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int x = wa[lane], y = wb[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int xa = __shfl_up_sync(0xffffffffu, x, o), yy = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) {
+        x += xa;
+        y += yy;
+      }
+    }
+    wa[lane] = x;
+    wb[lane] = y;
+  }
+  __syncthreads();
+  if (warp > 0) {
+    a += wa[warp - 1];
+    b += wb[warp - 1];
+  }
+  ta = wa[31];
+  tb = wb[31];
+  __syncthreads();  // wa / wb free for the next call
+}
+
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__restrict__ offsets,
                                                            const int32_t *__restrict__ masked_m,
                                                            int Mmax, int E, int BM, int64_t R,
@@ -198,7 +239,6 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
                                                            const int32_t *__restrict__ gate) {
   // the list of a gated exact recompute: not needed unless its flag is set
   if (gate != nullptr && *gate == 0) return;
-  __shared__ int32_t part[1024], part_s[1024];
   __shared__ int32_t hist[kMaxTileRows + 1];  // partial main tiles by row count, then cursors
   if (zero_word != nullptr && threadIdx.x < 2) zero_word[threadIdx.x] = 0;  // flag, item counter
   for (int i = threadIdx.x; i <= kMaxTileRows; i += blockDim.x) hist[i] = 0;
@@ -238,31 +278,21 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t *__rest
     if (nfull == 0 && part_main) atomicAdd(&hist[rem], 1);
     local_s += ts ? 1 : 0;
   }
-  part[threadIdx.x] = local;
-  part_s[threadIdx.x] = local_s;
-  __syncthreads();
-  for (int o = 1; o < int(blockDim.x); o <<= 1) {
-    const int v = threadIdx.x >= unsigned(o) ? part[threadIdx.x - o] : 0;
-    const int vs = threadIdx.x >= unsigned(o) ? part_s[threadIdx.x - o] : 0;
-    __syncthreads();
-    part[threadIdx.x] += v;
-    part_s[threadIdx.x] += vs;
-    __syncthreads();
-  }
-  const int nfull_total = part[blockDim.x - 1];  // tiles of the experts with full tiles
+  int incl = local, incl_s = local_s, nfull_total, nsmall_total;
+  block_scan2(incl, incl_s, nfull_total, nsmall_total);  // (the histogram is complete too)
+  // first position of the partial tiles of each row count, longest first:
+  // thread i takes row count BM - 1 - i (BM <= 384 < 1024)
+  const int rc = BM - 1 - int(threadIdx.x);
+  int c = rc >= 1 ? hist[rc] : 0, unused = 0, npart, unused_t;
+  const int c0 = c;
+  block_scan2(c, unused, npart, unused_t);
+  if (rc >= 1) hist[rc] = nfull_total + c - c0;
   if (threadIdx.x == 0) {
-    // first position of the partial tiles of each row count, longest first
-    int pos = nfull_total;
-    for (int r = BM - 1; r >= 1; --r) {
-      const int c = hist[r];
-      hist[r] = pos;
-      pos += c;
-    }
-    ntiles[0] = pos;
-    if (split) nsmall[0] = part_s[blockDim.x - 1];
+    ntiles[0] = nfull_total + npart;
+    if (split) nsmall[0] = nsmall_total;
   }
   __syncthreads();
-  int t = part[threadIdx.x] - local, ts_i = part_s[threadIdx.x] - local_s;
+  int t = incl - local, ts_i = incl_s - local_s;
   for (int e = e0; e < e0 + per && e < E; ++e) {
     int r0, len, nfull, rem;
     bool ts;
