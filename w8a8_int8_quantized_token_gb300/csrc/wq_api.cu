@@ -981,10 +981,17 @@ int forward_masked(const int8_t *a, const float *sa, const int32_t *masked_m, in
     g1.a_norm2 = w4 ? nullptr : norm;
   }
   WQ_TRY(launch_grouped_gemm(g1, stream));
-  WQ_TRY(launch_silu_mul_quant(gu, R, I, scheme == WQ_SCHEME_BLOCK ? 128 : 0, masked_m, Mmax, hq,
-                               sh, stream));
-  // GEMM1 has finished with the fp16 rows and norms (same stream): h's replace them
-  if (f16t) WQ_TRY(launch_row_norm_i8(hq, R, I, masked_m, Mmax, norm, stream, t16));
+  // GEMM1 has finished with the fp16 rows and norms (same stream): h's
+  // replace them, written by the SiLU pass itself (rows of at most 2048
+  // outputs), else by the widening pass after it
+  int rc = WQ_ERR_UNSUPPORTED;
+  if (f16t) rc = launch_silu_mul_quant_dual(gu, R, I, masked_m, Mmax, hq, t16, sh, norm, stream);
+  if (rc != WQ_OK && rc != WQ_ERR_UNSUPPORTED) return rc;
+  if (rc != WQ_OK) {
+    WQ_TRY(launch_silu_mul_quant(gu, R, I, scheme == WQ_SCHEME_BLOCK ? 128 : 0, masked_m, Mmax, hq,
+                                 sh, stream));
+    if (f16t) WQ_TRY(launch_row_norm_i8(hq, R, I, masked_m, Mmax, norm, stream, t16));
+  }
   GemmArgs g2{hq, nullptr, nullptr, sh, W2, sw2, nullptr, masked_m, Mmax, E, R,
               H, I, scheme, acc, WQ_OUT_BF16, y, gws, status};
   g2.w4 = w4 ? 1 : 0;

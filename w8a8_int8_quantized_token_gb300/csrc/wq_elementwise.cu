@@ -908,11 +908,15 @@ __device__ __forceinline__ float silu_outside(uint32_t b) {
 }
 }  // namespace silu2
 
-template <int VPL, int GV, bool F16, int WPR>
+// DUAL (int8 codes, one scale per row): also the same codes as fp16 values
+// in hq16, for the int8-code engine's fp16 token form
+template <int VPL, int GV, bool F16, int WPR, bool DUAL = false>
 __global__ void __launch_bounds__(512, 2) silu_mul_quant_tab_kernel(
     const uint16_t *__restrict__ gu, int64_t R, int64_t I, const int32_t *__restrict__ masked_m,
-    int Mmax, void *__restrict__ hq_out, float *__restrict__ sh, int32_t *__restrict__ norm2) {
+    int Mmax, void *__restrict__ hq_out, float *__restrict__ sh, int32_t *__restrict__ norm2,
+    uint16_t *__restrict__ hq16 = nullptr) {
   using namespace silu2;
+  static_assert(!DUAL || (!F16 && GV == 0), "the dual form writes int8 codes, one scale per row");
   static_assert(WPR == 1 || WPR == 2, "one or two warps per row");
   extern __shared__ float tab[];
   __shared__ float xmax[2][16];  // a warp's row maximum for the row's other warp
@@ -1010,6 +1014,7 @@ __global__ void __launch_bounds__(512, 2) silu_mul_quant_tab_kernel(
           reinterpret_cast<uint4 *>(static_cast<uint16_t *>(hq_out) + row * I)[v] = f16_codes8(r);
         else
           reinterpret_cast<uint2 *>(static_cast<int8_t *>(hq_out) + row * I)[v] = pack_codes8(t);
+        if constexpr (DUAL) reinterpret_cast<uint4 *>(hq16 + row * I)[v] = f16_codes8(r);
         if constexpr (GV == 0) {
           if (norm2 != nullptr) {
 #pragma unroll
@@ -1041,6 +1046,15 @@ __global__ void __launch_bounds__(512, 2) silu_mul_quant_tab_kernel(
 
 // The table kernel for rows of at most 2048 outputs; returns WQ_ERR_UNSUPPORTED
 // for wider rows (the callers then take the block-per-row kernels).
+// two CTAs of 16 warps per SM, fewer for short launches (rows of more than
+// 1024 outputs take two warps each)
+int64_t silu_tab_grid(int64_t R, int64_t nvec) {
+  const int64_t rows_per_cta = 16 / (nvec > 128 ? 2 : 1);
+  const int64_t grid = (R + rows_per_cta - 1) / rows_per_cta;
+  const int64_t cap = 2 * int64_t(num_sms());
+  return grid > cap ? cap : grid;
+}
+
 template <bool F16>
 int launch_silu_tab(const uint16_t *gu, int64_t R, int64_t I, int group, const int32_t *masked_m,
                     int Mmax, void *hq, float *sh, int32_t *norm2, cudaStream_t st) {
@@ -1049,11 +1063,7 @@ int launch_silu_tab(const uint16_t *gu, int64_t R, int64_t I, int group, const i
   // two CTAs of 16 warps per SM (the table fits the default 48 KB of shared
   // memory), fewer for short launches; rows of more than 1024 outputs take
   // two warps each
-  const int wpr = nvec > 128 ? 2 : 1;
-  const int64_t rows_per_cta = 16 / wpr;
-  int64_t grid = (R + rows_per_cta - 1) / rows_per_cta;
-  const int64_t cap = 2 * int64_t(num_sms());
-  if (grid > cap) grid = cap;
+  const int64_t grid = silu_tab_grid(R, nvec);
   const size_t smem = silu_tab::kBytes;
 #define WQ_SILU_TAB(VPL, GV, WPR)                                                               \
   silu_mul_quant_tab_kernel<VPL, GV, F16, WPR><<<unsigned(grid), 512, smem, st>>>(gu, R, I, masked_m, \
@@ -1078,6 +1088,27 @@ int launch_silu_tab(const uint16_t *gu, int64_t R, int64_t I, int group, const i
   }
 #undef WQ_SILU_TAB_G
 #undef WQ_SILU_TAB
+  return launched(1);
+}
+
+// int8 codes, one scale per row, the codes again as fp16 values and each
+// row's squared norm (table kernel only: rows of at most 2048 outputs)
+int launch_silu_mul_quant_dual(const uint16_t *gu, int64_t R, int64_t I, const int32_t *masked_m,
+                               int Mmax, int8_t *hq, uint16_t *hq16, float *sh, int32_t *norm2,
+                               cudaStream_t st) {
+  if (R == 0 || I == 0) return WQ_OK;
+  const int64_t nvec = I / 8;
+  if (R > 0x7fffffff || nvec > 256 || I % 8) return WQ_ERR_UNSUPPORTED;
+  const unsigned grid = unsigned(silu_tab_grid(R, nvec));
+  const size_t smem = silu_tab::kBytes;
+#define WQ_SILU_DUAL(VPL, WPR)                                                                  \
+  silu_mul_quant_tab_kernel<VPL, 0, false, WPR, true><<<grid, 512, smem, st>>>(gu, R, I, masked_m, \
+                                                                               Mmax, hq, sh, norm2, hq16)
+  if (nvec <= 32) WQ_SILU_DUAL(1, 1);
+  else if (nvec <= 64) WQ_SILU_DUAL(2, 1);
+  else if (nvec <= 128) WQ_SILU_DUAL(4, 1);
+  else WQ_SILU_DUAL(4, 2);
+#undef WQ_SILU_DUAL
   return launched(1);
 }
 
