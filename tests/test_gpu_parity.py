@@ -911,6 +911,73 @@ def test_layer_forward_masked_w4a8():
     assert np.all(O.bf16_to_f32(got[~valid]) == 3.0)
 
 
+@pytest.mark.parametrize("w4", [False, True])
+@pytest.mark.parametrize("Mmax, counts", [
+    (64, [64, 17, 16, 0, 1, 63]),     # 64-token plan: the engine widens its own tiles
+    (65, [65, 17, 16, 0, 1, 64]),     # the smallest buffer of the fp16 token form
+    (300, [300, 257, 17, 16, 0, 1]),  # two tiles (256 + 44, 256 + 1 to the small engine)
+])
+def test_layer_forward_masked_token_form_boundaries(w4, Mmax, counts):
+    """The masked layer around the fp16 token form's limits: more than 64
+    rows per expert buffer selects it; experts of 16 valid rows (or
+    remainders of at most 16) go to the small-token engine, 17 to the
+    tensor-core engine.  The workspace starts as 0xFF bytes, so every fp16
+    token row past a valid count reads as NaN: such rows may only reach MMA
+    columns that are never stored.  Outputs equal the oracle's bit for bit,
+    rows past the counts stay untouched."""
+    E, H, I = len(counts), 256, 256
+    g = torch.Generator().manual_seed(Mmax + (7 if w4 else 0))
+    w13 = (torch.randn(E, 2 * I, H, generator=g) * 0.02).to(torch.bfloat16)
+    w2 = (torch.randn(E, H, I, generator=g) * 0.02).to(torch.bfloat16)
+    x = synth.activations(E * Mmax, H, True, Mmax)
+    mm = np.array(counts, np.int32)
+    a, sa = wq.quantize_per_token(x.to(DEV))
+    aq, as_ = O.quantize_per_token(bits(x))
+    y = torch.full((E, Mmax, H), 3.0, dtype=torch.bfloat16, device=DEV)
+    st = wq.new_status()
+    if w4:
+        W13 = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=DEV)
+        W2 = torch.empty(E, H, I // 2, dtype=torch.uint8, device=DEV)
+        S13 = torch.empty(E, 2 * I, device=DEV)
+        S2 = torch.empty(E, H, device=DEV)
+        for e in range(E):
+            W13[e], S13[e] = wq.quantize_weight_int4(w13[e].to(DEV))
+            W2[e], S2[e] = wq.quantize_weight_int4(w2[e].to(DEV))
+        n = wq.lib().wq_moe_forward_masked_w4a8_workspace_size(E, Mmax, H, I)
+        ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=DEV)
+        wq.moe_forward_masked_w4a8(a.view(E, Mmax, H), sa.view(E, Mmax),
+                                   torch.from_numpy(mm).to(DEV), W13, S13, W2, S2, y=y, ws=ws,
+                                   status=st)
+        q13 = [O.quantize_weight_int4(bits(w13[e])) for e in range(E)]
+        q2 = [O.quantize_weight_int4(bits(w2[e])) for e in range(E)]
+        want, valid = O.moe_forward_masked_w4a8(
+            aq.reshape(E, Mmax, H), as_.reshape(E, Mmax), mm,
+            np.stack([O.pack_int4(q[0]) for q in q13]), np.stack([q[1] for q in q13]),
+            np.stack([O.pack_int4(q[0]) for q in q2]), np.stack([q[1] for q in q2]))
+    else:
+        W13 = torch.empty(E, 2 * I, H, dtype=torch.int8, device=DEV)
+        W2 = torch.empty(E, H, I, dtype=torch.int8, device=DEV)
+        S13 = torch.empty(E, 2 * I, device=DEV)
+        S2 = torch.empty(E, H, device=DEV)
+        q = []
+        for e in range(E):
+            wq.quantize_weight(w13[e].to(DEV), "channel", W13[e], S13[e])
+            wq.quantize_weight(w2[e].to(DEV), "channel", W2[e], S2[e])
+            q.append(O.quantize_weights(bits(w13[e]), bits(w2[e]), "channel"))
+        n = wq.lib().wq_moe_forward_masked_workspace_size(E, Mmax, H, I, 0)
+        ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=DEV)
+        wq.moe_forward_masked(a.view(E, Mmax, H), sa.view(E, Mmax), torch.from_numpy(mm).to(DEV),
+                              W13, S13, W2, S2, y=y, ws=ws, status=st)
+        want, valid = O.moe_forward_masked(aq.reshape(E, Mmax, H), as_.reshape(E, Mmax), mm,
+                                           np.stack([t[0] for t in q]), np.stack([t[1] for t in q]),
+                                           np.stack([t[2] for t in q]), np.stack([t[3] for t in q]))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = bits(y)
+    assert_bf16_equal(got[valid], want[valid], f"masked layer, Mmax {Mmax}, w4 {w4}")
+    assert np.all(O.bf16_to_f32(got[~valid]) == 3.0)
+
+
 # ---------------------------------------------------------------- empty inputs
 def test_empty_inputs_write_nothing():
     """Zero tokens, zero routed rows and all-zero masked counts: every entry
