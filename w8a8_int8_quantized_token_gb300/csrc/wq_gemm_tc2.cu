@@ -71,7 +71,9 @@ struct Plan {
   static constexpr int W16 = 2 * WM * BK, T16 = 2 * T8, TK16 = FT ? 2 * TN * BK : 0;
   static constexpr int ST8 = W8 + T8, ST16 = W16 + T16;
   static constexpr int OFF_F16 = 0;
-  static constexpr int OFF_TOK = OFF_F16 + S16 * ST16;  // 1024-aligned: every stage size is
+  // every stage size is a multiple of 1024 bytes, so each token stage starts
+  // 1024-aligned, as the 128-byte swizzle of its TMA copy requires
+  static constexpr int OFF_TOK = OFF_F16 + S16 * ST16;
   static constexpr int OFF_I8 = OFF_TOK + STK * TK16;
   static constexpr int OFF_BAR = OFF_I8 + S8 * ST8;
   static constexpr int B_S8_FULL = 0, B_S8_EMPTY = S8, B_F16_FULL = 2 * S8,
