@@ -62,6 +62,27 @@ def test_workspace_sizes(lib):
     assert lib.wq_grouped_gemm_workspace_size(R, E) > 0
 
 
+def test_masked_workspace_holds_the_fp16_token_rows(lib):
+    """The masked layer's workspace carries the fp16 copy of a GEMM input's
+    rows ([E*Mmax][max(H, I)], plus int32 norms) exactly when the int8-code
+    engine takes 256-token tiles on the channel scheme: more than 64 rows per
+    expert buffer.  Block scheme and Mmax <= 64 go without it."""
+    E, H, I = 32, 7168, 2048
+    per_row = 2 * I * 2 + I + 4  # GEMM1 output, h codes, h scale
+    f16_row = max(H, I) * 2 + 4
+    for Mmax in (64, 65, 512):
+        R = E * Mmax
+        ch = lib.wq_moe_forward_masked_workspace_size(E, Mmax, H, I, 0)
+        blk = lib.wq_moe_forward_masked_workspace_size(E, Mmax, H, I, 1)
+        w4 = lib.wq_moe_forward_masked_w4a8_workspace_size(E, Mmax, H, I)
+        assert w4 == ch
+        assert blk < R * (per_row + f16_row)
+        if Mmax > 64:
+            assert ch >= R * (per_row + f16_row)
+        else:
+            assert R * per_row <= ch < R * (per_row + f16_row)
+
+
 def test_invalid_arguments_rejected_on_host(lib):
     P = ctypes.c_void_p
     fake = P(4096)  # never dereferenced: argument checks fail first
