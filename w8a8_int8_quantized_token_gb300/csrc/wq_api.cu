@@ -985,7 +985,7 @@ int forward_masked(const int8_t *a, const float *sa, const int32_t *masked_m, in
   // replace them, written by the SiLU pass itself (rows of at most 2048
   // outputs), else by the widening pass after it
   int rc = WQ_ERR_UNSUPPORTED;
-  if (f16t) rc = launch_silu_mul_quant_dual(gu, R, I, masked_m, Mmax, hq, t16, sh, norm, stream);
+  if (f16t) rc = launch_silu_mul_quant_dual(gu, R, I, masked_m, Mmax, hq, t16, sh, norm, stream, w4);
   if (rc != WQ_OK && rc != WQ_ERR_UNSUPPORTED) return rc;
   if (rc != WQ_OK) {
     WQ_TRY(launch_silu_mul_quant(gu, R, I, scheme == WQ_SCHEME_BLOCK ? 128 : 0, masked_m, Mmax, hq,

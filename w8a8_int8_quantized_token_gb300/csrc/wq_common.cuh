@@ -293,10 +293,11 @@ int launch_quant_scatter_i8(const uint16_t *x, int64_t T, int64_t K, int64_t ldx
                             cudaStream_t st);
 // SiLU-and-mul + re-quantization to int8 codes (one scale per row, rows of
 // at most 2048 outputs) that also writes the codes as fp16 values and each
-// row's squared norm; WQ_ERR_UNSUPPORTED for wider rows
+// row's squared norm; WQ_ERR_UNSUPPORTED for wider rows.  zero_gates: the
+// GEMM output holds many exact zeros (int4 weights), served on the table path
 int launch_silu_mul_quant_dual(const uint16_t *gu, int64_t R, int64_t I, const int32_t *masked_m,
                                int Mmax, int8_t *hq, uint16_t *hq16, float *sh, int32_t *norm2,
-                               cudaStream_t st);
+                               cudaStream_t st, bool zero_gates = false);
 // squared norms of the valid rows of int8 codes A [R][K], and with out16 the
 // same codes as fp16 values [R][K] (rows past a masked count untouched)
 int launch_row_norm_i8(const int8_t *A, int64_t R, int64_t K, const int32_t *masked_m, int Mmax,

@@ -888,17 +888,27 @@ __device__ __forceinline__ void pair_bar(int id) {
   asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
 }
 // silu of the two bf16 gate values of word w from the table; `miss` is set
-// when either lies outside it (the entry read is then a stand-in)
+// when either lies outside it (the entry read is then a stand-in).  ZF: +-0
+// is served here too (silu(+-0) = +-0), for GEMM outputs with many exact
+// zeros (int4 weights); elsewhere the select costs more than it saves.
+template <bool ZF = false>
 __device__ __forceinline__ void silu_pair(uint32_t w, const float *tab, float &s0, float &s1,
                                           bool &miss) {
   using namespace silu_tab;
-  const uint32_t k0 = (w & 0x7fffu) - kLo;
-  const uint32_t k1 = ((w >> 16) & 0x7fffu) - kLo;
-  miss |= (k0 >= uint32_t(kHalf)) | (k1 >= uint32_t(kHalf));
+  const uint32_t m0 = w & 0x7fffu, m1 = (w >> 16) & 0x7fffu;
+  const uint32_t k0 = m0 - kLo, k1 = m1 - kLo;
+  if constexpr (ZF)
+    miss |= (k0 >= uint32_t(kHalf) && m0 != 0) | (k1 >= uint32_t(kHalf) && m1 != 0);
+  else
+    miss |= (k0 >= uint32_t(kHalf)) | (k1 >= uint32_t(kHalf));
   const uint32_t i0 = k0 + ((w >> 15) & 1u) * uint32_t(kHalf);
   const uint32_t i1 = k1 + (w >> 31) * uint32_t(kHalf);
   s0 = tab[min(i0, uint32_t(kSize - 1))];
   s1 = tab[min(i1, uint32_t(kSize - 1))];
+  if constexpr (ZF) {
+    s0 = m0 == 0 ? __uint_as_float((w & 0x8000u) << 16) : s0;
+    s1 = m1 == 0 ? __uint_as_float(w & 0x80000000u) : s1;
+  }
 }
 // silu of a bf16 value outside the table: the formula, except for +-0,
 // whose silu is +-0 / 2 = +-0 (an integer GEMM lands on exact zeros often
@@ -909,8 +919,9 @@ __device__ __forceinline__ float silu_outside(uint32_t b) {
 }  // namespace silu2
 
 // DUAL (int8 codes, one scale per row): also the same codes as fp16 values
-// in hq16, for the int8-code engine's fp16 token form
-template <int VPL, int GV, bool F16, int WPR, bool DUAL = false>
+// in hq16, for the int8-code engine's fp16 token form; ZF: zero gates on the
+// table path (silu_pair)
+template <int VPL, int GV, bool F16, int WPR, bool DUAL = false, bool ZF = false>
 __global__ void __launch_bounds__(512, 2) silu_mul_quant_tab_kernel(
     const uint16_t *__restrict__ gu, int64_t R, int64_t I, const int32_t *__restrict__ masked_m,
     int Mmax, void *__restrict__ hq_out, float *__restrict__ sh, int32_t *__restrict__ norm2,
@@ -951,7 +962,7 @@ __global__ void __launch_bounds__(512, 2) silu_mul_quant_tab_kernel(
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         float s0, s1;
-        silu_pair(gw[j], tab, s0, s1, miss);
+        silu_pair<ZF>(gw[j], tab, s0, s1, miss);
         mul2(s0, s1, bf16_lo(uw[j]), bf16_hi(uw[j]));
         h[i][2 * j] = s0;
         h[i][2 * j + 1] = s1;
@@ -1095,15 +1106,21 @@ int launch_silu_tab(const uint16_t *gu, int64_t R, int64_t I, int group, const i
 // row's squared norm (table kernel only: rows of at most 2048 outputs)
 int launch_silu_mul_quant_dual(const uint16_t *gu, int64_t R, int64_t I, const int32_t *masked_m,
                                int Mmax, int8_t *hq, uint16_t *hq16, float *sh, int32_t *norm2,
-                               cudaStream_t st) {
+                               cudaStream_t st, bool zero_gates) {
   if (R == 0 || I == 0) return WQ_OK;
   const int64_t nvec = I / 8;
   if (R > 0x7fffffff || nvec > 256 || I % 8) return WQ_ERR_UNSUPPORTED;
   const unsigned grid = unsigned(silu_tab_grid(R, nvec));
   const size_t smem = silu_tab::kBytes;
-#define WQ_SILU_DUAL(VPL, WPR)                                                                  \
-  silu_mul_quant_tab_kernel<VPL, 0, false, WPR, true><<<grid, 512, smem, st>>>(gu, R, I, masked_m, \
-                                                                               Mmax, hq, sh, norm2, hq16)
+#define WQ_SILU_DUAL(VPL, WPR)                                                                   \
+  do {                                                                                          \
+    if (zero_gates)                                                                             \
+      silu_mul_quant_tab_kernel<VPL, 0, false, WPR, true, true><<<grid, 512, smem, st>>>(         \
+          gu, R, I, masked_m, Mmax, hq, sh, norm2, hq16);                                       \
+    else                                                                                        \
+      silu_mul_quant_tab_kernel<VPL, 0, false, WPR, true><<<grid, 512, smem, st>>>(               \
+          gu, R, I, masked_m, Mmax, hq, sh, norm2, hq16);                                       \
+  } while (0)
   if (nvec <= 32) WQ_SILU_DUAL(1, 1);
   else if (nvec <= 64) WQ_SILU_DUAL(2, 1);
   else if (nvec <= 128) WQ_SILU_DUAL(4, 1);
