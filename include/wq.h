@@ -398,7 +398,10 @@ WQ_API int wq_moe_forward_host(const uint16_t *x_host, const float *logits_host,
  * [E][Mmax][H] with scales sa ([E][Mmax], or [E][Mmax][H/128] for BLOCK) and
  * valid counts masked_m [E] -> y bf16 [E][Mmax][H] (GEMM1 -> SiLU-mul +
  * re-quantize -> GEMM2 on the valid rows; other rows not written).
- * Workspace: wq_moe_forward_masked_workspace_size(). */
+ * Workspace: wq_moe_forward_masked_workspace_size().  With the CHANNEL
+ * scheme and Mmax > 64 it also holds an fp16 copy of each GEMM's valid input
+ * rows (E * Mmax * max(H, I) * 2 bytes, 235 MB at 32 x 512 x 7168), which
+ * the tensor-core engine loads as token tiles. */
 WQ_API size_t wq_moe_forward_masked_workspace_size(int E, int Mmax, int H, int I, int scheme);
 WQ_API int wq_moe_forward_masked(const int8_t *a, const float *sa, const int32_t *masked_m, int E,
                           int Mmax, const int8_t *W13, const float *sw13, const int8_t *W2,
