@@ -978,6 +978,30 @@ def test_layer_forward_masked_token_form_boundaries(w4, Mmax, counts):
     assert np.all(O.bf16_to_f32(got[~valid]) == 3.0)
 
 
+def test_layer_forward_masked_wide_intermediate():
+    """I = 2176 (more than the 2048 outputs the table SiLU pass takes): the
+    masked layer re-quantizes h with the general SiLU kernel and widens h's
+    rows for the fp16 token form in a separate pass.  Bit-exact."""
+    cfg = synth.small_config("masked_wide", T=0, H=256, I=2176, E=3, k=1)
+    Mmax = 80
+    x = synth.activations(cfg.E * Mmax, cfg.H, True, 11)
+    a, sa = wq.quantize_per_token(x.to(DEV))
+    qo, so = O.quantize_per_token(bits(x))
+    mm = np.array([80, 20, 5], np.int32)
+    (W13, S13, W2, S2), orc = quantized_weights(cfg, DEV)
+    y = torch.full((cfg.E, Mmax, cfg.H), 5.0, dtype=torch.bfloat16, device=DEV)
+    st = wq.new_status()
+    wq.moe_forward_masked(a.view(cfg.E, Mmax, cfg.H), sa.view(cfg.E, Mmax),
+                          torch.from_numpy(mm).to(DEV), W13, S13, W2, S2, y=y, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref, valid = O.moe_forward_masked(qo.reshape(cfg.E, Mmax, cfg.H), so.reshape(cfg.E, Mmax), mm,
+                                      *stack_oracle(orc, cfg.E))
+    yb = bits(y)
+    assert_bf16_equal(yb[valid], ref[valid], "masked layer, I = 2176")
+    assert np.all(O.bf16_to_f32(yb[~valid]) == 5.0)
+
+
 # ---------------------------------------------------------------- empty inputs
 def test_empty_inputs_write_nothing():
     """Zero tokens, zero routed rows and all-zero masked counts: every entry
